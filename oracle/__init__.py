@@ -1,0 +1,131 @@
+"""float64 CPU oracle for the G1 gated attention layer.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers. The GPU library never
+imports this package, and this package imports nothing from the GPU library.
+
+The arithmetic lives in ``gsdpa_oracle.c`` (plain C, double precision, the
+layer's definition written out; its header lists the page and section each
+step follows). This module compiles it with gcc on first use and exposes it
+to numpy.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants and a library routine (torch's CPU float64 SDPA); no
+function is left with parity unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gsdpa_oracle.c")
+_LIB = os.path.join(_HERE, "libgsdpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GATE_NONE, GATE_HEADWISE, GATE_ELEMENTWISE = 0, 1, 2
+_GATE_CODES = {"none": GATE_NONE, "headwise": GATE_HEADWISE, "elementwise": GATE_ELEMENTWISE}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared object next to its source."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)  # serial build without OpenMP
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.gsdpa_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
+                ip, ip, ctypes.c_long, ctypes.c_int]
+            lib.gsdpa_oracle_fwd.restype = ctypes.c_int
+            lib.gsdpa_oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().gsdpa_oracle_max_threads())
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor -> exact float64 upcast on the host
+        a = a.detach().to("cpu")
+        import torch
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a, t=ctypes.c_double):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(t))
+
+
+def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n_threads=0):
+    """Gated SDPA in float64.
+
+    Shapes: X [B, L_q, d_model], Q [B, L_q, H_q, d_k], K/V [B, L_k, H_kv, d_k],
+    W_g [d_model, H_q*d_k] (elementwise) or [d_model, H_q] (headwise), or None
+    when ``gate == "none"``.
+
+    ``rows``: None for every row, else a list/array of (b, i) pairs.
+    Returns (O, p0): O [B, L_q, H_q, d_k] (or [n_rows, H_q, d_k]) and the
+    attention weight on key 0 per row and head, [B, L_q, H_q] (or [n_rows, H_q]).
+    """
+    gm = _GATE_CODES[gate]
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Lq, Hq, dk = Q.shape
+    _, Lk, Hkv, _ = K.shape
+    if gm == GATE_NONE:
+        Xd, Wd, d_model = None, None, 0
+    else:
+        Xd, Wd = _f64(X), _f64(W_g)
+        d_model = Xd.shape[-1]
+        expect = Hq * dk if gm == GATE_ELEMENTWISE else Hq
+        if Wd.shape != (d_model, expect):
+            raise ValueError(f"W_g shape {Wd.shape} != {(d_model, expect)}")
+    if rows is None:
+        O = np.empty((B, Lq, Hq, dk), np.float64)
+        p0 = np.empty((B, Lq, Hq), np.float64)
+        rb = ri = None
+        n = -1
+    else:
+        rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
+        rb = np.ascontiguousarray(rows[:, 0])
+        ri = np.ascontiguousarray(rows[:, 1])
+        n = rows.shape[0]
+        O = np.empty((n, Hq, dk), np.float64)
+        p0 = np.empty((n, Hq), np.float64)
+    rc = _load().gsdpa_oracle_fwd(
+        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(O), _ptr(p0),
+        B, Lq, Lk, d_model, Hq, Hkv, dk, gm, int(bool(causal)),
+        _ptr(rb, ctypes.c_int), _ptr(ri, ctypes.c_int), n, int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes or rows")
+    return O, p0
+
+
+def sink_share(p0):
+    """First-token attention share per (b, h): the mean over query rows of p0.
+
+    p0 is the [B, L_q, H_q] output of :func:`gated_sdpa` over all rows.
+    """
+    return np.asarray(p0).mean(axis=1)

@@ -1,0 +1,173 @@
+/*
+ * gsdpa_oracle.c -- float64 CPU oracle for the G1 gated attention layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain definition of what the
+ * layer computes, written out in double precision with no tiling, fusion or
+ * reordering. Only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg may load it. The GPU library never links or calls it, and it
+ * shares no code with the GPU library.
+ *
+ * What it computes, for every batch b, query head h and query row i
+ * (sources, by page title and section):
+ *
+ *   a      = L_k - L_q + i         absolute position of query i; the causal
+ *                                  mask is aligned bottom-right so that one
+ *                                  decode query sees the whole cache (the
+ *                                  pages are silent for L_q < L_k; this is
+ *                                  the reading taken).
+ *   kv(h)  = h / (H_q / H_kv)      contiguous query-head groups share one
+ *                                  K/V head ("GatedAttention [2025]",
+ *                                  sec. 1.3.1, the GQA description: h query
+ *                                  heads in g groups).
+ *   s_j    = <Q[b,i,h,:], K[b,j,kv(h),:]> / sqrt(d_k)
+ *                                  for j <= a when causal, all j otherwise
+ *                                  ("GatedAttention [2025]", sec. 1.2.1, the
+ *                                  SDPA equation; sec. 1.4.1, the per-head
+ *                                  output sums over j = 0..i).
+ *   p_j    = exp(s_j - max s) / sum_j exp(s_j - max s)
+ *                                  (row-stochastic softmax, sec. 1.2.1).
+ *   y_c    = sum_j p_j V[b,j,kv(h),c]
+ *   gl     = sum_m X[b,i,m] W_g[m, h*d_k + c]   elementwise gate, n x q x d_k
+ *          = sum_m X[b,i,m] W_g[m, h]           headwise gate,    n x q
+ *                                  ("GatedAttention [2025]", sec. 1.2.2, the
+ *                                  gating equation Y' = Y (.) sigma(X W);
+ *                                  "10 . 门控", sec. 3.2, the G1 module: no
+ *                                  bias, head-major gate columns, one scalar
+ *                                  per head when headwise).
+ *   O[b,i,h,c] = y_c * 1/(1 + exp(-gl))         (gate NONE: O = y)
+ *   p0[b,i,h]  = p_0, the attention weight on key 0 ("10 . 门控", sec. 3.4,
+ *                the share of attention that lands on the first token).
+ *
+ * Precision: every input arrives as double (the exact upcast of the fp32 or
+ * bf16 values the GPU sees); nothing is rounded.
+ *
+ * Rows: the caller passes either all rows (n_rows < 0) or a list of (b, i)
+ * pairs; each listed row is computed exactly as above. Sampling rows changes
+ * nothing in the arithmetic of a row.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_GATE_NONE = 0, ORACLE_GATE_HEADWISE = 1, ORACLE_GATE_ELEMENTWISE = 2 };
+
+/* One query row (b, i), all heads. s is scratch of length >= L_k. */
+static void oracle_row(const double* X, const double* Q, const double* K, const double* V,
+                       const double* Wg, double* O_row, double* p0_row, double* s,
+                       int b, int i, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
+                       int gate_mode, int causal)
+{
+    const int group = Hq / Hkv;
+    const long a = (long)Lk - Lq + i;
+    const long n_keys = causal ? a + 1 : Lk;
+    const double inv_sqrt_dk = 1.0 / sqrt((double)dk);
+    const double* x = X + ((long)b * Lq + i) * d_model;
+    const long gate_cols = (gate_mode == ORACLE_GATE_ELEMENTWISE) ? (long)Hq * dk : Hq;
+
+    for (int h = 0; h < Hq; ++h) {
+        const int kvh = h / group;
+        const double* q = Q + (((long)b * Lq + i) * Hq + h) * dk;
+
+        /* scores */
+        double mx = -INFINITY;
+        for (long j = 0; j < n_keys; ++j) {
+            const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c) dot += q[c] * k[c];
+            s[j] = dot * inv_sqrt_dk;
+            if (s[j] > mx) mx = s[j];
+        }
+        /* softmax */
+        double denom = 0.0;
+        for (long j = 0; j < n_keys; ++j) {
+            s[j] = exp(s[j] - mx);
+            denom += s[j];
+        }
+        for (long j = 0; j < n_keys; ++j) s[j] /= denom;
+        if (p0_row) p0_row[h] = s[0];
+
+        /* headwise gate: one logit for the head */
+        double g_head = 1.0;
+        if (gate_mode == ORACLE_GATE_HEADWISE) {
+            double gl = 0.0;
+            for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + h];
+            g_head = 1.0 / (1.0 + exp(-gl));
+        }
+
+        double* o = O_row + (long)h * dk;
+        for (int c = 0; c < dk; ++c) {
+            double y = 0.0;
+            for (long j = 0; j < n_keys; ++j)
+                y += s[j] * V[(((long)b * Lk + j) * Hkv + kvh) * dk + c];
+            double g = g_head;
+            if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
+                double gl = 0.0;
+                const long col = (long)h * dk + c;
+                for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + col];
+                g = 1.0 / (1.0 + exp(-gl));
+            }
+            o[c] = y * g;
+        }
+    }
+}
+
+/*
+ * Returns 0 on success, -1 on a shape the definition does not cover.
+ *   O    : [B, L_q, H_q, d_k] when n_rows < 0, else [n_rows, H_q, d_k]
+ *   p0   : [B, L_q, H_q]      when n_rows < 0, else [n_rows, H_q]   (nullable)
+ *   rows_b, rows_i : the (b, i) pairs when n_rows >= 0
+ *   n_threads : OpenMP threads (<= 0: library default)
+ */
+int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const double* V,
+                     const double* Wg, double* O, double* p0,
+                     int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
+                     int gate_mode, int causal,
+                     const int* rows_b, const int* rows_i, long n_rows, int n_threads)
+{
+    if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
+    if (Lq > Lk) return -1;
+    if (gate_mode != ORACLE_GATE_NONE && (d_model < 1 || !X || !Wg)) return -1;
+    if (gate_mode < 0 || gate_mode > 2) return -1;
+
+    const long total = (n_rows < 0) ? (long)B * Lq : n_rows;
+    for (long r = 0; n_rows >= 0 && r < n_rows; ++r)
+        if (rows_b[r] < 0 || rows_b[r] >= B || rows_i[r] < 0 || rows_i[r] >= Lq) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < total; ++r) {
+            if (!s) continue;
+            int b, i;
+            if (n_rows < 0) { b = (int)(r / Lq); i = (int)(r % Lq); }
+            else            { b = rows_b[r];     i = rows_i[r]; }
+            oracle_row(X, Q, K, V, Wg, O + r * (long)Hq * dk, p0 ? p0 + r * (long)Hq : 0, s,
+                       b, i, Lq, Lk, d_model, Hq, Hkv, dk, gate_mode, causal);
+        }
+        free(s);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Number of threads an OpenMP region would use (1 without OpenMP). */
+int gsdpa_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
