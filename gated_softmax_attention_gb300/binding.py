@@ -1,0 +1,134 @@
+"""ctypes binding of libgsdpa.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels. Torch is
+used here for device memory (output and workspace tensors when the caller
+does not pass them) and for the current stream. If the library has not been
+built, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgsdpa.so")
+
+GATE_NONE, GATE_HEADWISE, GATE_ELEMENTWISE = 0, 1, 2
+GATE_CODES = {"none": GATE_NONE, "headwise": GATE_HEADWISE, "elementwise": GATE_ELEMENTWISE}
+F32, BF16 = 0, 1
+
+OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_LAUNCH, ERR_DEVICE_TIMEOUT = -1, -2, -3, -4, -5, -6
+
+# Every entry point the header declares, with its ctypes signature.
+_VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "gsdpa_workspace_bytes": (_SZ, [_I] * 10),
+    "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gsdpa_check_device_error": (_I, [_VP]),
+    "gsdpa_status_string": (ctypes.c_char_p, [_I]),
+    "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GsdpaError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load(path: str = LIB_PATH):
+    """Load libgsdpa.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m gated_softmax_attention_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gsdpa_status_string(int(status)).decode()
+
+
+def workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise", want_sink=False, dtype=BF16) -> int:
+    n = load().gsdpa_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, GATE_CODES[gate], int(bool(want_sink)),
+                                     dtype)
+    if n == ctypes.c_size_t(-1).value:
+        raise GsdpaError(ERR_INVALID_ARG, "gsdpa_workspace_bytes")
+    return int(n)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    load().gsdpa_set_wait_limit_ns(int(ns))
+
+
+def check_device_error(stream=None) -> int:
+    """Synchronise the stream and return the device error status (0 = none)."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().gsdpa_check_device_error(ctypes.c_void_p(s.cuda_stream)))
+
+
+def fwd_raw(X, Q, K, V, W_g, O, sink, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
+            workspace, workspace_bytes, stream) -> int:
+    """Direct call of gated_sdpa_fwd with integer pointers; returns the status."""
+    return int(load().gated_sdpa_fwd(X, Q, K, V, W_g, O, sink, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode,
+                                     int(bool(causal)), dtype, workspace, workspace_bytes, stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def gated_sdpa_fwd(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out=None, sink=None,
+                   want_sink=False, workspace=None, stream=None):
+    """Gated attention forward through the C ABI on torch CUDA tensors.
+
+    X [B, L_q, d_model], Q [B, L_q, H_q, d_k], K/V [B, L_k, H_kv, d_k],
+    W_g [d_model, H_q*d_k | H_q] (None for gate="none"). All contiguous, on
+    the current CUDA device, float32 or bfloat16 (all the same dtype).
+    Returns (O, sink) where sink is None unless requested.
+    """
+    import torch
+    if Q.dtype == torch.bfloat16:
+        dtype = BF16
+    elif Q.dtype == torch.float32:
+        dtype = F32
+    else:
+        raise TypeError(f"unsupported dtype {Q.dtype}")
+    gm = GATE_CODES[gate]
+    tensors = [Q, K, V] + ([X, W_g] if gm != GATE_NONE else [])
+    for t in tensors:
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
+            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
+    B, L_q, H_q, d_k = Q.shape
+    L_k, H_kv = K.shape[1], K.shape[2]
+    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    if out is None:
+        out = torch.empty_like(Q)
+    if sink is None and want_sink:
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
+    need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, sink is not None, dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = fwd_raw(_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V),
+                 _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink),
+                 B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, causal, dtype,
+                 _ptr(workspace) if need > 0 else None, need if need > 0 else 0,
+                 ctypes.c_void_p(s.cuda_stream))
+    if st != OK:
+        raise GsdpaError(st, "gated_sdpa_fwd")
+    return out, sink

@@ -1,0 +1,266 @@
+// gsdpa_api.cu -- the C ABI of libgsdpa.so (declared in include/gsdpa.h):
+// argument validation, workspace planning, dispatch to the kernels, and the
+// device error word that bounded waits report into.
+#include "gsdpa.h"
+#include "gsdpa_internal.h"
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+namespace gsdpa {
+
+// Set by a kernel's bounded wait when it runs out; read and cleared by
+// gsdpa_check_device_error().
+__device__ uint32_t g_error_word;
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+// Split-K factors are planned for a fixed SM count so that the workspace size
+// is a pure function of the problem (152 SMs on GB300; a little headroom).
+constexpr int kPlanSms = 160;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t* err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return nullptr;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        d.err = static_cast<uint32_t*>(p);
+        d.ready = true;
+    }
+    return &d;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side checks shared by gsdpa_workspace_bytes and gated_sdpa_fwd.
+int validate_shape(const Problem& p) {
+    if (p.B < 0 || p.Lq < 0 || p.Lk < 1 || p.Lq > p.Lk) return GSDPA_ERR_INVALID_ARG;
+    if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv != 0) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_mode < 0 || p.gate_mode > 2) return GSDPA_ERR_INVALID_ARG;
+    if (p.dtype != GSDPA_F32 && p.dtype != GSDPA_BF16) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_mode != GSDPA_GATE_NONE && p.d_model < 1) return GSDPA_ERR_INVALID_ARG;
+    if (p.dk != 64 && p.dk != 128) return GSDPA_ERR_UNSUPPORTED;
+    if (p.dtype == GSDPA_BF16) {
+        // TMA needs every row stride to be a multiple of 16 bytes.
+        if (p.gate_mode != GSDPA_GATE_NONE && p.d_model % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
+        if (p.gate_mode == GSDPA_GATE_HEADWISE && p.Hq % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
+    }
+    const long long units = (long long)((p.Lq + 127) / 128) * p.Hq * p.B;
+    if (units > 0x7fffffffLL) return GSDPA_ERR_UNSUPPORTED;
+    return GSDPA_OK;
+}
+
+int gate_cols(const Problem& p) {
+    if (p.gate_mode == GSDPA_GATE_ELEMENTWISE) return p.Hq * p.dk;
+    if (p.gate_mode == GSDPA_GATE_HEADWISE) return p.Hq;
+    return 0;
+}
+
+}  // namespace
+
+int gate_col_tile(int cols);  // gate_gemm_sm103.cu
+
+WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
+    WorkspacePlan w;
+    size_t off = 0;
+    const bool bf16 = p.dtype == GSDPA_BF16;
+    const bool decode = bf16 && p.Lq == 1;
+    if (p.sink) {
+        w.sink_tiles = bf16 ? (p.Lq + 127) / 128 : (p.Lq + 31) / 32;
+        w.sink_part = off;
+        off = align256(off + sizeof(float) * (size_t)p.B * p.Hq * w.sink_tiles);
+    }
+    // Gate logits computed ahead of the attention kernel: bf16 headwise
+    // prefill and bf16 decode (elementwise prefill keeps the gate in-CTA).
+    const bool gate_prepass = bf16 && p.gate_mode != GSDPA_GATE_NONE &&
+                              (decode || p.gate_mode == GSDPA_GATE_HEADWISE);
+    if (gate_prepass) {
+        w.gate_rows = p.B * p.Lq;
+        w.gate_cols = gate_cols(p);
+        const int nt = gate_col_tile(w.gate_cols);
+        const int tiles = ((w.gate_rows + 127) / 128) * ((w.gate_cols + nt - 1) / nt);
+        const int nkc = (p.d_model + 63) / 64;
+        int splits = (num_sms + tiles - 1) / tiles;
+        int max_splits = nkc / 4 > 0 ? nkc / 4 : 1;
+        if (splits > max_splits) splits = max_splits;
+        if (splits < 1) splits = 1;
+        w.gate_splits = splits;
+        w.gate_part = off;
+        off = align256(off + sizeof(float) * (size_t)splits * w.gate_rows * w.gate_cols);
+    }
+    w.total = off;
+    return w;
+}
+
+static std::once_flag g_encode_once;
+static EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_tiled_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+// sink[b,h] = (1 / L_q) * sum over query tiles of the per-tile sums of p(i -> key 0).
+__global__ void sink_finalize_kernel(const float* __restrict__ part, float* __restrict__ sink, int n, int tiles,
+                                     float inv_lq) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n) return;
+    float s = 0.f;
+    for (int t = 0; t < tiles; ++t) s += part[(long)idx * tiles + t];
+    sink[idx] = s * inv_lq;
+}
+
+cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s) {
+    const int n = p.B * p.Hq;
+    sink_finalize_kernel<<<(n + 127) / 128, 128, 0, s>>>(reinterpret_cast<const float*>(ws + w.sink_part), p.sink, n,
+                                                         w.sink_tiles, 1.0f / (float)p.Lq);
+    return cudaGetLastError();
+}
+
+}  // namespace gsdpa
+
+using namespace gsdpa;
+
+extern "C" {
+
+size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode,
+                             int want_sink, int dtype) {
+    Problem p{};
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.dtype = dtype;
+    p.sink = want_sink ? reinterpret_cast<float*>(16) : nullptr;
+    if (validate_shape(p) != GSDPA_OK) return (size_t)-1;
+    if (B == 0 || L_q == 0) return 0;
+    return plan_workspace(p, kPlanSms).total;
+}
+
+int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
+                   int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    Problem p{};
+    p.X = X;
+    p.Q = Q;
+    p.K = K;
+    p.V = V;
+    p.Wg = W_g;
+    p.O = O;
+    p.sink = sink;
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.causal = causal ? 1 : 0;
+    p.dtype = dtype;
+    int st = validate_shape(p);
+    if (st != GSDPA_OK) return st;
+    if (B == 0 || L_q == 0) return GSDPA_OK;
+    if (!Q || !K || !V || !O) return GSDPA_ERR_INVALID_ARG;
+    if (gate_mode != GSDPA_GATE_NONE && (!X || !W_g)) return GSDPA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return GSDPA_ERR_ALIGNMENT;
+    if (gate_mode != GSDPA_GATE_NONE && (!aligned16(X) || !aligned16(W_g))) return GSDPA_ERR_ALIGNMENT;
+    if (sink && (reinterpret_cast<uintptr_t>(sink) & 3u)) return GSDPA_ERR_ALIGNMENT;
+
+    const DeviceInfo* dev = device_info();
+    if (!dev) return GSDPA_ERR_LAUNCH;
+    if (dtype == GSDPA_BF16 && !(dev->cc_major == 10 && dev->cc_minor == 3)) return GSDPA_ERR_UNSUPPORTED;
+    if (dtype == GSDPA_BF16 && !encode_tiled_fn()) return GSDPA_ERR_UNSUPPORTED;
+
+    const WorkspacePlan w = plan_workspace(p, kPlanSms);
+    if (w.total > 0) {
+        if (!workspace || workspace_bytes < w.total) return GSDPA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSDPA_ERR_ALIGNMENT;
+    }
+    char* ws = static_cast<char*>(workspace);
+    Runtime rt;
+    rt.err = dev->err;
+    rt.limit_ns = g_wait_limit_ns.load();
+    rt.num_sms = dev->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e = cudaSuccess;
+    if (dtype == GSDPA_F32) {
+        e = launch_f32_simt(p, w, ws, rt, s);
+        if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
+    } else {
+        bool gate_launched = false;
+        e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
+        if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
+        if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
+    }
+    if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
+    return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
+}
+
+int gsdpa_check_device_error(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GSDPA_ERR_LAUNCH;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return GSDPA_ERR_LAUNCH;
+    if (v != 0) {
+        const uint32_t zero = 0;
+        cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+        return GSDPA_ERR_DEVICE_TIMEOUT;
+    }
+    return GSDPA_OK;
+}
+
+const char* gsdpa_status_string(int status) {
+    switch (status) {
+        case GSDPA_OK: return "GSDPA_OK";
+        case GSDPA_ERR_INVALID_ARG: return "GSDPA_ERR_INVALID_ARG";
+        case GSDPA_ERR_UNSUPPORTED: return "GSDPA_ERR_UNSUPPORTED";
+        case GSDPA_ERR_ALIGNMENT: return "GSDPA_ERR_ALIGNMENT";
+        case GSDPA_ERR_WORKSPACE: return "GSDPA_ERR_WORKSPACE";
+        case GSDPA_ERR_LAUNCH: return "GSDPA_ERR_LAUNCH";
+        case GSDPA_ERR_DEVICE_TIMEOUT: return "GSDPA_ERR_DEVICE_TIMEOUT";
+        default: return "GSDPA_ERR_UNKNOWN";
+    }
+}
+
+int gsdpa_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
+    return GSDPA_OK;
+}
+
+}  // extern "C"

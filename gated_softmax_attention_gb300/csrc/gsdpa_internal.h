@@ -1,0 +1,66 @@
+// gsdpa_internal.h -- host-side launch interfaces shared by the .cu files of
+// libgsdpa.so. Not part of the public ABI (include/gsdpa.h is).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gsdpa {
+
+struct Problem {
+    const void* X;
+    const void* Q;
+    const void* K;
+    const void* V;
+    const void* Wg;
+    void* O;
+    float* sink;
+    int B, Lq, Lk, d_model, Hq, Hkv, dk;
+    int gate_mode;   // 0 none, 1 headwise, 2 elementwise
+    int causal;
+    int dtype;       // 0 f32, 1 bf16
+};
+
+struct Runtime {
+    uint32_t* err;                 // device error word
+    unsigned long long limit_ns;   // bounded-wait limit
+    int num_sms;
+};
+
+// Workspace carve-up (byte offsets, all 256-aligned) for one problem.
+struct WorkspacePlan {
+    size_t total = 0;
+    size_t sink_part = 0;   // float [B, Hq, n_tiles]          (sink partial sums)
+    int sink_tiles = 0;
+    size_t gate_part = 0;   // float [gate_splits, rows, cols] (gate logits, split-K partials)
+    int gate_splits = 0;
+    int gate_rows = 0, gate_cols = 0;
+    size_t dec_ml = 0;      // float [B, Hq, splits, 2]        (decode running max, sum)
+    size_t dec_o = 0;       // float [B, Hq, splits, dk]       (decode partial outputs)
+    size_t dec_cnt = 0;     // int   [B, Hkv * head_chunks]     (decode arrival counters)
+    int dec_splits = 0;
+    int dec_heads_per_cta = 0;
+    size_t dec_cnt_bytes = 0;
+};
+
+WorkspacePlan plan_workspace(const Problem& p, int num_sms);
+
+// Driver entry point for tensor-map encoding (resolved once, no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Launchers: return cudaSuccess or the launch error. `ws` is the workspace base.
+cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                            cudaStream_t s);
+cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                    cudaStream_t s, bool* launched);
+cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                cudaStream_t s);
+cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                               cudaStream_t s);
+cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);
+
+}  // namespace gsdpa

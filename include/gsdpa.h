@@ -1,0 +1,157 @@
+/*
+ * gsdpa.h -- C ABI of the GB300 gated softmax attention library (libgsdpa.so).
+ *
+ * The operation: for each batch b, query head h and query row i,
+ *
+ *     O[b,i,h,:] = softmax_j( Q[b,i,h,:] . K[b,j,kv(h),:] / sqrt(d_k)  + causal mask )
+ *                  @ V[b,:,kv(h),:]
+ *                  (.) sigmoid( X[b,i,:] W_g[:, cols(h)] )
+ *
+ * Sources (page title and section):
+ *   - SDPA, rows non-negative and summing to one:
+ *       "GatedAttention [2025]", sec. 1.2.1 (the Attention(Q,K,V) equation).
+ *   - The gate Y' = Y (.) sigma(X W_theta), X the hidden state after
+ *     pre-normalisation, sigma the logistic sigmoid, multiplicative and
+ *     head-specific by default:
+ *       "GatedAttention [2025]", sec. 1.2.2.
+ *   - Position G1 (on the SDPA output of each head, before the heads are
+ *     concatenated), elementwise gate (n x q x d_k) and headwise gate (n x q):
+ *       "GatedAttention [2025]", sec. 1.2.2 and 1.3.2; "10 . 门控", sec. 3.2
+ *       (position table, Table 1 excerpt rows 5 and 10, and the G1 module with
+ *       no bias and head-major gate columns).
+ *   - Grouped-query K/V heads: "GatedAttention [2025]", sec. 1.3.1.
+ *   - Causal sums over j <= i: "GatedAttention [2025]", sec. 1.4.1.
+ *   - First-token attention share: "10 . 门控", sec. 3.4; "GatedAttention
+ *     [2025]", sec. 1.4.3 (the F-Attn column).
+ *
+ * Readings where the pages are silent (the library's choices):
+ *   - kv(h) = h / (H_q / H_kv): query heads form contiguous groups.
+ *   - When L_q < L_k the causal mask is aligned bottom-right: query i sits at
+ *     absolute position L_k - L_q + i and sees keys 0 .. L_k - L_q + i. A single
+ *     decode query therefore sees the whole cache (the current token included).
+ *   - The gate has no bias. cols(h) = h*d_k .. h*d_k + d_k - 1 (elementwise)
+ *     or the single column h (headwise).
+ *   - The first-token share is measured on the ungated attention weights and
+ *     averaged over query rows: sink[b,h] = mean_i p(i -> key 0).
+ *
+ * Layouts (all row-major, contiguous, no padding):
+ *   X    [B, L_q, d_model]
+ *   Q    [B, L_q, H_q,  d_k]
+ *   K, V [B, L_k, H_kv, d_k]
+ *   W_g  [d_model, H_q*d_k] (elementwise) or [d_model, H_q] (headwise)
+ *   O    [B, L_q, H_q,  d_k]  == the concatenated [B, L_q, H_q*d_k]
+ *   sink [B, H_q] float32
+ * The element type of X, Q, K, V, W_g and O is float32 (GSDPA_F32) or
+ * bfloat16 (GSDPA_BF16); sink is always float32.
+ *
+ * Ownership: the caller owns every buffer (inputs, outputs, workspace) and
+ * the stream. All pointers passed to gated_sdpa_fwd are DEVICE pointers of
+ * the current device. The library never allocates device memory and never
+ * synchronises inside gated_sdpa_fwd: the call enqueues kernels (and small
+ * memset nodes on the workspace) on `stream` and returns.
+ *
+ * Errors: every function returns a gsdpa_status. Argument errors are detected
+ * on the host before anything is enqueued. Kernels never wait without a limit:
+ * a wait that runs out records a device error word and the kernel returns;
+ * gsdpa_check_device_error() reads that word.
+ */
+#ifndef GSDPA_H_
+#define GSDPA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GSDPA_API __attribute__((visibility("default")))
+#else
+#define GSDPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GSDPA_GATE_NONE = 0,         /* plain SDPA, W_g and X may be NULL */
+    GSDPA_GATE_HEADWISE = 1,     /* one sigmoid per (token, head)     */
+    GSDPA_GATE_ELEMENTWISE = 2   /* one sigmoid per (token, head, c)  */
+} gsdpa_gate_mode;
+
+typedef enum {
+    GSDPA_F32 = 0,               /* float32 in/out, float32 arithmetic (SIMT) */
+    GSDPA_BF16 = 1               /* bfloat16 in/out, fp32 accumulation (tcgen05) */
+} gsdpa_dtype;
+
+typedef enum {
+    GSDPA_OK = 0,
+    GSDPA_ERR_INVALID_ARG = -1,      /* a size, mode or pointer is invalid      */
+    GSDPA_ERR_UNSUPPORTED = -2,      /* valid, but not built (d_k, device, ...) */
+    GSDPA_ERR_ALIGNMENT = -3,        /* a pointer is not 16-byte aligned        */
+    GSDPA_ERR_WORKSPACE = -4,        /* workspace NULL or smaller than needed   */
+    GSDPA_ERR_LAUNCH = -5,           /* the CUDA runtime refused a launch       */
+    GSDPA_ERR_DEVICE_TIMEOUT = -6    /* a kernel wait ran out (see below)       */
+} gsdpa_status;
+
+/*
+ * Bytes of device workspace gated_sdpa_fwd needs for this problem, or 0 if
+ * none. Same arguments as gated_sdpa_fwd (want_sink != 0 when a sink pointer
+ * will be passed). Returns (size_t)-1 for arguments gated_sdpa_fwd would
+ * reject. Host-only; touches no device.
+ */
+GSDPA_API size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                             int gate_mode, int want_sink, int dtype);
+
+/*
+ * The gated attention forward (prefill when L_q > 1, decode when L_q == 1).
+ *
+ *   X, Q, K, V, W_g : device inputs in the layouts above. X and W_g may be
+ *                     NULL when gate_mode == GSDPA_GATE_NONE.
+ *   O               : device output [B, L_q, H_q, d_k], same dtype as inputs.
+ *   sink            : device float32 [B, H_q] or NULL (not computed).
+ *   B, L_q, L_k     : batch, query rows, key rows; 1 <= L_q <= L_k. B, L_q == 0
+ *                     is an empty problem: nothing is enqueued, GSDPA_OK.
+ *   d_model         : width of X (>= 1 when a gate is used; for bf16 a
+ *                     multiple of 8, since every row must start on 16 bytes).
+ *   H_q, H_kv       : query and K/V heads, H_q % H_kv == 0 (bf16 headwise
+ *                     gate: H_q a multiple of 8, for the same reason).
+ *   d_k             : head dimension, 64 or 128.
+ *   gate_mode       : gsdpa_gate_mode.
+ *   causal          : nonzero for the bottom-right causal mask.
+ *   dtype           : gsdpa_dtype. GSDPA_BF16 needs an sm_103 device.
+ *   workspace       : device scratch of at least gsdpa_workspace_bytes(...)
+ *                     bytes, 256-byte aligned; contents need not be
+ *                     initialised and are overwritten. NULL allowed when 0.
+ *   stream          : a cudaStream_t (NULL = legacy default stream).
+ *
+ * X, Q, K, V, W_g and O must be 16-byte aligned and sink 4-byte aligned
+ * (GSDPA_ERR_ALIGNMENT otherwise).
+ * Calls that share a workspace must not overlap on the device.
+ */
+GSDPA_API int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                   void* O, float* sink,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits inside the kernels set when they run out. Returns GSDPA_OK,
+ * GSDPA_ERR_DEVICE_TIMEOUT, or GSDPA_ERR_LAUNCH if the stream itself reports
+ * a CUDA error.
+ */
+GSDPA_API int gsdpa_check_device_error(void* stream);
+
+/* A static, human-readable name for a gsdpa_status value. */
+GSDPA_API const char* gsdpa_status_string(int status);
+
+/*
+ * Test hook, not part of the operation: sets the wait limit, in nanoseconds,
+ * that every bounded wait inside the kernels uses from the next launch on
+ * (0 restores the default of 2 s). Lets a test make a wait run out quickly.
+ */
+GSDPA_API int gsdpa_set_wait_limit_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSDPA_H_ */

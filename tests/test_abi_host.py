@@ -1,0 +1,104 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every
+symbol include/gsdpa.h declares, and rejects bad arguments before it touches
+a device. No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_softmax_attention_gb300 import binding as gb
+from gated_softmax_attention_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gsdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gb.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"GSDPA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    assert {"gated_sdpa_fwd", "gsdpa_workspace_bytes", "gsdpa_check_device_error",
+            "gsdpa_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in gb.SIGNATURES, f"binding lacks a signature for {n}"
+
+
+def test_only_the_abi_is_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gb.LIB_PATH], capture_output=True, text=True).stdout
+    ours = {line.split()[-1] for line in out.splitlines() if line.split()[-1].startswith("gsdpa")
+            or line.split()[-1].startswith("gated_sdpa")}
+    assert ours == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "GSDPA_OK"), (-1, "GSDPA_ERR_INVALID_ARG"), (-2, "GSDPA_ERR_UNSUPPORTED"),
+                       (-3, "GSDPA_ERR_ALIGNMENT"), (-4, "GSDPA_ERR_WORKSPACE"), (-5, "GSDPA_ERR_LAUNCH"),
+                       (-6, "GSDPA_ERR_DEVICE_TIMEOUT")]:
+        assert gb.status_string(code) == name
+    assert gb.status_string(99) == "GSDPA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    # elementwise bf16 prefill keeps the gate in-CTA: no workspace without sink
+    assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", False, gb.BF16) == 0
+    # sink partials: B*H_q*ceil(L/128) floats, 256-aligned
+    n = gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", True, gb.BF16)
+    assert n >= 2 * 16 * 16 * 4 and n % 256 == 0
+    # headwise bf16: split-K gate logits [splits, B*L, H_q]
+    n = gb.workspace_bytes(1, 4096, 4096, 4096, 32, 4, 128, "headwise", False, gb.BF16)
+    assert n >= 4096 * 32 * 4 and n % 256 == 0
+    # empty problems need nothing
+    assert gb.workspace_bytes(0, 16, 16, 64, 4, 4, 64, "elementwise", True, gb.BF16) == 0
+    # rejected shapes
+    for args in [(1, 8, 4, 64, 4, 4, 64), (1, 8, 8, 64, 3, 2, 64), (1, 8, 8, 64, 4, 4, 96)]:
+        with pytest.raises(gb.GsdpaError):
+            gb.workspace_bytes(*args, "elementwise", False, gb.BF16)
+    with pytest.raises(gb.GsdpaError):  # bf16 headwise needs H_q % 8 == 0
+        gb.workspace_bytes(1, 8, 8, 64, 4, 4, 64, "headwise", False, gb.BF16)
+    assert gb.workspace_bytes(1, 8, 8, 64, 4, 4, 64, "headwise", False, gb.F32) == 0
+
+
+def call(**kw):
+    base = dict(X=16, Q=16, K=16, V=16, W_g=16, O=16, sink=None, B=1, L_q=8, L_k=8, d_model=64, H_q=4, H_kv=4,
+                d_k=64, gate_mode=2, causal=1, dtype=0, workspace=None, workspace_bytes=0, stream=None)
+    base.update(kw)
+    return gb.fwd_raw(**base)
+
+
+def test_argument_validation_before_any_device_work(lib):
+    assert call(L_q=9, L_k=8) == gb.ERR_INVALID_ARG        # L_q > L_k
+    assert call(L_k=0, L_q=0) == gb.ERR_INVALID_ARG        # no keys
+    assert call(H_q=6, H_kv=4) == gb.ERR_INVALID_ARG       # H_q % H_kv
+    assert call(gate_mode=3) == gb.ERR_INVALID_ARG
+    assert call(dtype=7) == gb.ERR_INVALID_ARG
+    assert call(d_k=96) == gb.ERR_UNSUPPORTED
+    assert call(Q=None) == gb.ERR_INVALID_ARG
+    assert call(W_g=None) == gb.ERR_INVALID_ARG            # gated without W_g
+    assert call(X=24) == gb.ERR_ALIGNMENT
+    assert call(O=8) == gb.ERR_ALIGNMENT
+    assert call(B=0) == gb.OK                              # empty problem: nothing enqueued
+    assert call(L_q=0) == gb.OK
+    assert call(dtype=1, d_model=60) == gb.ERR_UNSUPPORTED  # bf16 rows must start on 16 bytes
+
+
+def test_fwd_signature_matches_header(lib):
+    # 7 pointers, 10 ints, workspace pointer, size, stream
+    res, args = gb.SIGNATURES["gated_sdpa_fwd"]
+    assert len(args) == 20 and res is ctypes.c_int
