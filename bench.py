@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one gated_sdpa_fwd call on the headline prefill workload
+(bf16, B=2, L=2048, d_model=2048, 16 heads of 128, causal, elementwise gate,
+first-token share on): head map and schedule, S = QK^T, online softmax, PV,
+the in-CTA gate GEMM, the sigmoid-multiply epilogue and the first-token share.
+The same run also times the decode workload (bf16, 64 single-query rows
+against an 8192-token cache, GQA 32/8, elementwise gate) and reports it under
+"decode" in GB/s, since the metric names both.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise; each step is timed with CUDA events on the stream
+the kernels run on, and L2 is flushed (256 MiB write) before every step since
+the prefill inputs (92 MB) fit in L2. value = FLOPs of all steps on all ranks
+/ the slowest rank's summed step time. Under torchrun every rank runs its own
+replica (no collective on the data path): scaling is weak.
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+build) on the host cores, on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gated causal attention fwd TFLOP/s (bf16) and decode HBM GB/s, % of roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_mha_elementwise_L2048")
+    ap.add_argument("--decode-workload", default="bf16_decode_gqa_elementwise_Lk8192")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=0, help="0: same as --steps, capped at 200")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: min(--steps, 50)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", default="", help="comma-separated workloads to time as extra lines on stderr")
+    ap.add_argument("--profile-workload", default="",
+                    help="for profilers: only run --profile-calls untimed calls of this workload and exit")
+    ap.add_argument("--profile-calls", type=int, default=3)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+class Dist:
+    def __init__(self, backend):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.torch = torch
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64,
+                              device="cuda" if self.pg.get_backend() == "nccl" else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ helpers
+
+def row_flops(w, rows):
+    """Algorithmic FLOPs of the listed (b, i) query rows (all heads)."""
+    off = w.L_k - w.L_q
+    n = 0
+    for _, i in rows:
+        keys = (off + i + 1) if w.causal else w.L_k
+        n += 4 * w.H_q * w.d_k * keys + 2 * w.d_model * w.gate_cols
+    return n
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def oracle_cpu_baseline(w, inputs, seconds, seed=0):
+    """Time the float64 oracle on a bounded, seeded row sample of workload w."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    all_rows = [(b, i) for b in range(w.B) for i in range(w.L_q)]
+    cal = [all_rows[k] for k in rng.choice(len(all_rows), size=min(64, len(all_rows)), replace=False)]
+    t0 = time.perf_counter()
+    oracle.gated_sdpa(inputs["X"], inputs["Q"], inputs["K"], inputs["V"], inputs["W_g"], gate=w.gate,
+                      causal=w.causal, rows=cal)
+    dt = time.perf_counter() - t0
+    rate = row_flops(w, cal) / max(dt, 1e-9)                     # FLOP/s
+    per_row = row_flops(w, all_rows) / len(all_rows)
+    n = int(min(len(all_rows), max(64, seconds * rate / per_row)))
+    rows = [all_rows[k] for k in rng.choice(len(all_rows), size=n, replace=False)]
+    t0 = time.perf_counter()
+    oracle.gated_sdpa(inputs["X"], inputs["Q"], inputs["K"], inputs["V"], inputs["W_g"], gate=w.gate,
+                      causal=w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": row_flops(w, rows) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{n} of {len(all_rows)} query rows (all {w.H_q} heads each), uniform over (b, i), seed {seed}"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms, with timestamps
+    so that only samples taken inside the timed region are summarised."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = ["-i", str(self.dev)]
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.4)  # nvidia-smi start-up
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, windows):
+        """windows: list of (t0, t1) time.time() intervals, tried in order until one holds >= 3 samples."""
+        import datetime
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for label, (t0, t1) in windows:
+            sel = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+            if len(sel) >= 3 or label == windows[-1][0]:
+                break
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0, "window": label}
+        reasons = sorted({names[k] for *_, r in sel for k in range(4) if r[k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel), "window": label}
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_calls(torch, call, K, W, flush, stream):
+    for _ in range(W):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        flush()
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_ours(args, d: Dist):
+    import torch
+    from gated_softmax_attention_gb300 import binding as gb
+    from gated_softmax_attention_gb300 import build as gbuild
+    from gated_softmax_attention_gb300.workloads import WORKLOADS, make_inputs
+
+    if d.rank == 0 or not os.path.exists(gbuild.LIB):
+        gbuild.build()
+    d.barrier()
+    gb.load()
+    torch.cuda.set_device(d.local)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    K, W = args.steps, args.warmup
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    # ---- CPU baseline first (before any long GPU work), rank 0 only
+    w = WORKLOADS[args.workload]
+    host = make_inputs(w)
+    cpu_base = None
+    if d.rank == 0 and not args.no_cpu_baseline:
+        cpu_base = oracle_cpu_baseline(w, host, args.cpu_seconds)
+
+    dev = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
+    O = torch.empty_like(dev["Q"])
+    sink = torch.empty((w.B, w.H_q), dtype=torch.float32, device="cuda")
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate, True, gb.BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def step(gate=w.gate, want_sink=True):
+        gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=gate, causal=w.causal,
+                          out=O, sink=sink if want_sink else None, workspace=ws, stream=stream)
+
+    # ---- headline: K timed steps
+    for _ in range(W):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    d.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(d.local) as clk:
+        t_start = time.time()
+        wall0 = time.perf_counter()
+        for k in range(K):
+            flush()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        t_end = time.time()
+        d.barrier()
+        torch.cuda.synchronize()
+        # the dominant kernel alone (the call without the first-token share), same clocks window
+        kern_ms = time_calls(torch, lambda: step(want_sink=False), max(K, 200), W, flush, stream)
+        t_end2 = time.time()
+    clocks = clk.summary([("timed region", (t_start, t_end)),
+                          ("timed region + prefill-kernel re-timing", (t_start, t_end2))])
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error during the timed region: {gb.status_string(st)}")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    local_s = sum(step_ms) / 1e3
+    max_s = d.max(local_s)
+    flops = w.flops()
+    value = flops * K * d.world / max_s / 1e12
+
+    kern_avg = statistics.mean(kern_ms)
+    achieved = flops / (kern_avg / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"] + " burst bf16 (cuBLAS)", "traffic": None,
+                "kernel": "prefill_kernel<128,2>", "kernel_ms": round(kern_avg, 4)}
+    # attention-only throughput and the gated / ungated time ratio
+    none_ms = time_calls(torch, lambda: step(gate="none", want_sink=False), K, W, flush, stream)
+    none_avg = statistics.mean(none_ms)
+
+    # ---- end to end: pinned host inputs -> device -> call -> O back to the host
+    E = args.e2e_steps or min(K, 50)
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    O_host = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    sink_host = torch.empty(sink.shape, dtype=sink.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = O.numel() * O.element_size() + sink.numel() * sink.element_size()
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                dev[k].copy_(v, non_blocking=True)
+        step()
+        O_host.copy_(O, non_blocking=True)
+        sink_host.copy_(sink, non_blocking=True)
+
+    e2e_ms = time_calls(torch, e2e_step, E, min(W, 3), flush, stream)
+    e2e_s = d.max(sum(e2e_ms) / 1e3)
+    e2e = {"value": round(flops * E * d.world / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
+
+    launches_per_step = 2  # prefill kernel + first-token-share finalize
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": d.world, "steps": K,
+        "warmup": W, "ms_per_step": round(max_s * 1e3 / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) X/Q/K/V, W_g ~ N(0, 0.02^2), rounded once to bf16",
+        "config": {"workload": w.name, "B": w.B, "L_q": w.L_q, "L_k": w.L_k, "d_model": w.d_model, "H_q": w.H_q,
+                   "H_kv": w.H_kv, "d_k": w.d_k, "gate": w.gate, "causal": w.causal, "first_token_share": True,
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{d.world}", "flops_per_step": flops},
+        "clocks": clocks, "wall_s_timed_region": round(wall, 4),
+        "e2e": e2e, "gpu_launches": launches_per_step * K,
+        "roofline": roofline,
+        "attention_only_tflops": round(w.attn_flops() / (none_avg / 1e3) / 1e12, 2),
+        "gated_vs_ungated_time_ratio": round(kern_avg / none_avg, 4),
+        "cpu_baseline": cpu_base,
+    }
+
+    # ---- decode leg
+    if not args.no_decode:
+        out["decode"] = run_decode(args, d, torch, gb, WORKLOADS[args.decode_workload], make_inputs, flush, stream,
+                                   peaks)
+        out["gpu_launches"] += out["decode"]["gpu_launches"]
+
+    # ---- extra workloads (context only), one stderr line each
+    for name in [x for x in args.extra.split(",") if x]:
+        wx = WORKLOADS[name]
+        hx = {k: (v.cuda() if v is not None else None) for k, v in make_inputs(wx).items()}
+        Ox = torch.empty_like(hx["Q"])
+        t = time_calls(torch, lambda: gb.gated_sdpa_fwd(hx["X"], hx["Q"], hx["K"], hx["V"], hx["W_g"], gate=wx.gate,
+                                                         causal=wx.causal, out=Ox, stream=stream),
+                       max(3, min(K, 20)), 2, flush, stream)
+        ms = statistics.mean(t)
+        print(json.dumps({"extra": name, "ms": round(ms, 4), "TFLOP/s": round(wx.flops() / ms / 1e9, 2),
+                          "frac_of_bf16_peak": round(wx.flops() / ms / 1e9 / peaks["bf16_tflops"], 4)}),
+              file=sys.stderr)
+        del hx, Ox
+    return out
+
+
+def run_decode(args, d, torch, gb, w, make_inputs, flush, stream, peaks):
+    host = make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
+    O = torch.empty_like(dev["Q"])
+    sink = torch.empty((w.B, w.H_q), dtype=torch.float32, device="cuda")
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate, True, gb.BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def step():
+        gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate, causal=w.causal, out=O,
+                          sink=sink, workspace=ws, stream=stream)
+
+    K = args.decode_steps or min(args.steps, 200)
+    d.barrier()
+    ms = time_calls(torch, step, K, args.warmup, flush, stream)
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in decode: {gb.status_string(st)}")
+    s = d.max(sum(ms) / 1e3)
+    nbytes = w.algorithmic_bytes()
+    gbs = nbytes * K * d.world / s / 1e9
+    per_gpu = nbytes / (s / K) / 1e9
+    # e2e with the 2 GiB cache copied from pinned host memory every step
+    E = min(args.e2e_steps or 10, 10)
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    O_host = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                dev[k].copy_(v, non_blocking=True)
+        step()
+        O_host.copy_(O, non_blocking=True)
+
+    e2e_ms = time_calls(torch, e2e_step, E, 2, flush, stream)
+    e2e_s = d.max(sum(e2e_ms) / 1e3)
+    return {"workload": w.name, "value": round(gbs, 2), "unit": "GB/s", "steps": K,
+            "ms_per_step": round(s * 1e3 / K, 5), "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(per_gpu / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"] + " STREAM-style copy",
+                         "scope": "whole call (gate-logit pre-pass + decode kernel)", "traffic": None},
+            "e2e": {"value": round(nbytes * E * d.world / e2e_s / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": O.numel() * O.element_size(), "steps": E},
+            "gpu_launches": 2 * K}
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def run_reference(args, d: Dist):
+    from gated_softmax_attention_gb300.workloads import WORKLOADS, make_inputs
+    import numpy as np
+    import oracle
+    w = WORKLOADS[args.workload]
+    host = make_inputs(w)
+    oracle.build()
+    K, W = args.steps, args.warmup
+    # each step: a seeded row sample sized so that all W + K steps take about two minutes
+    budget = 120.0 / max(1, K + W)
+    rng = np.random.default_rng(0)
+    all_rows = [(b, i) for b in range(w.B) for i in range(w.L_q)]
+    cal = [all_rows[k] for k in rng.choice(len(all_rows), size=32, replace=False)]
+    t0 = time.perf_counter()
+    oracle.gated_sdpa(host["X"], host["Q"], host["K"], host["V"], host["W_g"], gate=w.gate, causal=w.causal, rows=cal)
+    rate = row_flops(w, cal) / (time.perf_counter() - t0)
+    per_row = row_flops(w, all_rows) / len(all_rows)
+    n = int(min(len(all_rows), max(8, budget * rate / per_row)))
+    samples = [[all_rows[k] for k in rng.choice(len(all_rows), size=n, replace=False)] for _ in range(K + W)]
+    for r in samples[:W]:
+        oracle.gated_sdpa(host["X"], host["Q"], host["K"], host["V"], host["W_g"], gate=w.gate, causal=w.causal,
+                          rows=r)
+    total_s, total_f = 0.0, 0
+    for r in samples[W:]:
+        t0 = time.perf_counter()
+        oracle.gated_sdpa(host["X"], host["Q"], host["K"], host["V"], host["W_g"], gate=w.gate, causal=w.causal,
+                          rows=r)
+        total_s += time.perf_counter() - t0
+        total_f += row_flops(w, r)
+    value = total_f / total_s / 1e12
+    sample = f"{n} of {len(all_rows)} query rows per step (all {w.H_q} heads), uniform over (b, i), seed 0"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": d.world,
+        "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) X/Q/K/V, W_g ~ N(0, 0.02^2), rounded once to bf16, upcast to f64",
+        "config": {"workload": w.name, "B": w.B, "L_q": w.L_q, "L_k": w.L_k, "d_model": w.d_model, "H_q": w.H_q,
+                   "H_kv": w.H_kv, "d_k": w.d_k, "gate": w.gate, "causal": w.causal, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def run_profile(args):
+    """Untimed calls of one workload (1 GPU), for ncu: nothing else runs on the device."""
+    import torch
+    from gated_softmax_attention_gb300 import binding as gb
+    from gated_softmax_attention_gb300 import build as gbuild
+    from gated_softmax_attention_gb300.workloads import WORKLOADS, make_inputs
+    gbuild.build()
+    w = WORKLOADS[args.profile_workload]
+    dev = {k: (v.cuda() if v is not None else None) for k, v in make_inputs(w).items()}
+    O = torch.empty_like(dev["Q"])
+    for _ in range(args.profile_calls):
+        gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate, causal=w.causal, out=O)
+    st = gb.check_device_error()
+    print(json.dumps({"profile_workload": w.name, "calls": args.profile_calls, "status": gb.status_string(st)}))
+    if st != gb.OK:
+        sys.exit(1)
+
+
+def main():
+    args = parse()
+    if args.profile_workload:
+        run_profile(args)
+        return
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; other ranks exit without work or rendezvous
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        d = Dist.__new__(Dist)
+        d.world = int(os.environ.get("WORLD_SIZE", "1"))
+        print(json.dumps(run_reference(args, d)))
+        return
+    d = Dist("nccl")
+    out = run_ours(args, d)
+    if d.rank == 0:
+        print(json.dumps(out))
+    d.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -87,8 +87,8 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
     WorkspacePlan w;
     size_t off = 0;
     const bool bf16 = p.dtype == GSDPA_BF16;
-    const bool decode = bf16 && p.Lq == 1;
-    if (p.sink) {
+    const bool decode = decode_supported(p);
+    if (p.sink && !decode) {
         w.sink_tiles = bf16 ? (p.Lq + 127) / 128 : (p.Lq + 31) / 32;
         w.sink_part = off;
         off = align256(off + sizeof(float) * (size_t)p.B * p.Hq * w.sink_tiles);
@@ -110,6 +110,20 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
         w.gate_splits = splits;
         w.gate_part = off;
         off = align256(off + sizeof(float) * (size_t)splits * w.gate_rows * w.gate_cols);
+    }
+    if (decode) {
+        const int chunks = (p.Hq / p.Hkv) / 4;
+        w.dec_splits = decode_splits(p, num_sms);
+        w.dec_heads_per_cta = 4;
+        w.dec_ml = off;
+        off = align256(off + sizeof(float) * 2 * (size_t)p.B * p.Hq * w.dec_splits);
+        w.dec_o = off;
+        off = align256(off + sizeof(float) * (size_t)p.B * p.Hq * w.dec_splits * p.dk);
+        w.dec_x0 = off;
+        off = align256(off + sizeof(float) * (size_t)p.B * p.Hq);
+        w.dec_cnt = off;
+        w.dec_cnt_bytes = sizeof(int) * (size_t)p.B * p.Hkv * chunks;
+        off = align256(off + w.dec_cnt_bytes);
     }
     w.total = off;
     return w;
@@ -225,8 +239,12 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
     } else {
         bool gate_launched = false;
         e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
-        if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
-        if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
+        if (decode_supported(p)) {
+            if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s);
+        } else {
+            if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
+            if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
+        }
     }
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
     return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;

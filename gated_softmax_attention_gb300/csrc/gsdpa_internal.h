@@ -38,6 +38,7 @@ struct WorkspacePlan {
     int gate_rows = 0, gate_cols = 0;
     size_t dec_ml = 0;      // float [B, Hq, splits, 2]        (decode running max, sum)
     size_t dec_o = 0;       // float [B, Hq, splits, dk]       (decode partial outputs)
+    size_t dec_x0 = 0;      // float [B, Hq]                   (decode: scaled score of key 0)
     size_t dec_cnt = 0;     // int   [B, Hkv * head_chunks]     (decode arrival counters)
     int dec_splits = 0;
     int dec_heads_per_cta = 0;
@@ -45,6 +46,11 @@ struct WorkspacePlan {
 };
 
 WorkspacePlan plan_workspace(const Problem& p, int num_sms);
+
+// The dedicated decode kernel covers bf16, L_q == 1, d_k == 128 and query
+// groups of a multiple of 4 heads; other decode shapes use the prefill kernel.
+bool decode_supported(const Problem& p);
+int decode_splits(const Problem& p, int num_sms);
 
 // Driver entry point for tensor-map encoding (resolved once, no -lcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
