@@ -1,30 +1,40 @@
 // prefill_sm103.cu -- bf16 gated attention forward on sm_103a tensor cores.
 //
-// One CTA computes one unit (b, h, 128-row query tile):
-//   S_j = Q K_j^T                       tcgen05.mma, fp32 accumulator in TMEM
-//   P_j = exp2(S_j * log2(e)/sqrt(d_k) - m)  online softmax in registers
-//   O  += P_j V_j                       tcgen05.mma, fp32 accumulator in TMEM
-//   G   = X_tile W_g[:, h*d_k : (h+1)*d_k]   (elementwise gate, same CTA, TMEM)
-//   out = O / l (.) sigmoid(G)          epilogue, bf16, TMA store
-// ("GatedAttention [2025]", sec. 1.2.1 SDPA and sec. 1.2.2 gate;
-//  "10 . 门控", sec. 3.2: G1 sits on each head's SDPA output before concat.)
-// The ungated SDPA output never leaves the SM.
+// One CTA computes one unit (b, h, pair of 128-row query tiles t = 0, 1):
+//   S_t = Q_t K_j^T                      tcgen05.mma (A, B in shared memory)
+//   P_t = exp2(S_t log2(e)/sqrt(d_k) - m_t)   online softmax, one thread per row
+//   O_t += P_t V_j                       tcgen05.mma with P read from TMEM
+//   G_t = X_t W_g[:, h*d_k:(h+1)*d_k]    elementwise gate GEMM, same CTA
+//   out_t = O_t / l_t (.) sigmoid(G_t)   epilogue: bf16, TMA store
+// ("GatedAttention [2025]", sec. 1.2.1 SDPA and sec. 1.2.2 the gate
+//  Y' = Y (.) sigma(X W); "10 . 门控", sec. 3.2: G1 gates each head's SDPA
+//  output before the heads are concatenated.) The ungated output never leaves
+//  the SM.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, gate X/W_g chunks, then K_0, K_1, V_0,
-//               K_2, V_1, ... through a ring of NS shared-memory stages;
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma and commit;
-//   warps 2..5  softmax + epilogue, one thread per query row (TMEM lane).
-// S is double-buffered in TMEM so that S_{j+1} = Q K_{j+1}^T runs while the
-// softmax warps work on S_j. P goes through shared memory (K-major, 128B
-// swizzle) as the A operand of the PV MMA.
+// Warp roles (384 threads):
+//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ... and
+//                the gate chunks (X_t [128 x 64], W_g [64 x d_k]) through a
+//                ring of NS shared-memory stages;
+//   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma / commit;
+//   warps 2, 3   spare;
+//   warps 4..7   softmax + epilogue of query tile 0 (one thread per row);
+//   warps 8..11  softmax + epilogue of query tile 1.
+// Both query tiles consume the same K_j / V_j tiles, so each K/V tile is
+// loaded once per 256 query rows. The MMA warp issues, per key tile j,
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+// so that the tensor pipe works on one tile while the other tile's softmax
+// runs. tcgen05.commit tracks every earlier MMA of the issuing thread, so once
+// S_t(j) is complete PV_t(j-1) is complete too: the softmax may rescale O_t
+// and overwrite S_t with P_t without further waits.
 //
-// TMEM columns: S0 [0,128)  S1 [128,256)  O [256,256+d_k)  G [384,384+d_k).
+// TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d_k)
+//                     O_1 [384,384+d_k); P_t is packed bf16 in S_t [0,64);
+//                     G_t (elementwise gate) reuses S_t after the last PV_t.
 //
 // The causal mask is aligned bottom-right (query i at absolute position
 // L_k - L_q + i); key tiles entirely above the diagonal are never loaded.
-// Units are numbered heaviest first (last query tiles first) so that the
-// hardware block scheduler hands out the long causal units early.
+// Units are numbered heaviest first so the block scheduler starts the long
+// causal units early.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -33,32 +43,35 @@
 namespace gsdpa {
 namespace {
 
-constexpr int kTile = 128;           // query rows per unit, keys per K/V tile
-constexpr int kThreads = 192;
+constexpr int kTile = 128;           // query rows per tile, keys per K/V tile
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// Register split: warpgroup 0 (producer, MMA, spare) gives registers to the
+// two softmax warpgroups. The launch must provide 384 x kRegsLaunchMin.
+constexpr int kRegsLow = 40;
+constexpr int kRegsHigh = 216;
+constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 
 template <int HD, int GATE>
 struct PrefillCfg {
-    static constexpr uint32_t Q_BYTES = kTile * HD * 2;
-    static constexpr uint32_t P_BYTES = kTile * kTile * 2;
+    static constexpr uint32_t Q_BYTES = kTile * HD * 2;   // one query tile
     static constexpr uint32_t KV_BYTES = kTile * HD * 2;
     static constexpr uint32_t GX_BYTES = kTile * 64 * 2;
     static constexpr uint32_t GW_BYTES = 64 * HD * 2;
     static constexpr uint32_t STAGE_BYTES =
         (GATE == 2 && GX_BYTES + GW_BYTES > KV_BYTES) ? GX_BYTES + GW_BYTES : KV_BYTES;
     static constexpr int NS = (HD == 128) ? 4 : 6;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_RING = OFF_P + P_BYTES;
+    static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
+    static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
-    static constexpr int NBAR = 2 * NS + 9;
+    static constexpr int NBAR = 2 * NS + 8;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
 
 struct PrefillArgs {
-    int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles;
+    int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_pairs;
     const float* gate_part;  // headwise: [splits, B*Lq, Hq]
     int gate_splits;
     float* sink_part;        // [B, Hq, n_qtiles] or null
@@ -79,41 +92,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::OFF_Q;
-    uint8_t* sP = smem + C::OFF_P;
     uint8_t* ring = smem + C::OFF_RING;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;                 // [NS]
     uint64_t* empty = bars + C::NS;        // [NS]
     uint64_t* q_full = bars + 2 * C::NS;
-    uint64_t* s_full = q_full + 1;         // [2]
-    uint64_t* s_free = q_full + 3;         // [2]
-    uint64_t* p_full = q_full + 5;
-    uint64_t* o_done = q_full + 6;
-    uint64_t* g_full = q_full + 7;
-    uint64_t* drain = q_full + 8;
+    uint64_t* s_full = q_full + 1;         // [2] per query tile
+    uint64_t* p_full = q_full + 3;         // [2]
+    uint64_t* g_full = q_full + 5;         // [2]: all MMAs of the tile (and its gate GEMM) done
+    uint64_t* drain = q_full + 7;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [4]
+    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
     // ---- unit (heaviest first when causal)
-    const int per_tile = args.Hq * args.B;
+    const int per_pair = args.Hq * args.B;
     const int u = blockIdx.x;
-    const int qt = args.causal ? (args.n_qtiles - 1 - u / per_tile) : (u / per_tile);
-    const int rem = u % per_tile;
+    const int pr = args.causal ? (args.n_pairs - 1 - u / per_pair) : (u / per_pair);
+    const int rem = u % per_pair;
     const int h = rem % args.Hq;
     const int b = rem / args.Hq;
     const int kvh = h / (args.Hq / args.Hkv);
-    const int q0 = qt * kTile;
     const long off = (long)args.Lk - args.Lq;
-    long kend = args.Lk;
-    if (args.causal) {
-        const long last = off + q0 + kTile;  // keys 0 .. off+q0+127 can be visible
-        kend = last < kend ? last : kend;
+    int q0[2], nkv[2];
+    bool act[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        q0[t] = (2 * pr + t) * kTile;
+        act[t] = q0[t] < args.Lq;
+        long kend = args.Lk;
+        if (args.causal) {
+            const long last = off + q0[t] + kTile;  // keys 0 .. off+q0+127 can be visible
+            kend = last < kend ? last : kend;
+        }
+        nkv[t] = act[t] ? (int)((kend + kTile - 1) / kTile) : 0;
     }
-    const int n_kv = (int)((kend + kTile - 1) / kTile);
+    const int nj = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
     const int nkc = (args.d_model + 63) / 64;
 
     if (threadIdx.x == 0) {
@@ -122,13 +139,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(&empty[s], 1);
         }
         mbar_init(q_full, 1);
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(&s_free[0], 128);
-        mbar_init(&s_free[1], 128);
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
-        mbar_init(g_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&g_full[t], 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -148,243 +163,248 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
+    // (each setmaxnreg sits inside the branch of the role it serves, so that
+    // the compiler can give each role its own register budget)
+    if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            uint32_t armed_phase[C::NS];
-            bool armed[C::NS];
-            for (int s = 0; s < C::NS; ++s) armed[s] = false;
+            uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-            for (int cb = 0; cb < HD / 64; ++cb) tma_load_4d(sQ + cb * 16384, &tmQ, cb * 64, h, q0, b, q_full);
-
-            auto acquire = [&](uint32_t bytes) -> uint8_t* {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.ctl)) return nullptr;
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                armed[stage] = true;
-                armed_phase[stage] = phase;
-                return ring + stage * C::STAGE_BYTES;
-            };
-            auto advance = [&]() {
-                if (++stage == (uint32_t)C::NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            if (GATE == 2) {
-                for (int kc = 0; kc < nkc && ok; ++kc) {
-                    uint8_t* st = acquire(C::GX_BYTES + C::GW_BYTES);
-                    if (!st) { ok = false; break; }
-                    tma_load_3d(st, &tmX, kc * 64, q0, b, &full[stage]);
+            mbar_arrive_expect_tx(q_full, (act[1] ? 2 : 1) * C::Q_BYTES);
+            for (int t = 0; t < 2; ++t)
+                if (act[t])
                     for (int cb = 0; cb < HD / 64; ++cb)
-                        tma_load_2d(st + C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64, &full[stage]);
-                    advance();
+                        tma_load_4d(sQ + t * C::Q_BYTES + cb * 16384, &tmQ, cb * 64, h, q0[t], b, q_full);
+
+            int item = 0;
+            auto acquire = [&](uint32_t bytes) -> uint8_t* {
+                const int s = item % C::NS;
+                const uint32_t ph = (item / C::NS) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.ctl)) return nullptr;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                armed |= 1u << s;
+                armed_phase = (armed_phase & ~(1u << s)) | (ph << s);
+                return ring + s * C::STAGE_BYTES;
+            };
+            for (int j = 0; j < nj && ok; ++j) {
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    uint8_t* st = acquire(C::KV_BYTES);
+                    if (!st) { ok = false; break; }
+                    const CUtensorMap* m = kv ? &tmV : &tmK;
+                    for (int cb = 0; cb < HD / 64; ++cb)
+                        tma_load_4d(st + cb * 16384, m, cb * 64, kvh, j * kTile, b, &full[item % C::NS]);
+                    ++item;
                 }
             }
-            auto load_kv = [&](const CUtensorMap* m, int j) -> bool {
-                uint8_t* st = acquire(C::KV_BYTES);
-                if (!st) return false;
-                for (int cb = 0; cb < HD / 64; ++cb)
-                    tma_load_4d(st + cb * 16384, m, cb * 64, kvh, j * kTile, b, &full[stage]);
-                advance();
-                return true;
-            };
-            if (ok) ok = load_kv(&tmK, 0);
-            for (int j = 1; j < n_kv && ok; ++j) {
-                ok = load_kv(&tmK, j);
-                if (ok) ok = load_kv(&tmV, j - 1);
+            if (GATE == 2) {
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (!act[t]) continue;
+                    for (int kc = 0; kc < nkc; ++kc) {
+                        uint8_t* st = acquire(C::GX_BYTES + C::GW_BYTES);
+                        if (!st) { ok = false; break; }
+                        tma_load_3d(st, &tmX, kc * 64, q0[t], b, &full[item % C::NS]);
+                        for (int cb = 0; cb < HD / 64; ++cb)
+                            tma_load_2d(st + C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64,
+                                        &full[item % C::NS]);
+                        ++item;
+                    }
+                }
             }
-            if (ok) ok = load_kv(&tmV, n_kv - 1);
             if (!ok) {
                 // Let every copy already issued land before the CTA can exit.
-                WaitCtl c2 = args.ctl;
                 volatile int never = 0;
+                WaitCtl c2 = args.ctl;
+                if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
                 mbar_wait(q_full, 0, &never, c2);
                 for (int s = 0; s < C::NS; ++s)
-                    if (armed[s]) mbar_wait(&full[s], armed_phase[s], &never, c2);
+                    if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, c2);
             }
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
             bool ok = true;
-            const uint32_t tS0 = tmem, tO = tmem + 256, tG = tmem + 384;
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(128, HD, false, true);
-            const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP), ringa = smem_u32(ring);
-            auto advance = [&]() {
-                if (++stage == (uint32_t)C::NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            ok = mbar_wait(q_full, 0, abort_flag, args.ctl);
-            tc_fence_after();
-            if (GATE == 2) {
-                for (int kc = 0; kc < nkc && ok; ++kc) {
-                    if (!(ok = mbar_wait(&full[stage], phase, abort_flag, args.ctl))) break;
-                    tc_fence_after();
-                    const uint32_t st = ringa + stage * C::STAGE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(st + C::GX_BYTES + kk * 2048, 8192, 1024);
-                        mma_bf16_ss(tG, ad, bd, idO, (kc | kk) != 0);
-                    }
-                    mma_commit(&empty[stage]);
-                    advance();
-                }
-                if (ok) mma_commit(g_full);
-            }
-            auto issue_S = [&](int j) -> bool {
-                if (j >= 2 && !mbar_wait(&s_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, args.ctl)) return false;
-                if (!mbar_wait(&full[stage], phase, abort_flag, args.ctl)) return false;
+            const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
+            auto stage_addr = [&](int item) { return ringa + (item % C::NS) * C::STAGE_BYTES; };
+            auto wait_full = [&](int item) -> bool {
+                if (!mbar_wait(&full[item % C::NS], (item / C::NS) & 1, abort_flag, args.ctl)) return false;
                 tc_fence_after();
-                const uint32_t st = ringa + stage * C::STAGE_BYTES;
+                return true;
+            };
+            auto issue_S = [&](int t, int j) {
+                const uint32_t kst = stage_addr(2 * j);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tS0 + (j & 1) * 128, smem_desc_sw128(sQa + koff, 16, 1024),
-                                smem_desc_sw128(st + koff, 16, 1024), idS, kk != 0);
+                    mma_bf16_ss(tmem + t * 128, smem_desc_sw128(sQa + t * C::Q_BYTES + koff, 16, 1024),
+                                smem_desc_sw128(kst + koff, 16, 1024), idS, kk != 0);
                 }
-                mma_commit(&empty[stage]);
-                mma_commit(&s_full[j & 1]);
-                advance();
-                return true;
+                mma_commit(&s_full[t]);
             };
-            auto issue_PV = [&](int t) -> bool {
-                if (!mbar_wait(p_full, t & 1, abort_flag, args.ctl)) return false;
+            auto issue_PV = [&](int t, int j) -> bool {
+                if (!mbar_wait(&p_full[t], j & 1, abort_flag, args.ctl)) return false;
                 tc_fence_after();
-                if (!mbar_wait(&full[stage], phase, abort_flag, args.ctl)) return false;
-                tc_fence_after();
-                const uint32_t st = ringa + stage * C::STAGE_BYTES;
+                const uint32_t vst = stage_addr(2 * j + 1);
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tO, smem_desc_sw128(sPa + poff, 16, 1024),
-                                smem_desc_sw128(st + kk * 2048, 16384, 1024), idO, (t | kk) != 0);
-                }
-                mma_commit(&empty[stage]);
-                mma_commit(o_done);
-                advance();
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                                smem_desc_sw128(vst + kk * 2048, 16384, 1024), idO, (j | kk) != 0);
                 return true;
             };
-            if (ok) ok = issue_S(0);
-            for (int j = 1; j < n_kv && ok; ++j) {
-                ok = issue_S(j);
-                if (ok) ok = issue_PV(j - 1);
+
+            ok = mbar_wait(q_full, 0, abort_flag, args.ctl);
+            tc_fence_after();
+            if (ok) ok = wait_full(0);
+            if (ok) {
+                if (act[0]) issue_S(0, 0);
+                if (act[1]) issue_S(1, 0);
+                mma_commit(&empty[0]);
             }
-            if (ok) ok = issue_PV(n_kv - 1);
+            for (int j = 0; j < nj && ok; ++j) {
+                if (!(ok = wait_full(2 * j + 1))) break;   // V_j
+                bool k_ready = false;
+                if (j < nkv[0]) {
+                    if (!(ok = issue_PV(0, j))) break;
+                    if (j + 1 < nkv[0]) {
+                        if (!(ok = wait_full(2 * j + 2))) break;
+                        k_ready = true;
+                        issue_S(0, j + 1);
+                    }
+                }
+                if (j < nkv[1]) {
+                    if (!(ok = issue_PV(1, j))) break;
+                }
+                mma_commit(&empty[(2 * j + 1) % C::NS]);     // V_j done
+                if (j + 1 < nkv[1]) {
+                    if (!k_ready && !(ok = wait_full(2 * j + 2))) break;
+                    k_ready = true;
+                    issue_S(1, j + 1);
+                }
+                if (k_ready) mma_commit(&empty[(2 * j + 2) % C::NS]);  // K_{j+1} done
+            }
+            // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogue
+            int item = 2 * nj;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (!act[t]) continue;
+                if (GATE == 2) {
+                    constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
+                    for (int kc = 0; kc < nkc; ++kc, ++item) {
+                        if (!(ok = wait_full(item))) break;
+                        const uint32_t st = stage_addr(item);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(tmem + t * 128, smem_desc_sw128(st + kk * 32, 16, 1024),
+                                        smem_desc_sw128(st + C::GX_BYTES + kk * 2048, 8192, 1024), idG,
+                                        (kc | kk) != 0);
+                        mma_commit(&empty[item % C::NS]);
+                    }
+                }
+                if (ok) mma_commit(&g_full[t]);
+            }
             if (!ok) {
                 // Gave up: let every MMA issued so far complete before TMEM is freed.
                 volatile int never = 0;
+                WaitCtl c2 = args.ctl;
+                if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
                 mma_commit(drain);
-                mbar_wait(drain, 0, &never, args.ctl);
+                mbar_wait(drain, 0, &never, c2);
             }
         }
-    } else {
+    } else if (warp >= 4) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ================================================================ softmax + epilogue
+        const int t = (warp - 4) / 4;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-        const int i = q0 + row;
+        const uint32_t tS = tmem + lane_base + t * 128;
+        const uint32_t tO = tmem + lane_base + 256 + t * 128;
+        const int i = q0[t] + row;
         const long a_pos = off + i;
         const float sl2 = kLog2e / sqrtf((float)HD);
         float m = -INFINITY, l = 0.f, x0 = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, args.ctl));
+        for (int j = 0; j < nkv[t]; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, args.ctl));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + (j & 1) * 128 + c * 32, sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&s_free[j & 1]);
 
             const int kv0 = j * kTile;
-            const bool need_mask = (args.causal && (long)kv0 + kTile - 1 > off + q0) || (kv0 + kTile > args.Lk);
-            float tmax = -INFINITY;
+            // last visible column of this row in this key tile (>= 127: no mask)
+            long lim_l = (long)args.Lk - 1 - kv0;
+            if (args.causal && a_pos - kv0 < lim_l) lim_l = a_pos - kv0;
+            const int lim = lim_l > 127 ? 127 : (int)lim_l;
+            float mx[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     float x = __uint_as_float(sr[c][e]) * sl2;
-                    if (need_mask) {
-                        const long key = kv0 + c * 32 + e;
-                        if ((args.causal && key > a_pos) || key >= args.Lk) x = -INFINITY;
-                    }
+                    x = (c * 32 + e > lim) ? -INFINITY : x;
                     sr[c][e] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
+                    mx[e & 7] = fmaxf(mx[e & 7], x);
                 }
             }
+            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             if (j == 0) x0 = __uint_as_float(sr[0][0]);
             const float m_new = fmaxf(m, tmax);
-            bool waited = false;
             if (j == 0) {
                 m = m_new;
             } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, args.ctl));
-                if (!ok) break;
-                tc_fence_after();
-                waited = true;
+                // PV_t(j-1) is complete (S_t(j)'s commit covers it): rescale O_t in place.
                 const float alpha = ex2_approx(m - m_new);
 #pragma unroll
                 for (int cb = 0; cb < HD / 32; ++cb) {
                     uint32_t orr[32];
-                    tmem_ld32(tmem + lane_base + 256 + cb * 32, orr);
+                    tmem_ld32(tO + cb * 32, orr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(tmem + lane_base + 256 + cb * 32, orr);
+                    tmem_st32(tO + cb * 32, orr);
                 }
-                tmem_wait_st();
                 l *= alpha;
                 m = m_new;
             }
-            // P = exp2(x - m), packed to bf16 pairs
-            uint32_t pk[64];
-            float rs = 0.f;
+            // P = exp2(x - m): packed bf16 pairs written over S_t[0, 64) for the PV MMA
+            float rs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rs[e] = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float p0 = ex2_approx(__uint_as_float(sr[c][e]) - m);
                     const float p1 = ex2_approx(__uint_as_float(sr[c][e + 1]) - m);
-                    rs += p0 + p1;
-                    pk[(c * 32 + e) / 2] = pack_bf16x2(p0, p1);
+                    rs[(e >> 1) & 7] += p0 + p1;
+                    pk[e >> 1] = pack_bf16x2(p0, p1);
                 }
+                tmem_st16(tS + c * 16, pk);
             }
-            l += rs;
-            if (j > 0 && !waited) {
-                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, args.ctl));
-                if (!ok) break;
-            }
-            // P row -> shared memory, K-major, 128B swizzle (keys 0..63 box, keys 64..127 box)
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const uint32_t addr = smem_u32(sP) + (ch >> 3) * 16384 + sw128_offset(row, ch & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[ch * 4]),
-                             "r"(pk[ch * 4 + 1]), "r"(pk[ch * 4 + 2]), "r"(pk[ch * 4 + 3])
-                             : "memory");
-            }
-            fence_proxy_async_smem();
+            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[t]);
         }
 
-        if (ok) ok = mbar_wait(o_done, (n_kv - 1) & 1, abort_flag, args.ctl);
-        if (ok && GATE == 2) ok = mbar_wait(g_full, 0, abort_flag, args.ctl);
+        if (ok && nkv[t] > 0) ok = mbar_wait(&g_full[t], 0, abort_flag, args.ctl);
         tc_fence_after();
-        // Every softmax thread takes the same branch (the epilogue has named barriers).
-        ok = named_bar_and(1, 128, ok);
+        // Every thread of this warpgroup takes the same branch (the epilogue has named barriers).
+        ok = named_bar_and(1 + t, 128, ok && nkv[t] > 0);
         if (ok) {
-            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> sQ (swizzled) -> TMA store
+            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> Q_t buffer (swizzled) -> TMA store
+            uint8_t* stage_out = sQ + t * C::Q_BYTES;
             const float inv_l = 1.0f / l;
             float g_head = 1.0f;
             if (GATE == 1) {
@@ -399,9 +419,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int cb = 0; cb < HD / 32; ++cb) {
                 uint32_t orr[32];
-                tmem_ld32(tmem + lane_base + 256 + cb * 32, orr);
+                tmem_ld32(tO + cb * 32, orr);
                 uint32_t grr[32];
-                if (GATE == 2) tmem_ld32(tmem + lane_base + 384 + cb * 32, grr);
+                if (GATE == 2) tmem_ld32(tS + cb * 32, grr);
                 tmem_wait_ld();
                 uint32_t packed[16];
 #pragma unroll
@@ -420,16 +440,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int chunk = (cb & 1) * 4 + q;
-                    const uint32_t addr = smem_u32(sQ) + (cb >> 1) * 16384 + sw128_offset(row, chunk);
+                    const uint32_t addr = smem_u32(stage_out) + (cb >> 1) * 16384 + sw128_offset(row, chunk);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[q * 4]),
                                  "r"(packed[q * 4 + 1]), "r"(packed[q * 4 + 2]), "r"(packed[q * 4 + 3])
                                  : "memory");
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1 + t, 128);
             if (row == 0) {
-                for (int cb = 0; cb < HD / 64; ++cb) tma_store_4d(&tmO, sQ + cb * 16384, cb * 64, h, q0, b);
+                for (int cb = 0; cb < HD / 64; ++cb)
+                    tma_store_4d(&tmO, stage_out + cb * 16384, cb * 64, h, q0[t], b);
                 tma_store_commit();
                 tma_store_wait_read0();
             }
@@ -437,10 +458,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 float p0 = (i < args.Lq) ? ex2_approx(x0 - m) * inv_l : 0.f;
 #pragma unroll
                 for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
-                if (lane == 0) sred[qd] = p0;
-                named_bar_sync(1, 128);
+                if (lane == 0) sred[t * 4 + qd] = p0;
+                named_bar_sync(1 + t, 128);
                 if (row == 0)
-                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + qt] = sred[0] + sred[1] + sred[2] + sred[3];
+                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + 2 * pr + t] =
+                        sred[t * 4] + sred[t * 4 + 1] + sred[t * 4 + 2] + sred[t * 4 + 3];
             }
         }
         tc_fence_before();
@@ -505,6 +527,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.d_model = p.d_model;
     a.causal = p.causal;
     a.n_qtiles = (p.Lq + kTile - 1) / kTile;
+    a.n_pairs = (a.n_qtiles + 1) / 2;
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
@@ -513,12 +536,18 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
 
     static bool attr_done = false;  // per template instance
     if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(prefill_kernel<HD, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM_BYTES);
+        // The register split above only fits if the launch allocates enough
+        // registers per thread; refuse to launch otherwise (it would not finish).
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE>);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
+        r = cudaFuncSetAttribute(prefill_kernel<HD, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::SMEM_BYTES);
         if (r != cudaSuccess) return r;
         attr_done = true;
     }
-    const long units = (long)a.n_qtiles * p.Hq * p.B;
+    const long units = (long)a.n_pairs * p.Hq * p.B;
     prefill_kernel<HD, GATE><<<(unsigned)units, kThreads, C::SMEM_BYTES, s>>>(tmQ, tmK, tmV, tmX, tmW, tmO, a);
     return cudaGetLastError();
 }
