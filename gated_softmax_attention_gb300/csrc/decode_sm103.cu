@@ -57,6 +57,14 @@ struct DecodeArgs {
     WaitCtl ctl;
 };
 
+// bf16 pairs -> float2 pairs (the low half of each 32-bit word is the even element)
+__device__ __forceinline__ void unpack8x2(const uint4& w, float2 (&f)[4]) {
+    f[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+    f[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    f[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+    f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+}
+
 __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
     f[0] = __uint_as_float(w.x << 16);
     f[1] = __uint_as_float(w.x & 0xffff0000u);
@@ -134,7 +142,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
     // q for this lane's 16 dims and the 4 heads, scaled into log2 units
     const float qs = kLog2e / sqrtf((float)HD);
-    float q[HPC][16];
+    float2 q[HPC][8];   // (dims 8j..8j+7, 64+8j..64+8j+7) as float pairs
 #pragma unroll
     for (int h = 0; h < HPC; ++h) {
         const __nv_bfloat16* qp = args.Q + ((long)b * args.Hq + h0 + h) * HD;
@@ -143,17 +151,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         float f[8];
         unpack8(w0, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[h][e] = f[e] * qs;
+        for (int e = 0; e < 4; ++e) q[h][e] = make_float2(f[2 * e] * qs, f[2 * e + 1] * qs);
         unpack8(w1, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[h][8 + e] = f[e] * qs;
+        for (int e = 0; e < 4; ++e) q[h][4 + e] = make_float2(f[2 * e] * qs, f[2 * e + 1] * qs);
     }
 
-    float o[HPC][16];
+    float2 o[HPC][8];
 #pragma unroll
     for (int h = 0; h < HPC; ++h)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
+        for (int e = 0; e < 8; ++e) o[h][e] = make_float2(0.f, 0.f);
     float m_cur[HPC];
 #pragma unroll
     for (int h = 0; h < HPC; ++h) m_cur[h] = -INFINITY;
@@ -177,17 +185,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const int key = grp + 32 * sl;
             const uint4 w0 = *reinterpret_cast<const uint4*>(Kt + key * (HD * 2) + j * 16);
             const uint4 w1 = *reinterpret_cast<const uint4*>(Kt + key * (HD * 2) + 128 + j * 16);
-            float k0[8], k1[8];
-            unpack8(w0, k0);
-            unpack8(w1, k1);
+            float2 k2[8];
+            unpack8x2(w0, *reinterpret_cast<float2(*)[4]>(&k2[0]));
+            unpack8x2(w1, *reinterpret_cast<float2(*)[4]>(&k2[4]));
 #pragma unroll
             for (int h = 0; h < HPC; ++h) {
-                float acc = 0.f;
+                float2 acc = __fmul2_rn(q[h][0], k2[0]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(q[h][e], k0[e], acc);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(q[h][8 + e], k1[e], acc);
-                v[sl * HPC + h] = acc;
+                for (int e = 1; e < 8; ++e) acc = __ffma2_rn(q[h][e], k2[e], acc);
+                v[sl * HPC + h] = acc.x + acc.y;
             }
         }
         // reduce-scatter over the 8 lanes: lane j ends with value index j = slot*4 + head
@@ -224,9 +230,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 m_cur[h] = mn;
             }
 #pragma unroll
-            for (int h = 0; h < HPC; ++h)
+            for (int h = 0; h < HPC; ++h) {
+                const float2 a2 = make_float2(alpha[h], alpha[h]);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) o[h][e] *= alpha[h];
+                for (int e = 0; e < 8; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
+            }
             l_lane *= alpha[my_head];
         }
         const float p = (s == -INFINITY) ? 0.f : ex2_approx(s - m_cur[my_head]);
@@ -241,16 +249,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const int key = grp + 32 * sl;
             const uint4 w0 = *reinterpret_cast<const uint4*>(Vt + key * (HD * 2) + j * 16);
             const uint4 w1 = *reinterpret_cast<const uint4*>(Vt + key * (HD * 2) + 128 + j * 16);
-            float v0[8], v1[8];
-            unpack8(w0, v0);
-            unpack8(w1, v1);
+            float2 v2[8];
+            unpack8x2(w0, *reinterpret_cast<float2(*)[4]>(&v2[0]));
+            unpack8x2(w1, *reinterpret_cast<float2(*)[4]>(&v2[4]));
 #pragma unroll
             for (int h = 0; h < HPC; ++h) {
-                const float ph = pp[sl * HPC + h];
+                const float2 ph = make_float2(pp[sl * HPC + h], pp[sl * HPC + h]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, v0[e], o[h][e]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][8 + e] = fmaf(ph, v1[e], o[h][8 + e]);
+                for (int e = 0; e < 8; ++e) o[h][e] = __ffma2_rn(ph, v2[e], o[h][e]);
             }
         }
         __syncwarp();
@@ -284,9 +290,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 #pragma unroll
     for (int h = 0; h < HPC; ++h) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            red_o[(grp * HPC + h) * HD + 8 * j + e] = o[h][e];
-            red_o[(grp * HPC + h) * HD + 64 + 8 * j + e] = o[h][8 + e];
+        for (int e = 0; e < 4; ++e) {
+            red_o[(grp * HPC + h) * HD + 8 * j + 2 * e] = o[h][e].x;
+            red_o[(grp * HPC + h) * HD + 8 * j + 2 * e + 1] = o[h][e].y;
+            red_o[(grp * HPC + h) * HD + 64 + 8 * j + 2 * e] = o[h][4 + e].x;
+            red_o[(grp * HPC + h) * HD + 64 + 8 * j + 2 * e + 1] = o[h][4 + e].y;
         }
     }
     if (j < HPC) red_m[grp * HPC + j] = m_cur[j];

@@ -59,13 +59,17 @@ struct PrefillCfg {
     static constexpr uint32_t KV_BYTES = kTile * HD * 2;
     static constexpr uint32_t GX_BYTES = kTile * 64 * 2;
     static constexpr uint32_t GW_BYTES = 64 * HD * 2;
-    static constexpr uint32_t STAGE_BYTES =
-        (GATE == 2 && GX_BYTES + GW_BYTES > KV_BYTES) ? GX_BYTES + GW_BYTES : KV_BYTES;
-    static constexpr int NS = (HD == 128) ? 4 : 6;
+    static constexpr uint32_t STAGE_BYTES = KV_BYTES;
+    static constexpr int NS = (HD == 128) ? 4 : 8;
     static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
     static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
-    static constexpr int NBAR = 2 * NS + 8;
+    // Gate phase (after every attention MMA has completed): the Q tiles and the
+    // K/V ring are reused as a ring of GNS stages, each X_0 | X_1 | W_g chunk.
+    static constexpr uint32_t GSTAGE_BYTES = 2 * GX_BYTES + GW_BYTES;
+    static constexpr int GNS = (int)(OFF_BAR / GSTAGE_BYTES) < 4 ? (int)(OFF_BAR / GSTAGE_BYTES) : 4;
+    static_assert(GNS >= 2, "gate ring needs two stages");
+    static constexpr int NBAR = 2 * NS + 2 * 4 + 9;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -78,8 +82,12 @@ struct PrefillArgs {
     WaitCtl ctl;
 };
 
+// sigma(x) = 1/2 + tanh(x/2)/2: one MUFU operation (tanh.approx, relative
+// error about 2^-11, i.e. at most ~2.5e-4 absolute on the gate value).
 __device__ __forceinline__ float sigmoidf_fast(float x) {
-    return 1.0f / (1.0f + ex2_approx(-x * kLog2e));
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
 }
 
 template <int HD, int GATE>
@@ -101,6 +109,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint64_t* p_full = q_full + 3;         // [2]
     uint64_t* g_full = q_full + 5;         // [2]: all MMAs of the tile (and its gate GEMM) done
     uint64_t* drain = q_full + 7;
+    uint64_t* attn_done = q_full + 8;      // every attention MMA has completed
+    uint64_t* gfull = q_full + 9;          // [4] gate ring
+    uint64_t* gempty = q_full + 13;        // [4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
@@ -145,6 +156,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(&g_full[t], 1);
         }
         mbar_init(drain, 1);
+        mbar_init(attn_done, 1);
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&gfull[s], 1);
+            mbar_init(&gempty[s], 1);
+        }
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -197,18 +213,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     ++item;
                 }
             }
-            if (GATE == 2) {
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!act[t]) continue;
-                    for (int kc = 0; kc < nkc; ++kc) {
-                        uint8_t* st = acquire(C::GX_BYTES + C::GW_BYTES);
-                        if (!st) { ok = false; break; }
-                        tma_load_3d(st, &tmX, kc * 64, q0[t], b, &full[item % C::NS]);
-                        for (int cb = 0; cb < HD / 64; ++cb)
-                            tma_load_2d(st + C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64,
-                                        &full[item % C::NS]);
-                        ++item;
-                    }
+            uint32_t garmed = 0, garmed_phase = 0;
+            if (GATE == 2 && ok) {
+                // The gate ring overlays Q and the K/V ring: start once they are idle.
+                ok = mbar_wait(attn_done, 0, abort_flag, args.ctl);
+                for (int kc = 0; kc < nkc && ok; ++kc) {
+                    const int gs = kc % C::GNS;
+                    const uint32_t ph = (kc / C::GNS) & 1;
+                    if (!(ok = mbar_wait(&gempty[gs], ph ^ 1u, abort_flag, args.ctl))) break;
+                    mbar_arrive_expect_tx(&gfull[gs], (act[1] ? 2 : 1) * C::GX_BYTES + C::GW_BYTES);
+                    garmed |= 1u << gs;
+                    garmed_phase = (garmed_phase & ~(1u << gs)) | (ph << gs);
+                    uint8_t* st = smem + gs * C::GSTAGE_BYTES;
+                    for (int t = 0; t < 2; ++t)
+                        if (act[t]) tma_load_3d(st + t * C::GX_BYTES, &tmX, kc * 64, q0[t], b, &gfull[gs]);
+                    for (int cb = 0; cb < HD / 64; ++cb)
+                        tma_load_2d(st + 2 * C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64, &gfull[gs]);
                 }
             }
             if (!ok) {
@@ -219,6 +239,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mbar_wait(q_full, 0, &never, c2);
                 for (int s = 0; s < C::NS; ++s)
                     if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, c2);
+                for (int s = 0; s < 4; ++s)
+                    if (garmed & (1u << s)) mbar_wait(&gfull[s], (garmed_phase >> s) & 1u, &never, c2);
             }
         }
     } else if (warp == 1) {
@@ -286,23 +308,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (k_ready) mma_commit(&empty[(2 * j + 2) % C::NS]);  // K_{j+1} done
             }
             // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogue
-            int item = 2 * nj;
-            for (int t = 0; t < 2 && ok; ++t) {
-                if (!act[t]) continue;
-                if (GATE == 2) {
-                    constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
-                    for (int kc = 0; kc < nkc; ++kc, ++item) {
-                        if (!(ok = wait_full(item))) break;
-                        const uint32_t st = stage_addr(item);
+            if (ok) mma_commit(attn_done);
+            if (GATE == 2) {
+                constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
+                const uint32_t base = smem_u32(smem);
+                for (int kc = 0; kc < nkc && ok; ++kc) {
+                    const int gs = kc % C::GNS;
+                    if (!(ok = mbar_wait(&gfull[gs], (kc / C::GNS) & 1, abort_flag, args.ctl))) break;
+                    tc_fence_after();
+                    const uint32_t st = base + gs * C::GSTAGE_BYTES;
+                    for (int t = 0; t < 2; ++t) {
+                        if (!act[t]) continue;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(tmem + t * 128, smem_desc_sw128(st + kk * 32, 16, 1024),
-                                        smem_desc_sw128(st + C::GX_BYTES + kk * 2048, 8192, 1024), idG,
+                            mma_bf16_ss(tmem + t * 128, smem_desc_sw128(st + t * C::GX_BYTES + kk * 32, 16, 1024),
+                                        smem_desc_sw128(st + 2 * C::GX_BYTES + kk * 2048, 8192, 1024), idG,
                                         (kc | kk) != 0);
-                        mma_commit(&empty[item % C::NS]);
                     }
+                    mma_commit(&gempty[gs]);
                 }
-                if (ok) mma_commit(&g_full[t]);
+            }
+            if (ok) {
+                mma_commit(&g_full[0]);
+                mma_commit(&g_full[1]);
             }
             if (!ok) {
                 // Gave up: let every MMA issued so far complete before TMEM is freed.
