@@ -129,12 +129,12 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                 if (!(ok = mbar_wait(&full[stage], phase, abort_flag, args.ctl))) break;
                 tc_fence_after();
                 const uint32_t st = base + stage * C::STAGE;
+                constexpr uint32_t HI = desc_sw128_hi(1024);
+                const uint32_t x0 = desc_sw128_lo(st, 16), w0 = desc_sw128_lo(st + C::X_BYTES, 8192);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(st + C::X_BYTES + kk * 2048, 8192, 1024);
-                    mma_bf16_ss(tmem, ad, bd, idG, (kc != kc0 || kk != 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_lohi(tmem, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
+                                (kc != kc0 || kk != 0) ? 1u : 0u);
                 mma_commit(&empty[stage]);
                 if (++stage == NS) {
                     stage = 0;

@@ -256,24 +256,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tc_fence_after();
                 return true;
             };
+            constexpr uint32_t HI = desc_sw128_hi(1024);   // every operand: 8-row groups 1024 B apart
             auto issue_S = [&](int t, int j) {
-                const uint32_t kst = stage_addr(2 * j);
+                const uint32_t a0 = desc_sw128_lo(sQa + t * C::Q_BYTES, 16);
+                const uint32_t b0 = desc_sw128_lo(stage_addr(2 * j), 16);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + t * 128, smem_desc_sw128(sQa + t * C::Q_BYTES + koff, 16, 1024),
-                                smem_desc_sw128(kst + koff, 16, 1024), idS, kk != 0);
+                    const uint32_t k16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss_lohi(tmem + t * 128, a0 + k16, HI, b0 + k16, HI, idS, kk != 0);
                 }
                 mma_commit(&s_full[t]);
             };
             auto issue_PV = [&](int t, int j) -> bool {
                 if (!mbar_wait(&p_full[t], j & 1, abort_flag, args.ctl)) return false;
                 tc_fence_after();
-                const uint32_t vst = stage_addr(2 * j + 1);
+                const uint32_t v0 = desc_sw128_lo(stage_addr(2 * j + 1), 16384);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                                smem_desc_sw128(vst + kk * 2048, 16384, 1024), idO, (j | kk) != 0);
+                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
+                                (j | kk) != 0);
                 return true;
             };
 
@@ -317,12 +318,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (!(ok = mbar_wait(&gfull[gs], (kc / C::GNS) & 1, abort_flag, args.ctl))) break;
                     tc_fence_after();
                     const uint32_t st = base + gs * C::GSTAGE_BYTES;
+                    const uint32_t w0 = desc_sw128_lo(st + 2 * C::GX_BYTES, 8192);
                     for (int t = 0; t < 2; ++t) {
                         if (!act[t]) continue;
+                        const uint32_t x0 = desc_sw128_lo(st + t * C::GX_BYTES, 16);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(tmem + t * 128, smem_desc_sw128(st + t * C::GX_BYTES + kk * 32, 16, 1024),
-                                        smem_desc_sw128(st + 2 * C::GX_BYTES + kk * 2048, 8192, 1024), idG,
+                            mma_ss_lohi(tmem + t * 128, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
                                         (kc | kk) != 0);
                     }
                     mma_commit(&gempty[gs]);
@@ -370,22 +372,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             long lim_l = (long)args.Lk - 1 - kv0;
             if (args.causal && a_pos - kv0 < lim_l) lim_l = a_pos - kv0;
             const int lim = lim_l > 127 ? 127 : (int)lim_l;
+            // raw scores; masked ones become -inf (the 1/sqrt(d_k)*log2(e) scale is
+            // folded into the exp2 argument below, max commutes with it)
+            if (lim < 127) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+            }
             float mx[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+            for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[0][e + 8]));
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int k = 16; k < 128; k += 16) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(sr[c][e]) * sl2;
-                    x = (c * 32 + e > lim) ? -INFINITY : x;
-                    sr[c][e] = __float_as_uint(x);
-                    mx[e & 7] = fmaxf(mx[e & 7], x);
-                }
+                for (int e = 0; e < 8; ++e)
+                    mx[e] = fmax3(mx[e], __uint_as_float(sr[k >> 5][(k & 31) + e]),
+                                  __uint_as_float(sr[(k + 8) >> 5][((k + 8) & 31) + e]));
             }
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (j == 0) x0 = __uint_as_float(sr[0][0]);
+            const float tmax = sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            if (j == 0) x0 = __uint_as_float(sr[0][0]) * sl2;
             const float m_new = fmaxf(m, tmax);
             if (j == 0) {
                 m = m_new;
@@ -404,23 +411,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 l *= alpha;
                 m = m_new;
             }
-            // P = exp2(x - m): packed bf16 pairs written over S_t[0, 64) for the PV MMA
-            float rs[8];
+            // P = exp2(s * scale - m): packed bf16 pairs written over S_t[0, 64) for the PV MMA
+            const float neg_m = -m;
+            float2 rs[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) rs[e] = 0.f;
+            for (int e = 0; e < 4; ++e) rs[e] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(__uint_as_float(sr[c][e]) - m);
-                    const float p1 = ex2_approx(__uint_as_float(sr[c][e + 1]) - m);
-                    rs[(e >> 1) & 7] += p0 + p1;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
+                    rs[(e >> 1) & 3] = __fadd2_rn(rs[(e >> 1) & 3], make_float2(p0, p1));
                     pk[e >> 1] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tS + c * 16, pk);
             }
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            l += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_full[t]);
