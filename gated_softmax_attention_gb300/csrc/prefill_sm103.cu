@@ -15,7 +15,8 @@
 //   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ... and
 //                the gate chunks (X_t [128 x 64], W_g [64 x d_k]) through a
 //                ring of NS shared-memory stages;
-//   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma / commit;
+//   warp 1       TMEM allocation; issues every tcgen05.mma / commit (the
+//                whole warp runs the loop, one elected lane issues);
 //   warps 2, 3   spare;
 //   warps 4..7   softmax + epilogue of query tile 0 (one thread per row);
 //   warps 8..11  softmax + epilogue of query tile 1.
@@ -49,8 +50,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 // Register split: warpgroup 0 (producer, MMA, spare) gives registers to the
 // two softmax warpgroups. The launch must provide 384 x kRegsLaunchMin.
-constexpr int kRegsLow = 40;
-constexpr int kRegsHigh = 216;
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 208;
 constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 
 template <int HD, int GATE>
@@ -245,14 +246,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
+        {   // the whole warp runs the issue loop (warp-uniform operands); one elected lane issues
             bool ok = true;
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(128, HD, false, true);
             const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
             auto stage_addr = [&](int item) { return ringa + (item % C::NS) * C::STAGE_BYTES; };
             auto wait_full = [&](int item) -> bool {
-                if (!mbar_wait(&full[item % C::NS], (item / C::NS) & 1, abort_flag, args.ctl)) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[item % C::NS], (item / C::NS) & 1, abort_flag, args.ctl)))
+                    return false;
                 tc_fence_after();
                 return true;
             };
@@ -263,28 +265,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t k16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss_lohi(tmem + t * 128, a0 + k16, HI, b0 + k16, HI, idS, kk != 0);
+                    mma_ss_elect(tmem + t * 128, a0 + k16, HI, b0 + k16, HI, idS, kk != 0);
                 }
-                mma_commit(&s_full[t]);
+                mma_commit_elect(&s_full[t]);
             };
             auto issue_PV = [&](int t, int j) -> bool {
-                if (!mbar_wait(&p_full[t], j & 1, abort_flag, args.ctl)) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1, abort_flag, args.ctl))) return false;
                 tc_fence_after();
                 const uint32_t v0 = desc_sw128_lo(stage_addr(2 * j + 1), 16384);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
+                    mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
                                 (j | kk) != 0);
                 return true;
             };
 
-            ok = mbar_wait(q_full, 0, abort_flag, args.ctl);
+            ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, args.ctl));
             tc_fence_after();
             if (ok) ok = wait_full(0);
             if (ok) {
                 if (act[0]) issue_S(0, 0);
                 if (act[1]) issue_S(1, 0);
-                mma_commit(&empty[0]);
+                mma_commit_elect(&empty[0]);
             }
             for (int j = 0; j < nj && ok; ++j) {
                 if (!(ok = wait_full(2 * j + 1))) break;   // V_j
@@ -300,22 +302,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (j < nkv[1]) {
                     if (!(ok = issue_PV(1, j))) break;
                 }
-                mma_commit(&empty[(2 * j + 1) % C::NS]);     // V_j done
+                mma_commit_elect(&empty[(2 * j + 1) % C::NS]);     // V_j done
                 if (j + 1 < nkv[1]) {
                     if (!k_ready && !(ok = wait_full(2 * j + 2))) break;
                     k_ready = true;
                     issue_S(1, j + 1);
                 }
-                if (k_ready) mma_commit(&empty[(2 * j + 2) % C::NS]);  // K_{j+1} done
+                if (k_ready) mma_commit_elect(&empty[(2 * j + 2) % C::NS]);  // K_{j+1} done
             }
             // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogue
-            if (ok) mma_commit(attn_done);
+            if (ok) mma_commit_elect(attn_done);
             if (GATE == 2) {
                 constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
                 const uint32_t base = smem_u32(smem);
                 for (int kc = 0; kc < nkc && ok; ++kc) {
                     const int gs = kc % C::GNS;
-                    if (!(ok = mbar_wait(&gfull[gs], (kc / C::GNS) & 1, abort_flag, args.ctl))) break;
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&gfull[gs], (kc / C::GNS) & 1, abort_flag, args.ctl))))
+                        break;
                     tc_fence_after();
                     const uint32_t st = base + gs * C::GSTAGE_BYTES;
                     const uint32_t w0 = desc_sw128_lo(st + 2 * C::GX_BYTES, 8192);
@@ -324,23 +327,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         const uint32_t x0 = desc_sw128_lo(st + t * C::GX_BYTES, 16);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss_lohi(tmem + t * 128, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
+                            mma_ss_elect(tmem + t * 128, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
                                         (kc | kk) != 0);
                     }
-                    mma_commit(&gempty[gs]);
+                    mma_commit_elect(&gempty[gs]);
                 }
             }
             if (ok) {
-                mma_commit(&g_full[0]);
-                mma_commit(&g_full[1]);
+                mma_commit_elect(&g_full[0]);
+                mma_commit_elect(&g_full[1]);
             }
             if (!ok) {
                 // Gave up: let every MMA issued so far complete before TMEM is freed.
                 volatile int never = 0;
                 WaitCtl c2 = args.ctl;
                 if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
-                mma_commit(drain);
+                mma_commit_elect(drain);
                 mbar_wait(drain, 0, &never, c2);
+                __syncwarp();
             }
         }
     } else if (warp >= 4) {
