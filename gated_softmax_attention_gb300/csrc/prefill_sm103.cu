@@ -34,8 +34,9 @@
 //
 // The causal mask is aligned bottom-right (query i at absolute position
 // L_k - L_q + i); key tiles entirely above the diagonal are never loaded.
-// Units are numbered heaviest first so the block scheduler starts the long
-// causal units early.
+// The grid is persistent (one CTA per SM): units, numbered heaviest first,
+// are dealt to the CTAs in snake order so that heavy and light causal units
+// share an SM; barrier phases carry over from one unit to the next.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -50,8 +51,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 // Register split: warpgroup 0 (producer, MMA, spare) gives registers to the
 // two softmax warpgroups. The launch must provide 384 x kRegsLaunchMin.
-constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 208;
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
 constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 
 template <int HD, int GATE>
@@ -70,7 +71,7 @@ struct PrefillCfg {
     static constexpr uint32_t GSTAGE_BYTES = 2 * GX_BYTES + GW_BYTES;
     static constexpr int GNS = (int)(OFF_BAR / GSTAGE_BYTES) < 4 ? (int)(OFF_BAR / GSTAGE_BYTES) : 4;
     static_assert(GNS >= 2, "gate ring needs two stages");
-    static constexpr int NBAR = 2 * NS + 2 * 4 + 9;
+    static constexpr int NBAR = 2 * NS + 2 * 4 + 10;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -80,6 +81,7 @@ struct PrefillArgs {
     const float* gate_part;  // headwise: [splits, B*Lq, Hq]
     int gate_splits;
     float* sink_part;        // [B, Hq, n_qtiles] or null
+    __nv_bfloat16* O;        // [B, Lq, Hq, HD]
     WaitCtl ctl;
 };
 
@@ -113,6 +115,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint64_t* attn_done = q_full + 8;      // every attention MMA has completed
     uint64_t* gfull = q_full + 9;          // [4] gate ring
     uint64_t* gempty = q_full + 13;        // [4]
+    uint64_t* tmem_free = q_full + 17;     // both epilogues have read O and G out of TMEM
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
@@ -120,30 +123,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // ---- unit (heaviest first when causal)
+    // ---- persistent schedule: the units, numbered heaviest first (last query
+    // pair first when causal), are dealt to the CTAs in snake order -- CTA c
+    // takes units c, 2G-1-c, 2G+c, 4G-1-c, ... -- so that heavy and light
+    // units share an SM.
     const int per_pair = args.Hq * args.B;
-    const int u = blockIdx.x;
-    const int pr = args.causal ? (args.n_pairs - 1 - u / per_pair) : (u / per_pair);
-    const int rem = u % per_pair;
-    const int h = rem % args.Hq;
-    const int b = rem / args.Hq;
-    const int kvh = h / (args.Hq / args.Hkv);
+    const int n_units = args.n_pairs * per_pair;
     const long off = (long)args.Lk - args.Lq;
-    int q0[2], nkv[2];
-    bool act[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        q0[t] = (2 * pr + t) * kTile;
-        act[t] = q0[t] < args.Lq;
-        long kend = args.Lk;
-        if (args.causal) {
-            const long last = off + q0[t] + kTile;  // keys 0 .. off+q0+127 can be visible
-            kend = last < kend ? last : kend;
-        }
-        nkv[t] = act[t] ? (int)((kend + kTile - 1) / kTile) : 0;
-    }
-    const int nj = nkv[0] > nkv[1] ? nkv[0] : nkv[1];
     const int nkc = (args.d_model + 63) / 64;
+    struct Unit {
+        int pr, h, b, kvh, nj;
+        int q0[2], nkv[2];
+        bool act[2];
+    };
+    auto unit_index = [&](int r) -> int {
+        const int G = gridDim.x, c = blockIdx.x;
+        return (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
+    };
+    auto decode_unit = [&](int u) -> Unit {
+        Unit x;
+        x.pr = args.causal ? (args.n_pairs - 1 - u / per_pair) : (u / per_pair);
+        const int rem = u % per_pair;
+        x.h = rem % args.Hq;
+        x.b = rem / args.Hq;
+        x.kvh = x.h / (args.Hq / args.Hkv);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            x.q0[t] = (2 * x.pr + t) * kTile;
+            x.act[t] = x.q0[t] < args.Lq;
+            long kend = args.Lk;
+            if (args.causal) {
+                const long last = off + x.q0[t] + kTile;  // keys 0 .. off+q0+127 can be visible
+                kend = last < kend ? last : kend;
+            }
+            x.nkv[t] = x.act[t] ? (int)((kend + kTile - 1) / kTile) : 0;
+        }
+        x.nj = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
+        return x;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
@@ -158,6 +175,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         mbar_init(drain, 1);
         mbar_init(attn_done, 1);
+        mbar_init(tmem_free, 2);
         for (int s = 0; s < 4; ++s) {
             mbar_init(&gfull[s], 1);
             mbar_init(&gempty[s], 1);
@@ -186,15 +204,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            uint32_t armed = 0, armed_phase = 0;
+            uint32_t armed = 0, armed_phase = 0, garmed = 0, garmed_phase = 0;
             bool ok = true;
+            int item = 0, gitem = 0;   // running counts of ring items / gate chunks (phases carry over units)
+            for (int r = 0; ok; ++r) {
+            const int uix = unit_index(r);
+            if (uix >= n_units) break;
+            const Unit U = decode_unit(uix);
+            const int h = U.h, b = U.b, kvh = U.kvh, nj = U.nj;
+            const int* q0 = U.q0;
+            const bool* act = U.act;
+            // every MMA of the previous unit must be complete (its gate ring overlays Q and K/V);
+            // its g_full[1] commit is the last of the unit and covers all of them
+            if (r > 0 && !(ok = mbar_wait(&g_full[1], (r - 1) & 1, abort_flag, args.ctl))) break;
             mbar_arrive_expect_tx(q_full, (act[1] ? 2 : 1) * C::Q_BYTES);
             for (int t = 0; t < 2; ++t)
                 if (act[t])
                     for (int cb = 0; cb < HD / 64; ++cb)
                         tma_load_4d(sQ + t * C::Q_BYTES + cb * 16384, &tmQ, cb * 64, h, q0[t], b, q_full);
 
-            int item = 0;
             auto acquire = [&](uint32_t bytes) -> uint8_t* {
                 const int s = item % C::NS;
                 const uint32_t ph = (item / C::NS) & 1;
@@ -214,13 +242,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     ++item;
                 }
             }
-            uint32_t garmed = 0, garmed_phase = 0;
             if (GATE == 2 && ok) {
                 // The gate ring overlays Q and the K/V ring: start once they are idle.
-                ok = mbar_wait(attn_done, 0, abort_flag, args.ctl);
-                for (int kc = 0; kc < nkc && ok; ++kc) {
-                    const int gs = kc % C::GNS;
-                    const uint32_t ph = (kc / C::GNS) & 1;
+                ok = mbar_wait(attn_done, r & 1, abort_flag, args.ctl);
+                for (int kc = 0; kc < nkc && ok; ++kc, ++gitem) {
+                    const int gs = gitem % C::GNS;
+                    const uint32_t ph = (gitem / C::GNS) & 1;
                     if (!(ok = mbar_wait(&gempty[gs], ph ^ 1u, abort_flag, args.ctl))) break;
                     mbar_arrive_expect_tx(&gfull[gs], (act[1] ? 2 : 1) * C::GX_BYTES + C::GW_BYTES);
                     garmed |= 1u << gs;
@@ -232,12 +259,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         tma_load_2d(st + 2 * C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64, &gfull[gs]);
                 }
             }
+            }   // units
             if (!ok) {
                 // Let every copy already issued land before the CTA can exit.
                 volatile int never = 0;
                 WaitCtl c2 = args.ctl;
                 if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
-                mbar_wait(q_full, 0, &never, c2);
                 for (int s = 0; s < C::NS; ++s)
                     if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, c2);
                 for (int s = 0; s < 4; ++s)
@@ -251,9 +278,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(128, HD, false, true);
             const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
-            auto stage_addr = [&](int item) { return ringa + (item % C::NS) * C::STAGE_BYTES; };
+            int ibase = 0, gbase = 0;      // running ring-item / gate-chunk counts
+            int sp_base[2] = {0, 0};       // completed s_full / p_full phases per tile
+            auto stage_addr = [&](int item) { return ringa + ((ibase + item) % C::NS) * C::STAGE_BYTES; };
             auto wait_full = [&](int item) -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[item % C::NS], (item / C::NS) & 1, abort_flag, args.ctl)))
+                const int it = ibase + item;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[it % C::NS], (it / C::NS) & 1, abort_flag, args.ctl)))
                     return false;
                 tc_fence_after();
                 return true;
@@ -270,7 +300,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mma_commit_elect(&s_full[t]);
             };
             auto issue_PV = [&](int t, int j) -> bool {
-                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1, abort_flag, args.ctl))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[t], (sp_base[t] + j) & 1, abort_flag, args.ctl)))
+                    return false;
                 tc_fence_after();
                 const uint32_t v0 = desc_sw128_lo(stage_addr(2 * j + 1), 16384);
 #pragma unroll
@@ -280,13 +311,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 return true;
             };
 
-            ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, args.ctl));
+            for (int r = 0; ok; ++r) {
+            const int uix = unit_index(r);
+            if (uix >= n_units) break;
+            const Unit U = decode_unit(uix);
+            const int nj = U.nj;
+            const int* nkv = U.nkv;
+            const bool* act = U.act;
+            ok = __all_sync(0xffffffffu, mbar_wait(q_full, r & 1, abort_flag, args.ctl));
+            // S_t and O_t of the previous unit (G_t, O_t) must have been read by its epilogue
+            if (ok && r > 0) ok = __all_sync(0xffffffffu, mbar_wait(tmem_free, (r - 1) & 1, abort_flag, args.ctl));
             tc_fence_after();
             if (ok) ok = wait_full(0);
             if (ok) {
                 if (act[0]) issue_S(0, 0);
                 if (act[1]) issue_S(1, 0);
-                mma_commit_elect(&empty[0]);
+                mma_commit_elect(&empty[ibase % C::NS]);
             }
             for (int j = 0; j < nj && ok; ++j) {
                 if (!(ok = wait_full(2 * j + 1))) break;   // V_j
@@ -302,13 +342,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (j < nkv[1]) {
                     if (!(ok = issue_PV(1, j))) break;
                 }
-                mma_commit_elect(&empty[(2 * j + 1) % C::NS]);     // V_j done
+                mma_commit_elect(&empty[(ibase + 2 * j + 1) % C::NS]);     // V_j done
                 if (j + 1 < nkv[1]) {
                     if (!k_ready && !(ok = wait_full(2 * j + 2))) break;
                     k_ready = true;
                     issue_S(1, j + 1);
                 }
-                if (k_ready) mma_commit_elect(&empty[(2 * j + 2) % C::NS]);  // K_{j+1} done
+                if (k_ready) mma_commit_elect(&empty[(ibase + 2 * j + 2) % C::NS]);  // K_{j+1} done
             }
             // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogue
             if (ok) mma_commit_elect(attn_done);
@@ -316,8 +356,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
                 const uint32_t base = smem_u32(smem);
                 for (int kc = 0; kc < nkc && ok; ++kc) {
-                    const int gs = kc % C::GNS;
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&gfull[gs], (kc / C::GNS) & 1, abort_flag, args.ctl))))
+                    const int gi = gbase + kc;
+                    const int gs = gi % C::GNS;
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&gfull[gs], (gi / C::GNS) & 1, abort_flag, args.ctl))))
                         break;
                     tc_fence_after();
                     const uint32_t st = base + gs * C::GSTAGE_BYTES;
@@ -337,6 +378,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mma_commit_elect(&g_full[0]);
                 mma_commit_elect(&g_full[1]);
             }
+            ibase += 2 * nj;
+            if (GATE == 2) gbase += nkc;
+            sp_base[0] += nkv[0];
+            sp_base[1] += nkv[1];
+            }   // units
             if (!ok) {
                 // Gave up: let every MMA issued so far complete before TMEM is freed.
                 volatile int never = 0;
@@ -356,14 +402,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * 128;
         const uint32_t tO = tmem + lane_base + 256 + t * 128;
+        const float sl2 = kLog2e / sqrtf((float)HD);
+        bool ok = true;
+        int sp_base = 0;     // completed s_full / p_full phases of this tile
+        int g_base = 0;      // completed g_full phases of this tile
+        for (int r = 0; ok; ++r) {
+        const int uix = unit_index(r);
+        if (uix >= n_units) break;
+        const Unit U = decode_unit(uix);
+        const int pr = U.pr, h = U.h, b = U.b;
+        const int* q0 = U.q0;
+        const int* nkv = U.nkv;
         const int i = q0[t] + row;
         const long a_pos = off + i;
-        const float sl2 = kLog2e / sqrtf((float)HD);
         float m = -INFINITY, l = 0.f, x0 = 0.f;
-        bool ok = true;
 
         for (int j = 0; j < nkv[t]; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, args.ctl));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], (sp_base + j) & 1, abort_flag, args.ctl));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
@@ -438,13 +493,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_arrive(&p_full[t]);
         }
 
-        if (ok && nkv[t] > 0) ok = mbar_wait(&g_full[t], 0, abort_flag, args.ctl);
+        if (ok && nkv[t] > 0) ok = mbar_wait(&g_full[t], g_base & 1, abort_flag, args.ctl);
         tc_fence_after();
         // Every thread of this warpgroup takes the same branch (the epilogue has named barriers).
-        ok = named_bar_and(1 + t, 128, ok && nkv[t] > 0);
-        if (ok) {
-            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> Q_t buffer (swizzled) -> TMA store
-            uint8_t* stage_out = sQ + t * C::Q_BYTES;
+        const bool ok_epi = named_bar_and(1 + t, 128, ok && nkv[t] > 0);
+        ok = named_bar_and(1 + t, 128, ok);
+        if (ok_epi) {
+            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> global (one 2*d_k-byte row per thread)
             const float inv_l = 1.0f / l;
             float g_head = 1.0f;
             if (GATE == 1) {
@@ -456,6 +511,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 g_head = sigmoidf_fast(gl);
             }
+            uint32_t packed[HD / 2];
 #pragma unroll
             for (int cb = 0; cb < HD / 32; ++cb) {
                 uint32_t orr[32];
@@ -463,7 +519,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 uint32_t grr[32];
                 if (GATE == 2) tmem_ld32(tS + cb * 32, grr);
                 tmem_wait_ld();
-                uint32_t packed[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float v0 = __uint_as_float(orr[e]) * inv_l;
@@ -475,24 +530,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         v0 *= g_head;
                         v1 *= g_head;
                     }
-                    packed[e / 2] = pack_bf16x2(v0, v1);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = (cb & 1) * 4 + q;
-                    const uint32_t addr = smem_u32(stage_out) + (cb >> 1) * 16384 + sw128_offset(row, chunk);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[q * 4]),
-                                 "r"(packed[q * 4 + 1]), "r"(packed[q * 4 + 2]), "r"(packed[q * 4 + 3])
-                                 : "memory");
+                    packed[cb * 16 + e / 2] = pack_bf16x2(v0, v1);
                 }
             }
-            fence_proxy_async_smem();
+            // TMEM is no longer needed by this tile: the next unit's MMAs may start
+            tc_fence_before();
             named_bar_sync(1 + t, 128);
-            if (row == 0) {
-                for (int cb = 0; cb < HD / 64; ++cb)
-                    tma_store_4d(&tmO, stage_out + cb * 16384, cb * 64, h, q0[t], b);
-                tma_store_commit();
-                tma_store_wait_read0();
+            if (row == 0) mbar_arrive(tmem_free);
+            if (i < args.Lq) {
+                uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * HD);
+#pragma unroll
+                for (int q = 0; q < HD / 8; ++q)
+                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
             }
             if (args.sink_part) {
                 float p0 = (i < args.Lq) ? ex2_approx(x0 - m) * inv_l : 0.f;
@@ -505,6 +554,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         sred[t * 4] + sred[t * 4 + 1] + sred[t * 4 + 2] + sred[t * 4 + 3];
             }
         }
+        if (!ok_epi) {   // no epilogue for this tile in this unit: nothing to read from TMEM
+            named_bar_sync(1 + t, 128);
+            if (row == 0) mbar_arrive(tmem_free);
+        }
+        sp_base += nkv[t];
+        g_base += 1;
+        }   // units
         tc_fence_before();
     }
 
@@ -571,6 +627,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
+    a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 
@@ -588,7 +645,8 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
         attr_done = true;
     }
     const long units = (long)a.n_pairs * p.Hq * p.B;
-    prefill_kernel<HD, GATE><<<(unsigned)units, kThreads, C::SMEM_BYTES, s>>>(tmQ, tmK, tmV, tmX, tmW, tmO, a);
+    const long grid = units < rt.num_sms ? units : rt.num_sms;   // persistent: one CTA per SM
+    prefill_kernel<HD, GATE><<<(unsigned)grid, kThreads, C::SMEM_BYTES, s>>>(tmQ, tmK, tmV, tmX, tmW, tmO, a);
     return cudaGetLastError();
 }
 
