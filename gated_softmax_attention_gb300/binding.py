@@ -29,6 +29,8 @@ SIGNATURES = {
     "gsdpa_check_device_error": (_I, [_VP]),
     "gsdpa_status_string": (ctypes.c_char_p, [_I]),
     "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+    "gated_sdpa_decode_noalloc": (_I, [_VP] * 7 + [_I] * 7 + [_VP]),
+    "gsdpa_decode_noalloc_max_scratch": (_SZ, []),
 }
 
 _lock = threading.Lock()
@@ -131,4 +133,28 @@ def gated_sdpa_fwd(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out
                  ctypes.c_void_p(s.cuda_stream))
     if st != OK:
         raise GsdpaError(st, "gated_sdpa_fwd")
+    return out, sink
+
+
+def decode_noalloc(X, Q, K, V, W_g=None, *, gate="elementwise", out=None, sink=None, want_sink=False, stream=None):
+    """The decode call (L_q == 1, bf16) without a workspace: the library's fixed
+    scratch array is used instead (for callers that cannot allocate device
+    memory). Same tensors as gated_sdpa_fwd with L_q == 1."""
+    import torch
+    gm = GATE_CODES[gate]
+    B, L_q, H_q, d_k = Q.shape
+    if L_q != 1:
+        raise ValueError("decode_noalloc takes one query row per sequence")
+    L_k, H_kv = K.shape[1], K.shape[2]
+    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    if out is None:
+        out = torch.empty_like(Q)
+    if sink is None and want_sink:
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gated_sdpa_decode_noalloc(
+        _ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
+        _ptr(out), _ptr(sink), B, L_k, d_model, H_q, H_kv, d_k, gm, ctypes.c_void_p(s.cuda_stream)))
+    if st != OK:
+        raise GsdpaError(st, "gated_sdpa_decode_noalloc")
     return out, sink

@@ -83,6 +83,21 @@ int gate_cols(const Problem& p) {
 
 int gate_col_tile(int cols);  // gate_gemm_sm103.cu
 
+// Runtime facts of the current device (SM count, compute capability, the
+// device address of the error word) for entry points defined in other files.
+bool current_runtime(Runtime* rt, int* cc_major, int* cc_minor) {
+    const DeviceInfo* d = device_info();
+    if (!d) return false;
+    rt->err = d->err;
+    rt->limit_ns = g_wait_limit_ns.load();
+    rt->num_sms = d->num_sms;
+    *cc_major = d->cc_major;
+    *cc_minor = d->cc_minor;
+    return true;
+}
+
+int plan_sms() { return kPlanSms; }
+
 WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
     WorkspacePlan w;
     size_t off = 0;

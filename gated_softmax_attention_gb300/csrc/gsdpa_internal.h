@@ -52,6 +52,10 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms);
 bool decode_supported(const Problem& p);
 int decode_splits(const Problem& p, int num_sms);
 
+// Current-device runtime facts (gsdpa_api.cu); the SM count workspace plans use.
+bool current_runtime(Runtime* rt, int* cc_major, int* cc_minor);
+int plan_sms();
+
 // Driver entry point for tensor-map encoding (resolved once, no -lcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

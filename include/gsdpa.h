@@ -144,6 +144,39 @@ GSDPA_API int gsdpa_check_device_error(void* stream);
 GSDPA_API const char* gsdpa_status_string(int status);
 
 /*
+ * gated_sdpa_decode_noalloc -- the decode call (one query row per sequence,
+ * L_q == 1) for callers that cannot allocate device memory. (The pages
+ * describe no such entry point; it belongs to this library's interface only.)
+ *
+ * Some callers cannot hand the library a workspace: code that must never make
+ * the device synchronise (cudaMalloc and cudaFree can), plugin or callback
+ * hooks that provide no allocator, or processes with a device memory budget
+ * fixed in advance. This entry point takes no workspace: its scratch (the
+ * split-K partials, the gate-logit partials and the arrival counters) lives
+ * in a 16 MiB array inside the library that every GPU loading the library
+ * holds until the process exits (see gsdpa_decode_noalloc_max_scratch()).
+ *
+ *   Arguments are those of gated_sdpa_fwd with L_q = 1, causal, bf16 implied.
+ *   Covered shapes: d_k == 128 and H_q / H_kv a multiple of 4 (the dedicated
+ *   decode kernel); others return GSDPA_ERR_UNSUPPORTED. A problem whose
+ *   scratch exceeds the fixed array returns GSDPA_ERR_WORKSPACE (the size a
+ *   problem needs is gsdpa_workspace_bytes(B, 1, L_k, ..., dtype = GSDPA_BF16)).
+ *
+ * The first call on a device resolves the array's device address (a runtime
+ * query, no allocation); make that first call before any stream capture. The
+ * array is shared by all calls on a device and keeps the last call's
+ * contents; counters are cleared at the start of each call. Calls that overlap
+ * on the device race on the array: serialise them.
+ */
+GSDPA_API int gated_sdpa_decode_noalloc(const void* X, const void* Q, const void* K, const void* V,
+                                        const void* W_g, void* O, float* sink,
+                                        int B, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                                        int gate_mode, void* stream);
+
+/* Size in bytes of the fixed scratch array used by gated_sdpa_decode_noalloc. */
+GSDPA_API size_t gsdpa_decode_noalloc_max_scratch(void);
+
+/*
  * Test hook, not part of the operation: sets the wait limit, in nanoseconds,
  * that every bounded wait inside the kernels uses from the next launch on
  * (0 restores the default of 2 s). Lets a test make a wait run out quickly.
