@@ -115,6 +115,22 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def captured_traffic(profile_name, sources):
+    """dram bytes per launch from a committed ncu summary in profiles/, or None
+    when the kernel's sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in sources:
+        h.update(open(os.path.join(ROOT, "gated_softmax_attention_gb300", "csrc", f), "rb").read())
+    fields = dict(line.split(":", 1) for line in open(path) if line.startswith(("source_sha256:", "dram_bytes_per_launch:")))
+    if fields.get("source_sha256", "").split()[0:1] != [h.hexdigest()[:16]]:
+        return None
+    return int(fields["dram_bytes_per_launch"].strip())
+
+
 def oracle_cpu_baseline(w, inputs, seconds, seed=0):
     """Time the float64 oracle on a bounded, seeded row sample of workload w."""
     import numpy as np
@@ -325,7 +341,9 @@ def run_ours(args, d: Dist):
     achieved = flops / (kern_avg / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["source"] + " burst bf16 (cuBLAS)", "traffic": None,
+                "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
+                "traffic": captured_traffic("prefill_kernel_bf16_mha_elementwise_L2048.md",
+                                            ["prefill_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h"]),
                 "kernel": "prefill_kernel<128,2>", "kernel_ms": round(kern_avg, 4)}
     # attention-only throughput and the gated / ungated time ratio
     none_avg = time_calls(torch, lambda k: g_none[k % R].replay(), K, W, stream)
@@ -434,7 +452,9 @@ def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):
             "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
                          "peak_source": peaks["source"] + " STREAM-style copy",
-                         "scope": "whole call (gate-logit pre-pass + decode kernel)", "traffic": None},
+                         "scope": "whole call (gate-logit pre-pass + decode kernel)",
+                         "traffic_decode_kernel": captured_traffic("decode_kernel_bf16_decode_gqa_elementwise_Lk8192.md",
+                                                                   ["decode_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h"])},
             "e2e": {"value": round(nbytes * E * d.world / e2e_s / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": O.numel() * O.element_size(), "steps": E},
             "gpu_launches": 2 * K}
