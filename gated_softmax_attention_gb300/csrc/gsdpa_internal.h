@@ -69,6 +69,11 @@ cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, ch
                                     cudaStream_t s, bool* launched);
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s);
+// d_k = 128 on CTA pairs (prefill_pair_sm103.cu); launch_prefill_bf16 routes
+// problems with at least kPairMinKeys keys there.
+constexpr long kPairMinKeys = 16384;
+cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                     cudaStream_t s);
 cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                cudaStream_t s);
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);

@@ -655,6 +655,10 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s) {
     if (p.dk == 128) {
+        // Long key sequences: CTA pairs (M = 256 MMAs, half the operand
+        // traffic per SM). Shorter ones keep single-CTA units, whose finer
+        // granularity balances causal work better across the SMs.
+        if ((long)p.Lk >= kPairMinKeys) return launch_prefill_pair_bf16(p, w, ws, rt, s);
         if (p.gate_mode == 2) return launch_prefill_t<128, 2>(p, w, ws, rt, s);
         if (p.gate_mode == 1) return launch_prefill_t<128, 1>(p, w, ws, rt, s);
         return launch_prefill_t<128, 0>(p, w, ws, rt, s);

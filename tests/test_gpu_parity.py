@@ -100,6 +100,41 @@ def test_small_shapes(dtype, case):
     np.testing.assert_allclose(sink, oracle.sink_share(p0), atol=sink_tol(w))
 
 
+# Long key sequences (>= 16384 keys) run on the CTA-pair kernel: its units
+# are four query tiles, two per CTA, and an MMA slot pairs tile 4u+2t of one
+# CTA with tile 4u+2t+1 of the other. These cases cover a pair whose odd tile
+# has no rows, a unit whose second slot has no rows, ragged L_k, GQA, both
+# gates, no gate and no mask.
+PAIR_CASES = [
+    dict(L_q=300, L_k=16500),                                       # 3 tiles: odd tile of slot 1 empty
+    dict(L_q=600, L_k=16384, gate="headwise", H_q=8, H_kv=2),       # 5 tiles: second unit has one tile
+    dict(L_q=256, L_k=16448, gate="none", causal=False, H_q=2, H_kv=1),
+    dict(L_q=512, L_k=16384, H_q=4, H_kv=4, d_model=512),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: ",".join(f"{k}={v}" for k, v in c.items()))
+def test_pair_kernel_long_keys(case):
+    w = small("bf16", B=1, **case)
+    t = make_inputs(w)
+    O, sink = run_gpu(w, t)
+    ref, p0 = run_oracle(w, t)
+    assert_close(w, O, ref, "O")
+    np.testing.assert_allclose(sink, oracle.sink_share(p0), atol=sink_tol(w))
+
+
+def test_pair_kernel_square_sampled():
+    # L_q = L_k = 16384: many units per pair (phases carried across units), sampled rows
+    w = small("bf16", B=1, L_q=16384, L_k=16384, H_q=2, H_kv=1, d_model=256, seed=23)
+    t = make_inputs(w)
+    O, sink = run_gpu(w, t)
+    rows = sample_rows(w, 32)
+    ref, p0 = run_oracle(w, t, rows=rows)
+    got = np.stack([O[b, i] for b, i in rows])
+    assert_close(w, got, ref, "O")
+    assert np.isfinite(O).all()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("sign", [1.0, -1.0])
 @pytest.mark.parametrize("gate", ["elementwise", "headwise"])
