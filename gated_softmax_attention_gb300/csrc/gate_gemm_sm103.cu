@@ -63,6 +63,7 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    pdl_trigger();   // the consumer (attention or decode) may start; it reads the logits late
     const int u = blockIdx.x;
     const int rt = u % args.row_tiles;
     const int ct = (u / args.row_tiles) % args.col_tiles;

@@ -1,0 +1,284 @@
+// gate_sigmoid_sm103.cu -- the elementwise gate sigma(X W_g) for the bf16
+// prefill path, as fp16, on pairs of SMs.
+//
+// Computes gate[r, c] = fp16( sigma( sum_m X[r, m] W_g[m, c] ) ) for every row
+// r of X viewed as [rows = B*L_q, d_model] and every column c of W_g
+// [d_model, cols = H_q*d_k] ("GatedAttention [2025]", sec. 1.2.2: the gate
+// is sigma(X W_theta), applied elementwise to the SDPA output; no bias,
+// "10 . 门控", sec. 3.2). The attention epilogue multiplies its output rows by
+// these values, so the ungated SDPA output never leaves the SM; the gate
+// values (values in (0, 1), where fp16 keeps 11 significant bits) make one
+// round trip through L2 / HBM.
+//
+// This is a plain GEMM with a sigmoid epilogue, kept out of the attention
+// kernel: there, one head's 128 gate columns per unit re-read X once per head
+// from L2 and the tile shape (256 x 128) needs more L2 bandwidth per flop
+// than the SMs get. Here a pair of CTAs (cluster of two, tcgen05.mma
+// .cta_group::2) computes a 256 x 512 tile in the whole of tensor memory:
+// per K chunk of 64, each CTA loads its 128 rows of X (16 KB) and a
+// contiguous block of 256 columns of W_g (32 KB, one copy request) for 1024
+// MMA cycles.
+//
+// Column order. A pair MMA takes the first half of its N columns from the
+// even CTA and the second half from the odd one. CTA rho holds W_g columns
+// [256 rho, 256 rho + 256) of the tile; MMA h (h = 0, 1) takes columns
+// [128 h, 128 h + 128) of each CTA's block, so accumulator column c holds
+// tile column 256 * ((c % 256) / 128) + 128 * (c / 256) + c % 128.
+//
+// Per CTA: warp 0 TMA producer (both CTAs), warp 1 TMEM allocation (both) and
+// MMA issue (even CTA), warps 2..9 epilogue: two warps per TMEM lane quadrant,
+// each converting half of the 512 accumulator columns of its 32 rows (the
+// tensor-memory load of the next 32 columns in flight while the current ones
+// are converted). The fp16 tile is staged in the idle K-chunk ring as 64-column
+// 128B-swizzled blocks and written with two 64 KB bulk copies: one thread per
+// row writing 16-byte pieces of its own row would cost one memory transaction
+// per piece.
+// Rows past the end of X, columns past the end of W_g and the K tail load as
+// zeros (TMA out-of-bounds fill) and are not stored.
+#include "gsdpa_internal.h"
+#include "sm103_pair.cuh"
+#include "sm103_ptx.cuh"
+
+#include <cuda_fp16.h>
+
+namespace gsdpa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kNS = 4;                                  // K-chunk ring stages
+constexpr uint32_t kXBytes = 128 * 64 * 2;              // X chunk: this CTA's 128 rows x 64
+constexpr uint32_t kWBytes = 64 * 256 * 2;              // W_g chunk: 64 x this CTA's 256 columns
+constexpr uint32_t kStage = kXBytes + kWBytes;
+constexpr uint32_t kOffBar = kNS * kStage;
+constexpr uint32_t kOffMisc = kOffBar + (2 * kNS + 2) * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+
+struct SigArgs {
+    __half* out;     // [rows, cols]
+    int rows, cols, d_model;
+    int row_tiles, nkc;   // tiles of 256 rows; K chunks of 64
+    WaitCtl ctl;
+};
+
+// sigma(x) = 1/2 + tanh(x/2)/2 (tanh.approx: relative error about 2^-11)
+__device__ __forceinline__ float sigmoid_fast(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmG, const SigArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* full = bars;              // [NS] even CTA: both CTAs' halves of the chunk landed
+    uint64_t* empty = bars + kNS;       // [NS] both: the MMAs reading the stage completed
+    uint64_t* acc_full = bars + 2 * kNS;     // both: the accumulator is complete
+    uint64_t* drain = bars + 2 * kNS + 1;    // even
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    int* abort_word = reinterpret_cast<int*>(smem + kOffMisc + 4);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = pair::cta_rank();
+    const pair::PairAbort ab{abort_word, pair::map_to(abort_word, rank ^ 1u)};
+    pdl_trigger();   // the attention kernel may start; it reads the gate only in its epilogue
+    const int tile = (int)pair::cluster_id();
+    const int r0 = (tile % args.row_tiles) * 256;   // the pair's first row
+    const int c0 = (tile / args.row_tiles) * 512;   // the pair's first column
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_word = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmG);
+    }
+    if (warp == 1) {
+        pair::tmem_alloc(tmem_slot, 512);
+        tc_fence_before();
+    }
+    __syncthreads();
+    pair::cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---- TMA producer: this CTA's rows of X and its 256 columns of W_g
+        if (lane == 0) {
+            for (int kc = 0; kc < args.nkc; ++kc) {
+                const int s = kc % kNS;
+                const uint32_t ph = (kc / kNS) & 1;
+                if (!pair::wait(&empty[s], ph ^ 1u, ab, args.ctl)) break;
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kStage);   // both CTAs' bytes
+                const uint32_t fb = pair::map_to(&full[s], 0);
+                uint8_t* st = smem + s * kStage;
+                pair::tma_load_2d(st, &tmX, kc * 64, r0 + (int)rank * 128, fb);
+                // W_g viewed as (64 columns, d_model rows, cols/64 blocks): four 64-column blocks
+                pair::tma_load_3d(st + kXBytes, &tmW, 0, kc * 64, (c0 + (int)rank * 256) / 64, fb);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issue (even CTA): D[256 x 512] += X[256 x 64] W_g[64 x 512] per chunk, as two N = 256 MMAs
+        if (rank == 0) {
+            constexpr uint32_t idG = idesc_bf16_f32(256, 256, false, true);
+            constexpr uint32_t HI = desc_sw128_hi(1024);
+            const uint32_t base = smem_u32(smem);
+            bool ok = true;
+            for (int kc = 0; kc < args.nkc && ok; ++kc) {
+                const int s = kc % kNS;
+                if (!(ok = __all_sync(0xffffffffu, pair::wait(&full[s], (kc / kNS) & 1, ab, args.ctl)))) break;
+                tc_fence_after();
+                const uint32_t st = base + s * kStage;
+                // X: K-major, one 64-column box; W_g: MN-major, 64-column blocks 8 KB apart;
+                // MMA h reads blocks 2h, 2h + 1 of each CTA
+                const uint32_t x0 = desc_sw128_lo(st, 16), w0 = desc_sw128_lo(st + kXBytes, 8192);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        pair::mma_ss(tmem + hh * 256, x0 + kk * (32 >> 4), HI, w0 + ((hh * 16384 + kk * 2048) >> 4), HI,
+                                     idG, (kc | kk) != 0);
+                pair::commit_both(&empty[s]);
+            }
+            if (ok) {
+                pair::commit_both(acc_full);
+            } else {
+                WaitCtl c2 = args.ctl;
+                if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
+                int never = 0;
+                const pair::PairAbort quiet{&never, ab.peer};
+                asm volatile(
+                    "{\n\t.reg .pred e;\n\t"
+                    "elect.sync _|e, 0xffffffff;\n\t"
+                    "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                        smem_u32(drain))
+                    : "memory");
+                pair::wait(drain, 0, quiet, c2);
+                __syncwarp();
+            }
+        }
+    } else {
+        // ---- epilogue: sigma, fp16, 512 bytes of one row per thread
+        const int qd = warp & 3;
+        const int half = (warp - 2) >> 2;      // which 256 accumulator columns
+        const int row = qd * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        const bool ok = __all_sync(0xffffffffu, pair::wait(acc_full, 0, ab, args.ctl));
+        tc_fence_after();
+        if (ok) {
+            // (every MMA has completed, so the ring is idle: stage the tile there as
+            // [8 blocks of 64 columns][128 rows], 128-byte rows, 128B swizzle)
+            uint32_t buf[2][32];
+            tmem_ld32(tmem + lane_base + half * 256, buf[0]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                tmem_wait_ld_regs(buf[k & 1]);
+                if (k + 1 < 8) tmem_ld32(tmem + lane_base + half * 256 + (k + 1) * 32, buf[(k + 1) & 1]);
+                const uint32_t* v = buf[k & 1];
+                const int c = half * 256 + k * 32;   // accumulator column -> tile column (see the column order above)
+                const int tc = 256 * ((c & 255) >> 7) + 128 * (c >> 8) + (c & 127);
+                uint32_t hv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const __half2 h2 = __floats2half2_rn(sigmoid_fast(__uint_as_float(v[2 * e])),
+                                                         sigmoid_fast(__uint_as_float(v[2 * e + 1])));
+                    hv[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                uint8_t* blk = smem + (tc >> 6) * 16384;
+                const uint32_t chunk0 = (uint32_t)(tc & 63) >> 3;   // 16-byte chunk of the 128-byte row
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(blk + sw128_offset((uint32_t)row, chunk0 + q)) =
+                        make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+            }
+            fence_proxy_async_smem();   // the staged tile is read by the bulk copies below
+        }
+        named_bar_sync(1, 256);   // the eight epilogue warps
+        if (ok && warp == 2 && lane == 0) {
+            // rows / columns past the end of the output are clipped by the copy
+            const int rr = r0 + (int)rank * 128;
+            for (int g = 0; g < 2; ++g) tma_store_3d(&tmG, smem + g * 65536, 0, rr, (c0 + g * 256) / 64);
+            tma_store_commit();
+            tma_store_wait_read0();   // the staging area stays valid until the copies have read it
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    pair::cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        pair::tmem_dealloc(tmem, 512);
+    }
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d, const cuuint64_t* st,
+              const cuuint32_t* box) {
+    cuuint32_t es[3] = {1, 1, 1};
+    return encode_tiled_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, box, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                     cudaStream_t s) {
+    alignas(64) CUtensorMap tmX, tmW, tmG;
+    const int rows = p.B * p.Lq, cols = p.Hq * p.dk;
+    if (rows == 0) return cudaSuccess;
+    {
+        const cuuint64_t d[2] = {(cuuint64_t)p.d_model, (cuuint64_t)rows};
+        const cuuint64_t st[1] = {(cuuint64_t)p.d_model * 2};
+        const cuuint32_t box[2] = {64, 128};
+        if (!make_map(&tmX, p.X, 2, d, st, box)) return cudaErrorInvalidValue;
+    }
+    {
+        // (64 columns, d_model rows, cols/64 column blocks; the blocks 128 bytes apart)
+        const cuuint64_t d[3] = {64, (cuuint64_t)p.d_model, (cuuint64_t)cols / 64};
+        const cuuint64_t st[2] = {(cuuint64_t)cols * 2, 128};
+        const cuuint32_t box[3] = {64, 64, 4};
+        if (!make_map(&tmW, p.Wg, 3, d, st, box)) return cudaErrorInvalidValue;
+    }
+    {
+        // output (fp16, [rows, cols]) as (64 columns, rows, cols/64 blocks): 128 rows x 256 columns per copy
+        const cuuint64_t d[3] = {64, (cuuint64_t)rows, (cuuint64_t)cols / 64};
+        const cuuint64_t st[2] = {(cuuint64_t)cols * 2, 128};
+        const cuuint32_t box[3] = {64, 128, 4};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (encode_tiled_fn()(&tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ws + w.gate_sig, d, st, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    SigArgs a;
+    a.out = reinterpret_cast<__half*>(ws + w.gate_sig);
+    a.rows = rows;
+    a.cols = cols;
+    a.d_model = p.d_model;
+    a.row_tiles = (rows + 255) / 256;
+    a.nkc = (p.d_model + 63) / 64;
+    a.ctl.err = rt.err;
+    a.ctl.limit_ns = rt.limit_ns;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (r != cudaSuccess) return r;
+        attr_done = true;
+    }
+    const long tiles = (long)a.row_tiles * ((cols + 511) / 512);
+    gate_sigmoid_kernel<<<(unsigned)(2 * tiles), kThreads, kSmemBytes, s>>>(tmX, tmW, tmG, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gsdpa

@@ -126,6 +126,20 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
         w.gate_part = off;
         off = align256(off + sizeof(float) * (size_t)splits * w.gate_rows * w.gate_cols);
     }
+    // bf16 prefill: the counter from which the CTAs of the attention kernel
+    // claim their units (dynamic schedule), zeroed at the start of every call.
+    if (bf16 && !decode) {
+        w.has_sched = true;
+        w.sched = off;
+        off = align256(off + sizeof(int));
+    }
+    // Elementwise bf16 prefill: the gate sigma(X W_g) computed ahead of the
+    // attention kernel, whose epilogue multiplies by it.
+    if (bf16 && !decode && p.gate_mode == GSDPA_GATE_ELEMENTWISE) {
+        w.has_gate_sig = true;
+        w.gate_sig = off;
+        off = align256(off + 2 * (size_t)p.B * p.Lq * p.Hq * p.dk);
+    }
     if (decode) {
         const int chunks = (p.Hq / p.Hkv) / 4;
         w.dec_splits = decode_splits(p, num_sms);
@@ -253,7 +267,9 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
         if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
     } else {
         bool gate_launched = false;
-        e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
+        if (w.has_sched) e = cudaMemsetAsync(ws + w.sched, 0, sizeof(int), s);
+        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
+        if (e == cudaSuccess && w.has_gate_sig) e = launch_gate_sigmoid_bf16(p, w, ws, rt, s);
         if (decode_supported(p)) {
             if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s);
         } else {

@@ -34,6 +34,10 @@ struct WorkspacePlan {
     size_t sink_part = 0;   // float [B, Hq, n_tiles]          (sink partial sums)
     int sink_tiles = 0;
     size_t gate_part = 0;   // float [gate_splits, rows, cols] (gate logits, split-K partials)
+    size_t gate_sig = 0;    // fp16  [B*L_q, H_q*d_k]          (elementwise prefill: sigma(X W_g))
+    bool has_gate_sig = false;
+    size_t sched = 0;       // int   [1] bf16 prefill: next unit to claim (zeroed per call)
+    bool has_sched = false;
     int gate_splits = 0;
     int gate_rows = 0, gate_cols = 0;
     size_t dec_ml = 0;      // float [B, Hq, splits, 2]        (decode running max, sum)
@@ -67,6 +71,9 @@ cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, 
                             cudaStream_t s);
 cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                     cudaStream_t s, bool* launched);
+// Elementwise bf16 prefill: sigma(X W_g) as fp16 into the workspace (gate_sigmoid_sm103.cu).
+cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                     cudaStream_t s);
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s);
 // d_k = 128 on CTA pairs (prefill_pair_sm103.cu); launch_prefill_bf16 routes

@@ -1,60 +1,74 @@
 // prefill_pair_sm103.cu -- bf16 gated attention forward for d_k = 128 on pairs
 // of SMs (clusters of two CTAs) sharing M = 256 tcgen05 MMAs.
 //
-// A pair computes one unit (b, h, four 128-row query tiles). MMA slot t
-// (t = 0, 1) stacks query tile 4u+2t of the even CTA over tile 4u+2t+1 of
-// the odd CTA into one 256-row operand:
-//   S_t = Q_t K_j^T                      tcgen05.mma.cta_group::2, A and B in smem
-//   P_t = exp2(S_t log2(e)/sqrt(d_k) - m_t)   online softmax, one thread per row,
-//                                        each CTA on its own 128 rows
-//   O_t += P_t V_j                       tcgen05.mma.cta_group::2, P read from TMEM
-//   G_t = X_t W_g[:, h*d_k:(h+1)*d_k]    elementwise gate GEMM, same pair
-//   out_t = O_t / l_t (.) sigmoid(G_t)   epilogue, bf16 rows straight to HBM
+// A pair computes one unit (b, h, 256 query rows): query tile 2u sits in the
+// even CTA and tile 2u+1 in the odd one, stacked into the 256-row A operand
+// of every MMA. The key tiles j = 0, 1, 2, ... of the unit alternate between
+// two softmax warpgroups (p = j mod 2), each with its own score buffer S_p,
+// output accumulator O_p and running row max m_p / row sum l_p:
+//   S_p  = Q K_j^T                          tcgen05.mma.cta_group::2, A and B in smem
+//   P_p  = exp2(S_p log2(e)/sqrt(d_k) - m_p)  online softmax of warpgroup p
+//   O_p += P_p V_j                          tcgen05.mma.cta_group::2, P read from TMEM
+// and the epilogue merges the two halves of the key range (with m = max(m_0, m_1)),
+//   O = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),
+// multiplies by the gate g and stores bf16 rows, where g = sigma(X W_g)
+// (elementwise, fp16, computed ahead by the gate GEMM) or sigma(x_i . w_h)
+// (headwise, logits computed ahead).
 // ("GatedAttention [2025]", sec. 1.2.1 SDPA and sec. 1.2.2 the gate
 //  Y' = Y (.) sigma(X W); "10 . 门控", sec. 3.2: G1 gates each head's SDPA
-//  output before the heads are concatenated.)
+//  output before the heads are concatenated.) The ungated output never leaves
+//  the SM. Splitting the key range and merging the partial results is exact
+//  (the merge is the same rescaling the online softmax applies tile by tile).
+//
+// Why two warpgroups over alternating key tiles: the QK MMA of key tile j+2
+// needs only S_p free (P_p(j) consumed by its PV MMA, queued before it), so it
+// runs while the other warpgroup computes the softmax of tile j+1. Each
+// softmax has the MMAs of two key tiles to hide behind, where one tile's
+// worth (two query tiles sharing one S buffer each) left the tensor pipe idle
+// whenever a softmax took longer than the other tile's MMAs.
 //
 // Why pairs: a single-CTA 128 x 128 x 16 MMA reads 8 KB of operands from
 // shared memory in its 64 cycles, the whole shared-memory bandwidth of the
 // SM, and the K/V copies arriving in the same memory then stall it. In a
 // pair each SM reads its own 128 A rows and only half of B (6 KB per 64
-// cycles), each CTA loads only half of every K, V and W_g tile, and one
-// thread issues the MMAs of both SMs.
+// cycles), each CTA loads only half of every K and V tile, and one thread
+// issues the MMAs of both SMs.
 //
 // Operand split. K_j [128 keys x 128]: the even CTA holds keys 0..63, the odd
 // CTA keys 64..127 (the N half of the S MMA). V_j [128 keys x 128]: the even
 // CTA holds columns 0..63, the odd one columns 64..127 (the N half of the PV
-// MMA). W_g chunk [64 x 128]: split by columns the same way. Q_t, X_t and P_t
-// (A operands) stay with the CTA whose rows they are.
+// MMA). Q and P (A operands) stay with the CTA whose rows they are.
 //
 // Warp roles (384 threads per CTA):
 //   warp 0       TMA producer of this CTA's halves (both CTAs);
 //   warp 1       TMEM allocation (both CTAs, collectively); in the even CTA it
 //                also issues every MMA and commit of the pair;
 //   warps 2, 3   spare;
-//   warps 4..7   softmax + epilogue of this CTA's tile of slot 0;
-//   warps 8..11  softmax + epilogue of this CTA's tile of slot 1.
+//   warps 4..7   softmax of the even key tiles, epilogue of output columns 0..63;
+//   warps 8..11  softmax of the odd key tiles, epilogue of output columns 64..127.
 // Barriers the issuing thread waits on (ring stages full, Q loaded, P
-// written, TMEM free, gate stages full) live in the even CTA; the odd CTA
-// reaches them through cluster addresses. The copies of both CTAs complete
-// their bytes on the even CTA's barriers, and the even CTA alone arms them
-// with the byte count of both halves (the odd CTA's bytes may land first: a
-// barrier's pending byte count may go below zero until it is armed). MMA
-// completions (S ready, ring stages free, gate done) are multicast to both
-// CTAs.
+// written) live in the even CTA; the odd CTA reaches them through cluster
+// addresses. The copies of both CTAs complete their bytes on the even CTA's
+// barriers, and the even CTA alone arms them with the byte count of both
+// halves (the odd CTA's bytes may land first: a barrier's pending byte count
+// may go below zero until it is armed). MMA completions (S ready, ring stages
+// free, unit done) are multicast to both CTAs.
 //
 // TMEM (512 columns, same layout in both CTAs): S_0 [0,128) S_1 [128,256)
-// O_0 [256,384) O_1 [384,512); P_t packed bf16 in S_t [0,64); G_t reuses S_t.
+// O_0 [256,384) O_1 [384,512); P_p packed bf16 in S_p [0,64).
 //
 // Causal mask aligned bottom-right (query i at absolute position
-// L_k - L_q + i). A slot runs over the key tiles its later query tile can
-// see; the even CTA's rows mask the extra tile. Persistent grid: units
-// (heaviest first) are dealt to the pairs in snake order.
+// L_k - L_q + i). A unit runs over the key tiles its odd CTA's rows can see;
+// the even CTA's rows mask the extra tile. Persistent grid: the even CTA's
+// producer claims the next unit from a counter in global memory (units
+// numbered heaviest first: a longest-first greedy schedule) and hands it to
+// every role of both CTAs through a small ring in shared memory.
 #include "gsdpa_internal.h"
 #include "sm103_pair.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
+#include <cuda_fp16.h>
 
 namespace gsdpa {
 namespace {
@@ -64,33 +78,36 @@ constexpr int kHD = 128;
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// Register split: warpgroup 0 (producer, MMA, spare) gives registers to the
+// two softmax warpgroups. The launch must provide 384 x kRegsLaunchMin.
 constexpr int kRegsLow = 64;
 constexpr int kRegsHigh = 216;
 constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 
 struct PairCfg {
-    static constexpr uint32_t Q_BYTES = kTile * kHD * 2;      // this CTA's query tile of one slot
-    static constexpr uint32_t STAGE_BYTES = 64 * kHD * 2;     // K half (64 keys) or V half (64 columns)
-    static constexpr int NS = 8;
-    static constexpr uint32_t GX_BYTES = kTile * 64 * 2;      // X chunk of this CTA's rows
-    static constexpr uint32_t GW_BYTES = 64 * 64 * 2;         // W_g chunk, this CTA's 64 columns
-    static constexpr uint32_t OFF_Q = 0;                      // Q of slot 0, slot 1
-    static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
+    static constexpr uint32_t Q_BYTES = kTile * kHD * 2;      // this CTA's query tile
+    static constexpr uint32_t HALF_BYTES = 64 * kHD * 2;      // K half (64 keys) or V half (64 columns)
+    // A ring stage holds what one step of the MMA issue consumes: V_j and K_{j+2}
+    // (the first stage of a unit: K_0 and K_1), one barrier wait per key tile.
+    static constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;
+    static constexpr int NS = 5;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_RING = Q_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
-    // Gate phase (after every attention MMA has completed): Q and the ring are
-    // reused as GNS stages, each X_0 | X_1 | W_g half.
-    static constexpr uint32_t GSTAGE_BYTES = 2 * GX_BYTES + GW_BYTES;
-    static constexpr int GNS = 4;
-    static_assert(GNS * GSTAGE_BYTES <= OFF_BAR, "gate ring must fit over Q and the K/V ring");
-    static constexpr int NBAR = 2 * NS + 2 * GNS + 10;
+    static constexpr int NBAR = 2 * NS + 11;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    // misc: TMEM address, abort flag, sink partials [4], unit ring [4]; then the
+    // row statistics (m, l) of both warpgroups [2][128] for the merge
+    static constexpr uint32_t OFF_STATS = OFF_MISC + 64;
+    static constexpr uint32_t SMEM_BYTES = OFF_STATS + 2 * 128 * 8 + 1024;  // + alignment slack
 };
 
 struct PairArgs {
-    int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_quads;
+    int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_blk;
     const float* gate_part;  // headwise: [splits, B*Lq, Hq]
     int gate_splits;
+    const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*d_k]
+    int* sched_counter;      // next unit to claim (0 at launch)
     float* sink_part;        // [B, Hq, n_qtiles] or null
     __nv_bfloat16* O;        // [B, Lq, Hq, d_k]
     WaitCtl ctl;
@@ -107,8 +124,7 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
 template <int GATE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmX,
-                    const __grid_constant__ CUtensorMap tmW, const PairArgs args) {
+                    const __grid_constant__ CUtensorMap tmV, const PairArgs args) {
     using C = PairCfg;
     extern __shared__ uint8_t smem_raw[];
     // (both CTAs run the same code, so this offset -- which the MMA
@@ -117,64 +133,55 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     uint8_t* sQ = smem + C::OFF_Q;
     uint8_t* ring = smem + C::OFF_RING;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* full = bars;                  // [NS] even CTA: both halves of a ring item landed (armed by the even CTA)
+    uint64_t* full = bars;                  // [NS] even CTA: both halves of a ring item landed
     uint64_t* empty = bars + C::NS;         // [NS] both: the MMAs reading the item completed
     uint64_t* q_full = bars + 2 * C::NS;    // even: both CTAs' query tiles landed
-    uint64_t* s_full = q_full + 1;          // [2] both: S_t complete (and every earlier MMA)
-    uint64_t* p_full = q_full + 3;          // [2] even: the 8 softmax warps of slot t wrote P_t
-    uint64_t* g_full = q_full + 5;          // [2] both: every MMA of slot t, gate included, complete
-    uint64_t* drain = q_full + 7;           // even
-    uint64_t* attn_done = q_full + 8;       // both: every attention MMA of the unit complete
-    uint64_t* tmem_free = q_full + 9;       // even: the four epilogues of the pair read TMEM out
-    uint64_t* gfull = q_full + 10;          // [GNS] even
-    uint64_t* gempty = gfull + C::GNS;      // [GNS] both
+    uint64_t* s_full = q_full + 1;          // [2] both: S_p complete (and every earlier MMA)
+    uint64_t* p_full = q_full + 3;          // [2] even: the 8 warps of warpgroup p (both CTAs) wrote P_p
+    uint64_t* g_full = q_full + 5;          // both: every MMA of the unit complete
+    uint64_t* drain = q_full + 6;           // even
+    uint64_t* sched_full = q_full + 7;      // [4] both: unit r published in sched[r % 4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     int* abort_word = reinterpret_cast<int*>(smem + C::OFF_MISC + 4);
     volatile int* abort_flag = abort_word;
-    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
+    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);                  // [4]
+    volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
+    float2* stats = reinterpret_cast<float2*>(smem + C::OFF_STATS);                   // [2][128]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t rank = pair::cta_rank();
     const pair::PairAbort ab{abort_flag, pair::map_to(abort_word, rank ^ 1u)};
 
-    // ---- persistent schedule: units numbered heaviest first (last query quad
-    // first when causal), dealt to the pairs in snake order.
-    const int per_quad = args.Hq * args.B;
-    const int n_units = args.n_quads * per_quad;
+    // ---- units (b, h, block of 256 query rows), numbered heaviest first
+    // (last query block first when causal)
+    const int per_blk = args.Hq * args.B;
+    const int n_units = args.n_blk * per_blk;
     const long off = (long)args.Lk - args.Lq;
-    const int nkc = (args.d_model + 63) / 64;
-    const int G = (int)pair::n_clusters();
-    const int cid = (int)pair::cluster_id();
     struct Unit {
-        int qd, h, b, kvh, nj;
-        int q0[2], nkv[2];   // q0: first row of this CTA's tile in slot t
-        bool act[2];         // slot t has rows (in either CTA)
-        bool mine[2];        // this CTA's tile of slot t has rows
+        int h, b, kvh, nkv;
+        int q0;        // first row of this CTA's query tile
+        bool mine;     // this CTA's tile has rows
+        int tiles;     // query tiles with rows in the pair (1 or 2)
     };
-    auto unit_index = [&](int r) -> int { return (r & 1) ? (r + 1) * G - 1 - cid : r * G + cid; };
     auto decode_unit = [&](int u) -> Unit {
         Unit x;
-        x.qd = args.causal ? (args.n_quads - 1 - u / per_quad) : (u / per_quad);
-        const int rem = u % per_quad;
+        const int blk = args.causal ? (args.n_blk - 1 - u / per_blk) : (u / per_blk);
+        const int rem = u % per_blk;
         x.h = rem % args.Hq;
         x.b = rem / args.Hq;
         x.kvh = x.h / (args.Hq / args.Hkv);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int lo = (4 * x.qd + 2 * t) * kTile;          // the even CTA's tile
-            x.q0[t] = lo + (int)rank * kTile;
-            x.act[t] = lo < args.Lq;
-            x.mine[t] = x.q0[t] < args.Lq;
-            const int last = (lo + kTile < args.Lq) ? lo + kTile : lo;   // the slot's last tile with rows
-            long kend = args.Lk;
-            if (args.causal) {
-                const long e = off + last + kTile;   // keys 0 .. off+last+127 can be visible
-                kend = e < kend ? e : kend;
-            }
-            x.nkv[t] = x.act[t] ? (int)((kend + kTile - 1) / kTile) : 0;
+        const int lo = blk * 2 * kTile;                       // the even CTA's tile
+        x.q0 = lo + (int)rank * kTile;
+        x.mine = x.q0 < args.Lq;
+        x.tiles = (lo + kTile < args.Lq) ? 2 : 1;
+        const int last = (x.tiles == 2) ? lo + kTile : lo;    // the pair's last tile with rows
+        long kend = args.Lk;
+        if (args.causal) {
+            const long e = off + last + kTile;                // keys 0 .. off+last+127 can be visible
+            kend = e < kend ? e : kend;
         }
-        x.nj = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
+        x.nkv = (int)((kend + kTile - 1) / kTile);
         return x;
     };
 
@@ -184,27 +191,18 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&empty[s], 1);
         }
         mbar_init(q_full, 1);
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 8);
-            mbar_init(&g_full[t], 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(&s_full[p], 1);
+            mbar_init(&p_full[p], 8);
         }
+        mbar_init(g_full, 1);
         mbar_init(drain, 1);
-        mbar_init(attn_done, 1);
-        mbar_init(tmem_free, 4);
-        for (int s = 0; s < C::GNS; ++s) {
-            mbar_init(&gfull[s], 1);
-            mbar_init(&gempty[s], 1);
-        }
+        for (int k = 0; k < 4; ++k) mbar_init(&sched_full[k], 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        if (GATE == 2) {
-            tma_prefetch_desc(&tmX);
-            tma_prefetch_desc(&tmW);
-        }
     }
     if (warp == 1) {
         pair::tmem_alloc(tmem_slot, 512);
@@ -219,60 +217,50 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // ================================================================ TMA producer (both CTAs)
         if (lane == 0) {
             bool ok = true;
-            int item = 0, gitem = 0;   // running counts: phases carry over units
+            int item = 0;   // running count of ring items: phases carry over units
             const uint32_t q_full_e = pair::map_to(q_full, 0);
             for (int r = 0; ok; ++r) {
-            const int uix = unit_index(r);
+            // the even CTA claims the next unit and publishes it in both CTAs (the
+            // slot's previous unit, r - 4, was read long ago: both producers have
+            // seen every MMA of unit r - 2 complete); the odd CTA takes it from there
+            int uix;
+            if (rank == 0) {
+                uix = atomicAdd(args.sched_counter, 1);
+                sched[r & 3] = uix;
+                pair::store_remote_u32(pair::map_to(const_cast<int*>(&sched[r & 3]), 1), (uint32_t)uix);
+                mbar_arrive(&sched_full[r & 3]);
+                pair::arrive_remote_release(pair::map_to(&sched_full[r & 3], 1));
+            } else {
+                if (!(ok = pair::wait_acquire_cluster(&sched_full[r & 3], (r >> 2) & 1, ab, args.ctl))) break;
+                uix = sched[r & 3];
+            }
             if (uix >= n_units) break;
             const Unit U = decode_unit(uix);
-            // every MMA of the previous unit is complete (its gate ring overlays Q and K/V)
-            if (r > 0 && !(ok = pair::wait(&g_full[1], (r - 1) & 1, ab, args.ctl))) break;
-            // tiles with rows, both CTAs (the odd CTA's tile of a slot starts one tile later)
-            const uint32_t q_tiles = (U.act[0] ? 1u : 0u) + (U.act[1] ? 1u : 0u) +
-                                     (U.act[0] && U.q0[0] - (int)rank * kTile + kTile < args.Lq ? 1u : 0u) +
-                                     (U.act[1] && U.q0[1] - (int)rank * kTile + kTile < args.Lq ? 1u : 0u);
-            if (rank == 0) mbar_arrive_expect_tx(q_full, q_tiles * C::Q_BYTES);
-            for (int t = 0; t < 2; ++t)
-                if (U.mine[t])
-                    for (int cb = 0; cb < 2; ++cb)
-                        pair::tma_load_4d(sQ + t * C::Q_BYTES + cb * 16384, &tmQ, cb * 64, U.h, U.q0[t], U.b,
-                                          q_full_e);
-            auto acquire = [&]() -> uint8_t* {
+            // the previous unit's QK MMAs have read Q (its g_full commit covers every MMA)
+            if (r > 0 && !(ok = pair::wait(g_full, (r - 1) & 1, ab, args.ctl))) break;
+            if (rank == 0) mbar_arrive_expect_tx(q_full, (uint32_t)U.tiles * C::Q_BYTES);
+            if (U.mine) pair::tma_load_5d(sQ, &tmQ, 0, U.h, U.q0, U.b, 0, q_full_e);
+            // ring stages in the order the MMAs consume them: [K_0 | K_1], then [V_j | K_{j+2}]
+            // (halves: V_j all 128 keys x columns [64 rank, 64 rank + 64); K_j keys
+            // [64 rank, 64 rank + 64) x all columns; a missing K_1 / K_{j+2} is not loaded)
+            auto load = [&](int v, int k0, int k1) -> bool {
                 const int s = item % C::NS;
                 const uint32_t ph = (item / C::NS) & 1;
-                if (!pair::wait(&empty[s], ph ^ 1u, ab, args.ctl)) return nullptr;
-                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
-                return ring + s * C::STAGE_BYTES;
+                if (!pair::wait(&empty[s], ph ^ 1u, ab, args.ctl)) return false;
+                const int halves = (v >= 0) + (k0 >= 0) + (k1 >= 0);
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * halves * C::HALF_BYTES);   // both CTAs' bytes
+                const uint32_t fb = pair::map_to(&full[s], 0);
+                uint8_t* st = ring + s * C::STAGE_BYTES;
+                if (v >= 0) pair::tma_load_4d(st, &tmV, (int)rank * 64, U.kvh, v * kTile, U.b, fb);
+                if (k0 >= 0) pair::tma_load_5d(st, &tmK, 0, U.kvh, k0 * kTile + (int)rank * 64, U.b, 0, fb);
+                if (k1 >= 0)
+                    pair::tma_load_5d(st + C::HALF_BYTES, &tmK, 0, U.kvh, k1 * kTile + (int)rank * 64, U.b, 0, fb);
+                ++item;
+                return true;
             };
-            for (int j = 0; j < U.nj && ok; ++j) {
-                // K_j: keys [64 rank, 64 rank + 64) of the tile, all d_k columns (two 64-column boxes)
-                uint8_t* st = acquire();
-                if (!st) { ok = false; break; }
-                const uint32_t fk = pair::map_to(&full[item % C::NS], 0);
-                for (int cb = 0; cb < 2; ++cb)
-                    pair::tma_load_4d(st + cb * 8192, &tmK, cb * 64, U.kvh, j * kTile + (int)rank * 64, U.b, fk);
-                ++item;
-                // V_j: all 128 keys, columns [64 rank, 64 rank + 64)
-                st = acquire();
-                if (!st) { ok = false; break; }
-                pair::tma_load_4d(st, &tmV, (int)rank * 64, U.kvh, j * kTile, U.b, pair::map_to(&full[item % C::NS], 0));
-                ++item;
-            }
-            if (GATE == 2 && ok) {
-                // The gate ring overlays Q and the K/V ring: start once they are idle.
-                ok = pair::wait(attn_done, r & 1, ab, args.ctl);
-                for (int kc = 0; kc < nkc && ok; ++kc, ++gitem) {
-                    const int gs = gitem % C::GNS;
-                    const uint32_t ph = (gitem / C::GNS) & 1;
-                    if (!(ok = pair::wait(&gempty[gs], ph ^ 1u, ab, args.ctl))) break;
-                    const uint32_t gf = pair::map_to(&gfull[gs], 0);
-                    if (rank == 0) mbar_arrive_expect_tx(&gfull[gs], (q_tiles * C::GX_BYTES) + 2 * C::GW_BYTES);
-                    uint8_t* st = smem + gs * C::GSTAGE_BYTES;
-                    for (int t = 0; t < 2; ++t)
-                        if (U.mine[t]) pair::tma_load_3d(st + t * C::GX_BYTES, &tmX, kc * 64, U.q0[t], U.b, gf);
-                    pair::tma_load_2d(st + 2 * C::GX_BYTES, &tmW, U.h * kHD + (int)rank * 64, kc * 64, gf);
-                }
-            }
+            // stage 0: K_0 in the first half, K_1 in the second; stage j + 1: V_j, K_{j+2}
+            ok = load(-1, 0, U.nkv > 1 ? 1 : -1);
+            for (int j = 0; j < U.nkv && ok; ++j) ok = load(j, -1, j + 2 < U.nkv ? j + 2 : -1);
             }   // units
             if (!ok) {
                 // Gave up: the other CTA stops too (both abort flags are raised);
@@ -288,113 +276,73 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             bool ok = true;
             constexpr uint32_t idS = idesc_bf16_f32(256, 128, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(256, kHD, false, true);
-            const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
-            int ibase = 0, gbase = 0;      // running ring-item / gate-chunk counts
-            int sp_base[2] = {0, 0};       // completed s_full / p_full phases per slot
-            auto stage_addr = [&](int it) { return ringa + ((ibase + it) % C::NS) * C::STAGE_BYTES; };
-            auto wait_full = [&](int it) -> bool {
-                const int x = ibase + it;
-                if (!__all_sync(0xffffffffu, pair::wait(&full[x % C::NS], (x / C::NS) & 1, ab, args.ctl)))
-                    return false;
-                tc_fence_after();
-                return true;
-            };
             constexpr uint32_t HI = desc_sw128_hi(1024);   // every operand: 8-row groups 1024 B apart
-            auto issue_S = [&](int t, int j) {
-                const uint32_t a0 = desc_sw128_lo(sQa + t * C::Q_BYTES, 16);
-                const uint32_t b0 = desc_sw128_lo(stage_addr(2 * j), 16);
+            const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
+            int it = 0;                    // running ring-item count
+            int sp[2] = {0, 0};            // completed s_full / p_full phases per buffer
+            auto take = [&]() -> int {     // wait for the next ring item; returns its stage
+                const int s = it % C::NS;
+                if (!__all_sync(0xffffffffu, pair::wait(&full[s], (it / C::NS) & 1, ab, args.ctl))) return -1;
+                tc_fence_after();
+                return s;
+            };
+            auto release = [&](int s) {    // the MMAs just issued are the last readers of stage s
+                pair::commit_both(&empty[s]);
+                ++it;
+            };
+            auto issue_S = [&](int p, int s, uint32_t k_off) {
+                const uint32_t a0 = desc_sw128_lo(sQa, 16);
+                const uint32_t b0 = desc_sw128_lo(ringa + s * C::STAGE_BYTES + k_off, 16);
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
-                    // K-major, 64-column boxes: Q boxes are 128 rows (16 KB), K halves 64 rows (8 KB)
+                    // K-major, 64-column blocks: Q blocks are 128 rows (16 KB), K halves 64 rows (8 KB)
                     const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                     const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    pair::mma_ss(tmem + t * 128, a0 + ka, HI, b0 + kb, HI, idS, kk != 0);
+                    pair::mma_ss(tmem + p * 128, a0 + ka, HI, b0 + kb, HI, idS, kk != 0);
                 }
-                pair::commit_both(&s_full[t]);
+                pair::commit_both(&s_full[p]);
             };
-            auto issue_PV = [&](int t, int j) -> bool {
-                if (!__all_sync(0xffffffffu, pair::wait(&p_full[t], (sp_base[t] + j) & 1, ab, args.ctl)))
-                    return false;
-                tc_fence_after();
+            auto issue_PV = [&](int p, int s, bool acc) {
                 // V half: MN-major, one 64-column block; 16 keys = 2 KB per K step
-                const uint32_t v0 = desc_sw128_lo(stage_addr(2 * j + 1), 8192);
+                const uint32_t v0 = desc_sw128_lo(ringa + s * C::STAGE_BYTES, 8192);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    pair::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
-                                 (j | kk) != 0);
-                return true;
+                    pair::mma_ts(tmem + 256 + p * 128, tmem + p * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
+                                 (acc || kk != 0) ? 1u : 0u);
             };
 
             for (int r = 0; ok; ++r) {
-            const int uix = unit_index(r);
+            if (!(ok = __all_sync(0xffffffffu, pair::wait(&sched_full[r & 3], (r >> 2) & 1, ab, args.ctl)))) break;
+            const int uix = sched[r & 3];
             if (uix >= n_units) break;
             const Unit U = decode_unit(uix);
-            const int nj = U.nj;
-            const int* nkv = U.nkv;
+            const int nkv = U.nkv;
+            // (S_0 / S_1 are free: the previous unit's last PV MMAs, queued before
+            // these, have read its last P. O_p is not written before PV(p) of this
+            // unit, which waits for P_p from threads that first finished the
+            // previous unit's epilogue -- so these QK MMAs overlap that epilogue.)
             ok = __all_sync(0xffffffffu, pair::wait(q_full, r & 1, ab, args.ctl));
-            // S_t and O_t of the previous unit must have been read by its epilogues
-            if (ok && r > 0) ok = __all_sync(0xffffffffu, pair::wait(tmem_free, (r - 1) & 1, ab, args.ctl));
             tc_fence_after();
-            if (ok) ok = wait_full(0);
-            if (ok) {
-                if (U.act[0]) issue_S(0, 0);
-                if (U.act[1]) issue_S(1, 0);
-                pair::commit_both(&empty[ibase % C::NS]);
+            int s;
+            if (ok && (ok = (s = take()) >= 0)) {                               // [K_0 | K_1]
+                issue_S(0, s, 0);
+                if (nkv > 1) issue_S(1, s, C::HALF_BYTES);
+                release(s);
             }
-            for (int j = 0; j < nj && ok; ++j) {
-                if (!(ok = wait_full(2 * j + 1))) break;   // V_j
-                bool k_ready = false;
-                if (j < nkv[0]) {
-                    if (!(ok = issue_PV(0, j))) break;
-                    if (j + 1 < nkv[0]) {
-                        if (!(ok = wait_full(2 * j + 2))) break;
-                        k_ready = true;
-                        issue_S(0, j + 1);
-                    }
-                }
-                if (j < nkv[1]) {
-                    if (!(ok = issue_PV(1, j))) break;
-                }
-                pair::commit_both(&empty[(ibase + 2 * j + 1) % C::NS]);     // V_j done
-                if (j + 1 < nkv[1]) {
-                    if (!k_ready && !(ok = wait_full(2 * j + 2))) break;
-                    k_ready = true;
-                    issue_S(1, j + 1);
-                }
-                if (k_ready) pair::commit_both(&empty[(ibase + 2 * j + 2) % C::NS]);  // K_{j+1} done
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int p = j & 1;
+                if (!(ok = (s = take()) >= 0)) break;                          // [V_j | K_{j+2}]
+                if (!(ok = __all_sync(0xffffffffu,
+                                      pair::wait(&p_full[p], (sp[p] + (j >> 1)) & 1, ab, args.ctl))))
+                    break;
+                tc_fence_after();
+                issue_PV(p, s, j >= 2);
+                if (j + 2 < nkv) issue_S(p, s, C::HALF_BYTES);
+                release(s);
             }
-            // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogues
-            if (ok) pair::commit_both(attn_done);
-            if (GATE == 2) {
-                constexpr uint32_t idG = idesc_bf16_f32(256, kHD, false, true);
-                const uint32_t base = smem_u32(smem);
-                for (int kc = 0; kc < nkc && ok; ++kc) {
-                    const int gi = gbase + kc;
-                    const int gs = gi % C::GNS;
-                    if (!(ok = __all_sync(0xffffffffu, pair::wait(&gfull[gs], (gi / C::GNS) & 1, ab, args.ctl))))
-                        break;
-                    tc_fence_after();
-                    const uint32_t st = base + gs * C::GSTAGE_BYTES;
-                    const uint32_t w0 = desc_sw128_lo(st + 2 * C::GX_BYTES, 8192);
-                    for (int t = 0; t < 2; ++t) {
-                        if (!U.act[t]) continue;
-                        const uint32_t x0 = desc_sw128_lo(st + t * C::GX_BYTES, 16);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            pair::mma_ss(tmem + t * 128, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
-                                         (kc | kk) != 0);
-                    }
-                    pair::commit_both(&gempty[gs]);
-                }
-            }
-            if (ok) {
-                pair::commit_both(&g_full[0]);
-                pair::commit_both(&g_full[1]);
-            }
-            ibase += 2 * nj;
-            if (GATE == 2) gbase += nkc;
-            sp_base[0] += nkv[0];
-            sp_base[1] += nkv[1];
+            if (ok) pair::commit_both(g_full);   // every MMA of the unit issued: signal on completion
+            sp[0] += (nkv + 1) >> 1;
+            sp[1] += nkv >> 1;
             }   // units
             if (!ok) {
                 // Gave up: let every MMA issued so far complete before TMEM is freed.
@@ -415,141 +363,196 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     } else if (warp >= 4) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ================================================================ softmax + epilogue (both CTAs)
-        const int t = (warp - 4) >> 2;        // slot
+        const int p = (warp - 4) >> 2;         // key-tile parity of this warpgroup
         const int qd = warp & 3;               // TMEM lane quadrant of this warp
         const int row = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-        const uint32_t tS = tmem + lane_base + t * 128;
-        const uint32_t tO = tmem + lane_base + 256 + t * 128;
-        const uint32_t p_full_e = pair::map_to(&p_full[t], 0);
-        const uint32_t tmem_free_e = pair::map_to(tmem_free, 0);
+        const uint32_t tS = tmem + lane_base + p * 128;
+        const uint32_t tOp = tmem + lane_base + 256 + p * 128;   // this warpgroup's accumulator
+        const uint32_t tO0 = tmem + lane_base + 256;
+        const uint32_t tO1 = tmem + lane_base + 384;
+        const uint32_t p_full_e = pair::map_to(&p_full[p], 0);
         const float sl2 = kLog2e / sqrtf((float)kHD);
         bool ok = true;
-        int sp_base = 0;     // completed s_full / p_full phases of this slot
-        int g_base = 0;      // completed g_full phases of this slot
+        int sp = 0;          // completed s_full[p] / p_full[p] phases
         for (int r = 0; ok; ++r) {
-        const int uix = unit_index(r);
+        if (!(ok = __all_sync(0xffffffffu, pair::wait_acquire_cluster(&sched_full[r & 3], (r >> 2) & 1, ab,
+                                                                      args.ctl))))
+            break;
+        const int uix = sched[r & 3];
         if (uix >= n_units) break;
-        const Unit U = decode_unit(uix);
-        const int h = U.h, b = U.b;
-        const int nkv = U.nkv[t];
-        const int i = U.q0[t] + row;
-        const long a_pos = off + i;
+        const int nkv = decode_unit(uix).nkv;
+        const long a_pos = off + decode_unit(uix).q0 + row;
         float m = -INFINITY, l = 0.f, x0 = 0.f;
 
-        for (int j = 0; j < nkv; ++j) {
-            ok = __all_sync(0xffffffffu, pair::wait(&s_full[t], (sp_base + j) & 1, ab, args.ctl));
+        int c = 0;   // key tiles of this warpgroup processed in this unit
+        for (int jj = p; jj < nkv; jj += 2, ++c) {
+            ok = __all_sync(0xffffffffu, pair::wait(&s_full[p], (sp + c) & 1, ab, args.ctl));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
             tmem_wait_ld();
 
-            const int kv0 = j * kTile;
+            const int kv0 = jj * kTile;
             // last visible column of this row in this key tile (>= 127: no mask)
             long lim_l = (long)args.Lk - 1 - kv0;
             if (args.causal && a_pos - kv0 < lim_l) lim_l = a_pos - kv0;
-            const int lim = lim_l > 127 ? 127 : (int)lim_l;
+            const int lim = lim_l > 127 ? 127 : (lim_l < -1 ? -1 : (int)lim_l);
             // raw scores; masked ones become -inf (the 1/sqrt(d_k)*log2(e) scale is
             // folded into the exp2 argument below, max commutes with it)
             if (lim < 127) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                        if (q * 32 + e > lim) sr[q][e] = __float_as_uint(-INFINITY);
             }
-            float mx[8];
+            // tile row max (scaled to log2 units; the scale is folded into the exp2 argument)
+            auto tile_max = [&]() -> float {
+                float mx[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[0][e + 8]));
+                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[0][e + 8]));
 #pragma unroll
-            for (int k = 16; k < 128; k += 16) {
+                for (int k = 16; k < 128; k += 16) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    mx[e] = fmax3(mx[e], __uint_as_float(sr[k >> 5][(k & 31) + e]),
-                                  __uint_as_float(sr[(k + 8) >> 5][((k + 8) & 31) + e]));
-            }
-            const float tmax = sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            if (j == 0) x0 = __uint_as_float(sr[0][0]) * sl2;
-            // (a row with no visible key in this tile keeps m; -inf - -inf never reaches exp2)
-            const float m_new = fmaxf(m, tmax);
-            if (j == 0) {
-                m = m_new;
-            } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-                // PV_t(j-1) is complete (S_t(j)'s commit covers it): rescale O_t in place.
-                const float alpha = ex2_approx(m - m_new);
-#pragma unroll
-                for (int cb = 0; cb < kHD / 32; ++cb) {
-                    uint32_t orr[32];
-                    tmem_ld32(tO + cb * 32, orr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(tO + cb * 32, orr);
+                    for (int e = 0; e < 8; ++e)
+                        mx[e] = fmax3(mx[e], __uint_as_float(sr[k >> 5][(k & 31) + e]),
+                                      __uint_as_float(sr[(k + 8) >> 5][((k + 8) & 31) + e]));
                 }
-                l *= alpha;
-                m = m_new;
-            }
-            // P = exp2(s * scale - m): packed bf16 pairs written over S_t[0, 64) for the PV MMA
-            const float neg_m = -m;
-            float2 rs[4];
+                return sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            };
+            // P = exp2(s * scale - mref): packed bf16 pairs written over S_p[0, 64) for
+            // the PV MMA; returns the row sum of P (a row with no visible key so far,
+            // mref = -inf, has all scores -inf and P = 0)
+            auto exps = [&](float mref) -> float {
+                const float neg_m = (mref == -INFINITY) ? 0.f : -mref;
+                float2 rs[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) rs[e] = make_float2(0.f, 0.f);
+                for (int e = 0; e < 4; ++e) rs[e] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
-                    rs[(e >> 1) & 3] = __fadd2_rn(rs[(e >> 1) & 3], make_float2(p0, p1));
-                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][e]), sl2, neg_m));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), sl2, neg_m));
+                        rs[(e >> 1) & 3] = __fadd2_rn(rs[(e >> 1) & 3], make_float2(p0, p1));
+                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + q * 16, pk);
                 }
-                tmem_st16(tS + c * 16, pk);
+                return ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
+            };
+            if (jj == 0) x0 = __uint_as_float(sr[0][0]) * sl2;
+            float rsum;
+            if (c == 0) {
+                m = tile_max();
+                rsum = exps(m);
+            } else {
+                // The running max m is raised only when a tile's max exceeds it by more
+                // than 2^8 (log2 units), so the exponentials usually need only m: compute
+                // them against it while the tile max is reduced alongside, and redo them
+                // in the rare case that the max must move (before P is released).
+                rsum = exps(m);
+                const float tmax = tile_max();
+                if (__any_sync(0xffffffffu, tmax > m + kRescaleThreshold)) {
+                    const float m_new = fmaxf(m, tmax);
+                    // PV(jj-2) is complete (S_p(jj)'s commit covers it): rescale O_p in place.
+                    const float alpha = ex2_approx(m - m_new);
+#pragma unroll
+                    for (int cb = 0; cb < kHD / 32; ++cb) {
+                        uint32_t orr[32];
+                        tmem_ld32(tOp + cb * 32, orr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(tOp + cb * 32, orr);
+                    }
+                    l *= alpha;
+                    m = m_new;
+                    rsum = exps(m);
+                }
             }
-            l += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
+            l += rsum;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) pair::arrive_remote(p_full_e);   // one arrival per warp, 8 per slot and step
+            if (lane == 0) pair::arrive_remote(p_full_e);   // one arrival per warp, 8 per phase
         }
+        sp += (nkv + 1 - p) >> 1;
+        // (the unit is decoded again from its ring slot, valid until unit r + 4 is
+        // claimed, so that none of its fields stays live through the loop above)
+        const Unit U = decode_unit(sched[r & 3]);
+        const int h = U.h, b = U.b;
+        const int i = U.q0 + row;
 
-        if (ok && nkv > 0) ok = pair::wait(&g_full[t], g_base & 1, ab, args.ctl);
+        // elementwise gate: this row's 64 values of sigma(X W_g) for this warpgroup's
+        // output columns, loaded before the last MMAs complete (hides the L2 latency)
+        uint4 gq[GATE == 2 ? 8 : 1];
+        if (GATE != 0 && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
+        if (GATE == 2) {
+            if (U.mine && i < args.Lq) {
+                const uint4* gsrc = reinterpret_cast<const uint4*>(
+                    args.gate_sig + (((long)b * args.Lq + i) * args.Hq + h) * kHD + p * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) gq[q] = __ldg(gsrc + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) gq[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (ok) ok = pair::wait(g_full, r & 1, ab, args.ctl);
         tc_fence_after();
-        // Every thread of this warpgroup takes the same branch (the epilogue has named barriers).
-        const bool ok_epi = named_bar_and(1 + t, 128, ok && nkv > 0);
-        ok = named_bar_and(1 + t, 128, ok);
-        if (ok_epi) {
-            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> global (one 2*d_k-byte row per thread)
-            const float inv_l = 1.0f / l;
+        stats[p * 128 + row] = make_float2(m, l);
+        // Both warpgroups take the same branch (the merge reads both accumulators).
+        ok = named_bar_and(1, 256, ok);
+        if (ok) {
+            // ---- merge the two key halves, gate, bf16, this warpgroup's 64 output columns
+            const float2 o = stats[(p ^ 1) * 128 + row];
+            float mm = fmaxf(m, o.x);
+            if (mm == -INFINITY) mm = 0.f;   // (rows past L_q only)
+            const float a_me = (m == -INFINITY) ? 0.f : ex2_approx(m - mm);
+            const float a_ot = (o.x == -INFINITY) ? 0.f : ex2_approx(o.x - mm);
+            const float inv = 1.0f / (l * a_me + o.y * a_ot);
+            const float s0 = (p == 0 ? a_me : a_ot) * inv;   // weight of O_0
+            const float s1 = (p == 0 ? a_ot : a_me) * inv;   // weight of O_1
+            const bool has1 = nkv > 1;                        // O_1 holds results only then
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
-                if (i < args.Lq) {
+                if (U.mine && i < args.Lq) {
                     const long rows = (long)args.B * args.Lq;
                     const long idx = ((long)b * args.Lq + i) * args.Hq + h;
-                    for (int s = 0; s < args.gate_splits; ++s) gl += args.gate_part[s * rows * args.Hq + idx];
+                    for (int sg = 0; sg < args.gate_splits; ++sg) gl += args.gate_part[sg * rows * args.Hq + idx];
                 }
                 g_head = sigmoid_fast(gl);
             }
-            const bool store = U.mine[t] && i < args.Lq;
-            uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * kHD);
-#pragma unroll 1
-            for (int cb = 0; cb < kHD / 32; ++cb) {
-                uint32_t orr[32];
-                tmem_ld32(tO + cb * 32, orr);
-                uint32_t grr[32];
-                if (GATE == 2) tmem_ld32(tS + cb * 32, grr);
-                tmem_wait_ld();
-                uint32_t packed[16];
+            const bool store = U.mine && i < args.Lq;
+            uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * kHD + p * 64);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float v0 = __uint_as_float(orr[e]) * inv_l;
-                    float v1 = __uint_as_float(orr[e + 1]) * inv_l;
+            for (int cb = 0; cb < 4; ++cb) {
+                const int col = p * 64 + cb * 16;
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tO0 + col, r0);
+                if (has1) tmem_ld16(tO1 + col, r1);
+                tmem_wait_ld();
+                uint32_t packed[8];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    float v0 = __uint_as_float(r0[e]) * s0;
+                    float v1 = __uint_as_float(r0[e + 1]) * s0;
+                    if (has1) {
+                        v0 = fmaf(__uint_as_float(r1[e]), s1, v0);
+                        v1 = fmaf(__uint_as_float(r1[e + 1]), s1, v1);
+                    }
                     if (GATE == 2) {
-                        v0 *= sigmoid_fast(__uint_as_float(grr[e]));
-                        v1 *= sigmoid_fast(__uint_as_float(grr[e + 1]));
+                        // columns cb*16 + e, + 1 of this half: half2 number (e/2) % 4 of uint4 cb*2 + e/8
+                        const uint32_t hw = (&gq[cb * 2 + (e >> 3)].x)[(e >> 1) & 3];
+                        const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
+                        v0 *= g2.x;
+                        v1 *= g2.y;
                     } else if (GATE == 1) {
                         v0 *= g_head;
                         v1 *= g_head;
@@ -558,31 +561,26 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 if (store) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[cb * 4 + q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    for (int q = 0; q < 2; ++q)
+                        dst[cb * 2 + q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
             }
-            // TMEM is no longer needed by this tile: the pair's next unit may start
-            tc_fence_before();
-            named_bar_sync(1 + t, 128);
-            if (row == 0) pair::arrive_remote(tmem_free_e);
-            if (args.sink_part && U.mine[t]) {
-                float p0 = (i < args.Lq) ? ex2_approx(x0 - m) * inv_l : 0.f;
+            if (args.sink_part && p == 0 && U.mine) {
+                // share of key 0 (it lies in key tile 0, a tile of warpgroup 0)
+                float p0 = (i < args.Lq) ? ex2_approx(x0 - mm) * inv : 0.f;
 #pragma unroll
                 for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
-                if (lane == 0) sred[t * 4 + qd] = p0;
-                named_bar_sync(1 + t, 128);
+                if (lane == 0) sred[qd] = p0;
+                named_bar_sync(2, 128);
                 if (row == 0)
-                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + U.q0[t] / kTile] =
-                        sred[t * 4] + sred[t * 4 + 1] + sred[t * 4 + 2] + sred[t * 4 + 3];
+                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + U.q0 / kTile] =
+                        sred[0] + sred[1] + sred[2] + sred[3];
             }
         }
-        if (!ok_epi) {   // no epilogue for this tile in this unit: nothing to read from TMEM
-            named_bar_sync(1 + t, 128);
-            if (row == 0) pair::arrive_remote(tmem_free_e);
-        }
-        sp_base += nkv;
-        g_base += 1;
+        // both warpgroups have read O_0 and O_1 before either starts the next
+        // unit (its first PV MMAs overwrite them)
+        tc_fence_before();
+        named_bar_sync(1, 256);
         }   // units
         tc_fence_before();
     }
@@ -609,34 +607,24 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int GATE>
 cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
     using C = PairCfg;
-    alignas(64) CUtensorMap tmQ, tmK, tmV, tmX, tmW;
+    alignas(64) CUtensorMap tmQ, tmK, tmV;
     const cuuint64_t e = 2;
+    // [B, L, H, d] viewed as (64 columns, H, L, B, 2 column blocks): one request
+    // loads a tile with both 64-column swizzled blocks
     {
-        cuuint64_t d[4] = {(cuuint64_t)kHD, (cuuint64_t)p.Hq, (cuuint64_t)p.Lq, (cuuint64_t)p.B};
-        cuuint64_t st[3] = {kHD * e, (cuuint64_t)p.Hq * kHD * e, (cuuint64_t)p.Lq * p.Hq * kHD * e};
-        cuuint32_t box[4] = {64, 1, 128, 1};
-        if (!make_map(&tmQ, p.Q, 4, d, st, box)) return cudaErrorInvalidValue;
+        cuuint64_t d[5] = {64, (cuuint64_t)p.Hq, (cuuint64_t)p.Lq, (cuuint64_t)p.B, 2};
+        cuuint64_t st[4] = {kHD * e, (cuuint64_t)p.Hq * kHD * e, (cuuint64_t)p.Lq * p.Hq * kHD * e, 128};
+        cuuint32_t box[5] = {64, 1, 128, 1, 2};
+        if (!make_map(&tmQ, p.Q, 5, d, st, box)) return cudaErrorInvalidValue;
     }
     {
-        cuuint64_t d[4] = {(cuuint64_t)kHD, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B};
-        cuuint64_t st[3] = {kHD * e, (cuuint64_t)p.Hkv * kHD * e, (cuuint64_t)p.Lk * p.Hkv * kHD * e};
-        cuuint32_t box_k[4] = {64, 1, 64, 1};     // half a key tile
-        cuuint32_t box_v[4] = {64, 1, 128, 1};    // a key tile, half the columns
-        if (!make_map(&tmK, p.K, 4, d, st, box_k)) return cudaErrorInvalidValue;
-        if (!make_map(&tmV, p.V, 4, d, st, box_v)) return cudaErrorInvalidValue;
-    }
-    if (GATE == 2) {
-        cuuint64_t d[3] = {(cuuint64_t)p.d_model, (cuuint64_t)p.Lq, (cuuint64_t)p.B};
-        cuuint64_t st[2] = {(cuuint64_t)p.d_model * e, (cuuint64_t)p.Lq * p.d_model * e};
-        cuuint32_t box[3] = {64, 128, 1};
-        if (!make_map(&tmX, p.X, 3, d, st, box)) return cudaErrorInvalidValue;
-        cuuint64_t dw[2] = {(cuuint64_t)p.Hq * kHD, (cuuint64_t)p.d_model};
-        cuuint64_t sw[1] = {(cuuint64_t)p.Hq * kHD * e};
-        cuuint32_t bw[2] = {64, 64};
-        if (!make_map(&tmW, p.Wg, 2, dw, sw, bw)) return cudaErrorInvalidValue;
-    } else {
-        tmX = tmQ;  // unused
-        tmW = tmQ;
+        cuuint64_t d[5] = {64, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B, 2};
+        cuuint64_t st[4] = {kHD * e, (cuuint64_t)p.Hkv * kHD * e, (cuuint64_t)p.Lk * p.Hkv * kHD * e, 128};
+        cuuint32_t box_k[5] = {64, 1, 64, 1, 2};     // half a key tile, all columns
+        if (!make_map(&tmK, p.K, 5, d, st, box_k)) return cudaErrorInvalidValue;
+        cuuint64_t dv[4] = {(cuuint64_t)kHD, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B};
+        cuuint32_t box_v[4] = {64, 1, 128, 1};       // a key tile, half the columns
+        if (!make_map(&tmV, p.V, 4, dv, st, box_v)) return cudaErrorInvalidValue;
     }
     PairArgs a;
     a.B = p.B;
@@ -647,9 +635,11 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.d_model = p.d_model;
     a.causal = p.causal;
     a.n_qtiles = (p.Lq + kTile - 1) / kTile;
-    a.n_quads = (a.n_qtiles + 3) / 4;
+    a.n_blk = (a.n_qtiles + 1) / 2;
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
+    a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
+    a.sched_counter = reinterpret_cast<int*>(ws + w.sched);
     a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
@@ -678,10 +668,21 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
         if (n < 1) return cudaErrorInvalidConfiguration;
         max_pairs = n;
     }
-    const long units = (long)a.n_quads * p.Hq * p.B;
+    const long units = (long)a.n_blk * p.Hq * p.B;
     const long pairs = units < max_pairs ? units : max_pairs;
-    prefill_pair_kernel<GATE><<<(unsigned)(2 * pairs), kThreads, C::SMEM_BYTES, s>>>(tmQ, tmK, tmV, tmX, tmW, a);
-    return cudaGetLastError();
+    // With a gate, the gate kernel just before this one lets it start early
+    // (programmatic dependent launch); the epilogues wait for it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = GATE != 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE>, tmQ, tmK, tmV, a);
 }
 
 }  // namespace

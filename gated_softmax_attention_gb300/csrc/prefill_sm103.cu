@@ -4,17 +4,17 @@
 //   S_t = Q_t K_j^T                      tcgen05.mma (A, B in shared memory)
 //   P_t = exp2(S_t log2(e)/sqrt(d_k) - m_t)   online softmax, one thread per row
 //   O_t += P_t V_j                       tcgen05.mma with P read from TMEM
-//   G_t = X_t W_g[:, h*d_k:(h+1)*d_k]    elementwise gate GEMM, same CTA
-//   out_t = O_t / l_t (.) sigmoid(G_t)   epilogue: bf16, TMA store
+//   out_t = O_t / l_t (.) g_t            epilogue: bf16 rows straight to HBM
+// where g = sigma(X W_g) (elementwise gate, fp16, computed ahead by the gate
+// GEMM) or sigma(x_i . w_h) (headwise gate, logits computed ahead).
 // ("GatedAttention [2025]", sec. 1.2.1 SDPA and sec. 1.2.2 the gate
 //  Y' = Y (.) sigma(X W); "10 . 门控", sec. 3.2: G1 gates each head's SDPA
 //  output before the heads are concatenated.) The ungated output never leaves
 //  the SM.
 //
 // Warp roles (384 threads):
-//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ... and
-//                the gate chunks (X_t [128 x 64], W_g [64 x d_k]) through a
-//                ring of NS shared-memory stages;
+//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ...
+//                through a ring of NS shared-memory stages;
 //   warp 1       TMEM allocation; issues every tcgen05.mma / commit (the
 //                whole warp runs the loop, one elected lane issues);
 //   warps 2, 3   spare;
@@ -29,18 +29,21 @@
 // and overwrite S_t with P_t without further waits.
 //
 // TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d_k)
-//                     O_1 [384,384+d_k); P_t is packed bf16 in S_t [0,64);
-//                     G_t (elementwise gate) reuses S_t after the last PV_t.
+//                     O_1 [384,384+d_k); P_t is packed bf16 in S_t [0,64).
 //
 // The causal mask is aligned bottom-right (query i at absolute position
 // L_k - L_q + i); key tiles entirely above the diagonal are never loaded.
-// The grid is persistent (one CTA per SM): units, numbered heaviest first,
-// are dealt to the CTAs in snake order so that heavy and light causal units
-// share an SM; barrier phases carry over from one unit to the next.
+// The grid is persistent (one CTA per SM): each CTA's producer claims the
+// next unit from a counter in global memory (units numbered heaviest first,
+// so the claims form a longest-first greedy schedule that keeps the SMs
+// evenly loaded, also when some CTAs start late) and hands it to the other
+// roles through a small ring in shared memory; barrier phases carry over
+// from one unit to the next.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
+#include <cuda_fp16.h>
 
 namespace gsdpa {
 namespace {
@@ -59,19 +62,12 @@ template <int HD, int GATE>
 struct PrefillCfg {
     static constexpr uint32_t Q_BYTES = kTile * HD * 2;   // one query tile
     static constexpr uint32_t KV_BYTES = kTile * HD * 2;
-    static constexpr uint32_t GX_BYTES = kTile * 64 * 2;
-    static constexpr uint32_t GW_BYTES = 64 * HD * 2;
     static constexpr uint32_t STAGE_BYTES = KV_BYTES;
     static constexpr int NS = (HD == 128) ? 4 : 8;
     static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
     static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
-    // Gate phase (after every attention MMA has completed): the Q tiles and the
-    // K/V ring are reused as a ring of GNS stages, each X_0 | X_1 | W_g chunk.
-    static constexpr uint32_t GSTAGE_BYTES = 2 * GX_BYTES + GW_BYTES;
-    static constexpr int GNS = (int)(OFF_BAR / GSTAGE_BYTES) < 4 ? (int)(OFF_BAR / GSTAGE_BYTES) : 4;
-    static_assert(GNS >= 2, "gate ring needs two stages");
-    static constexpr int NBAR = 2 * NS + 2 * 4 + 10;
+    static constexpr int NBAR = 2 * NS + 11;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -80,6 +76,8 @@ struct PrefillArgs {
     int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_pairs;
     const float* gate_part;  // headwise: [splits, B*Lq, Hq]
     int gate_splits;
+    const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*HD]
+    int* sched_counter;      // next unit to claim (0 at launch)
     float* sink_part;        // [B, Hq, n_qtiles] or null
     __nv_bfloat16* O;        // [B, Lq, Hq, HD]
     WaitCtl ctl;
@@ -96,9 +94,7 @@ __device__ __forceinline__ float sigmoidf_fast(float x) {
 template <int HD, int GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmX,
-               const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmO,
-               const PrefillArgs args) {
+               const __grid_constant__ CUtensorMap tmV, const PrefillArgs args) {
     using C = PrefillCfg<HD, GATE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,35 +106,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint64_t* q_full = bars + 2 * C::NS;
     uint64_t* s_full = q_full + 1;         // [2] per query tile
     uint64_t* p_full = q_full + 3;         // [2]
-    uint64_t* g_full = q_full + 5;         // [2]: all MMAs of the tile (and its gate GEMM) done
+    uint64_t* g_full = q_full + 5;         // [2]: every MMA of the unit done
     uint64_t* drain = q_full + 7;
-    uint64_t* attn_done = q_full + 8;      // every attention MMA has completed
-    uint64_t* gfull = q_full + 9;          // [4] gate ring
-    uint64_t* gempty = q_full + 13;        // [4]
-    uint64_t* tmem_free = q_full + 17;     // both epilogues have read O and G out of TMEM
+    uint64_t* sched_full = q_full + 8;     // [4] unit r published in sched[r % 4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
+    volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // ---- persistent schedule: the units, numbered heaviest first (last query
-    // pair first when causal), are dealt to the CTAs in snake order -- CTA c
-    // takes units c, 2G-1-c, 2G+c, 4G-1-c, ... -- so that heavy and light
-    // units share an SM.
+    // ---- units, numbered heaviest first (last query pair first when causal)
     const int per_pair = args.Hq * args.B;
     const int n_units = args.n_pairs * per_pair;
     const long off = (long)args.Lk - args.Lq;
-    const int nkc = (args.d_model + 63) / 64;
     struct Unit {
         int pr, h, b, kvh, nj;
         int q0[2], nkv[2];
         bool act[2];
-    };
-    auto unit_index = [&](int r) -> int {
-        const int G = gridDim.x, c = blockIdx.x;
-        return (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
     };
     auto decode_unit = [&](int u) -> Unit {
         Unit x;
@@ -174,22 +160,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(&g_full[t], 1);
         }
         mbar_init(drain, 1);
-        mbar_init(attn_done, 1);
-        mbar_init(tmem_free, 2);
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&gfull[s], 1);
-            mbar_init(&gempty[s], 1);
-        }
+        for (int k = 0; k < 4; ++k) mbar_init(&sched_full[k], 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmO);
-        if (GATE == 2) {
-            tma_prefetch_desc(&tmX);
-            tma_prefetch_desc(&tmW);
-        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -204,24 +180,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            uint32_t armed = 0, armed_phase = 0, garmed = 0, garmed_phase = 0;
+            uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
-            int item = 0, gitem = 0;   // running counts of ring items / gate chunks (phases carry over units)
+            int item = 0;   // running count of ring items (phases carry over units)
             for (int r = 0; ok; ++r) {
-            const int uix = unit_index(r);
+            // claim the next unit and publish it to the MMA and softmax roles (the
+            // slot's previous unit, r - 4, was read long ago: this thread has seen
+            // every MMA of unit r - 2 complete)
+            const int uix = atomicAdd(args.sched_counter, 1);
+            sched[r & 3] = uix;
+            mbar_arrive(&sched_full[r & 3]);
             if (uix >= n_units) break;
             const Unit U = decode_unit(uix);
             const int h = U.h, b = U.b, kvh = U.kvh, nj = U.nj;
             const int* q0 = U.q0;
             const bool* act = U.act;
-            // every MMA of the previous unit must be complete (its gate ring overlays Q and K/V);
-            // its g_full[1] commit is the last of the unit and covers all of them
+            // the previous unit's S MMAs have read Q: its g_full[1] commit is the
+            // last of the unit and covers all of them
             if (r > 0 && !(ok = mbar_wait(&g_full[1], (r - 1) & 1, abort_flag, args.ctl))) break;
             mbar_arrive_expect_tx(q_full, (act[1] ? 2 : 1) * C::Q_BYTES);
             for (int t = 0; t < 2; ++t)
-                if (act[t])
-                    for (int cb = 0; cb < HD / 64; ++cb)
-                        tma_load_4d(sQ + t * C::Q_BYTES + cb * 16384, &tmQ, cb * 64, h, q0[t], b, q_full);
+                if (act[t]) tma_load_5d(sQ + t * C::Q_BYTES, &tmQ, 0, h, q0[t], b, 0, q_full);
 
             auto acquire = [&](uint32_t bytes) -> uint8_t* {
                 const int s = item % C::NS;
@@ -236,27 +215,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     uint8_t* st = acquire(C::KV_BYTES);
                     if (!st) { ok = false; break; }
-                    const CUtensorMap* m = kv ? &tmV : &tmK;
-                    for (int cb = 0; cb < HD / 64; ++cb)
-                        tma_load_4d(st + cb * 16384, m, cb * 64, kvh, j * kTile, b, &full[item % C::NS]);
+                    tma_load_5d(st, kv ? &tmV : &tmK, 0, kvh, j * kTile, b, 0, &full[item % C::NS]);
                     ++item;
-                }
-            }
-            if (GATE == 2 && ok) {
-                // The gate ring overlays Q and the K/V ring: start once they are idle.
-                ok = mbar_wait(attn_done, r & 1, abort_flag, args.ctl);
-                for (int kc = 0; kc < nkc && ok; ++kc, ++gitem) {
-                    const int gs = gitem % C::GNS;
-                    const uint32_t ph = (gitem / C::GNS) & 1;
-                    if (!(ok = mbar_wait(&gempty[gs], ph ^ 1u, abort_flag, args.ctl))) break;
-                    mbar_arrive_expect_tx(&gfull[gs], (act[1] ? 2 : 1) * C::GX_BYTES + C::GW_BYTES);
-                    garmed |= 1u << gs;
-                    garmed_phase = (garmed_phase & ~(1u << gs)) | (ph << gs);
-                    uint8_t* st = smem + gs * C::GSTAGE_BYTES;
-                    for (int t = 0; t < 2; ++t)
-                        if (act[t]) tma_load_3d(st + t * C::GX_BYTES, &tmX, kc * 64, q0[t], b, &gfull[gs]);
-                    for (int cb = 0; cb < HD / 64; ++cb)
-                        tma_load_2d(st + 2 * C::GX_BYTES + cb * 8192, &tmW, h * HD + cb * 64, kc * 64, &gfull[gs]);
                 }
             }
             }   // units
@@ -267,8 +227,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
                 for (int s = 0; s < C::NS; ++s)
                     if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, c2);
-                for (int s = 0; s < 4; ++s)
-                    if (garmed & (1u << s)) mbar_wait(&gfull[s], (garmed_phase >> s) & 1u, &never, c2);
             }
         }
     } else if (warp == 1) {
@@ -278,7 +236,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(128, HD, false, true);
             const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
-            int ibase = 0, gbase = 0;      // running ring-item / gate-chunk counts
+            int ibase = 0;                 // running ring-item count
             int sp_base[2] = {0, 0};       // completed s_full / p_full phases per tile
             auto stage_addr = [&](int item) { return ringa + ((ibase + item) % C::NS) * C::STAGE_BYTES; };
             auto wait_full = [&](int item) -> bool {
@@ -312,15 +270,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             };
 
             for (int r = 0; ok; ++r) {
-            const int uix = unit_index(r);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sched_full[r & 3], (r >> 2) & 1, abort_flag, args.ctl))))
+                break;
+            const int uix = sched[r & 3];
             if (uix >= n_units) break;
             const Unit U = decode_unit(uix);
             const int nj = U.nj;
             const int* nkv = U.nkv;
             const bool* act = U.act;
+            // (the S columns are free: the previous unit's last PV MMAs, queued before
+            // these, have read its last P. O_t is not written before PV_t(0), which
+            // waits for P_t(0) from the threads that first finish the epilogue of the
+            // previous unit -- so this unit's QK MMAs overlap that epilogue.)
             ok = __all_sync(0xffffffffu, mbar_wait(q_full, r & 1, abort_flag, args.ctl));
-            // S_t and O_t of the previous unit (G_t, O_t) must have been read by its epilogue
-            if (ok && r > 0) ok = __all_sync(0xffffffffu, mbar_wait(tmem_free, (r - 1) & 1, abort_flag, args.ctl));
             tc_fence_after();
             if (ok) ok = wait_full(0);
             if (ok) {
@@ -350,36 +312,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 if (k_ready) mma_commit_elect(&empty[(ibase + 2 * j + 2) % C::NS]);  // K_{j+1} done
             }
-            // gate GEMM G_t = X_t W_g[:, cols(h)] into the S_t columns, then signal the epilogue
-            if (ok) mma_commit_elect(attn_done);
-            if (GATE == 2) {
-                constexpr uint32_t idG = idesc_bf16_f32(128, HD, false, true);
-                const uint32_t base = smem_u32(smem);
-                for (int kc = 0; kc < nkc && ok; ++kc) {
-                    const int gi = gbase + kc;
-                    const int gs = gi % C::GNS;
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&gfull[gs], (gi / C::GNS) & 1, abort_flag, args.ctl))))
-                        break;
-                    tc_fence_after();
-                    const uint32_t st = base + gs * C::GSTAGE_BYTES;
-                    const uint32_t w0 = desc_sw128_lo(st + 2 * C::GX_BYTES, 8192);
-                    for (int t = 0; t < 2; ++t) {
-                        if (!act[t]) continue;
-                        const uint32_t x0 = desc_sw128_lo(st + t * C::GX_BYTES, 16);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss_elect(tmem + t * 128, x0 + kk * (32 >> 4), HI, w0 + kk * (2048 >> 4), HI, idG,
-                                        (kc | kk) != 0);
-                    }
-                    mma_commit_elect(&gempty[gs]);
-                }
-            }
+            // every MMA of the unit issued: signal the epilogues (and the producer) on completion
             if (ok) {
                 mma_commit_elect(&g_full[0]);
                 mma_commit_elect(&g_full[1]);
             }
             ibase += 2 * nj;
-            if (GATE == 2) gbase += nkc;
             sp_base[0] += nkv[0];
             sp_base[1] += nkv[1];
             }   // units
@@ -407,7 +345,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         int sp_base = 0;     // completed s_full / p_full phases of this tile
         int g_base = 0;      // completed g_full phases of this tile
         for (int r = 0; ok; ++r) {
-        const int uix = unit_index(r);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sched_full[r & 3], (r >> 2) & 1, abort_flag, args.ctl)))) break;
+        const int uix = sched[r & 3];
         if (uix >= n_units) break;
         const Unit U = decode_unit(uix);
         const int pr = U.pr, h = U.h, b = U.b;
@@ -493,13 +432,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_arrive(&p_full[t]);
         }
 
+        // elementwise gate: this row's d_k values of sigma(X W_g), loaded before the
+        // last MMAs complete so that the L2 / HBM latency hides behind the wait
+        uint4 gq[GATE == 2 ? HD / 8 : 1];
+        if (GATE != 0 && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
+        if (GATE == 2) {
+            if (i < args.Lq && nkv[t] > 0) {
+                const uint4* gsrc =
+                    reinterpret_cast<const uint4*>(args.gate_sig + (((long)b * args.Lq + i) * args.Hq + h) * HD);
+#pragma unroll
+                for (int q = 0; q < HD / 8; ++q) gq[q] = __ldg(gsrc + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < HD / 8; ++q) gq[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         if (ok && nkv[t] > 0) ok = mbar_wait(&g_full[t], g_base & 1, abort_flag, args.ctl);
         tc_fence_after();
         // Every thread of this warpgroup takes the same branch (the epilogue has named barriers).
         const bool ok_epi = named_bar_and(1 + t, 128, ok && nkv[t] > 0);
         ok = named_bar_and(1 + t, 128, ok);
         if (ok_epi) {
-            // ---- epilogue: out = O / l (.) sigmoid(gate) -> bf16 -> global (one 2*d_k-byte row per thread)
+            // ---- epilogue: out = O / l (.) gate -> bf16 -> global (one 2*d_k-byte row per thread)
             const float inv_l = 1.0f / l;
             float g_head = 1.0f;
             if (GATE == 1) {
@@ -516,16 +470,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             for (int cb = 0; cb < HD / 32; ++cb) {
                 uint32_t orr[32];
                 tmem_ld32(tO + cb * 32, orr);
-                uint32_t grr[32];
-                if (GATE == 2) tmem_ld32(tS + cb * 32, grr);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float v0 = __uint_as_float(orr[e]) * inv_l;
                     float v1 = __uint_as_float(orr[e + 1]) * inv_l;
                     if (GATE == 2) {
-                        v0 *= sigmoidf_fast(__uint_as_float(grr[e]));
-                        v1 *= sigmoidf_fast(__uint_as_float(grr[e + 1]));
+                        // columns cb*32 + e, + 1: half2 number (e/2) % 4 of uint4 cb*4 + e/8
+                        const uint32_t hw = (&gq[cb * 4 + (e >> 3)].x)[(e >> 1) & 3];
+                        const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
+                        v0 *= g2.x;
+                        v1 *= g2.y;
                     } else if (GATE == 1) {
                         v0 *= g_head;
                         v1 *= g_head;
@@ -533,10 +488,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     packed[cb * 16 + e / 2] = pack_bf16x2(v0, v1);
                 }
             }
-            // TMEM is no longer needed by this tile: the next unit's MMAs may start
-            tc_fence_before();
-            named_bar_sync(1 + t, 128);
-            if (row == 0) mbar_arrive(tmem_free);
             if (i < args.Lq) {
                 uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * HD);
 #pragma unroll
@@ -553,10 +504,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + 2 * pr + t] =
                         sred[t * 4] + sred[t * 4 + 1] + sred[t * 4 + 2] + sred[t * 4 + 3];
             }
-        }
-        if (!ok_epi) {   // no epilogue for this tile in this unit: nothing to read from TMEM
-            named_bar_sync(1 + t, 128);
-            if (row == 0) mbar_arrive(tmem_free);
         }
         sp_base += nkv[t];
         g_base += 1;
@@ -585,34 +532,22 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int HD, int GATE>
 cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
     using C = PrefillCfg<HD, GATE>;
-    alignas(64) CUtensorMap tmQ, tmK, tmV, tmX, tmW, tmO;
+    alignas(64) CUtensorMap tmQ, tmK, tmV;
     const cuuint64_t e = 2;
+    // [B, L, H, d] viewed as (64 columns, H, L, B, d/64 blocks): one request
+    // loads a 128-row tile with all d_k columns as d_k/64 swizzled blocks
     {
-        cuuint64_t d[4] = {(cuuint64_t)HD, (cuuint64_t)p.Hq, (cuuint64_t)p.Lq, (cuuint64_t)p.B};
-        cuuint64_t st[3] = {HD * e, (cuuint64_t)p.Hq * HD * e, (cuuint64_t)p.Lq * p.Hq * HD * e};
-        cuuint32_t box[4] = {64, 1, 128, 1};
-        if (!make_map(&tmQ, p.Q, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-        if (!make_map(&tmO, p.O, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        cuuint64_t d[5] = {64, (cuuint64_t)p.Hq, (cuuint64_t)p.Lq, (cuuint64_t)p.B, (cuuint64_t)(HD / 64)};
+        cuuint64_t st[4] = {HD * e, (cuuint64_t)p.Hq * HD * e, (cuuint64_t)p.Lq * p.Hq * HD * e, 128};
+        cuuint32_t box[5] = {64, 1, 128, 1, HD / 64};
+        if (!make_map(&tmQ, p.Q, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
-        cuuint64_t d[4] = {(cuuint64_t)HD, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B};
-        cuuint64_t st[3] = {HD * e, (cuuint64_t)p.Hkv * HD * e, (cuuint64_t)p.Lk * p.Hkv * HD * e};
-        cuuint32_t box[4] = {64, 1, 128, 1};
-        if (!make_map(&tmK, p.K, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-        if (!make_map(&tmV, p.V, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    }
-    if (GATE == 2) {
-        cuuint64_t d[3] = {(cuuint64_t)p.d_model, (cuuint64_t)p.Lq, (cuuint64_t)p.B};
-        cuuint64_t st[2] = {(cuuint64_t)p.d_model * e, (cuuint64_t)p.Lq * p.d_model * e};
-        cuuint32_t box[3] = {64, 128, 1};
-        if (!make_map(&tmX, p.X, 3, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-        cuuint64_t dw[2] = {(cuuint64_t)p.Hq * HD, (cuuint64_t)p.d_model};
-        cuuint64_t sw[1] = {(cuuint64_t)p.Hq * HD * e};
-        cuuint32_t bw[2] = {64, 64};
-        if (!make_map(&tmW, p.Wg, 2, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    } else {
-        tmX = tmQ;  // unused
-        tmW = tmQ;
+        cuuint64_t d[5] = {64, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B, (cuuint64_t)(HD / 64)};
+        cuuint64_t st[4] = {HD * e, (cuuint64_t)p.Hkv * HD * e, (cuuint64_t)p.Lk * p.Hkv * HD * e, 128};
+        cuuint32_t box[5] = {64, 1, 128, 1, HD / 64};
+        if (!make_map(&tmK, p.K, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!make_map(&tmV, p.V, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     PrefillArgs a;
     a.B = p.B;
@@ -626,6 +561,8 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.n_pairs = (a.n_qtiles + 1) / 2;
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
+    a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
+    a.sched_counter = reinterpret_cast<int*>(ws + w.sched);
     a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
@@ -646,8 +583,19 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     }
     const long units = (long)a.n_pairs * p.Hq * p.B;
     const long grid = units < rt.num_sms ? units : rt.num_sms;   // persistent: one CTA per SM
-    prefill_kernel<HD, GATE><<<(unsigned)grid, kThreads, C::SMEM_BYTES, s>>>(tmQ, tmK, tmV, tmX, tmW, tmO, a);
-    return cudaGetLastError();
+    // With a gate, the gate kernel just before this one lets it start early
+    // (programmatic dependent launch); the epilogues wait for it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = GATE != 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE>, tmQ, tmK, tmV, a);
 }
 
 }  // namespace

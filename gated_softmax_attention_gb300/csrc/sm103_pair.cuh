@@ -53,6 +53,23 @@ __device__ __forceinline__ uint32_t map_to(const void* p, uint32_t rank) {
 __device__ __forceinline__ void arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
+// Cluster-scope release arrive: orders this thread's earlier stores to the
+// other CTA's shared memory before the arrival (rare: about a thousand cycles).
+__device__ __forceinline__ void arrive_remote_release(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// Wait with cluster-scope acquire (pairs with arrive_remote_release).
+__device__ __forceinline__ bool try_wait_acquire_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void store_remote_u32(uint32_t addr_cluster, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
@@ -68,6 +85,26 @@ static __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, cons
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*ab.local) return false;
+            if (globaltimer_ns() - t0 > ctl.limit_ns) {
+                atomicOr(ctl.err, ERR_WAIT_TIMEOUT);
+                *ab.local = 1;
+                store_remote_u32(ab.peer, 1u);
+                __threadfence_block();
+                return false;
+            }
+        }
+    }
+}
+
+// wait() with cluster-scope acquire, for barriers armed by arrive_remote_release.
+static __device__ __forceinline__ bool wait_acquire_cluster(uint64_t* bar, uint32_t parity, const PairAbort& ab,
+                                                            const WaitCtl& ctl) {
+    if (try_wait_acquire_cluster(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (try_wait_acquire_cluster(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*ab.local) return false;
             if (globaltimer_ns() - t0 > ctl.limit_ns) {
@@ -103,6 +140,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, int c4,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
 

@@ -56,11 +56,15 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # elementwise bf16 prefill keeps the gate in-CTA: no workspace without sink
-    assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", False, gb.BF16) == 0
-    # sink partials: B*H_q*ceil(L/128) floats, 256-aligned
+    # bf16 prefill: one 256-byte slot for the unit counter of the dynamic schedule
+    counter = 256
+    assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "none", False, gb.BF16) == counter
+    # elementwise bf16 prefill: plus the gate sigma(X W_g) as fp16, [B*L_q, H_q*d_k]
+    gate = 2 * 2 * 2048 * 16 * 128
+    assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", False, gb.BF16) == counter + gate
+    # plus the sink partials: B*H_q*ceil(L/128) floats, 256-aligned
     n = gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", True, gb.BF16)
-    assert n >= 2 * 16 * 16 * 4 and n % 256 == 0
+    assert n >= counter + gate + 2 * 16 * 16 * 4 and n % 256 == 0
     # headwise bf16: split-K gate logits [splits, B*L, H_q]
     n = gb.workspace_bytes(1, 4096, 4096, 4096, 32, 4, 128, "headwise", False, gb.BF16)
     assert n >= 4096 * 32 * 4 and n % 256 == 0
