@@ -29,6 +29,7 @@ SIGNATURES = {
     "gsdpa_check_device_error": (_I, [_VP]),
     "gsdpa_status_string": (ctypes.c_char_p, [_I]),
     "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+    "gsdpa_wait_self_test": (_I, [_VP]),
     "gated_sdpa_decode_noalloc": (_I, [_VP] * 7 + [_I] * 7 + [_VP]),
     "gsdpa_decode_noalloc_max_scratch": (_SZ, []),
 }
@@ -74,6 +75,13 @@ def workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise", wa
 
 def set_wait_limit_ns(ns: int) -> None:
     load().gsdpa_set_wait_limit_ns(int(ns))
+
+
+def wait_self_test(stream=None) -> int:
+    """Enqueue the bounded-wait diagnostic (a wait nothing completes); returns the launch status."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().gsdpa_wait_self_test(ctypes.c_void_p(s.cuda_stream)))
 
 
 def check_device_error(stream=None) -> int:

@@ -3,6 +3,7 @@
 // device error word that bounded waits report into.
 #include "gsdpa.h"
 #include "gsdpa_internal.h"
+#include "sm103_ptx.cuh"
 
 #include <atomic>
 #include <cstdint>
@@ -183,6 +184,19 @@ __global__ void sink_finalize_kernel(const float* __restrict__ part, float* __re
     sink[idx] = s * inv_lq;
 }
 
+// One thread waits on an mbarrier that nothing arrives on: the bounded wait
+// gives up after the current limit and records ERR_WAIT_TIMEOUT.
+__global__ void wait_self_test_kernel(WaitCtl ctl) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        mbar_wait(&bar, 0, &abort_flag, ctl);
+    }
+}
+
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s) {
     const int n = p.B * p.Hq;
     sink_finalize_kernel<<<(n + 127) / 128, 128, 0, s>>>(reinterpret_cast<const float*>(ws + w.sink_part), p.sink, n,
@@ -305,6 +319,16 @@ const char* gsdpa_status_string(int status) {
         case GSDPA_ERR_DEVICE_TIMEOUT: return "GSDPA_ERR_DEVICE_TIMEOUT";
         default: return "GSDPA_ERR_UNKNOWN";
     }
+}
+
+int gsdpa_wait_self_test(void* stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return GSDPA_ERR_LAUNCH;
+    WaitCtl ctl;
+    ctl.err = dev->err;
+    ctl.limit_ns = g_wait_limit_ns.load();
+    wait_self_test_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctl);
+    return cudaGetLastError() == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
 }
 
 int gsdpa_set_wait_limit_ns(unsigned long long ns) {

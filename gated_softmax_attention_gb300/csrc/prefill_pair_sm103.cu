@@ -376,9 +376,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         bool ok = true;
         int sp = 0;          // completed s_full[p] / p_full[p] phases
         for (int r = 0; ok; ++r) {
-        if (!(ok = __all_sync(0xffffffffu, pair::wait_acquire_cluster(&sched_full[r & 3], (r >> 2) & 1, ab,
-                                                                      args.ctl))))
-            break;
+        // (both warpgroups leave together or not at all: the merge has named barriers)
+        ok = named_bar_and(1, 256, pair::wait_acquire_cluster(&sched_full[r & 3], (r >> 2) & 1, ab, args.ctl));
+        if (!ok) break;
         const int uix = sched[r & 3];
         if (uix >= n_units) break;
         const int nkv = decode_unit(uix).nkv;

@@ -345,7 +345,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         int sp_base = 0;     // completed s_full / p_full phases of this tile
         int g_base = 0;      // completed g_full phases of this tile
         for (int r = 0; ok; ++r) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sched_full[r & 3], (r >> 2) & 1, abort_flag, args.ctl)))) break;
+        // (the warpgroup leaves together or not at all: its epilogue has named barriers)
+        ok = named_bar_and(1 + t, 128, mbar_wait(&sched_full[r & 3], (r >> 2) & 1, abort_flag, args.ctl));
+        if (!ok) break;
         const int uix = sched[r & 3];
         if (uix >= n_units) break;
         const Unit U = decode_unit(uix);

@@ -183,6 +183,17 @@ GSDPA_API size_t gsdpa_decode_noalloc_max_scratch(void);
  */
 GSDPA_API int gsdpa_set_wait_limit_ns(unsigned long long ns);
 
+/*
+ * Diagnostic, not part of the operation: enqueues on `stream` one thread that
+ * waits, with the current wait limit, on a barrier that nothing ever
+ * completes. The wait gives up and records the timeout in the device error
+ * word, which the next gsdpa_check_device_error() returns as
+ * GSDPA_ERR_DEVICE_TIMEOUT (and clears). Lets a test exercise the bounded-wait
+ * path without faulting or hanging the device. Returns GSDPA_OK or
+ * GSDPA_ERR_LAUNCH.
+ */
+GSDPA_API int gsdpa_wait_self_test(void* stream);
+
 #ifdef __cplusplus
 }
 #endif
