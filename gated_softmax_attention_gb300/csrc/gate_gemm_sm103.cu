@@ -43,6 +43,7 @@ struct GateArgs {
     float* out;          // [splits, rows, cols]
     int rows, cols, d_model;
     int row_tiles, col_tiles, splits, nkc;
+    ZeroJob zero;        // per-call state of the attention kernel, zeroed by CTA 0
     WaitCtl ctl;
 };
 
@@ -63,6 +64,12 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    if (blockIdx.x == 0 && args.zero.n > 0) {
+        // the attention kernel's per-call state; visible before it can start
+        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
     pdl_trigger();   // the consumer (attention or decode) may start; it reads the logits late
     const int u = blockIdx.x;
     const int rt = u % args.row_tiles;
@@ -205,7 +212,8 @@ bool make_map2d(CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t d1, 
 }
 
 template <int NT>
-cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
+cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s,
+                          ZeroJob zero) {
     using C = GateCfg<NT>;
     alignas(64) CUtensorMap tmX, tmW;
     const int rows = w.gate_rows, cols = w.gate_cols;
@@ -222,6 +230,7 @@ cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.col_tiles = (cols + NT - 1) / NT;
     a.splits = w.gate_splits;
     a.nkc = (p.d_model + 63) / 64;
+    a.zero = zero;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
     static bool attr_done = false;
@@ -243,12 +252,12 @@ cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, co
 int gate_col_tile(int cols) { return cols > 64 ? 128 : 64; }
 
 cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                                    cudaStream_t s, bool* launched) {
+                                    cudaStream_t s, bool* launched, ZeroJob zero) {
     *launched = false;
     if (w.gate_splits == 0) return cudaSuccess;
     *launched = true;
-    if (gate_col_tile(w.gate_cols) == 128) return launch_gate_t<128>(p, w, ws, rt, s);
-    return launch_gate_t<64>(p, w, ws, rt, s);
+    if (gate_col_tile(w.gate_cols) == 128) return launch_gate_t<128>(p, w, ws, rt, s, zero);
+    return launch_gate_t<64>(p, w, ws, rt, s, zero);
 }
 
 }  // namespace gsdpa

@@ -30,9 +30,10 @@
 // each converting half of the 512 accumulator columns of its 32 rows (the
 // tensor-memory load of the next 32 columns in flight while the current ones
 // are converted). The fp16 tile is staged in the idle K-chunk ring as 64-column
-// 128B-swizzled blocks and written with two 64 KB bulk copies: one thread per
-// row writing 16-byte pieces of its own row would cost one memory transaction
-// per piece.
+// 128B-swizzled blocks and written with four 32 KB bulk copies, each issued by
+// the producer thread (idle by then) as soon as its 128 columns are staged, so
+// that the stores overlap the conversion: one thread per row writing 16-byte
+// pieces of its own row would cost one memory transaction per piece.
 // Rows past the end of X, columns past the end of W_g and the K tail load as
 // zeros (TMA out-of-bounds fill) and are not stored.
 #include "gsdpa_internal.h"
@@ -50,21 +51,28 @@ constexpr uint32_t kXBytes = 128 * 64 * 2;              // X chunk: this CTA's 1
 constexpr uint32_t kWBytes = 64 * 256 * 2;              // W_g chunk: 64 x this CTA's 256 columns
 constexpr uint32_t kStage = kXBytes + kWBytes;
 constexpr uint32_t kOffBar = kNS * kStage;
-constexpr uint32_t kOffMisc = kOffBar + (2 * kNS + 2) * 8;
+constexpr uint32_t kOffMisc = kOffBar + (2 * kNS + 2 + 4) * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 
 struct SigArgs {
     __half* out;     // [rows, cols]
     int rows, cols, d_model;
     int row_tiles, nkc;   // tiles of 256 rows; K chunks of 64
+    ZeroJob zero;         // per-call state of the attention kernel, zeroed by CTA 0
     WaitCtl ctl;
 };
 
-// sigma(x) = 1/2 + tanh(x/2)/2 (tanh.approx: relative error about 2^-11)
-__device__ __forceinline__ float sigmoid_fast(float x) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-    return fmaf(0.5f, t, 0.5f);
+// sigma of two values as fp16: 1/2 + tanh(x/2)/2 with one MUFU operation for
+// both (tanh.approx.f16x2, relative error about 2^-11 -- the precision the
+// fp16 result keeps anyway; the logits are rounded to fp16 first, |x| stays
+// far inside its range).
+__device__ __forceinline__ uint32_t sigmoid2_h(float x0, float x1) {
+    const __half2 hx = __floats2half2_rn(0.5f * x0, 0.5f * x1);
+    uint32_t t;
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&hx)));
+    const __half2 half2v = __floats2half2_rn(0.5f, 0.5f);
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&t), half2v, half2v);
+    return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -77,6 +85,7 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint64_t* empty = bars + kNS;       // [NS] both: the MMAs reading the stage completed
     uint64_t* acc_full = bars + 2 * kNS;     // both: the accumulator is complete
     uint64_t* drain = bars + 2 * kNS + 1;    // even
+    uint64_t* grp_ready = bars + 2 * kNS + 2;   // [4] the 4 warps staging 128-column group g are done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     int* abort_word = reinterpret_cast<int*>(smem + kOffMisc + 4);
 
@@ -84,6 +93,12 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int lane = threadIdx.x % 32;
     const uint32_t rank = pair::cta_rank();
     const pair::PairAbort ab{abort_word, pair::map_to(abort_word, rank ^ 1u)};
+    if (blockIdx.x == 0 && args.zero.n > 0) {
+        // the attention kernel's per-call state; visible before it can start
+        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
     pdl_trigger();   // the attention kernel may start; it reads the gate only in its epilogue
     const int tile = (int)pair::cluster_id();
     const int r0 = (tile % args.row_tiles) * 256;   // the pair's first row
@@ -96,6 +111,7 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
+        for (int g = 0; g < 4; ++g) mbar_init(&grp_ready[g], 4);
         *abort_word = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmX);
@@ -125,6 +141,16 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 // W_g viewed as (64 columns, d_model rows, cols/64 blocks): four 64-column blocks
                 pair::tma_load_3d(st + kXBytes, &tmW, 0, kc * 64, (c0 + (int)rank * 256) / 64, fb);
             }
+            // ---- then the stores: each 128-column group of the staged fp16 tile
+            // as soon as its 4 warps are done (group g = tile columns [128 g, 128 g + 128))
+            // (rows / columns past the end of the output are clipped by the copy)
+            bool ok = true;
+            for (int g = 0; g < 4 && ok; ++g) {   // (groups 0 and 1 are staged first, in parallel)
+                if (!(ok = pair::wait(&grp_ready[g], 0, ab, args.ctl))) break;
+                tma_store_3d(&tmG, smem + g * 32768, 0, r0 + (int)rank * 128, (c0 + g * 128) / 64);
+                tma_store_commit();
+            }
+            tma_store_wait_read0();   // the staging area stays valid until the copies have read it
         }
     } else if (warp == 1) {
         // ---- MMA issue (even CTA): D[256 x 512] += X[256 x 64] W_g[64 x 512] per chunk, as two N = 256 MMAs
@@ -189,9 +215,7 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 uint32_t hv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const __half2 h2 = __floats2half2_rn(sigmoid_fast(__uint_as_float(v[2 * e])),
-                                                         sigmoid_fast(__uint_as_float(v[2 * e + 1])));
-                    hv[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    hv[e] = sigmoid2_h(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
                 }
                 uint8_t* blk = smem + (tc >> 6) * 16384;
                 const uint32_t chunk0 = (uint32_t)(tc & 63) >> 3;   // 16-byte chunk of the 128-byte row
@@ -199,16 +223,14 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 for (int q = 0; q < 4; ++q)
                     *reinterpret_cast<uint4*>(blk + sw128_offset((uint32_t)row, chunk0 + q)) =
                         make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                if ((k & 3) == 3) {
+                    // this warp's rows of 128-column group (half, then 2 + half) are staged:
+                    // make them visible to the bulk copy and tell the storing thread
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&grp_ready[(k >> 2) * 2 + half]);
+                }
             }
-            fence_proxy_async_smem();   // the staged tile is read by the bulk copies below
-        }
-        named_bar_sync(1, 256);   // the eight epilogue warps
-        if (ok && warp == 2 && lane == 0) {
-            // rows / columns past the end of the output are clipped by the copy
-            const int rr = r0 + (int)rank * 128;
-            for (int g = 0; g < 2; ++g) tma_store_3d(&tmG, smem + g * 65536, 0, rr, (c0 + g * 256) / 64);
-            tma_store_commit();
-            tma_store_wait_read0();   // the staging area stays valid until the copies have read it
         }
         tc_fence_before();
     }
@@ -232,7 +254,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d, c
 }  // namespace
 
 cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, ZeroJob zero) {
     alignas(64) CUtensorMap tmX, tmW, tmG;
     const int rows = p.B * p.Lq, cols = p.Hq * p.dk;
     if (rows == 0) return cudaSuccess;
@@ -250,10 +272,10 @@ cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, c
         if (!make_map(&tmW, p.Wg, 3, d, st, box)) return cudaErrorInvalidValue;
     }
     {
-        // output (fp16, [rows, cols]) as (64 columns, rows, cols/64 blocks): 128 rows x 256 columns per copy
+        // output (fp16, [rows, cols]) as (64 columns, rows, cols/64 blocks): 128 rows x 128 columns per copy
         const cuuint64_t d[3] = {64, (cuuint64_t)rows, (cuuint64_t)cols / 64};
         const cuuint64_t st[2] = {(cuuint64_t)cols * 2, 128};
-        const cuuint32_t box[3] = {64, 128, 4};
+        const cuuint32_t box[3] = {64, 128, 2};
         const cuuint32_t es[3] = {1, 1, 1};
         if (encode_tiled_fn()(&tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ws + w.gate_sig, d, st, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -267,6 +289,7 @@ cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, c
     a.d_model = p.d_model;
     a.row_tiles = (rows + 255) / 256;
     a.nkc = (p.d_model + 63) / 64;
+    a.zero = zero;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
     static bool attr_done = false;

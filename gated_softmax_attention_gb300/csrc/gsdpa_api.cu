@@ -6,6 +6,7 @@
 #include "sm103_ptx.cuh"
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -104,8 +105,8 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
     size_t off = 0;
     const bool bf16 = p.dtype == GSDPA_BF16;
     const bool decode = decode_supported(p);
-    if (p.sink && !decode) {
-        w.sink_tiles = bf16 ? (p.Lq + 127) / 128 : (p.Lq + 31) / 32;
+    if (p.sink && !decode && !bf16) {
+        w.sink_tiles = (p.Lq + 31) / 32;
         w.sink_part = off;
         off = align256(off + sizeof(float) * (size_t)p.B * p.Hq * w.sink_tiles);
     }
@@ -128,11 +129,13 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
         off = align256(off + sizeof(float) * (size_t)splits * w.gate_rows * w.gate_cols);
     }
     // bf16 prefill: the counter from which the CTAs of the attention kernel
-    // claim their units (dynamic schedule), zeroed at the start of every call.
+    // claim their units (dynamic schedule) and, with the first-token share, one
+    // 64-bit word per (b, h) in which the warps add their rows' shares; zeroed
+    // at the start of every call.
     if (bf16 && !decode) {
-        w.has_sched = true;
-        w.sched = off;
-        off = align256(off + sizeof(int));
+        w.state = off;
+        w.state_ints = 2 + (p.sink ? 2 * p.B * p.Hq : 0);
+        off = align256(off + sizeof(int) * (size_t)w.state_ints);
     }
     // Elementwise bf16 prefill: the gate sigma(X W_g) computed ahead of the
     // attention kernel, whose epilogue multiplies by it.
@@ -197,6 +200,18 @@ __global__ void wait_self_test_kernel(WaitCtl ctl) {
     }
 }
 
+void set_sink_args(const Problem& p, const WorkspacePlan& w, char* ws, int n_qtiles, unsigned long long** word,
+                   float** sink, float* scale, double* inv, int* arrivals) {
+    int lg = 0;
+    while ((1L << lg) < (long)p.Lq + 1) ++lg;   // ceil(log2(L_q + 1))
+    const int F = 43 - lg;
+    *word = p.sink ? reinterpret_cast<unsigned long long*>(ws + w.state + 8) : nullptr;
+    *sink = p.sink;
+    *scale = std::ldexp(1.0f, F);
+    *inv = std::ldexp(1.0, -F) / (double)p.Lq;
+    *arrivals = 4 * n_qtiles;
+}
+
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s) {
     const int n = p.B * p.Hq;
     sink_finalize_kernel<<<(n + 127) / 128, 128, 0, s>>>(reinterpret_cast<const float*>(ws + w.sink_part), p.sink, n,
@@ -257,6 +272,7 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return GSDPA_ERR_ALIGNMENT;
     if (gate_mode != GSDPA_GATE_NONE && (!aligned16(X) || !aligned16(W_g))) return GSDPA_ERR_ALIGNMENT;
     if (sink && (reinterpret_cast<uintptr_t>(sink) & 3u)) return GSDPA_ERR_ALIGNMENT;
+    if (sink && dtype == GSDPA_BF16 && !decode_supported(p) && (long)L_q > kSinkMaxLq) return GSDPA_ERR_UNSUPPORTED;
 
     const DeviceInfo* dev = device_info();
     if (!dev) return GSDPA_ERR_LAUNCH;
@@ -280,15 +296,26 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
         e = launch_f32_simt(p, w, ws, rt, s);
         if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
     } else {
+        // The per-call state of the prefill kernel is zeroed by the gate kernel
+        // that runs first (before it lets the attention kernel start), else by a memset.
+        ZeroJob zero;
+        if (w.state_ints > 0) {
+            zero.p = reinterpret_cast<int*>(ws + w.state);
+            zero.n = w.state_ints;
+        }
         bool gate_launched = false;
-        if (w.has_sched) e = cudaMemsetAsync(ws + w.sched, 0, sizeof(int), s);
-        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
-        if (e == cudaSuccess && w.has_gate_sig) e = launch_gate_sigmoid_bf16(p, w, ws, rt, s);
+        if (w.has_gate_sig) {
+            e = launch_gate_sigmoid_bf16(p, w, ws, rt, s, zero);
+            zero.n = 0;
+        }
+        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched, zero);
+        if (gate_launched) zero.n = 0;
+        if (e == cudaSuccess && zero.n > 0) e = cudaMemsetAsync(zero.p, 0, sizeof(int) * (size_t)zero.n, s);
         if (decode_supported(p)) {
             if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s);
         } else {
+            // (the prefill kernel also finishes the first-token share)
             if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
-            if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
         }
     }
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;

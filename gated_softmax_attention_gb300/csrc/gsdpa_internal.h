@@ -36,8 +36,11 @@ struct WorkspacePlan {
     size_t gate_part = 0;   // float [gate_splits, rows, cols] (gate logits, split-K partials)
     size_t gate_sig = 0;    // fp16  [B*L_q, H_q*d_k]          (elementwise prefill: sigma(X W_g))
     bool has_gate_sig = false;
-    size_t sched = 0;       // int   [1] bf16 prefill: next unit to claim (zeroed per call)
-    bool has_sched = false;
+    // bf16 prefill, per-call state (zero at the start of every call): int [0]
+    // the next unit to claim; from byte 8, with the first-token share, one
+    // 64-bit word per (b, h): the share in fixed point and its arrivals
+    size_t state = 0;
+    int state_ints = 0;
     int gate_splits = 0;
     int gate_rows = 0, gate_cols = 0;
     size_t dec_ml = 0;      // float [B, Hq, splits, 2]        (decode running max, sum)
@@ -69,11 +72,17 @@ EncodeTiledFn encode_tiled_fn();
 // Launchers: return cudaSuccess or the launch error. `ws` is the workspace base.
 cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                             cudaStream_t s);
+// A kernel that runs first in a call and zeroes `n` ints at `p` (its CTA 0,
+// before it lets the dependent kernel start); n = 0: nothing to zero.
+struct ZeroJob {
+    int* p = nullptr;
+    int n = 0;
+};
 cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                                    cudaStream_t s, bool* launched);
+                                    cudaStream_t s, bool* launched, ZeroJob zero = ZeroJob());
 // Elementwise bf16 prefill: sigma(X W_g) as fp16 into the workspace (gate_sigmoid_sm103.cu).
 cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                                     cudaStream_t s);
+                                     cudaStream_t s, ZeroJob zero);
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s);
 // d_k = 128 on CTA pairs (prefill_pair_sm103.cu); launch_prefill_bf16 routes
@@ -84,5 +93,11 @@ cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, c
 cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                cudaStream_t s);
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);
+// bf16 prefill kernels: where the first-token share accumulates (null without
+// it), its fixed-point scale 2^F with F = 43 - ceil(log2(L_q + 1)), the factor
+// 2^-F / L_q back to the mean, and the arrivals of a full set (4 per query tile).
+constexpr long kSinkMaxLq = 1L << 24;   // keeps 4 x tiles below 2^20 (the count field)
+void set_sink_args(const Problem& p, const WorkspacePlan& w, char* ws, int n_qtiles, unsigned long long** word,
+                   float** sink, float* scale, double* inv, int* arrivals);
 
 }  // namespace gsdpa

@@ -96,7 +96,7 @@ struct PairCfg {
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
     static constexpr int NBAR = 2 * NS + 11;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    // misc: TMEM address, abort flag, sink partials [4], unit ring [4]; then the
+    // misc: TMEM address, abort flag, (unused), unit ring [4]; then the
     // row statistics (m, l) of both warpgroups [2][128] for the merge
     static constexpr uint32_t OFF_STATS = OFF_MISC + 64;
     static constexpr uint32_t SMEM_BYTES = OFF_STATS + 2 * 128 * 8 + 1024;  // + alignment slack
@@ -108,7 +108,11 @@ struct PairArgs {
     int gate_splits;
     const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*d_k]
     int* sched_counter;      // next unit to claim (0 at launch)
-    float* sink_part;        // [B, Hq, n_qtiles] or null
+    unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
+    float* sink;                    // [B, Hq] out
+    float sink_scale;               // 2^F
+    double sink_inv;                // 2^-F / L_q
+    int sink_arrivals;              // 4 warps per 128-row query tile
     __nv_bfloat16* O;        // [B, Lq, Hq, d_k]
     WaitCtl ctl;
 };
@@ -144,7 +148,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     int* abort_word = reinterpret_cast<int*>(smem + C::OFF_MISC + 4);
     volatile int* abort_flag = abort_word;
-    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);                  // [4]
     volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
     float2* stats = reinterpret_cast<float2*>(smem + C::OFF_STATS);                   // [2][128]
 
@@ -293,22 +296,14 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             auto issue_S = [&](int p, int s, uint32_t k_off) {
                 const uint32_t a0 = desc_sw128_lo(sQa, 16);
                 const uint32_t b0 = desc_sw128_lo(ringa + s * C::STAGE_BYTES + k_off, 16);
-#pragma unroll
-                for (int kk = 0; kk < kHD / 16; ++kk) {
-                    // K-major, 64-column blocks: Q blocks are 128 rows (16 KB), K halves 64 rows (8 KB)
-                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    pair::mma_ss(tmem + p * 128, a0 + ka, HI, b0 + kb, HI, idS, kk != 0);
-                }
+                // K-major, 64-column blocks: Q blocks are 128 rows (16 KB), K halves 64 rows (8 KB)
+                pair::mma_ss_k128<16384, 8192>(tmem + p * 128, a0, b0, HI, idS, 0);
                 pair::commit_both(&s_full[p]);
             };
             auto issue_PV = [&](int p, int s, bool acc) {
                 // V half: MN-major, one 64-column block; 16 keys = 2 KB per K step
                 const uint32_t v0 = desc_sw128_lo(ringa + s * C::STAGE_BYTES, 8192);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    pair::mma_ts(tmem + 256 + p * 128, tmem + p * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
-                                 (acc || kk != 0) ? 1u : 0u);
+                pair::mma_ts_k128(tmem + 256 + p * 128, tmem + p * 128, v0, HI, idO, acc ? 1u : 0u);
             };
 
             for (int r = 0; ok; ++r) {
@@ -519,6 +514,19 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const float s0 = (p == 0 ? a_me : a_ot) * inv;   // weight of O_0
             const float s1 = (p == 0 ? a_ot : a_me) * inv;   // weight of O_1
             const bool has1 = nkv > 1;                        // O_1 holds results only then
+            // first-token share of this warp's 32 rows (key 0 lies in key tile 0, a tile of
+            // warpgroup 0): added now, its result read after the stores
+            unsigned long long sink_old = 0, sink_add = 0;
+            const bool do_sink = args.sink_word && p == 0 && U.mine;
+            if (do_sink) {
+                float p0 = (i < args.Lq) ? ex2_approx(x0 - mm) * inv : 0.f;
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
+                if (lane == 0) {
+                    sink_add = sink_encode(p0, args.sink_scale);
+                    sink_old = atomicAdd(args.sink_word + (long)b * args.Hq + h, sink_add);
+                }
+            }
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
@@ -565,17 +573,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         dst[cb * 2 + q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
             }
-            if (args.sink_part && p == 0 && U.mine) {
-                // share of key 0 (it lies in key tile 0, a tile of warpgroup 0)
-                float p0 = (i < args.Lq) ? ex2_approx(x0 - mm) * inv : 0.f;
-#pragma unroll
-                for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
-                if (lane == 0) sred[qd] = p0;
-                named_bar_sync(2, 128);
-                if (row == 0)
-                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + U.q0 / kTile] =
-                        sred[0] + sred[1] + sred[2] + sred[3];
-            }
+            if (do_sink && lane == 0)
+                sink_finish(sink_old, sink_add, args.sink_arrivals, args.sink_inv, args.sink + (long)b * args.Hq + h);
         }
         // both warpgroups have read O_0 and O_1 before either starts the next
         // unit (its first PV MMAs overwrite them)
@@ -639,8 +638,8 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
-    a.sched_counter = reinterpret_cast<int*>(ws + w.sched);
-    a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
+    a.sched_counter = reinterpret_cast<int*>(ws + w.state);
+    set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;

@@ -78,7 +78,11 @@ struct PrefillArgs {
     int gate_splits;
     const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*HD]
     int* sched_counter;      // next unit to claim (0 at launch)
-    float* sink_part;        // [B, Hq, n_qtiles] or null
+    unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
+    float* sink;                    // [B, Hq] out
+    float sink_scale;               // 2^F
+    double sink_inv;                // 2^-F / L_q
+    int sink_arrivals;              // 4 warps per query tile
     __nv_bfloat16* O;        // [B, Lq, Hq, HD]
     WaitCtl ctl;
 };
@@ -111,7 +115,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint64_t* sched_full = q_full + 8;     // [4] unit r published in sched[r % 4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    float* sred = reinterpret_cast<float*>(smem + C::OFF_MISC + 16);  // [2][4]
     volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
 
     const int warp = threadIdx.x / 32;
@@ -250,10 +253,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             auto issue_S = [&](int t, int j) {
                 const uint32_t a0 = desc_sw128_lo(sQa + t * C::Q_BYTES, 16);
                 const uint32_t b0 = desc_sw128_lo(stage_addr(2 * j), 16);
+                if (HD == 128) {
+                    // 128-row tiles: the second 64-column block of K lies 16 KB on
+                    mma_ss_k128<16384, 16384>(tmem + t * 128, a0, b0, HI, idS, 0);
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t k16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    mma_ss_elect(tmem + t * 128, a0 + k16, HI, b0 + k16, HI, idS, kk != 0);
+                    for (int kk = 0; kk < HD / 16; ++kk)
+                        mma_ss_elect(tmem + t * 128, a0 + kk * (32 >> 4), HI, b0 + kk * (32 >> 4), HI, idS, kk != 0);
                 }
                 mma_commit_elect(&s_full[t]);
             };
@@ -262,10 +268,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     return false;
                 tc_fence_after();
                 const uint32_t v0 = desc_sw128_lo(stage_addr(2 * j + 1), 16384);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, v0 + kk * (2048 >> 4), HI, idO,
-                                (j | kk) != 0);
+                // 128 keys: eight K = 16 steps, P 8 TMEM columns and V 2 KB apart
+                mma_ts_k128(tmem + 256 + t * 128, tmem + t * 128, v0, HI, idO, j != 0);
                 return true;
             };
 
@@ -457,6 +461,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (ok_epi) {
             // ---- epilogue: out = O / l (.) gate -> bf16 -> global (one 2*d_k-byte row per thread)
             const float inv_l = 1.0f / l;
+            // first-token share of this warp's 32 rows: added now, its result read after the stores
+            unsigned long long sink_old = 0, sink_add = 0;
+            if (args.sink_word) {
+                float p0 = (i < args.Lq) ? ex2_approx(x0 - m) * inv_l : 0.f;
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
+                if (lane == 0) {
+                    sink_add = sink_encode(p0, args.sink_scale);
+                    sink_old = atomicAdd(args.sink_word + (long)b * args.Hq + h, sink_add);
+                }
+            }
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
@@ -496,16 +511,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 for (int q = 0; q < HD / 8; ++q)
                     dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
             }
-            if (args.sink_part) {
-                float p0 = (i < args.Lq) ? ex2_approx(x0 - m) * inv_l : 0.f;
-#pragma unroll
-                for (int sh = 16; sh > 0; sh >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, sh);
-                if (lane == 0) sred[t * 4 + qd] = p0;
-                named_bar_sync(1 + t, 128);
-                if (row == 0)
-                    args.sink_part[((long)b * args.Hq + h) * args.n_qtiles + 2 * pr + t] =
-                        sred[t * 4] + sred[t * 4 + 1] + sred[t * 4 + 2] + sred[t * 4 + 3];
-            }
+            if (args.sink_word && lane == 0)
+                sink_finish(sink_old, sink_add, args.sink_arrivals, args.sink_inv, args.sink + (long)b * args.Hq + h);
         }
         sp_base += nkv[t];
         g_base += 1;
@@ -564,8 +571,8 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
-    a.sched_counter = reinterpret_cast<int*>(ws + w.sched);
-    a.sink_part = p.sink ? reinterpret_cast<float*>(ws + w.sink_part) : nullptr;
+    a.sched_counter = reinterpret_cast<int*>(ws + w.state);
+    set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;

@@ -201,3 +201,100 @@ __device__ __forceinline__ void commit_both(uint64_t* bar) {
 
 }  // namespace pair
 }  // namespace gsdpa
+
+namespace gsdpa {
+namespace pair {
+// Pair forms of mma_ss_k128 / mma_ts_k128 (cta_group::2, issued by the even CTA).
+template <uint32_t A_BLK, uint32_t B_BLK>
+__device__ __forceinline__ void mma_ss_k128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t"
+        "add.u32 al, %1, 2;\n\t"
+        "add.u32 bl, %2, 2;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, 4;\n\t"
+        "add.u32 bl, %2, 4;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, 6;\n\t"
+        "add.u32 bl, %2, 6;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %6;\n\t"
+        "add.u32 bl, %2, %10;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %7;\n\t"
+        "add.u32 bl, %2, %11;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %8;\n\t"
+        "add.u32 bl, %2, %12;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %9;\n\t"
+        "add.u32 bl, %2, %13;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate),
+        "n"((A_BLK >> 4) + 0), "n"((A_BLK >> 4) + 2), "n"((A_BLK >> 4) + 4), "n"((A_BLK >> 4) + 6),
+        "n"((B_BLK >> 4) + 0), "n"((B_BLK >> 4) + 2), "n"((B_BLK >> 4) + 4), "n"((B_BLK >> 4) + 6)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t"
+        "add.u32 bl, %2, 128;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 16;\n\t"
+        "add.u32 bl, %2, 256;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 24;\n\t"
+        "add.u32 bl, %2, 384;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 32;\n\t"
+        "add.u32 bl, %2, 512;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 40;\n\t"
+        "add.u32 bl, %2, 640;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 48;\n\t"
+        "add.u32 bl, %2, 768;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 56;\n\t"
+        "add.u32 bl, %2, 896;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+}  // namespace pair
+}  // namespace gsdpa

@@ -453,3 +453,126 @@ namespace gsdpa {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 }  // namespace gsdpa
+
+namespace gsdpa {
+// A full K = 128 step of tcgen05.mma (eight K = 16 instructions) issued by one
+// elected lane under a single election, the K advances baked in as
+// immediates: fewer instructions per MMA for the issuing warp, which shares
+// its sub-partition with busy softmax warps (measured: ~12 vs ~21 cycles per
+// MMA in isolation). The first instruction takes `accumulate`, the others
+// always accumulate.
+// SS: A and B K-major, 128B-swizzled; the 64-column blocks of K lie A_BLK /
+// B_BLK bytes apart (rows x 128 bytes).
+template <uint32_t A_BLK, uint32_t B_BLK>
+__device__ __forceinline__ void mma_ss_k128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t"
+        "add.u32 al, %1, 2;\n\t"
+        "add.u32 bl, %2, 2;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, 4;\n\t"
+        "add.u32 bl, %2, 4;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, 6;\n\t"
+        "add.u32 bl, %2, 6;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %6;\n\t"
+        "add.u32 bl, %2, %10;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %7;\n\t"
+        "add.u32 bl, %2, %11;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %8;\n\t"
+        "add.u32 bl, %2, %12;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "add.u32 al, %1, %9;\n\t"
+        "add.u32 bl, %2, %13;\n\t"
+        "mov.b64 da, {al, %3};\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate),
+        "n"((A_BLK >> 4) + 0), "n"((A_BLK >> 4) + 2), "n"((A_BLK >> 4) + 4), "n"((A_BLK >> 4) + 6),
+        "n"((B_BLK >> 4) + 0), "n"((B_BLK >> 4) + 2), "n"((B_BLK >> 4) + 4), "n"((B_BLK >> 4) + 6)
+        : "memory");
+}
+// TS: A (P, packed bf16 pairs) from TMEM, 8 columns per K = 16 step; B MN-major,
+// 128B-swizzled, 16 K rows (2 KB) per step.
+__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t"
+        "add.u32 bl, %2, 128;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 16;\n\t"
+        "add.u32 bl, %2, 256;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 24;\n\t"
+        "add.u32 bl, %2, 384;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 32;\n\t"
+        "add.u32 bl, %2, 512;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 40;\n\t"
+        "add.u32 bl, %2, 640;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 48;\n\t"
+        "add.u32 bl, %2, 768;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, 56;\n\t"
+        "add.u32 bl, %2, 896;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+}  // namespace gsdpa
+
+namespace gsdpa {
+// First-token share in fixed point. One 64-bit word per (b, h) holds the
+// number of warps that have added their rows (bits 44..63) and the sum of
+// their shares times 2^F (bits 0..43); F is chosen so that L_q * 2^F stays
+// below 2^43. Integer addition is associative, so the total is the same
+// whatever order the warps arrive in, and the warp whose addition completes
+// the count knows the total from its own atomic: no fence, no second pass.
+constexpr int kSinkCountShift = 44;
+__device__ __forceinline__ unsigned long long sink_encode(float share, float scale) {
+    return (1ull << kSinkCountShift) + __float2ull_rn(share * scale);
+}
+// old: the word before this warp's addition `add`; arrivals: the count of a full set.
+__device__ __forceinline__ void sink_finish(unsigned long long old, unsigned long long add, int arrivals,
+                                            double inv, float* out) {
+    if ((int)(old >> kSinkCountShift) == arrivals - 1)
+        *out = (float)((double)((old + add) & ((1ull << kSinkCountShift) - 1)) * inv);
+}
+}  // namespace gsdpa

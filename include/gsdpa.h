@@ -106,7 +106,12 @@ GSDPA_API size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int
  *   X, Q, K, V, W_g : device inputs in the layouts above. X and W_g may be
  *                     NULL when gate_mode == GSDPA_GATE_NONE.
  *   O               : device output [B, L_q, H_q, d_k], same dtype as inputs.
- *   sink            : device float32 [B, H_q] or NULL (not computed).
+ *   sink            : device float32 [B, H_q] or NULL (not computed). With
+ *                     bf16 prefill the rows' shares are added in fixed point
+ *                     with 43 - ceil(log2(L_q + 1)) fraction bits, so the sum
+ *                     does not depend on the order of the additions and
+ *                     repeated calls give the same bits; there L_q <= 2^24
+ *                     (GSDPA_ERR_UNSUPPORTED otherwise).
  *   B, L_q, L_k     : batch, query rows, key rows; 1 <= L_q <= L_k. B, L_q == 0
  *                     is an empty problem: nothing is enqueued, GSDPA_OK.
  *   d_model         : width of X (>= 1 when a gate is used; for bf16 a

@@ -56,15 +56,20 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # bf16 prefill: one 256-byte slot for the unit counter of the dynamic schedule
+    # bf16 prefill: the per-call state, one 256-byte slot for the unit counter
+    # of the dynamic schedule (8 bytes) ...
     counter = 256
     assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "none", False, gb.BF16) == counter
     # elementwise bf16 prefill: plus the gate sigma(X W_g) as fp16, [B*L_q, H_q*d_k]
     gate = 2 * 2 * 2048 * 16 * 128
     assert gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", False, gb.BF16) == counter + gate
-    # plus the sink partials: B*H_q*ceil(L/128) floats, 256-aligned
+    # ... and, with the first-token share, one 64-bit word per (b, h) in the
+    # same block: 8 + 2*16*8 bytes, 256-aligned
     n = gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", True, gb.BF16)
-    assert n >= counter + gate + 2 * 16 * 16 * 4 and n % 256 == 0
+    assert n == 512 + gate
+    # the float32 path keeps per-tile partial sums: B*H_q*ceil(L/32) floats
+    n = gb.workspace_bytes(2, 2048, 2048, 2048, 16, 16, 128, "elementwise", True, gb.F32)
+    assert n >= 2 * 16 * 64 * 4 and n % 256 == 0
     # headwise bf16: split-K gate logits [splits, B*L, H_q]
     n = gb.workspace_bytes(1, 4096, 4096, 4096, 32, 4, 128, "headwise", False, gb.BF16)
     assert n >= 4096 * 32 * 4 and n % 256 == 0
@@ -100,6 +105,10 @@ def test_argument_validation_before_any_device_work(lib):
     assert call(B=0) == gb.OK                              # empty problem: nothing enqueued
     assert call(L_q=0) == gb.OK
     assert call(dtype=1, d_model=60) == gb.ERR_UNSUPPORTED  # bf16 rows must start on 16 bytes
+    # bf16 prefill adds the first-token share in a fixed-point word whose count
+    # field holds 4 arrivals per 128-row tile: L_q up to 2^24 with a share
+    big = 1 << 24
+    assert call(dtype=1, sink=4, L_q=big + 1, L_k=big + 1) == gb.ERR_UNSUPPORTED
 
 
 def test_fwd_signature_matches_header(lib):

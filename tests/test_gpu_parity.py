@@ -235,3 +235,40 @@ def test_full_size_decode_sampled():
         ref, p0 = oracle.gated_sdpa(sl["X"], sl["Q"], sl["K"], sl["V"], sl["W_g"], gate=w.gate, causal=w.causal)
         assert_close(w, O[b:b + 1], ref, f"decode b={b}")
         np.testing.assert_allclose(sink[b], p0[0, 0], atol=sink_tol(w))
+
+
+# ------------------------------------------------------------------ per-call state in a reused workspace
+
+REUSE_CASES = [
+    small("bf16", name="reuse_none", gate="none"),
+    small("bf16", name="reuse_headwise", gate="headwise", H_q=8, H_kv=2),
+    small("bf16", name="reuse_elementwise"),
+    small("bf16", name="reuse_pair_long_keys", B=1, L_q=384, L_k=16384, H_q=2, H_kv=1, causal=False),
+]
+
+
+@pytest.mark.parametrize("w", REUSE_CASES, ids=lambda w: w.name)
+def test_repeated_calls_on_one_workspace(w):
+    """The unit counter and the first-token-share arrivals live in the
+    workspace and are reset by every call (by the gate kernel that runs first,
+    or by a memset without a gate): three calls on one workspace, with the
+    outputs poisoned in between, give the same bits, and the oracle's values."""
+    t = make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model if w.gate != "none" else 0, w.H_q, w.H_kv, w.d_k, w.gate, True, gb.BF16)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    O = torch.empty(w.B, w.L_q, w.H_q, w.d_k, dtype=torch.bfloat16, device="cuda")
+    sink = torch.empty(w.B, w.H_q, dtype=torch.float32, device="cuda")
+    runs = []
+    for _ in range(3):
+        O.fill_(float("nan"))
+        sink.fill_(float("nan"))
+        gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate, causal=w.causal,
+                          out=O, sink=sink, workspace=ws)
+        assert gb.check_device_error() == gb.OK
+        runs.append((O.clone(), sink.clone()))
+    for O_r, s_r in runs[1:]:
+        assert torch.equal(O_r, runs[0][0]) and torch.equal(s_r, runs[0][1])
+    ref, p0 = run_oracle(w, t)
+    assert_close(w, runs[0][0].double().cpu().numpy(), ref, w.name)
+    np.testing.assert_allclose(runs[0][1].double().cpu().numpy(), oracle.sink_share(p0), atol=sink_tol(w))
