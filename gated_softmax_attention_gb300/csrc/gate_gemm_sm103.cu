@@ -64,13 +64,6 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (blockIdx.x == 0 && args.zero.n > 0) {
-        // the attention kernel's per-call state; visible before it can start
-        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
-        __threadfence();
-        __syncthreads();
-    }
-    pdl_trigger();   // the consumer (attention or decode) may start; it reads the logits late
     const int u = blockIdx.x;
     const int rt = u % args.row_tiles;
     const int ct = (u / args.row_tiles) % args.col_tiles;
@@ -99,6 +92,19 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // This kernel is a programmatic dependent of the previous kernel on the
+    // stream, so the prologue above can overlap that kernel's tail. Nothing in
+    // global memory is touched before it has completed: it may have produced
+    // the inputs, or be the previous call's attention kernel, which still
+    // reads this workspace.
+    pdl_wait();
+    if (blockIdx.x == 0 && args.zero.n > 0) {
+        // the attention kernel's per-call state; visible before it can start
+        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
+    pdl_trigger();   // the consumer (attention or decode) may start; it reads the logits late
 
     if (warp == 0) {
         if (lane == 0) {
@@ -241,8 +247,7 @@ cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, co
         attr_done = true;
     }
     const unsigned grid = (unsigned)(a.row_tiles * a.col_tiles * a.splits);
-    gate_logits_kernel<NT><<<grid, kThreads, C::SMEM_BYTES, s>>>(tmX, tmW, a);
-    return cudaGetLastError();
+    return launch_dependent(gate_logits_kernel<NT>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, s, tmX, tmW, a);
 }
 
 }  // namespace

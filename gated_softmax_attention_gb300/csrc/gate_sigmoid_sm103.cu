@@ -93,13 +93,6 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int lane = threadIdx.x % 32;
     const uint32_t rank = pair::cta_rank();
     const pair::PairAbort ab{abort_word, pair::map_to(abort_word, rank ^ 1u)};
-    if (blockIdx.x == 0 && args.zero.n > 0) {
-        // the attention kernel's per-call state; visible before it can start
-        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
-        __threadfence();
-        __syncthreads();
-    }
-    pdl_trigger();   // the attention kernel may start; it reads the gate only in its epilogue
     const int tile = (int)pair::cluster_id();
     const int r0 = (tile % args.row_tiles) * 256;   // the pair's first row
     const int c0 = (tile / args.row_tiles) * 512;   // the pair's first column
@@ -126,6 +119,19 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     pair::cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // This kernel is a programmatic dependent of the previous kernel on the
+    // stream, so the prologue above can overlap that kernel's tail. Nothing in
+    // global memory is touched before it has completed: it may have produced
+    // the inputs, or be the previous call's attention kernel, which still
+    // reads this workspace.
+    pdl_wait();
+    if (blockIdx.x == 0 && args.zero.n > 0) {
+        // the attention kernel's per-call state; visible before it can start
+        for (int k = threadIdx.x; k < args.zero.n; k += blockDim.x) args.zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
+    pdl_trigger();   // the attention kernel may start; it reads the gate only in its epilogues
 
     if (warp == 0) {
         // ---- TMA producer: this CTA's rows of X and its 256 columns of W_g
@@ -300,8 +306,8 @@ cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, c
         attr_done = true;
     }
     const long tiles = (long)a.row_tiles * ((cols + 511) / 512);
-    gate_sigmoid_kernel<<<(unsigned)(2 * tiles), kThreads, kSmemBytes, s>>>(tmX, tmW, tmG, a);
-    return cudaGetLastError();
+    return launch_dependent(gate_sigmoid_kernel, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX, tmW,
+                            tmG, a);
 }
 
 }  // namespace gsdpa

@@ -100,4 +100,24 @@ constexpr long kSinkMaxLq = 1L << 24;   // keeps 4 x tiles below 2^20 (the count
 void set_sink_args(const Problem& p, const WorkspacePlan& w, char* ws, int n_qtiles, unsigned long long** word,
                    float** sink, float* scale, double* inv, int* arrivals);
 
+// Launch `kernel` as a programmatic dependent of the previous kernel on the
+// stream: it may be scheduled once every CTA of that kernel has signalled
+// (griddepcontrol.launch_dependents) or exited, and must itself wait
+// (griddepcontrol.wait) before it relies on that kernel's memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace gsdpa

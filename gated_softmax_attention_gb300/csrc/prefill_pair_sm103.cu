@@ -237,7 +237,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!(ok = pair::wait_acquire_cluster(&sched_full[r & 3], (r >> 2) & 1, ab, args.ctl))) break;
                 uix = sched[r & 3];
             }
-            if (uix >= n_units) break;
+            if (uix >= n_units) {
+                // no unit left for this CTA: the next kernel on the stream may be
+                // scheduled (it waits for this grid to complete before it touches memory)
+                pdl_trigger();
+                break;
+            }
             const Unit U = decode_unit(uix);
             // the previous unit's QK MMAs have read Q (its g_full commit covers every MMA)
             if (r > 0 && !(ok = pair::wait(g_full, (r - 1) & 1, ab, args.ctl))) break;

@@ -69,7 +69,12 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
     static constexpr int NBAR = 2 * NS + 11;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    // output staging: per warpgroup two 8 KB buffers of 128 rows x 32 columns
+    // (64-byte rows, 64-byte swizzle) that the TMA stores read
+    static constexpr uint32_t STG_BYTES = kTile * 32 * 2;
+    static constexpr uint32_t OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;
+    static constexpr uint32_t SMEM_BYTES = OFF_STG + 4 * STG_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 };
 
 struct PrefillArgs {
@@ -83,7 +88,6 @@ struct PrefillArgs {
     float sink_scale;               // 2^F
     double sink_inv;                // 2^-F / L_q
     int sink_arrivals;              // 4 warps per query tile
-    __nv_bfloat16* O;        // [B, Lq, Hq, HD]
     WaitCtl ctl;
 };
 
@@ -98,7 +102,8 @@ __device__ __forceinline__ float sigmoidf_fast(float x) {
 template <int HD, int GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const PrefillArgs args) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const PrefillArgs args) {
     using C = PrefillCfg<HD, GATE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,6 +174,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -193,7 +199,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int uix = atomicAdd(args.sched_counter, 1);
             sched[r & 3] = uix;
             mbar_arrive(&sched_full[r & 3]);
-            if (uix >= n_units) break;
+            if (uix >= n_units) {
+                // no unit left for this CTA: the next kernel on the stream may be
+                // scheduled (it waits for this grid to complete before it touches memory)
+                pdl_trigger();
+                break;
+            }
             const Unit U = decode_unit(uix);
             const int h = U.h, b = U.b, kvh = U.kvh, nj = U.nj;
             const int* q0 = U.q0;
@@ -303,6 +314,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         if (!(ok = wait_full(2 * j + 2))) break;
                         k_ready = true;
                         issue_S(0, j + 1);
+                    } else if (nkv[0] < nj) {
+                        // tile 0 has fewer key tiles (causal): its epilogue need not
+                        // wait for tile 1's last step
+                        mma_commit_elect(&g_full[0]);
                     }
                 }
                 if (j < nkv[1]) {
@@ -318,7 +333,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             // every MMA of the unit issued: signal the epilogues (and the producer) on completion
             if (ok) {
-                mma_commit_elect(&g_full[0]);
+                if (nkv[0] == nj) mma_commit_elect(&g_full[0]);
                 mma_commit_elect(&g_full[1]);
             }
             ibase += 2 * nj;
@@ -355,14 +370,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int uix = sched[r & 3];
         if (uix >= n_units) break;
         const Unit U = decode_unit(uix);
-        const int pr = U.pr, h = U.h, b = U.b;
-        const int* q0 = U.q0;
-        const int* nkv = U.nkv;
-        const int i = q0[t] + row;
+        const int h = U.h, b = U.b;
+        // this warpgroup's tile, selected (not indexed by t) so that the unit
+        // stays in registers
+        const int my_q0 = t ? U.q0[1] : U.q0[0];
+        const int my_nkv = t ? U.nkv[1] : U.nkv[0];
+        const int i = my_q0 + row;
         const long a_pos = off + i;
         float m = -INFINITY, l = 0.f, x0 = 0.f;
 
-        for (int j = 0; j < nkv[t]; ++j) {
+        for (int j = 0; j < my_nkv; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], (sp_base + j) & 1, abort_flag, args.ctl));
             if (!ok) break;
             tc_fence_after();
@@ -443,7 +460,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         uint4 gq[GATE == 2 ? HD / 8 : 1];
         if (GATE != 0 && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
         if (GATE == 2) {
-            if (i < args.Lq && nkv[t] > 0) {
+            if (i < args.Lq && my_nkv > 0) {
                 const uint4* gsrc =
                     reinterpret_cast<const uint4*>(args.gate_sig + (((long)b * args.Lq + i) * args.Hq + h) * HD);
 #pragma unroll
@@ -453,10 +470,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 for (int q = 0; q < HD / 8; ++q) gq[q] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        if (ok && nkv[t] > 0) ok = mbar_wait(&g_full[t], g_base & 1, abort_flag, args.ctl);
+        if (ok && my_nkv > 0) ok = mbar_wait(&g_full[t], g_base & 1, abort_flag, args.ctl);
         tc_fence_after();
         // Every thread of this warpgroup takes the same branch (the epilogue has named barriers).
-        const bool ok_epi = named_bar_and(1 + t, 128, ok && nkv[t] > 0);
+        const bool ok_epi = named_bar_and(1 + t, 128, ok && my_nkv > 0);
         ok = named_bar_and(1 + t, 128, ok);
         if (ok_epi) {
             // ---- epilogue: out = O / l (.) gate -> bf16 -> global (one 2*d_k-byte row per thread)
@@ -482,12 +499,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 g_head = sigmoidf_fast(gl);
             }
-            uint32_t packed[HD / 2];
+            // 32 columns at a time: TMEM -> registers -> bf16 in a staging buffer ->
+            // one TMA store of the tile's 128 rows (rows past L_q are clipped by the
+            // tensor map). The issuing thread has seen the store two chunks back
+            // finish reading its buffer before the barrier of the chunk in between.
+            uint8_t* stg = smem + C::OFF_STG + t * 2 * C::STG_BYTES;
+            const int sw = (row >> 1) & 3;   // 64-byte swizzle of this row's 16-byte pieces
 #pragma unroll
             for (int cb = 0; cb < HD / 32; ++cb) {
                 uint32_t orr[32];
                 tmem_ld32(tO + cb * 32, orr);
                 tmem_wait_ld();
+                uint32_t packed[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float v0 = __uint_as_float(orr[e]) * inv_l;
@@ -502,21 +525,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         v0 *= g_head;
                         v1 *= g_head;
                     }
-                    packed[cb * 16 + e / 2] = pack_bf16x2(v0, v1);
+                    packed[e / 2] = pack_bf16x2(v0, v1);
                 }
-            }
-            if (i < args.Lq) {
-                uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * HD);
+                uint8_t* dst = stg + (cb & 1) * C::STG_BYTES + row * 64;
 #pragma unroll
-                for (int q = 0; q < HD / 8; ++q)
-                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(dst + ((q ^ sw) << 4)) =
+                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                fence_proxy_async_smem();
+                if (row == 0) tma_store_wait_read0();   // the previous chunk's store has read its buffer
+                named_bar_sync(1 + t, 128);
+                if (row == 0) {
+                    tma_store_4d(&tmO, stg + (cb & 1) * C::STG_BYTES, cb * 32, h, my_q0, b);
+                    tma_store_commit();
+                }
             }
             if (args.sink_word && lane == 0)
                 sink_finish(sink_old, sink_add, args.sink_arrivals, args.sink_inv, args.sink + (long)b * args.Hq + h);
         }
-        sp_base += nkv[t];
+        sp_base += my_nkv;
         g_base += 1;
         }   // units
+        if (row == 0) tma_store_wait_all();   // the output tiles have been written
         tc_fence_before();
     }
 
@@ -541,7 +571,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int HD, int GATE>
 cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
     using C = PrefillCfg<HD, GATE>;
-    alignas(64) CUtensorMap tmQ, tmK, tmV;
+    alignas(64) CUtensorMap tmQ, tmK, tmV, tmO;
     const cuuint64_t e = 2;
     // [B, L, H, d] viewed as (64 columns, H, L, B, d/64 blocks): one request
     // loads a 128-row tile with all d_k columns as d_k/64 swizzled blocks
@@ -558,6 +588,13 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
         if (!make_map(&tmK, p.K, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         if (!make_map(&tmV, p.V, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
+    // O [B, L_q, H_q, d] as (d, H_q, L_q, B): one store writes 32 columns of a 128-row tile
+    {
+        cuuint64_t d[4] = {(cuuint64_t)HD, (cuuint64_t)p.Hq, (cuuint64_t)p.Lq, (cuuint64_t)p.B};
+        cuuint64_t st[3] = {HD * e, (cuuint64_t)p.Hq * HD * e, (cuuint64_t)p.Lq * p.Hq * HD * e};
+        cuuint32_t box[4] = {32, 1, 128, 1};
+        if (!make_map(&tmO, p.O, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
+    }
     PrefillArgs a;
     a.B = p.B;
     a.Lq = p.Lq;
@@ -573,7 +610,6 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
-    a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 
@@ -604,7 +640,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = GATE != 0 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE>, tmQ, tmK, tmV, a);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE>, tmQ, tmK, tmV, tmO, a);
 }
 
 }  // namespace

@@ -152,6 +152,8 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void tma_store_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// every bulk store this thread committed has completed (global writes done)
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA stores, tcgen05.mma operand reads).
