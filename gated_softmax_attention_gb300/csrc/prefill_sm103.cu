@@ -67,7 +67,10 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
     static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + NS * STAGE_BYTES;
-    static constexpr int NBAR = 2 * NS + 11;
+    // mbarriers: full[NS], empty[NS], then q_full, s_full[2], p_full[2],
+    // g_full[2], drain, sched_full[4]
+    static constexpr int NBAR_AFTER_RING = 12;
+    static constexpr int NBAR = 2 * NS + NBAR_AFTER_RING;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     // output staging: per warpgroup two 8 KB buffers of 128 rows x 32 columns
     // (64-byte rows, 64-byte swizzle) that the TMA stores read
@@ -118,6 +121,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint64_t* g_full = q_full + 5;         // [2]: every MMA of the unit done
     uint64_t* drain = q_full + 7;
     uint64_t* sched_full = q_full + 8;     // [4] unit r published in sched[r % 4]
+    static_assert(8 + 4 == C::NBAR_AFTER_RING, "barrier layout");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
