@@ -378,11 +378,16 @@ bool decode_supported(const Problem& p) {
     return p.dtype == 1 && p.Lq == 1 && p.dk == HD && (p.Hq / p.Hkv) % HPC == 0;
 }
 
+// Splits of the cache per (b, kv head, chunk). Every CTA pays a fixed cost
+// of a few microseconds (its first copies' latency, the merge of its key
+// groups, the split combine), so the cache is cut into as few splits as give
+// about four CTAs per SM: enough for the SMs to stay busy to the end, few
+// enough that the fixed cost stays small next to the streaming.
 int decode_splits(const Problem& p, int num_sms) {
     const int chunks = (p.Hq / p.Hkv) / HPC;
     const long base = (long)p.B * p.Hkv * chunks;
     const int n_tiles = (p.Lk + KT - 1) / KT;
-    long s = (24L * num_sms + base - 1) / base;
+    long s = (4L * num_sms + base - 1) / base;
     long max_s = n_tiles / 4 > 0 ? n_tiles / 4 : 1;
     if (s > max_s) s = max_s;
     if (s < 1) s = 1;
