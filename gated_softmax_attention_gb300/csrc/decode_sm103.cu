@@ -348,6 +348,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const float inv = 1.0f / Lt;
     float g0 = 1.f, g1 = 1.f;
     if (args.gate_mode != 0) {
+        pdl_wait();   // the gate-logit kernel has completed (a no-op after an ordinary launch)
         float gl0 = 0.f, gl1 = 0.f;
         const long rowoff = (long)b * args.gate_cols;
         const long gsz = (long)args.B * args.gate_cols;
@@ -395,7 +396,7 @@ int decode_splits(const Problem& p, int num_sms) {
 }
 
 cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool dependent) {
     alignas(64) CUtensorMap tmK, tmV;
     cuuint64_t d[4] = {(cuuint64_t)HD, (cuuint64_t)p.Hkv, (cuuint64_t)p.Lk, (cuuint64_t)p.B};
     cuuint64_t st[3] = {HD * 2, (cuuint64_t)p.Hkv * HD * 2, (cuuint64_t)p.Lk * p.Hkv * HD * 2};
@@ -429,7 +430,8 @@ cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* w
     a.counters = reinterpret_cast<int*>(ws + w.dec_cnt);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, w.dec_cnt_bytes, s);
+    cudaError_t e = cudaSuccess;
+    if (!dependent) e = cudaMemsetAsync(a.counters, 0, w.dec_cnt_bytes, s);
     if (e != cudaSuccess) return e;
     static bool attr_done = false;
     if (!attr_done) {
@@ -438,6 +440,8 @@ cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* w
         attr_done = true;
     }
     const long units = (long)p.B * p.Hkv * a.chunks * a.splits;
+    if (dependent)
+        return launch_dependent(decode_kernel, dim3((unsigned)units), dim3(kThreads), SMEM_BYTES, s, tmK, tmV, a);
     decode_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, s>>>(tmK, tmV, a);
     return cudaGetLastError();
 }

@@ -296,24 +296,35 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
         e = launch_f32_simt(p, w, ws, rt, s);
         if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
     } else {
-        // The per-call state of the prefill kernel is zeroed by the gate kernel
-        // that runs first (before it lets the attention kernel start), else by a memset.
+        // The per-call state of the attention kernel (the prefill kernel's unit
+        // counter and share words, the decode kernel's split counters) is zeroed
+        // by the gate kernel that runs first, before it lets the attention kernel
+        // start; without a gate kernel, by a memset.
+        const bool decode = decode_supported(p);
         ZeroJob zero;
-        if (w.state_ints > 0) {
+        if (decode) {
+            zero.p = reinterpret_cast<int*>(ws + w.dec_cnt);
+            zero.n = (int)(w.dec_cnt_bytes / sizeof(int));
+        } else if (w.state_ints > 0) {
             zero.p = reinterpret_cast<int*>(ws + w.state);
             zero.n = w.state_ints;
         }
         bool gate_launched = false;
         if (w.has_gate_sig) {
             e = launch_gate_sigmoid_bf16(p, w, ws, rt, s, zero);
+            gate_launched = true;
             zero.n = 0;
         }
-        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched, zero);
-        if (gate_launched) zero.n = 0;
-        if (e == cudaSuccess && zero.n > 0) e = cudaMemsetAsync(zero.p, 0, sizeof(int) * (size_t)zero.n, s);
-        if (decode_supported(p)) {
-            if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s);
+        bool logits_launched = false;
+        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, w, ws, rt, s, &logits_launched, zero);
+        if (logits_launched) {
+            gate_launched = true;
+            zero.n = 0;
+        }
+        if (decode) {
+            if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s, gate_launched);
         } else {
+            if (e == cudaSuccess && zero.n > 0) e = cudaMemsetAsync(zero.p, 0, sizeof(int) * (size_t)zero.n, s);
             // (the prefill kernel also finishes the first-token share)
             if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
         }

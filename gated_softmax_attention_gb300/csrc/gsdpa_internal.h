@@ -90,8 +90,12 @@ cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* 
 constexpr long kPairMinKeys = 16384;
 cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                      cudaStream_t s);
+// dependent: the gate-logit kernel just before it has zeroed the split
+// counters and this launch is its programmatic dependent (the decode kernel
+// waits for it only where it reads the logits); otherwise the counters are
+// zeroed here and the launch is an ordinary one.
 cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                               cudaStream_t s);
+                               cudaStream_t s, bool dependent);
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);
 // bf16 prefill kernels: where the first-token share accumulates (null without
 // it), its fixed-point scale 2^F with F = 43 - ceil(log2(L_q + 1)), the factor

@@ -105,8 +105,11 @@ extern "C" GSDPA_API int gated_sdpa_decode_noalloc(const void* X, const void* Q,
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     bool gate_launched = false;
-    cudaError_t e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched);
-    if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s);   // clears its counters first
+    ZeroJob zero;   // the split counters, zeroed by the gate kernel when there is one
+    zero.p = reinterpret_cast<int*>(ws + w.dec_cnt);
+    zero.n = (int)(w.dec_cnt_bytes / sizeof(int));
+    cudaError_t e = launch_gate_logits_bf16(p, w, ws, rt, s, &gate_launched, zero);
+    if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s, gate_launched);
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
     return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
 }
