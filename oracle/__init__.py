@@ -53,9 +53,11 @@ def _load():
             lib = ctypes.CDLL(build())
             dp = ctypes.POINTER(ctypes.c_double)
             ip = ctypes.POINTER(ctypes.c_int)
-            lib.gsdpa_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
+            lib.gsdpa_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
                 ip, ip, ctypes.c_long, ctypes.c_int]
             lib.gsdpa_oracle_fwd.restype = ctypes.c_int
+            lib.gsdpa_oracle_bwd.argtypes = [dp] * 11 + [ctypes.c_int] * 9
+            lib.gsdpa_oracle_bwd.restype = ctypes.c_int
             lib.gsdpa_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -79,7 +81,7 @@ def _ptr(a, t=ctypes.c_double):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(t))
 
 
-def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n_threads=0):
+def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n_threads=0, return_lse=False):
     """Gated SDPA in float64.
 
     Shapes: X [B, L_q, d_model], Q [B, L_q, H_q, d_k], K/V [B, L_k, H_kv, d_k],
@@ -88,7 +90,9 @@ def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n
 
     ``rows``: None for every row, else a list/array of (b, i) pairs.
     Returns (O, p0): O [B, L_q, H_q, d_k] (or [n_rows, H_q, d_k]) and the
-    attention weight on key 0 per row and head, [B, L_q, H_q] (or [n_rows, H_q]).
+    attention weight on key 0 per row and head, [B, L_q, H_q] (or [n_rows, H_q]);
+    with ``return_lse``, also the natural-log softmax denominator per row and
+    head (max score + log of the sum of exp(score - max)), shaped like p0.
     """
     gm = _GATE_CODES[gate]
     Q, K, V = _f64(Q), _f64(K), _f64(V)
@@ -105,6 +109,7 @@ def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n
     if rows is None:
         O = np.empty((B, Lq, Hq, dk), np.float64)
         p0 = np.empty((B, Lq, Hq), np.float64)
+        lse = np.empty((B, Lq, Hq), np.float64) if return_lse else None
         rb = ri = None
         n = -1
     else:
@@ -114,13 +119,50 @@ def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n
         n = rows.shape[0]
         O = np.empty((n, Hq, dk), np.float64)
         p0 = np.empty((n, Hq), np.float64)
+        lse = np.empty((n, Hq), np.float64) if return_lse else None
     rc = _load().gsdpa_oracle_fwd(
-        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(O), _ptr(p0),
+        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(O), _ptr(p0), _ptr(lse),
         B, Lq, Lk, d_model, Hq, Hkv, dk, gm, int(bool(causal)),
         _ptr(rb, ctypes.c_int), _ptr(ri, ctypes.c_int), n, int(n_threads))
     if rc != 0:
         raise ValueError("oracle rejected the shapes or rows")
-    return O, p0
+    return (O, p0, lse) if return_lse else (O, p0)
+
+
+def gated_sdpa_bwd(X, Q, K, V, W_g, dO, *, gate="elementwise", causal=True):
+    """Backward of :func:`gated_sdpa` in float64, given dO = dL/dO [B, L_q, H_q, d_k].
+
+    Returns a dict with dQ, dK, dV and, with a gate, dX (the gate path's share)
+    and dW_g, each shaped like its input.
+    """
+    gm = _GATE_CODES[gate]
+    Q, K, V, dOd = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Lq, Hq, dk = Q.shape
+    _, Lk, Hkv, _ = K.shape
+    if dOd.shape != Q.shape:
+        raise ValueError(f"dO shape {dOd.shape} != {Q.shape}")
+    if gm == GATE_NONE:
+        Xd = Wd = dX = dW = None
+        d_model = 0
+    else:
+        Xd, Wd = _f64(X), _f64(W_g)
+        d_model = Xd.shape[-1]
+        dX = np.empty_like(Xd)
+        dW = np.empty_like(Wd)
+    dQ = np.empty_like(Q)
+    dK = np.empty_like(K)
+    dV = np.empty_like(V)
+    rc = _load().gsdpa_oracle_bwd(
+        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(dOd),
+        _ptr(dX), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dW),
+        B, Lq, Lk, d_model, Hq, Hkv, dk, gm, int(bool(causal)))
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes")
+    out = {"dQ": dQ, "dK": dK, "dV": dV}
+    if gm != GATE_NONE:
+        out["dX"] = dX
+        out["dW_g"] = dW
+    return out
 
 
 def sink_share(p0):

@@ -37,6 +37,25 @@
  *   O[b,i,h,c] = y_c * 1/(1 + exp(-gl))         (gate NONE: O = y)
  *   p0[b,i,h]  = p_0, the attention weight on key 0 ("10 . 门控", sec. 3.4,
  *                the share of attention that lands on the first token).
+ *   lse[b,i,h] = max s + log sum_j exp(s_j - max s), the log of the softmax
+ *                denominator (natural log), which a backward pass needs to
+ *                rebuild p without the forward's running statistics.
+ *
+ * The backward pass (gsdpa_oracle_bwd) is the chain rule of the same
+ * definition, given dO = dL/dO, written out term by term:
+ *   dy_c   = dO_c g_c                          (g = 1 without a gate)
+ *   dgl_c  = dO_c y_c g_c (1 - g_c)            elementwise; headwise: the sum
+ *                                              over c of the same product
+ *            ("解密NeurIPS最佳论文：Gated Attention…", sec. 2.2: the loss's
+ *            gradient on the gate is the upstream gradient times the ungated
+ *            context, and on the gate's input that times sigma (1 - sigma))
+ *   dW_g[m, col] += X[b,i,m] dgl_col,   dX[b,i,m] += sum_col dgl_col W_g[m, col]
+ *                                              (the gate path's share of dX)
+ *   dV[b,j,kv(h),c] += p_j dy_c
+ *   dp_j   = sum_c dy_c V[b,j,kv(h),c]
+ *   ds_j   = p_j (dp_j - sum_k p_k dp_k)       (softmax Jacobian)
+ *   dQ[b,i,h,:]     += sum_j ds_j K[b,j,kv(h),:] / sqrt(d_k)
+ *   dK[b,j,kv(h),:] += ds_j Q[b,i,h,:] / sqrt(d_k)
  *
  * Precision: every input arrives as double (the exact upcast of the fp32 or
  * bf16 values the GPU sees); nothing is rounded.
@@ -56,7 +75,7 @@ enum { ORACLE_GATE_NONE = 0, ORACLE_GATE_HEADWISE = 1, ORACLE_GATE_ELEMENTWISE =
 
 /* One query row (b, i), all heads. s is scratch of length >= L_k. */
 static void oracle_row(const double* X, const double* Q, const double* K, const double* V,
-                       const double* Wg, double* O_row, double* p0_row, double* s,
+                       const double* Wg, double* O_row, double* p0_row, double* lse_row, double* s,
                        int b, int i, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
                        int gate_mode, int causal)
 {
@@ -88,6 +107,7 @@ static void oracle_row(const double* X, const double* Q, const double* K, const 
         }
         for (long j = 0; j < n_keys; ++j) s[j] /= denom;
         if (p0_row) p0_row[h] = s[0];
+        if (lse_row) lse_row[h] = mx + log(denom);
 
         /* headwise gate: one logit for the head */
         double g_head = 1.0;
@@ -118,11 +138,12 @@ static void oracle_row(const double* X, const double* Q, const double* K, const 
  * Returns 0 on success, -1 on a shape the definition does not cover.
  *   O    : [B, L_q, H_q, d_k] when n_rows < 0, else [n_rows, H_q, d_k]
  *   p0   : [B, L_q, H_q]      when n_rows < 0, else [n_rows, H_q]   (nullable)
+ *   lse  : same shape as p0 (nullable)
  *   rows_b, rows_i : the (b, i) pairs when n_rows >= 0
  *   n_threads : OpenMP threads (<= 0: library default)
  */
 int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const double* V,
-                     const double* Wg, double* O, double* p0,
+                     const double* Wg, double* O, double* p0, double* lse,
                      int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
                      int gate_mode, int causal,
                      const int* rows_b, const int* rows_i, long n_rows, int n_threads)
@@ -154,12 +175,146 @@ int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const do
             int b, i;
             if (n_rows < 0) { b = (int)(r / Lq); i = (int)(r % Lq); }
             else            { b = rows_b[r];     i = rows_i[r]; }
-            oracle_row(X, Q, K, V, Wg, O + r * (long)Hq * dk, p0 ? p0 + r * (long)Hq : 0, s,
+            oracle_row(X, Q, K, V, Wg, O + r * (long)Hq * dk, p0 ? p0 + r * (long)Hq : 0,
+                       lse ? lse + r * (long)Hq : 0, s,
                        b, i, Lq, Lk, d_model, Hq, Hkv, dk, gate_mode, causal);
         }
         free(s);
     }
     return failed ? -1 : 0;
+}
+
+/*
+ * Backward of the layer (the chain rule in the header), serial: dK, dV and
+ * dW_g gather contributions from every row. Every output is overwritten.
+ *   dO          : [B, L_q, H_q, d_k]
+ *   dQ          : [B, L_q, H_q, d_k];  dK, dV : [B, L_k, H_kv, d_k]
+ *   dX, dW_g    : the gate path's gradients, shaped like X and W_g
+ *                 (ignored, and may be null, when gate_mode is NONE)
+ * Returns 0, or -1 on a shape the definition does not cover.
+ */
+int gsdpa_oracle_bwd(const double* X, const double* Q, const double* K, const double* V,
+                     const double* Wg, const double* dO,
+                     double* dX, double* dQ, double* dK, double* dV, double* dWg,
+                     int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
+                     int gate_mode, int causal)
+{
+    if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
+    if (Lq > Lk) return -1;
+    if (gate_mode < 0 || gate_mode > 2) return -1;
+    const int gated = gate_mode != ORACLE_GATE_NONE;
+    if (gated && (d_model < 1 || !X || !Wg || !dX || !dWg)) return -1;
+
+    const int group = Hq / Hkv;
+    const double inv_sqrt_dk = 1.0 / sqrt((double)dk);
+    const long gate_cols = (gate_mode == ORACLE_GATE_ELEMENTWISE) ? (long)Hq * dk : Hq;
+    for (long e = 0; e < (long)B * Lq * Hq * dk; ++e) dQ[e] = 0.0;
+    for (long e = 0; e < (long)B * Lk * Hkv * dk; ++e) dK[e] = dV[e] = 0.0;
+    if (gated) {
+        for (long e = 0; e < (long)B * Lq * d_model; ++e) dX[e] = 0.0;
+        for (long e = 0; e < (long)d_model * gate_cols; ++e) dWg[e] = 0.0;
+    }
+    double* p = (double*)malloc(sizeof(double) * (size_t)Lk);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
+    double* y = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* g = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* dy = (double*)malloc(sizeof(double) * (size_t)dk);
+    if (!p || !dp || !y || !g || !dy) {
+        free(p); free(dp); free(y); free(g); free(dy);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < Lq; ++i) {
+            const long a = (long)Lk - Lq + i;
+            const long n_keys = causal ? a + 1 : Lk;
+            const double* x = gated ? X + ((long)b * Lq + i) * d_model : 0;
+            for (int h = 0; h < Hq; ++h) {
+                const int kvh = h / group;
+                const double* q = Q + (((long)b * Lq + i) * Hq + h) * dk;
+                const double* dout = dO + (((long)b * Lq + i) * Hq + h) * dk;
+                /* forward quantities of the row: p, y, g */
+                double mx = -INFINITY;
+                for (long j = 0; j < n_keys; ++j) {
+                    const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double dot = 0.0;
+                    for (int c = 0; c < dk; ++c) dot += q[c] * k[c];
+                    p[j] = dot * inv_sqrt_dk;
+                    if (p[j] > mx) mx = p[j];
+                }
+                double denom = 0.0;
+                for (long j = 0; j < n_keys; ++j) {
+                    p[j] = exp(p[j] - mx);
+                    denom += p[j];
+                }
+                for (long j = 0; j < n_keys; ++j) p[j] /= denom;
+                for (int c = 0; c < dk; ++c) {
+                    double acc = 0.0;
+                    for (long j = 0; j < n_keys; ++j) acc += p[j] * V[(((long)b * Lk + j) * Hkv + kvh) * dk + c];
+                    y[c] = acc;
+                }
+                if (gate_mode == ORACLE_GATE_HEADWISE) {
+                    double gl = 0.0;
+                    for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + h];
+                    const double gh = 1.0 / (1.0 + exp(-gl));
+                    for (int c = 0; c < dk; ++c) g[c] = gh;
+                } else if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
+                    for (int c = 0; c < dk; ++c) {
+                        double gl = 0.0;
+                        const long col = (long)h * dk + c;
+                        for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + col];
+                        g[c] = 1.0 / (1.0 + exp(-gl));
+                    }
+                } else {
+                    for (int c = 0; c < dk; ++c) g[c] = 1.0;
+                }
+                /* gate path */
+                for (int c = 0; c < dk; ++c) dy[c] = dout[c] * g[c];
+                if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
+                    for (int c = 0; c < dk; ++c) {
+                        const double dgl = dout[c] * y[c] * g[c] * (1.0 - g[c]);
+                        const long col = (long)h * dk + c;
+                        double* dx = dX + ((long)b * Lq + i) * d_model;
+                        for (int m = 0; m < d_model; ++m) {
+                            dWg[(long)m * gate_cols + col] += x[m] * dgl;
+                            dx[m] += dgl * Wg[(long)m * gate_cols + col];
+                        }
+                    }
+                } else if (gate_mode == ORACLE_GATE_HEADWISE) {
+                    double dgl = 0.0;
+                    for (int c = 0; c < dk; ++c) dgl += dout[c] * y[c] * g[c] * (1.0 - g[c]);
+                    double* dx = dX + ((long)b * Lq + i) * d_model;
+                    for (int m = 0; m < d_model; ++m) {
+                        dWg[(long)m * gate_cols + h] += x[m] * dgl;
+                        dx[m] += dgl * Wg[(long)m * gate_cols + h];
+                    }
+                }
+                /* attention path */
+                double sum_pdp = 0.0;
+                for (long j = 0; j < n_keys; ++j) {
+                    const double* v = V + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double* dv = dV + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double acc = 0.0;
+                    for (int c = 0; c < dk; ++c) {
+                        acc += dy[c] * v[c];
+                        dv[c] += p[j] * dy[c];
+                    }
+                    dp[j] = acc;
+                    sum_pdp += p[j] * acc;
+                }
+                double* dq = dQ + (((long)b * Lq + i) * Hq + h) * dk;
+                for (long j = 0; j < n_keys; ++j) {
+                    const double ds = p[j] * (dp[j] - sum_pdp) * inv_sqrt_dk;
+                    const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double* dkk = dK + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    for (int c = 0; c < dk; ++c) {
+                        dq[c] += ds * k[c];
+                        dkk[c] += ds * q[c];
+                    }
+                }
+            }
+        }
+    free(p); free(dp); free(y); free(g); free(dy);
+    return 0;
 }
 
 /* Number of threads an OpenMP region would use (1 without OpenMP). */
