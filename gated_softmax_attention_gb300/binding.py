@@ -26,6 +26,7 @@ _VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "gsdpa_workspace_bytes": (_SZ, [_I] * 10),
     "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_check_device_error": (_I, [_VP]),
     "gsdpa_status_string": (ctypes.c_char_p, [_I]),
     "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
@@ -111,6 +112,22 @@ def gated_sdpa_fwd(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out
     the current CUDA device, float32 or bfloat16 (all the same dtype).
     Returns (O, sink) where sink is None unless requested.
     """
+    O, sink, _ = _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, None, workspace, stream)
+    return O, sink
+
+
+def gated_sdpa_fwd_train(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out=None, sink=None,
+                         want_sink=False, lse=None, workspace=None, stream=None):
+    """gated_sdpa_fwd that also returns lse [B, H_q, L_q] float32, the natural
+    log of each row's softmax denominator (bf16 prefill). Returns (O, sink, lse)."""
+    import torch
+    B, L_q, H_q, _ = Q.shape
+    if lse is None:
+        lse = torch.empty((B, H_q, L_q), dtype=torch.float32, device=Q.device)
+    return _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream)
+
+
+def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream):
     import torch
     if Q.dtype == torch.bfloat16:
         dtype = BF16
@@ -134,14 +151,19 @@ def gated_sdpa_fwd(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
-    st = fwd_raw(_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V),
-                 _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink),
-                 B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, causal, dtype,
-                 _ptr(workspace) if need > 0 else None, need if need > 0 else 0,
-                 ctypes.c_void_p(s.cuda_stream))
+    args = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V),
+            _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink)]
+    tail = [B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
+            _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)]
+    if lse is None:
+        st = int(load().gated_sdpa_fwd(*args, *tail))
+        where = "gated_sdpa_fwd"
+    else:
+        st = int(load().gated_sdpa_fwd_train(*args, _ptr(lse), *tail))
+        where = "gated_sdpa_fwd_train"
     if st != OK:
-        raise GsdpaError(st, "gated_sdpa_fwd")
-    return out, sink
+        raise GsdpaError(st, where)
+    return out, sink, lse
 
 
 def decode_noalloc(X, Q, K, V, W_g=None, *, gate="elementwise", out=None, sink=None, want_sink=False, stream=None):

@@ -243,10 +243,12 @@ size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int 
     return plan_workspace(p, kPlanSms).total;
 }
 
-int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
-                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
-                   int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
+             float* lse, int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     Problem p{};
+    p.lse = lse;
     p.X = X;
     p.Q = Q;
     p.K = K;
@@ -331,6 +333,25 @@ int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, c
     }
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
     return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
+}
+}  // namespace
+
+int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
+                   int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
+                    workspace, workspace_bytes, stream);
+}
+
+int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,
+                         float* sink, float* lse, int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                         int gate_mode, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    if (!lse) return GSDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return GSDPA_ERR_ALIGNMENT;
+    if (dtype != GSDPA_BF16 || L_q == 1) return GSDPA_ERR_UNSUPPORTED;   // the bf16 prefill kernels write it
+    return fwd_impl(X, Q, K, V, W_g, O, sink, lse, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
+                    workspace, workspace_bytes, stream);
 }
 
 int gsdpa_check_device_error(void* stream) {

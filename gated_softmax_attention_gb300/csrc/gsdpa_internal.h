@@ -16,6 +16,7 @@ struct Problem {
     const void* Wg;
     void* O;
     float* sink;
+    float* lse;      // [B, Hq, Lq] natural-log softmax denominators, or null
     int B, Lq, Lk, d_model, Hq, Hkv, dk;
     int gate_mode;   // 0 none, 1 headwise, 2 elementwise
     int causal;

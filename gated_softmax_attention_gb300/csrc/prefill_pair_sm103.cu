@@ -113,6 +113,7 @@ struct PairArgs {
     float sink_scale;               // 2^F
     double sink_inv;                // 2^-F / L_q
     int sink_arrivals;              // 4 warps per 128-row query tile
+    float* lse;                     // [B, Hq, Lq] or null
     __nv_bfloat16* O;        // [B, Lq, Hq, d_k]
     WaitCtl ctl;
 };
@@ -515,7 +516,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (mm == -INFINITY) mm = 0.f;   // (rows past L_q only)
             const float a_me = (m == -INFINITY) ? 0.f : ex2_approx(m - mm);
             const float a_ot = (o.x == -INFINITY) ? 0.f : ex2_approx(o.x - mm);
-            const float inv = 1.0f / (l * a_me + o.y * a_ot);
+            const float denom = l * a_me + o.y * a_ot;   // relative to 2^mm
+            const float inv = 1.0f / denom;
+            // log of the softmax denominator (natural log), from warpgroup 0
+            if (args.lse && p == 0 && U.mine && i < args.Lq)
+                args.lse[((long)b * args.Hq + h) * args.Lq + i] = (mm + log2f(denom)) * 0.6931471805599453f;
             const float s0 = (p == 0 ? a_me : a_ot) * inv;   // weight of O_0
             const float s1 = (p == 0 ? a_ot : a_me) * inv;   // weight of O_1
             const bool has1 = nkv > 1;                        // O_1 holds results only then
@@ -645,6 +650,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
+    a.lse = p.lse;
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;

@@ -51,6 +51,7 @@ namespace {
 constexpr int kTile = 128;           // query rows per tile, keys per K/V tile
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 // Register split: warpgroup 0 (producer, MMA, spare) gives registers to the
 // two softmax warpgroups. The launch must provide 384 x kRegsLaunchMin.
@@ -91,6 +92,7 @@ struct PrefillArgs {
     float sink_scale;               // 2^F
     double sink_inv;                // 2^-F / L_q
     int sink_arrivals;              // 4 warps per query tile
+    float* lse;                     // [B, Hq, Lq] or null
     WaitCtl ctl;
 };
 
@@ -482,6 +484,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (ok_epi) {
             // ---- epilogue: out = O / l (.) gate -> bf16 -> global (one 2*d_k-byte row per thread)
             const float inv_l = 1.0f / l;
+            // log of the softmax denominator (natural log; m and l are in log2 units)
+            if (args.lse && i < args.Lq)
+                args.lse[((long)b * args.Hq + h) * args.Lq + i] = (m + log2f(l)) * kLn2;
             // first-token share of this warp's 32 rows: added now, its result read after the stores
             unsigned long long sink_old = 0, sink_add = 0;
             if (args.sink_word) {
@@ -614,6 +619,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
+    a.lse = p.lse;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 

@@ -138,6 +138,23 @@ GSDPA_API int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const 
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The forward a training step runs: gated_sdpa_fwd, and also, for every
+ * batch b, query head h and query row i, the natural log of the softmax
+ * denominator, lse[b, h, i] = log sum_j exp(s_j) over the row's visible
+ * scores s_j = Q.K / sqrt(d_k) ("GatedAttention [2025]", sec. 1.2.1: the
+ * softmax of the SDPA equation; the backward rebuilds the weights from it).
+ *
+ *   lse : device float32 [B, H_q, L_q] (head-major), 4-byte aligned; required.
+ *   Other arguments and the workspace as for gated_sdpa_fwd.
+ * bf16 prefill only (L_q != 1): GSDPA_ERR_UNSUPPORTED otherwise.
+ */
+GSDPA_API int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                   void* O, float* sink, float* lse,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits inside the kernels set when they run out. Returns GSDPA_OK,
  * GSDPA_ERR_DEVICE_TIMEOUT, or GSDPA_ERR_LAUNCH if the stream itself reports

@@ -272,3 +272,32 @@ def test_repeated_calls_on_one_workspace(w):
     ref, p0 = run_oracle(w, t)
     assert_close(w, runs[0][0].double().cpu().numpy(), ref, w.name)
     np.testing.assert_allclose(runs[0][1].double().cpu().numpy(), oracle.sink_share(p0), atol=sink_tol(w))
+
+
+# ------------------------------------------------------------------ the training forward's log-sum-exp
+
+# The LSE's error comes from the fp32 scores (exact bf16 products, fp32 sums
+# of 128 terms: ~1e-5 relative to the score scale) and the fp32 sum of the
+# exponentials (ex2.approx, ~1e-6 relative): 2e-3 absolute leaves a wide margin.
+LSE_ATOL = 2e-3
+
+LSE_CASES = [
+    small("bf16", name="lse_elementwise"),
+    small("bf16", name="lse_gqa_headwise", gate="headwise", H_q=8, H_kv=2),
+    small("bf16", name="lse_no_gate_ragged_suffix", gate="none", L_q=77, L_k=300),
+    small("bf16", name="lse_pair_long_keys", B=1, L_q=384, L_k=16384, H_q=2, H_kv=1),
+]
+
+
+@pytest.mark.parametrize("w", LSE_CASES, ids=lambda w: w.name)
+def test_forward_train_writes_lse(w):
+    t = make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
+                                        causal=w.causal)
+    assert gb.check_device_error() == gb.OK
+    ref, _, lse_ref = oracle.gated_sdpa(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=w.gate, causal=w.causal,
+                                        return_lse=True)
+    assert_close(w, O.double().cpu().numpy(), ref, w.name)
+    got = lse.double().cpu().numpy()                      # [B, H_q, L_q]
+    np.testing.assert_allclose(got, lse_ref.transpose(0, 2, 1), atol=LSE_ATOL, rtol=0)
