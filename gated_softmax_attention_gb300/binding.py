@@ -27,6 +27,8 @@ SIGNATURES = {
     "gsdpa_workspace_bytes": (_SZ, [_I] * 10),
     "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gsdpa_bwd_workspace_bytes": (_SZ, [_I] * 8),
+    "gated_sdpa_bwd": (_I, [_VP] * 13 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_check_device_error": (_I, [_VP]),
     "gsdpa_status_string": (ctypes.c_char_p, [_I]),
     "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
@@ -164,6 +166,42 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
     if st != OK:
         raise GsdpaError(st, where)
     return out, sink, lse
+
+
+def bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise") -> int:
+    n = load().gsdpa_bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, GATE_CODES[gate])
+    if n == ctypes.c_size_t(-1).value:
+        raise GsdpaError(ERR_UNSUPPORTED, "gsdpa_bwd_workspace_bytes")
+    return int(n)
+
+
+def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=True, workspace=None, stream=None):
+    """Backward through the C ABI (bf16, d_k = 128): returns a dict with dQ, dK,
+    dV and, with a gate, dX (the gate path's share) and dW_g."""
+    import torch
+    gm = GATE_CODES[gate]
+    for t in [Q, K, V, O, dO] + ([X, W_g] if gm != GATE_NONE else []):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("inputs must be contiguous bf16 CUDA tensors")
+    B, L_q, H_q, d_k = Q.shape
+    L_k, H_kv = K.shape[1], K.shape[2]
+    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    out = {"dQ": torch.empty_like(Q), "dK": torch.empty_like(K), "dV": torch.empty_like(V)}
+    if gm != GATE_NONE:
+        out["dX"] = torch.empty_like(X)
+        out["dW_g"] = torch.empty_like(W_g)
+    need = bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gated_sdpa_bwd(
+        _ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
+        _ptr(O), _ptr(dO), _ptr(lse), _ptr(out.get("dX")), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+        _ptr(out.get("dW_g")), B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16,
+        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+    if st != OK:
+        raise GsdpaError(st, "gated_sdpa_bwd")
+    return out
 
 
 def decode_noalloc(X, Q, K, V, W_g=None, *, gate="elementwise", out=None, sink=None, want_sink=False, stream=None):

@@ -1,0 +1,942 @@
+// bwd_sm103.cu -- the backward pass of the gated attention layer (bf16,
+// d_k = 128) on sm_103a.
+//
+// Given dO = dL/dO for O = Y (.) G, Y = softmax(Q K^T / sqrt(d_k) + mask) V,
+// G = sigma(X W_g) ("GatedAttention [2025]", sec. 1.2.1 and 1.2.2), the chain
+// rule gives (the gate's part: "解密NeurIPS最佳论文：Gated Attention…", sec.
+// 2.2, gradient on the gate's input = upstream gradient x context x
+// sigma (1 - sigma)):
+//   dY   = dO (.) G                        the attention's upstream gradient
+//   dGl  = dO (.) Y (.) G (1 - G) = dO (.) O (.) (1 - G)       (Y G = O)
+//   D_i  = sum_c dY_ic Y_ic = sum_c dO_ic O_ic                  per row, head
+//   p_ij = exp(s_ij - lse_i)               lse from the training forward
+//   dS   = p (.) (dY V^T - D) / sqrt(d_k)
+//   dQ   = dS K,   dK = dS^T Q,   dV = p^T dY   (summed over a GQA group)
+//   dW_g = X^T dGl,   dX (gate path) = dGl W_g^T
+// Headwise gates broadcast G over d_k, so dGl sums over the head's columns.
+//
+// Kernels (all tcgen05, accumulators in TMEM, operands staged by TMA):
+//   bwd_prep_kernel    one warp per (row, head): dY, D, dGl and lse in log2
+//                      units into padded per-(b, h) arrays (whole 128-row
+//                      tiles are 512-byte bulk copies);
+//   bwd_dq_kernel      per (b, h, 128-row query tile): S = Q K^T and
+//                      dP = dY V^T (shared-memory operands), dS into TMEM,
+//                      dQ += dS K (dS read from TMEM);
+//   bwd_dkdv_kernel    per (b, kv head, 128-key tile): the key tile stays in
+//                      shared memory while (Q, dY, lse, D) of every query tile
+//                      of every head of the group stream through a ring;
+//                      S^T = K Q^T, dP^T = V dY^T, then dV += P^T dY and
+//                      dK += dS^T Q, so the group's sum needs no atomics;
+//   gemm_bf16_kernel   dX = dGl W_g^T (both operands K-major) and
+//                      dW_g = X^T dGl (both MN-major), read in place.
+// dQ and dK/dV recompute S and dP each (two passes instead of atomics: the
+// result does not depend on the order of the CTAs, and each pass keeps its
+// accumulators in tensor memory).
+#include "gsdpa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cuda_fp16.h>
+
+namespace gsdpa {
+namespace {
+
+constexpr int HD = 128;
+constexpr int kTile = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t TILE_BYTES = kTile * HD * 2;     // one [128 x 128] bf16 tile (two 64-column blocks)
+constexpr uint32_t STG_BYTES = kTile * 32 * 2;      // one 32-column output chunk (64-byte rows)
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) into
+// shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void unpack_bf16x4(uint2 w, float (&f)[4]) {
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xffff0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xffff0000u);
+}
+
+// ------------------------------------------------------------------ prep
+
+struct PrepArgs {
+    const __nv_bfloat16* dO;   // [B, Lq, Hq, HD]
+    const __nv_bfloat16* O;    // [B, Lq, Hq, HD]
+    const float* lse;          // [B, Hq, Lq] natural log
+    const __half* gate_sig;    // elementwise: sigma(X W_g) [B*Lq, Hq*HD] fp16, else null
+    const float* gate_part;    // headwise: logit partials [splits, B*Lq, Hq], else null
+    int gate_splits;
+    __nv_bfloat16* dY;         // [B, Lq, Hq, HD]
+    __nv_bfloat16* dGl;        // [B*Lq, G] (G = Hq*HD | Hq) or null
+    float* Dv;                 // [B, Hq, Lq_pad]
+    float* lse2;               // [B, Hq, Lq_pad]: lse * log2(e); padding rows +inf
+    int B, Lq, Hq, Lq_pad, gate_mode;
+};
+
+// One warp per (b, h, padded row i); lane c holds columns 4c .. 4c + 3.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepArgs a) {
+    const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long)a.B * a.Hq * a.Lq_pad) return;
+    const int i = (int)(wid % a.Lq_pad);
+    const long bh = wid / a.Lq_pad;
+    const int h = (int)(bh % a.Hq);
+    const int b = (int)(bh / a.Hq);
+    if (i >= a.Lq) {   // padding rows: no weight (p = exp2(s - inf) = 0), no D
+        if (lane == 0) {
+            a.Dv[wid] = 0.f;
+            a.lse2[wid] = INFINITY;
+        }
+        return;
+    }
+    const long row = (long)b * a.Lq + i;
+    const long base = (row * a.Hq + h) * HD + lane * 4;
+    float dof[4], of[4];
+    unpack_bf16x4(*reinterpret_cast<const uint2*>(a.dO + base), dof);
+    unpack_bf16x4(*reinterpret_cast<const uint2*>(a.O + base), of);
+    float g[4] = {1.f, 1.f, 1.f, 1.f};
+    if (a.gate_mode == 2) {
+        const uint2 gw = *reinterpret_cast<const uint2*>(a.gate_sig + base);
+        const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gw.x));
+        const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gw.y));
+        g[0] = g01.x;
+        g[1] = g01.y;
+        g[2] = g23.x;
+        g[3] = g23.y;
+    } else if (a.gate_mode == 1) {
+        float gl = 0.f;
+        const long rows = (long)a.B * a.Lq;
+        for (int s = 0; s < a.gate_splits; ++s) gl += a.gate_part[(s * rows + row) * a.Hq + h];
+        const float gh = 1.0f / (1.0f + exp2f(-gl * kLog2e));
+        g[0] = g[1] = g[2] = g[3] = gh;
+    }
+    float d = 0.f, dgl_h = 0.f, dgl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        d = fmaf(dof[e], of[e], d);
+        dgl[e] = dof[e] * of[e] * (1.0f - g[e]);
+        dgl_h += dgl[e];
+    }
+    *reinterpret_cast<uint2*>(a.dY + base) =
+        make_uint2(pack_bf16x2(dof[0] * g[0], dof[1] * g[1]), pack_bf16x2(dof[2] * g[2], dof[3] * g[3]));
+    if (a.gate_mode == 2)
+        *reinterpret_cast<uint2*>(a.dGl + base) =
+            make_uint2(pack_bf16x2(dgl[0], dgl[1]), pack_bf16x2(dgl[2], dgl[3]));
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+        d += __shfl_xor_sync(0xffffffffu, d, sh);
+        dgl_h += __shfl_xor_sync(0xffffffffu, dgl_h, sh);
+    }
+    if (lane == 0) {
+        a.Dv[wid] = d;
+        a.lse2[wid] = a.lse[((long)b * a.Hq + h) * a.Lq + i] * kLog2e;
+        if (a.gate_mode == 1) a.dGl[row * a.Hq + h] = __float2bfloat16_rn(dgl_h);
+    }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+// C [M x N] (bf16, row-major, ldc) = A B with fp32 accumulation in TMEM.
+// A_MN: A stored as [K][M] (M contiguous), else [M][K]; B_MN: B stored as
+// [K][N], else B^T stored as [N][K]. 128 x 128 tiles, K chunks of 64.
+constexpr int kGemmThreads = 192;
+constexpr int kGemmNS = 4;
+constexpr uint32_t kGemmOpBytes = 128 * 64 * 2;   // 16 KB per operand per chunk
+constexpr uint32_t kGemmStage = 2 * kGemmOpBytes;
+constexpr uint32_t kGemmOffBar = kGemmNS * kGemmStage;
+constexpr uint32_t kGemmOffMisc = kGemmOffBar + (2 * kGemmNS + 2) * 8;
+constexpr uint32_t kGemmSmem = kGemmOffMisc + 16 + 1024;
+
+struct GemmArgs {
+    __nv_bfloat16* C;
+    int M, N, K, ldc;
+    int m_tiles, nkc;
+    WaitCtl ctl;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemmOffBar);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kGemmNS;
+    uint64_t* acc_full = bars + 2 * kGemmNS;
+    uint64_t* drain = bars + 2 * kGemmNS + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kGemmOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kGemmOffMisc + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int m0 = (blockIdx.x % args.m_tiles) * 128;
+    const int n0 = (blockIdx.x / args.m_tiles) * 128;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGemmNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 128);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+            bool ok = true;
+            for (int kc = 0; kc < args.nkc; ++kc) {
+                if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.ctl))) break;
+                mbar_arrive_expect_tx(&full[stage], kGemmStage);
+                armed |= 1u << stage;
+                armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                uint8_t* st = smem + stage * kGemmStage;
+                if (A_MN) {
+                    for (int cb = 0; cb < 2; ++cb) tma_load_2d(st + cb * 8192, &tmA, m0 + cb * 64, kc * 64, &full[stage]);
+                } else {
+                    tma_load_2d(st, &tmA, kc * 64, m0, &full[stage]);
+                }
+                if (B_MN) {
+                    for (int cb = 0; cb < 2; ++cb)
+                        tma_load_2d(st + kGemmOpBytes + cb * 8192, &tmB, n0 + cb * 64, kc * 64, &full[stage]);
+                } else {
+                    tma_load_2d(st + kGemmOpBytes, &tmB, kc * 64, n0, &full[stage]);
+                }
+                if (++stage == kGemmNS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int s = 0; s < kGemmNS; ++s)
+                    if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, args.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        constexpr uint32_t idG = idesc_bf16_f32(128, 128, A_MN, B_MN);
+        constexpr uint32_t HI = desc_sw128_hi(1024);
+        const uint32_t base = smem_u32(smem);
+        for (int kc = 0; kc < args.nkc; ++kc) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            const uint32_t st = base + stage * kGemmStage;
+            // K-major: 64-element K rows of 128 B, K advances 32 B per MMA;
+            // MN-major: 64-wide M/N blocks 8 KB apart, K advances 16 rows (2 KB)
+            const uint32_t a0 = desc_sw128_lo(st, A_MN ? 8192 : 16);
+            const uint32_t b0 = desc_sw128_lo(st + kGemmOpBytes, B_MN ? 8192 : 16);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ss_elect(tmem, a0 + kk * (A_MN ? (2048 >> 4) : (32 >> 4)), HI,
+                             b0 + kk * (B_MN ? (2048 >> 4) : (32 >> 4)), HI, idG, (kc | kk) != 0 ? 1u : 0u);
+            mma_commit_elect(&empty[stage]);
+            if (++stage == kGemmNS) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (ok) {
+            mma_commit_elect(acc_full);
+        } else {
+            volatile int never = 0;
+            mma_commit_elect(drain);
+            mbar_wait(drain, 0, &never, args.ctl);
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        const bool ok = args.nkc > 0 && __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, args.ctl));
+        tc_fence_after();
+        const int r = m0 + row;
+        __nv_bfloat16* dst = args.C + (long)r * args.ldc;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t v[32];
+            if (ok) {   // (warp-uniform: every lane loads, only rows < M store)
+                tmem_ld32(tmem + lane_base + cb * 32, v);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            const int c = n0 + cb * 32;
+            if (r >= args.M) continue;
+            if (c + 32 <= args.N && (args.ldc & 7) == 0) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8)
+                    *reinterpret_cast<uint4*>(dst + c + e) = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                        pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                        pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5])),
+                        pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7])));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (c + e < args.N) dst[c + e] = __float2bfloat16_rn(__uint_as_float(v[e]));
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ------------------------------------------------------------------ shared by dQ and dK/dV
+
+constexpr int kAttnThreads = 256;   // warp 0 copies, warp 1 MMAs, warps 4..7 one row each
+constexpr int kRingNS = 4;          // dQ: K/V tile ring
+constexpr int kQNS = 2;             // dK/dV: (Q, dY, lse, D) ring
+constexpr uint32_t VEC_BYTES = kTile * 4;   // 128 floats
+
+struct AttnArgs {
+    int B, Lq, Lk, Hq, Hkv, causal, n_qtiles, n_ktiles, Lq_pad;
+    const float* lse2;   // [B, Hq, Lq_pad] log2 units
+    const float* Dv;     // [B, Hq, Lq_pad]
+    WaitCtl ctl;
+};
+
+// Let every MMA this warp issued complete (after a wait gave up), so that
+// tensor memory can be freed.
+__device__ __forceinline__ void drain_mmas(uint64_t* drain, const WaitCtl& ctl) {
+    volatile int never = 0;
+    WaitCtl c2 = ctl;
+    if (c2.limit_ns < 1000000000ull) c2.limit_ns = 1000000000ull;
+    mma_commit_elect(drain);
+    mbar_wait(drain, 0, &never, c2);
+    __syncwarp();
+}
+
+// 32 fp32 columns -> bf16 -> a 64-byte-swizzled [128 x 32] staging chunk
+__device__ __forceinline__ void stage_chunk32(uint8_t* chunk, int row, const uint32_t (&v)[32]) {
+    const int sw = (row >> 1) & 3;
+    uint8_t* dst = chunk + row * 64;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(dst + ((q ^ sw) << 4)) = make_uint4(
+            pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+}
+
+// ------------------------------------------------------------------ dQ
+
+struct DqCfg {
+    static constexpr uint32_t OFF_Q = 0;                        // Q tile
+    static constexpr uint32_t OFF_DY = TILE_BYTES;              // dY tile
+    static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // K_j, V_j, K_j+1, ...
+    static constexpr uint32_t OFF_STG = OFF_RING + kRingNS * TILE_BYTES;   // dQ output, 4 chunks
+    static constexpr uint32_t OFF_BAR = OFF_STG + 4 * STG_BYTES;
+    static constexpr int NBAR = 2 * kRingNS + 5;   // full, empty, q_full, s_full, p_full, g_full, drain
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+};
+
+// Unit = (b, h, 128-row query tile), heaviest first (last tiles first when causal).
+// TMEM: S [0, 128) (dS, packed bf16, over its first 64 columns), dP [128, 256), dQ [256, 384).
+__global__ void __launch_bounds__(kAttnThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdY,
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __grid_constant__ CUtensorMap tmdQ, const AttnArgs args) {
+    using C = DqCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kRingNS;
+    uint64_t* q_full = bars + 2 * kRingNS;
+    uint64_t* s_full = q_full + 1;
+    uint64_t* p_full = q_full + 2;
+    uint64_t* g_full = q_full + 3;
+    uint64_t* drain = q_full + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    const int per_tile = args.B * args.Hq;
+    const int qt = args.causal ? args.n_qtiles - 1 - (int)blockIdx.x / per_tile : (int)blockIdx.x / per_tile;
+    const int h = ((int)blockIdx.x % per_tile) % args.Hq;
+    const int b = ((int)blockIdx.x % per_tile) / args.Hq;
+    const int kvh = h / (args.Hq / args.Hkv);
+    const int q0 = qt * kTile;
+    const long off = (long)args.Lk - args.Lq;
+    long kend = args.Lk;
+    if (args.causal && off + q0 + kTile < kend) kend = off + q0 + kTile;
+    const int nkv = (int)((kend + kTile - 1) / kTile);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRingNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(g_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmdY);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdQ);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- copies: Q, dY once; then K_0, V_0, K_1, V_1, ... through the ring
+            mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+            tma_load_5d(smem + C::OFF_Q, &tmQ, 0, h, q0, b, 0, q_full);
+            tma_load_5d(smem + C::OFF_DY, &tmdY, 0, h, q0, b, 0, q_full);
+            uint32_t armed = 0, armed_phase = 0;
+            bool ok = true;
+            for (int item = 0; item < 2 * nkv && ok; ++item) {
+                const int s = item % kRingNS;
+                const uint32_t ph = (item / kRingNS) & 1;
+                if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.ctl))) break;
+                mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+                armed |= 1u << s;
+                armed_phase = (armed_phase & ~(1u << s)) | (ph << s);
+                tma_load_5d(smem + C::OFF_RING + s * TILE_BYTES, (item & 1) ? &tmV : &tmK, 0, kvh, (item >> 1) * kTile,
+                            b, 0, &full[s]);
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int s = 0; s < kRingNS; ++s)
+                    if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, args.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMAs: per key tile S = Q K^T, dP = dY V^T; then dQ += dS K
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t HI = desc_sw128_hi(1024);
+        const uint32_t base = smem_u32(smem);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, args.ctl));
+        tc_fence_after();
+        const uint32_t q_lo = desc_sw128_lo(base + C::OFF_Q, 16);
+        const uint32_t dy_lo = desc_sw128_lo(base + C::OFF_DY, 16);
+        for (int j = 0; j < nkv && ok; ++j) {
+            const int ik = 2 * j, iv = 2 * j + 1;
+            const uint32_t k_st = base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES;
+            const uint32_t v_st = base + C::OFF_RING + (iv % kRingNS) * TILE_BYTES;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[ik % kRingNS], (ik / kRingNS) & 1, abort_flag,
+                                                         args.ctl))))
+                break;
+            tc_fence_after();
+            mma_ss_k128<16384, 16384>(tmem + 0, q_lo, desc_sw128_lo(k_st, 16), HI, idS, 0);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[iv % kRingNS], (iv / kRingNS) & 1, abort_flag,
+                                                         args.ctl))))
+                break;
+            tc_fence_after();
+            mma_ss_k128<16384, 16384>(tmem + 128, dy_lo, desc_sw128_lo(v_st, 16), HI, idS, 0);
+            mma_commit_elect(&empty[iv % kRingNS]);   // V_j: read once
+            mma_commit_elect(s_full);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, j & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            // dQ += dS K_j: dS (packed bf16 over S) from TMEM, K_j as the MN-major B operand
+            mma_ts_k128(tmem + 256, tmem + 0, desc_sw128_lo(k_st, 16384), HI, idO, j != 0);
+            mma_commit_elect(&empty[ik % kRingNS]);
+        }
+        if (ok) {
+            mma_commit_elect(g_full);
+        } else {
+            drain_mmas(drain, args.ctl);
+        }
+    } else if (warp >= 4) {
+        // ---- one query row per thread: dS = p (dP - D) / sqrt(d_k), then the dQ epilogue
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        const long i = (long)q0 + row;
+        const long pidx = ((long)b * args.Hq + h) * args.Lq_pad + i;
+        const float lse2 = args.lse2[pidx];
+        const float D = args.Dv[pidx];
+        const float sl2 = kLog2e / sqrtf((float)HD);
+        const float isq = 1.0f / sqrtf((float)HD);
+        bool ok = true;
+        for (int j = 0; j < nkv && ok; ++j) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            const long kv0 = (long)j * kTile;
+            long lim_l = (long)args.Lk - 1 - kv0;   // last visible column of this row in this tile
+            if (args.causal && off + i - kv0 < lim_l) lim_l = off + i - kv0;
+            const int lim = lim_l > 127 ? 127 : (int)lim_l;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tmem + lane_base + c * 32, sv);
+                tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int col = c * 32 + e;
+                    const float p0 = (col <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
+                    const float p1 = (col + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
+                    pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - D) * isq,
+                                             p1 * (__uint_as_float(dp[e + 1]) - D) * isq);
+                }
+                tmem_st16(tmem + lane_base + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
+        tc_fence_after();
+        const bool ok_epi = named_bar_and(1, 128, ok);
+        if (ok_epi) {
+            uint8_t* stg = smem + C::OFF_STG;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+                tmem_wait_ld();
+                stage_chunk32(stg + c * STG_BYTES, row, v);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (row == 0) {
+                for (int c = 0; c < 4; ++c) tma_store_4d(&tmdQ, stg + c * STG_BYTES, c * 32, h, q0, b);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ dK, dV
+
+struct DkvCfg {
+    static constexpr uint32_t OFF_K = 0;                        // K_j
+    static constexpr uint32_t OFF_V = TILE_BYTES;               // V_j
+    static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // [Q_i | dY_i | lse2_i | D_i] per stage
+    static constexpr uint32_t STAGE = 2 * TILE_BYTES + 2 * VEC_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_RING + kQNS * STAGE;
+    static constexpr int NBAR = 2 * kQNS + 5;   // full, empty, kv_full, s_full, p_full, g_full, drain
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+    static_assert(8 * STG_BYTES <= kQNS * STAGE, "the output staging reuses the ring");
+};
+
+// Unit = (b, kv head, 128-key tile), key tile 0 first (the most query tiles when causal).
+// Per step (query head h of the group, query tile t): S^T = K Q^T, dP^T = V dY^T;
+// one key row per thread: P^T and dS^T (packed bf16) over their first 64 columns;
+// then dV += P^T dY, dK += dS^T Q.
+// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 384), dK [384, 512).
+__global__ void __launch_bounds__(kAttnThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdY,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                const AttnArgs args) {
+    using C = DkvCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kQNS;
+    uint64_t* kv_full = bars + 2 * kQNS;
+    uint64_t* s_full = kv_full + 1;
+    uint64_t* p_full = kv_full + 2;
+    uint64_t* g_full = kv_full + 3;
+    uint64_t* drain = kv_full + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    const int per_tile = args.B * args.Hkv;
+    const int kt = (int)blockIdx.x / per_tile;
+    const int kvh = ((int)blockIdx.x % per_tile) % args.Hkv;
+    const int b = ((int)blockIdx.x % per_tile) / args.Hkv;
+    const int group = args.Hq / args.Hkv;
+    const int k0 = kt * kTile;
+    const long off = (long)args.Lk - args.Lq;
+    // query tiles that see any key of this tile: query i sees key k0 when off + i >= k0
+    int t0 = 0;
+    if (args.causal && k0 - off > 0) t0 = (int)((k0 - off) / kTile);
+    const int nqt = args.n_qtiles - t0;
+    const int steps = group * nqt;   // (head of the group, query tile), head-major
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(kv_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(g_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmdY);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdK);
+        tma_prefetch_desc(&tmdV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
+            tma_load_5d(smem + C::OFF_K, &tmK, 0, kvh, k0, b, 0, kv_full);
+            tma_load_5d(smem + C::OFF_V, &tmV, 0, kvh, k0, b, 0, kv_full);
+            uint32_t armed = 0, armed_phase = 0;
+            bool ok = true;
+            for (int it = 0; it < steps && ok; ++it) {
+                const int s = it % kQNS;
+                const uint32_t ph = (it / kQNS) & 1;
+                const int h = kvh * group + it / nqt;
+                const int q0 = (t0 + it % nqt) * kTile;
+                if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.ctl))) break;
+                mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES + 2 * VEC_BYTES);
+                armed |= 1u << s;
+                armed_phase = (armed_phase & ~(1u << s)) | (ph << s);
+                uint8_t* st = smem + C::OFF_RING + s * C::STAGE;
+                tma_load_5d(st, &tmQ, 0, h, q0, b, 0, &full[s]);
+                tma_load_5d(st + TILE_BYTES, &tmdY, 0, h, q0, b, 0, &full[s]);
+                const long vidx = ((long)b * args.Hq + h) * args.Lq_pad + q0;
+                bulk_load_1d(st + 2 * TILE_BYTES, args.lse2 + vidx, VEC_BYTES, &full[s]);
+                bulk_load_1d(st + 2 * TILE_BYTES + VEC_BYTES, args.Dv + vidx, VEC_BYTES, &full[s]);
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int s = 0; s < kQNS; ++s)
+                    if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, &never, args.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t HI = desc_sw128_hi(1024);
+        const uint32_t base = smem_u32(smem);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort_flag, args.ctl));
+        tc_fence_after();
+        const uint32_t k_lo = desc_sw128_lo(base + C::OFF_K, 16);
+        const uint32_t v_lo = desc_sw128_lo(base + C::OFF_V, 16);
+        for (int it = 0; it < steps && ok; ++it) {
+            const int s = it % kQNS;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (it / kQNS) & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            const uint32_t st = base + C::OFF_RING + s * C::STAGE;
+            mma_ss_k128<16384, 16384>(tmem + 0, k_lo, desc_sw128_lo(st, 16), HI, idS, 0);                // S^T
+            mma_ss_k128<16384, 16384>(tmem + 128, v_lo, desc_sw128_lo(st + TILE_BYTES, 16), HI, idS, 0);  // dP^T
+            mma_commit_elect(s_full);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, it & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            // dV += P^T dY, dK += dS^T Q: A from TMEM, B (dY, Q) MN-major
+            mma_ts_k128(tmem + 256, tmem + 0, desc_sw128_lo(st + TILE_BYTES, 16384), HI, idO, it != 0);
+            mma_ts_k128(tmem + 384, tmem + 128, desc_sw128_lo(st, 16384), HI, idO, it != 0);
+            mma_commit_elect(&empty[s]);
+        }
+        if (ok) {
+            mma_commit_elect(g_full);
+        } else {
+            drain_mmas(drain, args.ctl);
+        }
+    } else if (warp >= 4) {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        const long kj = (long)k0 + row;   // this thread's key
+        const float sl2 = kLog2e / sqrtf((float)HD);
+        const float isq = 1.0f / sqrtf((float)HD);
+        bool ok = true;
+        for (int it = 0; it < steps && ok; ++it) {
+            const int s = it % kQNS;
+            const int q0 = (t0 + it % nqt) * kTile;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+            const float* L2 = reinterpret_cast<const float*>(smem + C::OFF_RING + s * C::STAGE + 2 * TILE_BYTES);
+            const float* Dd = L2 + kTile;
+            // query column c (row q0 + c) sees this key when off + q0 + c >= kj
+            long cmin_l = args.causal ? kj - off - q0 : 0;
+            const int cmin = cmin_l < 0 ? 0 : (cmin_l > 128 ? 128 : (int)cmin_l);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tmem + lane_base + c * 32, sv);
+                tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
+                tmem_wait_ld();
+                uint32_t ppk[16], dpk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int col = c * 32 + e;
+                    const float4 l4 = *reinterpret_cast<const float4*>(L2 + (col & ~3));
+                    const float4 d4 = *reinterpret_cast<const float4*>(Dd + (col & ~3));
+                    const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
+                    const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
+                    const float p0 = (col >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -la)) : 0.f;
+                    const float p1 = (col + 1 >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -lb)) : 0.f;
+                    ppk[e >> 1] = pack_bf16x2(p0, p1);
+                    dpk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - da) * isq,
+                                              p1 * (__uint_as_float(dp[e + 1]) - db) * isq);
+                }
+                tmem_st16(tmem + lane_base + c * 16, ppk);
+                tmem_st16(tmem + lane_base + 128 + c * 16, dpk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
+        tc_fence_after();
+        const bool ok_epi = named_bar_and(1, 128, ok);
+        if (ok_epi) {
+            // every MMA has completed and every copy landed: stage dV, dK in the ring
+            uint8_t* stg = smem + C::OFF_RING;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + 256 + c * 32, v);   // c < 4: dV, c >= 4: dK
+                tmem_wait_ld();
+                stage_chunk32(stg + c * STG_BYTES, row, v);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (row == 0) {
+                for (int c = 0; c < 4; ++c) tma_store_4d(&tmdV, stg + c * STG_BYTES, c * 32, kvh, k0, b);
+                for (int c = 0; c < 4; ++c) tma_store_4d(&tmdK, stg + (4 + c) * STG_BYTES, c * 32, kvh, k0, b);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+
+// ------------------------------------------------------------------ host side
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box, CUtensorMapSwizzle sw) {
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return encode_tiled_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+                             es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [B, L, H, 128] as (64 columns, H, L, B, 2 column blocks 128 B apart): one
+// request loads a [128 rows x 128] tile as two 128B-swizzled 64-column blocks.
+bool map_tile(CUtensorMap* m, const void* base, int B, int L, int H) {
+    const cuuint64_t e = 2;
+    cuuint64_t d[5] = {64, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B, 2};
+    cuuint64_t st[4] = {HD * e, (cuuint64_t)H * HD * e, (cuuint64_t)L * H * HD * e, 128};
+    cuuint32_t box[5] = {64, 1, 128, 1, 2};
+    return make_map(m, base, 5, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// [B, L, H, 128] as (128, H, L, B) for stores of [128 rows x 32 columns]
+bool map_out(CUtensorMap* m, const void* base, int B, int L, int H) {
+    const cuuint64_t e = 2;
+    cuuint64_t d[4] = {HD, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t st[3] = {HD * e, (cuuint64_t)H * HD * e, (cuuint64_t)L * H * HD * e};
+    cuuint32_t box[4] = {32, 1, 128, 1};
+    return make_map(m, base, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// GEMM operands: K-major [rows][K] (K contiguous) as 128 x 64 boxes; MN-major
+// [K][cols] (cols contiguous) as 64 x 64 boxes (two per 128-wide tile).
+bool map_kmajor(CUtensorMap* m, const void* base, int rows, int K) {
+    cuuint64_t d[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t st[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {64, 128};
+    return make_map(m, base, 2, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_mnmajor(CUtensorMap* m, const void* base, int K, int cols) {
+    cuuint64_t d[2] = {(cuuint64_t)cols, (cuuint64_t)K};
+    cuuint64_t st[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 64};
+    return make_map(m, base, 2, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool A_MN, bool B_MN>
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfloat16* C, int M, int N, int K,
+                        const Runtime& rt, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t r = cudaFuncSetAttribute(gemm_bf16_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kGemmSmem);
+        if (r != cudaSuccess) return r;
+        attr_done = true;
+    }
+    GemmArgs a;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ldc = N;
+    a.m_tiles = (M + 127) / 128;
+    a.nkc = (K + 63) / 64;
+    a.ctl.err = rt.err;
+    a.ctl.limit_ns = rt.limit_ns;
+    const long tiles = (long)a.m_tiles * ((N + 127) / 128);
+    gemm_bf16_kernel<A_MN, B_MN><<<(unsigned)tiles, kGemmThreads, kGemmSmem, s>>>(tmA, tmB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_supported(const Problem& p) { return p.dtype == 1 && p.dk == HD && p.Lq >= 1; }
+
+BwdPlan plan_bwd(const Problem& p, int num_sms) {
+    BwdPlan w;
+    Problem pf = p;
+    pf.sink = nullptr;
+    w.fwd = plan_workspace(pf, num_sms);   // the gate recompute uses the forward's gate buffers
+    size_t off = w.fwd.total;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = (off + bytes + 255) & ~size_t(255);
+        return at;
+    };
+    w.Lq_pad = (p.Lq + kTile - 1) / kTile * kTile;
+    w.dY = take((size_t)p.B * p.Lq * p.Hq * HD * 2);
+    w.Dv = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
+    w.lse2 = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
+    if (p.gate_mode != 0) w.dGl = take((size_t)p.B * p.Lq * gate_cols(p) * 2);
+    w.total = off;
+    return w;
+}
+
+cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w, char* ws, const Runtime& rt,
+                            cudaStream_t s) {
+    // 1. the gate again (sigma(X W_g) as fp16, or the headwise logits)
+    if (p.gate_mode == 2) {
+        cudaError_t e = launch_gate_sigmoid_bf16(p, w.fwd, ws, rt, s, ZeroJob());
+        if (e != cudaSuccess) return e;
+    } else if (p.gate_mode == 1) {
+        bool launched = false;
+        cudaError_t e = launch_gate_logits_bf16(p, w.fwd, ws, rt, s, &launched, ZeroJob());
+        if (e != cudaSuccess) return e;
+    }
+    // 2. dY, D, dGl, lse in log2 units
+    PrepArgs pa;
+    pa.dO = static_cast<const __nv_bfloat16*>(g.dO);
+    pa.O = static_cast<const __nv_bfloat16*>(g.O);
+    pa.lse = g.lse;
+    pa.gate_sig = p.gate_mode == 2 ? reinterpret_cast<const __half*>(ws + w.fwd.gate_sig) : nullptr;
+    pa.gate_part = p.gate_mode == 1 ? reinterpret_cast<const float*>(ws + w.fwd.gate_part) : nullptr;
+    pa.gate_splits = w.fwd.gate_splits;
+    pa.dY = reinterpret_cast<__nv_bfloat16*>(ws + w.dY);
+    pa.dGl = p.gate_mode ? reinterpret_cast<__nv_bfloat16*>(ws + w.dGl) : nullptr;
+    pa.Dv = reinterpret_cast<float*>(ws + w.Dv);
+    pa.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+    pa.B = p.B;
+    pa.Lq = p.Lq;
+    pa.Hq = p.Hq;
+    pa.Lq_pad = w.Lq_pad;
+    pa.gate_mode = p.gate_mode;
+    const long warps = (long)p.B * p.Hq * w.Lq_pad;
+    bwd_prep_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(pa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // 3. dQ, then dK and dV
+    alignas(64) CUtensorMap tmQ, tmdY, tmK, tmV, tmdQ, tmdK, tmdV;
+    if (!map_tile(&tmQ, p.Q, p.B, p.Lq, p.Hq) || !map_tile(&tmdY, ws + w.dY, p.B, p.Lq, p.Hq) ||
+        !map_tile(&tmK, p.K, p.B, p.Lk, p.Hkv) || !map_tile(&tmV, p.V, p.B, p.Lk, p.Hkv) ||
+        !map_out(&tmdQ, g.dQ, p.B, p.Lq, p.Hq) || !map_out(&tmdK, g.dK, p.B, p.Lk, p.Hkv) ||
+        !map_out(&tmdV, g.dV, p.B, p.Lk, p.Hkv))
+        return cudaErrorInvalidValue;
+    AttnArgs aa;
+    aa.B = p.B;
+    aa.Lq = p.Lq;
+    aa.Lk = p.Lk;
+    aa.Hq = p.Hq;
+    aa.Hkv = p.Hkv;
+    aa.causal = p.causal;
+    aa.n_qtiles = (p.Lq + kTile - 1) / kTile;
+    aa.n_ktiles = (p.Lk + kTile - 1) / kTile;
+    aa.Lq_pad = w.Lq_pad;
+    aa.lse2 = reinterpret_cast<const float*>(ws + w.lse2);
+    aa.Dv = reinterpret_cast<const float*>(ws + w.Dv);
+    aa.ctl.err = rt.err;
+    aa.ctl.limit_ns = rt.limit_ns;
+    static bool attr_done = false;
+    if (!attr_done) {
+        e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DkvCfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    bwd_dq_kernel<<<(unsigned)((long)aa.n_qtiles * p.B * p.Hq), kAttnThreads, DqCfg::SMEM_BYTES, s>>>(
+        tmQ, tmdY, tmK, tmV, tmdQ, aa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dkdv_kernel<<<(unsigned)((long)aa.n_ktiles * p.B * p.Hkv), kAttnThreads, DkvCfg::SMEM_BYTES, s>>>(
+        tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.gate_mode == 0) return e;
+
+    // 4. the gate's weight and input gradients
+    const int rows = p.B * p.Lq, G = gate_cols(p);
+    alignas(64) CUtensorMap tA, tB;
+    // dX [rows x d_model] = dGl [rows x G] W_g^T: A = dGl (K = G contiguous), B^T = W_g [d_model][G]
+    if (!map_kmajor(&tA, ws + w.dGl, rows, G) || !map_kmajor(&tB, p.Wg, p.d_model, G)) return cudaErrorInvalidValue;
+    e = launch_gemm<false, false>(tA, tB, static_cast<__nv_bfloat16*>(g.dX), rows, p.d_model, G, rt, s);
+    if (e != cudaSuccess) return e;
+    // dW_g [d_model x G] = X^T dGl: A stored as X [rows][d_model], B as dGl [rows][G]
+    alignas(64) CUtensorMap tA2, tB2;
+    if (!map_mnmajor(&tA2, p.X, rows, p.d_model) || !map_mnmajor(&tB2, ws + w.dGl, rows, G))
+        return cudaErrorInvalidValue;
+    return launch_gemm<true, true>(tA2, tB2, static_cast<__nv_bfloat16*>(g.dWg), p.d_model, G, rows, rt, s);
+}
+
+}  // namespace gsdpa

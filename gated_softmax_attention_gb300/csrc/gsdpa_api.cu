@@ -75,12 +75,6 @@ int validate_shape(const Problem& p) {
     return GSDPA_OK;
 }
 
-int gate_cols(const Problem& p) {
-    if (p.gate_mode == GSDPA_GATE_ELEMENTWISE) return p.Hq * p.dk;
-    if (p.gate_mode == GSDPA_GATE_HEADWISE) return p.Hq;
-    return 0;
-}
-
 }  // namespace
 
 int gate_col_tile(int cols);  // gate_gemm_sm103.cu
@@ -241,6 +235,80 @@ size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int 
     if (validate_shape(p) != GSDPA_OK) return (size_t)-1;
     if (B == 0 || L_q == 0) return 0;
     return plan_workspace(p, kPlanSms).total;
+}
+
+size_t gsdpa_bwd_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode) {
+    Problem p{};
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.dtype = GSDPA_BF16;
+    p.causal = 1;
+    if (validate_shape(p) != GSDPA_OK || !bwd_supported(p)) return (size_t)-1;
+    if (B == 0 || L_q == 0) return 0;
+    return plan_bwd(p, kPlanSms).total;
+}
+
+int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, const void* O,
+                   const void* dO, const float* lse, void* dX, void* dQ, void* dK, void* dV, void* dW_g, int B,
+                   int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    Problem p{};
+    p.X = X;
+    p.Q = Q;
+    p.K = K;
+    p.V = V;
+    p.Wg = W_g;
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.causal = causal ? 1 : 0;
+    p.dtype = dtype;
+    int st = validate_shape(p);
+    if (st != GSDPA_OK) return st;
+    if (B == 0 || L_q == 0) return GSDPA_OK;
+    if (!bwd_supported(p)) return GSDPA_ERR_UNSUPPORTED;
+    const bool gated = gate_mode != GSDPA_GATE_NONE;
+    if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV) return GSDPA_ERR_INVALID_ARG;
+    if (gated && (!X || !W_g || !dX || !dW_g)) return GSDPA_ERR_INVALID_ARG;
+    for (const void* t : {Q, K, V, O, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                          static_cast<const void*>(dV)})
+        if (!aligned16(t)) return GSDPA_ERR_ALIGNMENT;
+    if (gated && (!aligned16(X) || !aligned16(W_g) || !aligned16(dX) || !aligned16(dW_g))) return GSDPA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return GSDPA_ERR_ALIGNMENT;
+
+    const DeviceInfo* dev = device_info();
+    if (!dev) return GSDPA_ERR_LAUNCH;
+    if (!(dev->cc_major == 10 && dev->cc_minor == 3) || !encode_tiled_fn()) return GSDPA_ERR_UNSUPPORTED;
+    const BwdPlan w = plan_bwd(p, kPlanSms);
+    if (!workspace || workspace_bytes < w.total) return GSDPA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSDPA_ERR_ALIGNMENT;
+    Runtime rt;
+    rt.err = dev->err;
+    rt.limit_ns = g_wait_limit_ns.load();
+    rt.num_sms = dev->num_sms;
+    BwdArgs g;
+    g.O = O;
+    g.dO = dO;
+    g.lse = lse;
+    g.dX = dX;
+    g.dQ = dQ;
+    g.dK = dK;
+    g.dV = dV;
+    g.dWg = dW_g;
+    const cudaError_t e = launch_bwd_bf16(p, g, w, static_cast<char*>(workspace), rt, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
+    return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
 }
 
 namespace {

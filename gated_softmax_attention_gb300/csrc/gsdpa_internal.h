@@ -54,6 +54,10 @@ struct WorkspacePlan {
 };
 
 WorkspacePlan plan_workspace(const Problem& p, int num_sms);
+// columns of W_g: H_q * d_k (elementwise), H_q (headwise), 0 (no gate)
+inline int gate_cols(const Problem& p) {
+    return p.gate_mode == 2 ? p.Hq * p.dk : (p.gate_mode == 1 ? p.Hq : 0);
+}
 
 // The dedicated decode kernel covers bf16, L_q == 1, d_k == 128 and query
 // groups of a multiple of 4 heads; other decode shapes use the prefill kernel.
@@ -98,6 +102,31 @@ cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, c
 cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                cudaStream_t s, bool dependent);
 cudaError_t launch_sink_finalize(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);
+
+// ---- backward (bwd_sm103.cu): bf16, d_k = 128
+struct BwdArgs {
+    const void* O;       // the training forward's output
+    const void* dO;      // dL/dO
+    const float* lse;    // [B, Hq, Lq] from the training forward
+    void* dX;            // gate path's share, like X (gated only)
+    void* dQ;
+    void* dK;
+    void* dV;
+    void* dWg;           // like W_g (gated only)
+};
+struct BwdPlan {
+    size_t total = 0;
+    WorkspacePlan fwd;   // the gate recompute's buffers (the forward's plan)
+    int Lq_pad = 0;      // rows of the per-(b, h) arrays, a multiple of 128
+    size_t dY = 0;       // bf16 [B, Lq, Hq, 128]
+    size_t Dv = 0;       // float [B, Hq, Lq_pad]
+    size_t lse2 = 0;     // float [B, Hq, Lq_pad]
+    size_t dGl = 0;      // bf16 [B*Lq, G]
+};
+bool bwd_supported(const Problem& p);
+BwdPlan plan_bwd(const Problem& p, int num_sms);
+cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w, char* ws, const Runtime& rt,
+                            cudaStream_t s);
 // bf16 prefill kernels: where the first-token share accumulates (null without
 // it), its fixed-point scale 2^F with F = 43 - ceil(log2(L_q + 1)), the factor
 // 2^-F / L_q back to the mean, and the arrivals of a full set (4 per query tile).

@@ -155,6 +155,41 @@ GSDPA_API int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, 
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Workspace bytes gated_sdpa_bwd needs for this problem (bf16, d_k = 128);
+ * (size_t)-1 for an invalid or unsupported shape, 0 for an empty one.
+ */
+GSDPA_API size_t gsdpa_bwd_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode);
+
+/*
+ * The backward pass of the layer: given dO = dL/dO, the gradients of the
+ * loss with respect to Q, K, V and, with a gate, W_g and X (the gate path's
+ * share of dX; X also feeds projections this library does not own).
+ * The chain rule of the forward ("GatedAttention [2025]", sec. 1.2.1 and
+ * 1.2.2); the gate's part as in "解密NeurIPS最佳论文：Gated Attention…",
+ * sec. 2.2: the gradient on the gate's input is dO times the ungated output
+ * times sigma (1 - sigma).
+ *
+ *   X, Q, K, V, W_g : the forward's inputs (same layouts as gated_sdpa_fwd).
+ *   O, lse          : the forward's output [B, L_q, H_q, d_k] and its
+ *                     log-denominators [B, H_q, L_q] (gated_sdpa_fwd_train).
+ *   dO              : device [B, L_q, H_q, d_k], same dtype.
+ *   dQ              : out, like Q.   dK, dV : out, like K and V (each the sum
+ *                     over the query heads of the kv head's group).
+ *   dX, dW_g        : out, like X and W_g (gated only; NULL allowed without a gate).
+ *   workspace       : gsdpa_bwd_workspace_bytes(...) bytes, 256-byte aligned.
+ * Every output is overwritten. bf16 and d_k = 128 only (GSDPA_ERR_UNSUPPORTED
+ * otherwise); sm_103 device. Tensors 16-byte aligned, lse 4-byte aligned.
+ * Asynchronous on `stream`; errors as for gated_sdpa_fwd.
+ */
+GSDPA_API int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                   const void* O, const void* dO, const float* lse,
+                   void* dX, void* dQ, void* dK, void* dV, void* dW_g,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits inside the kernels set when they run out. Returns GSDPA_OK,
  * GSDPA_ERR_DEVICE_TIMEOUT, or GSDPA_ERR_LAUNCH if the stream itself reports

@@ -115,3 +115,24 @@ def test_fwd_signature_matches_header(lib):
     # 7 pointers, 10 ints, workspace pointer, size, stream
     res, args = gb.SIGNATURES["gated_sdpa_fwd"]
     assert len(args) == 20 and res is ctypes.c_int
+
+
+def test_bwd_workspace_and_validation(lib):
+    # bf16, d_k = 128: gate recompute buffers + dY + D, lse (padded to 128 rows) + dGl
+    n = gb.bwd_workspace_bytes(2, 300, 300, 256, 4, 2, 128, "elementwise")
+    assert n >= 2 * 300 * 4 * 128 * 2 + 2 * (2 * 4 * 384 * 4) + 2 * 300 * 512 * 2 and n % 256 == 0
+    assert gb.bwd_workspace_bytes(0, 16, 16, 64, 4, 4, 128, "none") == 0
+    with pytest.raises(gb.GsdpaError):   # d_k = 64 is not covered
+        gb.bwd_workspace_bytes(1, 8, 8, 64, 4, 4, 64, "elementwise")
+    # argument checks happen before any device work (fake pointers)
+    lib_ = gb.load()
+    args = [16] * 13 + [1, 8, 8, 64, 4, 4, 128, 2, 1, gb.BF16, None, 0, None]
+    bad = list(args)
+    bad[13 + 6] = 64                      # d_k 64
+    assert lib_.gated_sdpa_bwd(*bad) == gb.ERR_UNSUPPORTED
+    bad = list(args)
+    bad[6] = None                         # no dO
+    assert lib_.gated_sdpa_bwd(*bad) == gb.ERR_INVALID_ARG
+    bad = list(args)
+    bad[8] = 24                           # dQ misaligned
+    assert lib_.gated_sdpa_bwd(*bad) == gb.ERR_ALIGNMENT
