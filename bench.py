@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--workload", default="bf16_mha_elementwise_L2048")
     ap.add_argument("--decode-workload", default="bf16_decode_gqa_elementwise_Lk8192")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--profile-backward", action="store_true",
+                    help="with --profile-workload: the training forward once, then --profile-calls backward calls")
     ap.add_argument("--decode-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: min(--steps, 50)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
@@ -427,6 +430,11 @@ def run_ours(args, d: Dist):
         out["decode"] = run_decode(args, d, torch, gb, WORKLOADS[args.decode_workload], make_inputs, stream, peaks)
         out["gpu_launches"] += out["decode"]["gpu_launches"]
 
+    # ---- backward leg (the layer's gradients for a training step), context beside the metric
+    if not args.no_backward:
+        out["backward"] = run_backward(args, d, torch, gb, w, host, stream, peaks)
+        out["gpu_launches"] += out["backward"]["gpu_launches"]
+
     # ---- extra workloads (context only), one stderr line each
     for name in [x for x in args.extra.split(",") if x]:
         wx = WORKLOADS[name]
@@ -440,6 +448,52 @@ def run_ours(args, d: Dist):
               file=sys.stderr)
         del hx, Ox
     return out
+
+
+def backward_flops(w):
+    """Algorithmic FLOPs of the backward: five attention products of the
+    forward's size (S, dP, dV, dK, dQ; 2.5x the forward's attention FLOPs) and
+    the gate's two (dW_g = X^T dGl, dX = dGl W_g^T). Recomputation is not counted."""
+    return int(2.5 * w.attn_flops()) + 2 * (w.flops() - w.attn_flops())
+
+
+def run_backward(args, d, torch, gb, w, host, stream, peaks):
+    """The backward call on the headline workload: graph replays of R calls,
+    each reading its own copy of the inputs (inputs larger than L2 in total)."""
+    dev = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
+    g = torch.Generator().manual_seed(4242)
+    dO = torch.randn(dev["Q"].shape, generator=g).to(torch.bfloat16).cuda()
+    O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
+                                        causal=w.causal)
+    per_set = sum(v.numel() * v.element_size() for v in list(dev.values()) + [O, dO, lse] if v is not None)
+    R = n_rotating_sets(per_set)
+    sets = [dict(dev, O=O, dO=dO, lse=lse)]
+    for _ in range(R - 1):
+        sets.append({k: (v.clone() if v is not None else None) for k, v in sets[0].items()})
+    need = gb.bwd_workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def call(k):
+        st = sets[k % R]
+        gb.gated_sdpa_bwd(st["X"], st["Q"], st["K"], st["V"], st["W_g"], st["O"], st["dO"], st["lse"], gate=w.gate,
+                          causal=w.causal, workspace=ws)
+
+    graphs = capture_steps(torch, call, R)
+    K = max(3, min(args.steps, 100))
+    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in the backward leg: {gb.status_string(st)}")
+    flops = backward_flops(w)
+    tf = flops / (ms / 1e3) / 1e12
+    kernels = 6 if w.gate != "none" else 3
+    return {"workload": w.name, "metric": "gated attention bwd TFLOP/s (bf16; algorithmic: 5 attention products "
+                                          "+ 2 gate GEMMs)", "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "flops_per_step": flops, "steps": K,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "scope": "whole call (gate recompute, prep, dQ, dK/dV, dX and dW_g GEMMs)"},
+            "gpu_launches": kernels * K}
 
 
 def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):
@@ -550,7 +604,14 @@ def run_profile(args):
     dev = {k: (v.cuda() if v is not None else None) for k, v in make_inputs(w).items()}
     O = torch.empty_like(dev["Q"])
     gate = args.profile_gate or w.gate
-    for _ in range(args.profile_calls):
+    if args.profile_backward:
+        O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=gate,
+                                            causal=w.causal)
+        dO = torch.randn(dev["Q"].shape, generator=torch.Generator().manual_seed(4242)).to(torch.bfloat16).cuda()
+        for _ in range(args.profile_calls):
+            gb.gated_sdpa_bwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], O, dO, lse, gate=gate,
+                              causal=w.causal)
+    for _ in range(0 if args.profile_backward else args.profile_calls):
         gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=gate, causal=w.causal, out=O)
     st = gb.check_device_error()
     print(json.dumps({"profile_workload": w.name, "gate": gate, "calls": args.profile_calls,
