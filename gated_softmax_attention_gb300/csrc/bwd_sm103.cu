@@ -305,13 +305,21 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
 // ------------------------------------------------------------------ shared by dQ and dK/dV
 
-constexpr int kAttnThreads = 256;   // warp 0 copies, warp 1 MMAs, warps 4..7 one row each
+// warp 0 copies, warp 1 MMAs, warps 4..7 and 8..11: two warpgroups, one row
+// per thread each, splitting the 128 columns of a tile (64 each)
+constexpr int kAttnThreads = 384;
+// Register split: warpgroup 0 (copies, MMAs, two idle warps) gives registers
+// to the two row warpgroups; the launch must provide 384 x kRegsLaunchMin.
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
+constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 constexpr int kRingNS = 4;          // dQ: K/V tile ring
 constexpr int kQNS = 2;             // dK/dV: (Q, dY, lse, D) ring
 constexpr uint32_t VEC_BYTES = kTile * 4;   // 128 floats
 
 struct AttnArgs {
     int B, Lq, Lk, Hq, Hkv, causal, n_qtiles, n_ktiles, Lq_pad;
+    int per_head;        // dK/dV: one unit per query head, fp32 partials summed afterwards (GQA)
     const float* lse2;   // [B, Hq, Lq_pad] log2 units
     const float* Dv;     // [B, Hq, Lq_pad]
     WaitCtl ctl;
@@ -356,7 +364,9 @@ struct DqCfg {
 };
 
 // Unit = (b, h, 128-row query tile), heaviest first (last tiles first when causal).
-// TMEM: S [0, 128) (dS, packed bf16, over its first 64 columns), dP [128, 256), dQ [256, 384).
+// TMEM: S [0, 128), dP [128, 256), dQ [256, 384), dS (packed bf16) [384, 448):
+// apart from S and dP, so that each warpgroup writes its half while the other
+// still reads.
 __global__ void __launch_bounds__(kAttnThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdY,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -395,7 +405,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         mbar_init(q_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 256);
         mbar_init(g_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -413,6 +423,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 
     if (warp == 0) {
         if (lane == 0) {
@@ -466,8 +477,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_commit_elect(s_full);
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, j & 1, abort_flag, args.ctl)))) break;
             tc_fence_after();
-            // dQ += dS K_j: dS (packed bf16 over S) from TMEM, K_j as the MN-major B operand
-            mma_ts_k128(tmem + 256, tmem + 0, desc_sw128_lo(k_st, 16384), HI, idO, j != 0);
+            // dQ += dS K_j: dS (packed bf16) from TMEM, K_j as the MN-major B operand
+            mma_ts_k128(tmem + 256, tmem + 384, desc_sw128_lo(k_st, 16384), HI, idO, j != 0);
             mma_commit_elect(&empty[ik % kRingNS]);
         }
         if (ok) {
@@ -476,7 +487,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             drain_mmas(drain, args.ctl);
         }
     } else if (warp >= 4) {
-        // ---- one query row per thread: dS = p (dP - D) / sqrt(d_k), then the dQ epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ---- one query row per thread, columns [64 wg, 64 wg + 64) of every key tile:
+        // dS = p (dP - D) / sqrt(d_k); then the dQ epilogue
+        const int wg = (warp - 4) >> 2;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
@@ -495,7 +509,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (args.causal && off + i - kv0 < lim_l) lim_l = off + i - kv0;
             const int lim = lim_l > 127 ? 127 : (int)lim_l;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tmem + lane_base + c * 32, sv);
                 tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
@@ -509,7 +524,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - D) * isq,
                                              p1 * (__uint_as_float(dp[e + 1]) - D) * isq);
                 }
-                tmem_st16(tmem + lane_base + c * 16, pk);
+                tmem_st16(tmem + lane_base + 384 + c * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -517,19 +532,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
         tc_fence_after();
-        const bool ok_epi = named_bar_and(1, 128, ok);
+        // (both warpgroups take the same branch: the epilogue has a 256-thread barrier)
+        const bool ok_epi = named_bar_and(1, 256, ok);
         if (ok_epi) {
             uint8_t* stg = smem + C::OFF_STG;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + 256 + c * 32, v);
                 tmem_wait_ld();
                 stage_chunk32(stg + c * STG_BYTES, row, v);
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (row == 0) {
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 128) {
                 for (int c = 0; c < 4; ++c) tma_store_4d(&tmdQ, stg + c * STG_BYTES, c * 32, h, q0, b);
                 tma_store_commit();
                 tma_store_wait_all();
@@ -556,7 +573,7 @@ struct DkvCfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
-    static_assert(8 * STG_BYTES <= kQNS * STAGE, "the output staging reuses the ring");
+    static_assert(16 * STG_BYTES <= kQNS * STAGE, "the output staging (fp32 partials) reuses the ring");
 };
 
 // Unit = (b, kv head, 128-key tile), key tile 0 first (the most query tiles when causal).
@@ -585,18 +602,24 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    const int per_tile = args.B * args.Hkv;
-    const int kt = (int)blockIdx.x / per_tile;
-    const int kvh = ((int)blockIdx.x % per_tile) % args.Hkv;
-    const int b = ((int)blockIdx.x % per_tile) / args.Hkv;
+    // unit: (b, kv head, key tile) summing over the group's heads, or with
+    // per_head (b, query head, key tile) writing that head's share
     const int group = args.Hq / args.Hkv;
+    const int heads = args.per_head ? args.Hq : args.Hkv;
+    const int per_tile = args.B * heads;
+    const int kt = (int)blockIdx.x / per_tile;
+    const int hu = ((int)blockIdx.x % per_tile) % heads;
+    const int b = ((int)blockIdx.x % per_tile) / heads;
+    const int kvh = args.per_head ? hu / group : hu;
+    const int h_first = args.per_head ? hu : kvh * group;   // query heads of the unit: h_first ..
+    const int n_heads = args.per_head ? 1 : group;
     const int k0 = kt * kTile;
     const long off = (long)args.Lk - args.Lq;
     // query tiles that see any key of this tile: query i sees key k0 when off + i >= k0
     int t0 = 0;
     if (args.causal && k0 - off > 0) t0 = (int)((k0 - off) / kTile);
     const int nqt = args.n_qtiles - t0;
-    const int steps = group * nqt;   // (head of the group, query tile), head-major
+    const int steps = n_heads * nqt;   // (head, query tile), head-major
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQNS; ++s) {
@@ -605,7 +628,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mbar_init(kv_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 256);
         mbar_init(g_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -624,6 +647,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 
     if (warp == 0) {
         if (lane == 0) {
@@ -635,7 +659,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int it = 0; it < steps && ok; ++it) {
                 const int s = it % kQNS;
                 const uint32_t ph = (it / kQNS) & 1;
-                const int h = kvh * group + it / nqt;
+                const int h = h_first + it / nqt;
                 const int q0 = (t0 + it % nqt) * kTile;
                 if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.ctl))) break;
                 mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES + 2 * VEC_BYTES);
@@ -684,6 +708,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             drain_mmas(drain, args.ctl);
         }
     } else if (warp >= 4) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ---- one key row per thread, query columns [64 wg, 64 wg + 64) of every step
+        const int wg = (warp - 4) >> 2;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
@@ -694,35 +721,52 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int it = 0; it < steps && ok; ++it) {
             const int s = it % kQNS;
             const int q0 = (t0 + it % nqt) * kTile;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, args.ctl)))) break;
+            // (both warpgroups decide together: the step has a 256-thread barrier)
+            ok = named_bar_and(2, 256, __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, args.ctl)));
+            if (!ok) break;
             tc_fence_after();
             const float* L2 = reinterpret_cast<const float*>(smem + C::OFF_RING + s * C::STAGE + 2 * TILE_BYTES);
             const float* Dd = L2 + kTile;
             // query column c (row q0 + c) sees this key when off + q0 + c >= kj
             long cmin_l = args.causal ? kj - off - q0 : 0;
             const int cmin = cmin_l < 0 ? 0 : (cmin_l > 128 ? 128 : (int)cmin_l);
+            // each chunk of 32 columns: load S^T and dP^T, compute, keep only the packed
+            // bf16 P^T and dS^T (the stores wait until both warpgroups have loaded)
+            uint32_t ppk[2][16], dpk[2][16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tmem + lane_base + c * 32, sv);
                 tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
                 tmem_wait_ld();
-                uint32_t ppk[16], dpk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int col = c * 32 + e;
-                    const float4 l4 = *reinterpret_cast<const float4*>(L2 + (col & ~3));
-                    const float4 d4 = *reinterpret_cast<const float4*>(Dd + (col & ~3));
-                    const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
-                    const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
-                    const float p0 = (col >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -la)) : 0.f;
-                    const float p1 = (col + 1 >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -lb)) : 0.f;
-                    ppk[e >> 1] = pack_bf16x2(p0, p1);
-                    dpk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - da) * isq,
-                                              p1 * (__uint_as_float(dp[e + 1]) - db) * isq);
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(L2 + c * 32 + 4 * g4);
+                    const float4 d4 = *reinterpret_cast<const float4*>(Dd + c * 32 + 4 * g4);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dsv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int e = 4 * g4 + q;
+                        pv[q] = (c * 32 + e >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lv[q])) : 0.f;
+                        dsv[q] = pv[q] * (__uint_as_float(dp[e]) - dv[q]) * isq;
+                    }
+                    ppk[cc][2 * g4] = pack_bf16x2(pv[0], pv[1]);
+                    ppk[cc][2 * g4 + 1] = pack_bf16x2(pv[2], pv[3]);
+                    dpk[cc][2 * g4] = pack_bf16x2(dsv[0], dsv[1]);
+                    dpk[cc][2 * g4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
-                tmem_st16(tmem + lane_base + c * 16, ppk);
-                tmem_st16(tmem + lane_base + 128 + c * 16, dpk);
+            }
+            // both warpgroups have read their columns of S^T and dP^T: the packed P^T
+            // and dS^T (over the first 64 columns of each) may now overwrite them
+            named_bar_sync(2, 256);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
+                tmem_st16(tmem + lane_base + c * 16, ppk[cc]);
+                tmem_st16(tmem + lane_base + 128 + c * 16, dpk[cc]);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -730,22 +774,53 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
         tc_fence_after();
-        const bool ok_epi = named_bar_and(1, 128, ok);
-        if (ok_epi) {
-            // every MMA has completed and every copy landed: stage dV, dK in the ring
+        const bool ok_epi = named_bar_and(1, 256, ok);
+        if (ok_epi && !args.per_head) {
+            // every MMA has completed and every copy landed: stage dV, dK (bf16) in the ring
             uint8_t* stg = smem + C::OFF_RING;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_base + 256 + c * 32, v);   // c < 4: dV, c >= 4: dK
+                tmem_ld32(tmem + lane_base + 256 + c * 32, v);   // dV
                 tmem_wait_ld();
                 stage_chunk32(stg + c * STG_BYTES, row, v);
+                tmem_ld32(tmem + lane_base + 384 + c * 32, v);   // dK
+                tmem_wait_ld();
+                stage_chunk32(stg + (4 + c) * STG_BYTES, row, v);
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (row == 0) {
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 128) {
                 for (int c = 0; c < 4; ++c) tma_store_4d(&tmdV, stg + c * STG_BYTES, c * 32, kvh, k0, b);
                 for (int c = 0; c < 4; ++c) tma_store_4d(&tmdK, stg + (4 + c) * STG_BYTES, c * 32, kvh, k0, b);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        } else if (ok_epi) {
+            // this head's share as fp32: [128 rows x 32 columns] chunks of 128-byte rows
+            // (128-byte swizzle), summed over the group by the reduction kernel
+            uint8_t* stg = smem + C::OFF_RING;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * wg + cc;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {   // t = 0: dV, 1: dK
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + 256 + t * 128 + c * 32, v);
+                    tmem_wait_ld();
+                    uint8_t* dst = stg + (t * 4 + c) * (2 * STG_BYTES) + row * 128;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4*>(dst + ((q ^ (row & 7)) << 4)) =
+                            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 128) {
+                for (int c = 0; c < 4; ++c) tma_store_4d(&tmdV, stg + c * (2 * STG_BYTES), c * 32, hu, k0, b);
+                for (int c = 0; c < 4; ++c) tma_store_4d(&tmdK, stg + (4 + c) * (2 * STG_BYTES), c * 32, hu, k0, b);
                 tma_store_commit();
                 tma_store_wait_all();
             }
@@ -760,14 +835,50 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 
+// ------------------------------------------------------------------ GQA: sum the heads' shares
+
+// out[b, j, kvh, c] = bf16( sum over the group's heads h of part[b, j, h, c] ),
+// the heads added in order (the same bits whatever order the units ran in).
+// One thread per 4 columns.
+__global__ void __launch_bounds__(256) bwd_group_sum_kernel(const float* __restrict__ part,
+                                                            __nv_bfloat16* __restrict__ out, long rows_kv, int Hkv,
+                                                            int group) {
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;   // over rows_kv * Hkv * 32
+    if (idx >= rows_kv * Hkv * (HD / 4)) return;
+    const int c4 = (int)(idx % (HD / 4));
+    const long rk = idx / (HD / 4);          // (b, j, kvh)
+    const int kvh = (int)(rk % Hkv);
+    const long bj = rk / Hkv;
+    const float* src = part + ((bj * Hkv + kvh) * group) * HD + c4 * 4;   // heads kvh*group .. contiguous
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    for (int g = 1; g < group; ++g) {
+        const float4 v = *reinterpret_cast<const float4*>(src + (long)g * HD);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    *reinterpret_cast<uint2*>(out + rk * HD + c4 * 4) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+}
+
 // ------------------------------------------------------------------ host side
 
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box, CUtensorMapSwizzle sw) {
+              const cuuint32_t* box, CUtensorMapSwizzle sw,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return encode_tiled_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
-                             es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return encode_tiled_fn()(m, dt, rank, const_cast<void*>(base), dims, strides, box, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 [B, L, H, 128] as (128, H, L, B) for stores of [128 rows x 32 columns]
+bool map_out_f32(CUtensorMap* m, const void* base, int B, int L, int H) {
+    const cuuint64_t e = 4;
+    cuuint64_t d[4] = {HD, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t st[3] = {HD * e, (cuuint64_t)H * HD * e, (cuuint64_t)L * H * HD * e};
+    cuuint32_t box[4] = {32, 1, 128, 1};
+    return make_map(m, base, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
 // [B, L, H, 128] as (64 columns, H, L, B, 2 column blocks 128 B apart): one
@@ -849,6 +960,10 @@ BwdPlan plan_bwd(const Problem& p, int num_sms) {
     w.Dv = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     w.lse2 = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     if (p.gate_mode != 0) w.dGl = take((size_t)p.B * p.Lq * gate_cols(p) * 2);
+    if (p.Hq != p.Hkv) {   // GQA: dK, dV per query head, then summed over each group
+        w.part_dK = take((size_t)p.B * p.Lk * p.Hq * HD * 4);
+        w.part_dV = take((size_t)p.B * p.Lk * p.Hq * HD * 4);
+    }
     w.total = off;
     return w;
 }
@@ -888,10 +1003,14 @@ cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w
 
     // 3. dQ, then dK and dV
     alignas(64) CUtensorMap tmQ, tmdY, tmK, tmV, tmdQ, tmdK, tmdV;
+    const bool per_head = p.Hq != p.Hkv;
     if (!map_tile(&tmQ, p.Q, p.B, p.Lq, p.Hq) || !map_tile(&tmdY, ws + w.dY, p.B, p.Lq, p.Hq) ||
         !map_tile(&tmK, p.K, p.B, p.Lk, p.Hkv) || !map_tile(&tmV, p.V, p.B, p.Lk, p.Hkv) ||
-        !map_out(&tmdQ, g.dQ, p.B, p.Lq, p.Hq) || !map_out(&tmdK, g.dK, p.B, p.Lk, p.Hkv) ||
-        !map_out(&tmdV, g.dV, p.B, p.Lk, p.Hkv))
+        !map_out(&tmdQ, g.dQ, p.B, p.Lq, p.Hq))
+        return cudaErrorInvalidValue;
+    if (per_head ? !(map_out_f32(&tmdK, ws + w.part_dK, p.B, p.Lk, p.Hq) &&
+                     map_out_f32(&tmdV, ws + w.part_dV, p.B, p.Lk, p.Hq))
+                 : !(map_out(&tmdK, g.dK, p.B, p.Lk, p.Hkv) && map_out(&tmdV, g.dV, p.B, p.Lk, p.Hkv)))
         return cudaErrorInvalidValue;
     AttnArgs aa;
     aa.B = p.B;
@@ -903,12 +1022,22 @@ cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w
     aa.n_qtiles = (p.Lq + kTile - 1) / kTile;
     aa.n_ktiles = (p.Lk + kTile - 1) / kTile;
     aa.Lq_pad = w.Lq_pad;
+    aa.per_head = per_head ? 1 : 0;
     aa.lse2 = reinterpret_cast<const float*>(ws + w.lse2);
     aa.Dv = reinterpret_cast<const float*>(ws + w.Dv);
     aa.ctl.err = rt.err;
     aa.ctl.limit_ns = rt.limit_ns;
     static bool attr_done = false;
     if (!attr_done) {
+        // The register split only fits if the launch allocates enough registers
+        // per thread; refuse to launch otherwise (it would not finish).
+        for (const void* k : {reinterpret_cast<const void*>(bwd_dq_kernel),
+                              reinterpret_cast<const void*>(bwd_dkdv_kernel)}) {
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, k);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
+        }
         e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::SMEM_BYTES);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -920,10 +1049,22 @@ cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w
         tmQ, tmdY, tmK, tmV, tmdQ, aa);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dkdv_kernel<<<(unsigned)((long)aa.n_ktiles * p.B * p.Hkv), kAttnThreads, DkvCfg::SMEM_BYTES, s>>>(
-        tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
+    bwd_dkdv_kernel<<<(unsigned)((long)aa.n_ktiles * p.B * (per_head ? p.Hq : p.Hkv)), kAttnThreads,
+                      DkvCfg::SMEM_BYTES, s>>>(tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
     e = cudaGetLastError();
-    if (e != cudaSuccess || p.gate_mode == 0) return e;
+    if (e != cudaSuccess) return e;
+    if (per_head) {
+        const long rows_kv = (long)p.B * p.Lk;
+        const long threads = rows_kv * p.Hkv * (HD / 4);
+        const unsigned blocks = (unsigned)((threads + 255) / 256);
+        bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(ws + w.part_dK),
+                                                    static_cast<__nv_bfloat16*>(g.dK), rows_kv, p.Hkv, p.Hq / p.Hkv);
+        bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(ws + w.part_dV),
+                                                    static_cast<__nv_bfloat16*>(g.dV), rows_kv, p.Hkv, p.Hq / p.Hkv);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (p.gate_mode == 0) return e;
 
     // 4. the gate's weight and input gradients
     const int rows = p.B * p.Lq, G = gate_cols(p);

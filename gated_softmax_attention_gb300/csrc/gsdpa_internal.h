@@ -122,6 +122,8 @@ struct BwdPlan {
     size_t Dv = 0;       // float [B, Hq, Lq_pad]
     size_t lse2 = 0;     // float [B, Hq, Lq_pad]
     size_t dGl = 0;      // bf16 [B*Lq, G]
+    size_t part_dK = 0;  // GQA: float [B, Lk, Hq, 128], each query head's share
+    size_t part_dV = 0;
 };
 bool bwd_supported(const Problem& p);
 BwdPlan plan_bwd(const Problem& p, int num_sms);
