@@ -357,7 +357,8 @@ struct DqCfg {
     static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // K_j, V_j, K_j+1, ...
     static constexpr uint32_t OFF_STG = OFF_RING + kRingNS * TILE_BYTES;   // dQ output, 4 chunks
     static constexpr uint32_t OFF_BAR = OFF_STG + 4 * STG_BYTES;
-    static constexpr int NBAR = 2 * kRingNS + 5;   // full, empty, q_full, s_full, p_full, g_full, drain
+    // full, empty, q_full, s_full, p_full, g_full, drain, s_read, dq_done
+    static constexpr int NBAR = 2 * kRingNS + 7;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
@@ -378,10 +379,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint64_t* full = bars;
     uint64_t* empty = bars + kRingNS;
     uint64_t* q_full = bars + 2 * kRingNS;
-    uint64_t* s_full = q_full + 1;
-    uint64_t* p_full = q_full + 2;
-    uint64_t* g_full = q_full + 3;
+    uint64_t* s_full = q_full + 1;    // S_j, dP_j in tensor memory
+    uint64_t* p_full = q_full + 2;    // dS_j written (256 row threads)
+    uint64_t* g_full = q_full + 3;    // every MMA done
     uint64_t* drain = q_full + 4;
+    uint64_t* s_read = q_full + 5;    // the rows have loaded S_j, dP_j (256 row threads)
+    uint64_t* dq_done = q_full + 6;   // dQ += dS_j K_j done: dS may be overwritten
+    static_assert(2 * kRingNS + 7 == C::NBAR, "barrier layout");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const int warp = threadIdx.x / 32;
@@ -408,6 +412,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(p_full, 256);
         mbar_init(g_full, 1);
         mbar_init(drain, 1);
+        mbar_init(s_read, 256);
+        mbar_init(dq_done, 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -450,7 +456,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         }
     } else if (warp == 1) {
-        // ---- MMAs: per key tile S = Q K^T, dP = dY V^T; then dQ += dS K
+        // ---- MMAs: S_j = Q K_j^T, dP_j = dY V_j^T; S_{j+1}, dP_{j+1} as soon as the
+        // rows have loaded S_j, dP_j (dS has its own columns), then dQ += dS_j K_j
         constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
         constexpr uint32_t HI = desc_sw128_hi(1024);
@@ -459,26 +466,38 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_after();
         const uint32_t q_lo = desc_sw128_lo(base + C::OFF_Q, 16);
         const uint32_t dy_lo = desc_sw128_lo(base + C::OFF_DY, 16);
-        for (int j = 0; j < nkv && ok; ++j) {
+        auto ring_ready = [&](int item) -> bool {
+            const bool r = __all_sync(0xffffffffu, mbar_wait(&full[item % kRingNS], (item / kRingNS) & 1, abort_flag,
+                                                            args.ctl));
+            tc_fence_after();
+            return r;
+        };
+        auto issue_S_dP = [&](int j) -> bool {
             const int ik = 2 * j, iv = 2 * j + 1;
-            const uint32_t k_st = base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES;
-            const uint32_t v_st = base + C::OFF_RING + (iv % kRingNS) * TILE_BYTES;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[ik % kRingNS], (ik / kRingNS) & 1, abort_flag,
-                                                         args.ctl))))
-                break;
-            tc_fence_after();
-            mma_ss_k128<16384, 16384>(tmem + 0, q_lo, desc_sw128_lo(k_st, 16), HI, idS, 0);
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[iv % kRingNS], (iv / kRingNS) & 1, abort_flag,
-                                                         args.ctl))))
-                break;
-            tc_fence_after();
-            mma_ss_k128<16384, 16384>(tmem + 128, dy_lo, desc_sw128_lo(v_st, 16), HI, idS, 0);
+            if (!ring_ready(ik)) return false;
+            mma_ss_k128<16384, 16384>(tmem + 0, q_lo, desc_sw128_lo(base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES, 16),
+                                      HI, idS, 0);
+            if (!ring_ready(iv)) return false;
+            mma_ss_k128<16384, 16384>(tmem + 128, dy_lo,
+                                      desc_sw128_lo(base + C::OFF_RING + (iv % kRingNS) * TILE_BYTES, 16), HI, idS, 0);
             mma_commit_elect(&empty[iv % kRingNS]);   // V_j: read once
             mma_commit_elect(s_full);
+            return true;
+        };
+        if (ok && nkv > 0) ok = issue_S_dP(0);
+        for (int j = 0; j < nkv && ok; ++j) {
+            if (j + 1 < nkv) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_read, j & 1, abort_flag, args.ctl)))) break;
+                tc_fence_after();
+                if (!(ok = issue_S_dP(j + 1))) break;
+            }
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, j & 1, abort_flag, args.ctl)))) break;
             tc_fence_after();
-            // dQ += dS K_j: dS (packed bf16) from TMEM, K_j as the MN-major B operand
-            mma_ts_k128(tmem + 256, tmem + 384, desc_sw128_lo(k_st, 16384), HI, idO, j != 0);
+            // dQ += dS_j K_j: dS (packed bf16) from TMEM, K_j as the MN-major B operand
+            const int ik = 2 * j;
+            mma_ts_k128(tmem + 256, tmem + 384, desc_sw128_lo(base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES, 16384),
+                        HI, idO, j != 0);
+            mma_commit_elect(dq_done);
             mma_commit_elect(&empty[ik % kRingNS]);
         }
         if (ok) {
@@ -508,24 +527,42 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             long lim_l = (long)args.Lk - 1 - kv0;   // last visible column of this row in this tile
             if (args.causal && off + i - kv0 < lim_l) lim_l = off + i - kv0;
             const int lim = lim_l > 127 ? 127 : (int)lim_l;
+            uint32_t sv[2][32], dp[2][32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                tmem_ld32(tmem + lane_base + (2 * wg + cc) * 32, sv[cc]);
+                tmem_ld32(tmem + lane_base + 128 + (2 * wg + cc) * 32, dp[cc]);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(s_read);   // S_{j+1}, dP_{j+1} may now overwrite S_j, dP_j
+            // dS = p (dP - D), two columns per packed fp32 instruction (the 1/sqrt(d_k)
+            // is applied to dQ in the epilogue); masks only where the tile needs them
+            uint32_t pk[2][16];
+            const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2), nD = make_float2(-D, -D);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * wg + cc;
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tmem + lane_base + c * 32, sv);
-                tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
-                tmem_wait_ld();
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const int col = c * 32 + e;
-                    const float p0 = (col <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
-                    const float p1 = (col + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
-                    pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - D) * isq,
-                                             p1 * (__uint_as_float(dp[e + 1]) - D) * isq);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[cc][e]), __uint_as_float(sv[cc][e + 1])),
+                                                sl2x2, nl2);
+                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (lim < 127) {
+                        const int col = c * 32 + e;
+                        if (col > lim) pr.x = 0.f;
+                        if (col + 1 > lim) pr.y = 0.f;
+                    }
+                    const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dp[cc][e]),
+                                                                            __uint_as_float(dp[cc][e + 1])), nD));
+                    pk[cc][e >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
-                tmem_st16(tmem + lane_base + 384 + c * 16, pk);
             }
+            // dQ_{j-1} has read dS_{j-1}
+            if (j > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(dq_done, (j - 1) & 1, abort_flag, args.ctl)))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) tmem_st16(tmem + lane_base + 384 + (2 * wg + cc) * 16, pk[cc]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_full);
@@ -542,6 +579,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + 256 + c * 32, v);
                 tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * isq);
                 stage_chunk32(stg + c * STG_BYTES, row, v);
             }
             fence_proxy_async_smem();
@@ -740,23 +779,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tmem_ld32(tmem + lane_base + c * 32, sv);
                 tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
                 tmem_wait_ld();
+                // p = exp2(s sl2 - lse2), dS = p (dP - D) (the 1/sqrt(d_k) is applied to
+                // dK in the epilogue), two columns per packed fp32 instruction
+                const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(L2 + c * 32 + 4 * g4);
                     const float4 d4 = *reinterpret_cast<const float4*>(Dd + c * 32 + 4 * g4);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e = 4 * g4 + q;
-                        pv[q] = (c * 32 + e >= cmin) ? ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lv[q])) : 0.f;
-                        dsv[q] = pv[q] * (__uint_as_float(dp[e]) - dv[q]) * isq;
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int e = 4 * g4 + 2 * h2;
+                        const float2 nl = h2 ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+                        const float2 nd = h2 ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                        const float2 x =
+                            __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl);
+                        float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (cmin > 0) {
+                            if (c * 32 + e < cmin) pr.x = 0.f;
+                            if (c * 32 + e + 1 < cmin) pr.y = 0.f;
+                        }
+                        const float2 ds = __fmul2_rn(
+                            pr, __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+                        ppk[cc][2 * g4 + h2] = pack_bf16x2(pr.x, pr.y);
+                        dpk[cc][2 * g4 + h2] = pack_bf16x2(ds.x, ds.y);
                     }
-                    ppk[cc][2 * g4] = pack_bf16x2(pv[0], pv[1]);
-                    ppk[cc][2 * g4 + 1] = pack_bf16x2(pv[2], pv[3]);
-                    dpk[cc][2 * g4] = pack_bf16x2(dsv[0], dsv[1]);
-                    dpk[cc][2 * g4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
             }
             // both warpgroups have read their columns of S^T and dP^T: the packed P^T
@@ -785,8 +831,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tmem_ld32(tmem + lane_base + 256 + c * 32, v);   // dV
                 tmem_wait_ld();
                 stage_chunk32(stg + c * STG_BYTES, row, v);
-                tmem_ld32(tmem + lane_base + 384 + c * 32, v);   // dK
+                tmem_ld32(tmem + lane_base + 384 + c * 32, v);   // dK (times 1/sqrt(d_k))
                 tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * isq);
                 stage_chunk32(stg + (4 + c) * STG_BYTES, row, v);
             }
             fence_proxy_async_smem();
@@ -809,6 +857,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + 256 + t * 128 + c * 32, v);
                     tmem_wait_ld();
+                    if (t == 1) {   // dK times 1/sqrt(d_k)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * isq);
+                    }
                     uint8_t* dst = stg + (t * 4 + c) * (2 * STG_BYTES) + row * 128;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
@@ -833,7 +885,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_dealloc(tmem, 512);
     }
 }
-
 
 // ------------------------------------------------------------------ GQA: sum the heads' shares
 
