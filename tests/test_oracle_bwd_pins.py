@@ -204,3 +204,19 @@ def test_lse_closed_forms():
     mask = (torch.arange(Lk)[None, :] <= torch.arange(Lq)[:, None] + (Lk - Lq))
     ref = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1).permute(0, 2, 1).numpy()
     np.testing.assert_allclose(lse2, ref, rtol=1e-13)
+
+
+@pytest.mark.parametrize("case", [(2, 7, 9, 4, 2, 4, 5, "elementwise", True), (1, 6, 6, 2, 2, 8, 3, "headwise", False),
+                                  (1, 5, 5, 3, 1, 4, 0, "none", True)], ids=["gqa_elementwise_causal",
+                                                                             "headwise_full", "mqa_none"])
+def test_bwd_rows_equals_full_backward(case):
+    # the sampled-row form (used at sizes the full form cannot reach) against the pinned full form
+    B, Lq, Lk, Hq, Hkv, dk, dm, gate, causal = case
+    X, Q, K, V, W, dO = _inputs(B, Lq, Lk, Hq, Hkv, dk, max(dm, 1), gate, seed=21)
+    full = oracle.gated_sdpa_bwd(X, Q, K, V, W, dO, gate=gate, causal=causal)
+    q_rows = [(b, i) for b in range(B) for i in range(Lq)]
+    k_rows = [(b, j) for b in range(B) for j in range(Lk)]
+    rows = oracle.gated_sdpa_bwd_rows(X, Q, K, V, W, dO, q_rows, k_rows, gate=gate, causal=causal)
+    np.testing.assert_allclose(rows["dQ"], full["dQ"].reshape(-1, Hq, dk), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(rows["dK"], full["dK"].reshape(-1, Hkv, dk), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(rows["dV"], full["dV"].reshape(-1, Hkv, dk), rtol=1e-10, atol=1e-13)
