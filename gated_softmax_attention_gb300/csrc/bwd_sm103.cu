@@ -28,7 +28,9 @@
 //                      S^T = K Q^T, dP^T = V dY^T, then dV += P^T dY and
 //                      dK += dS^T Q, so the group's sum needs no atomics;
 //   gemm_bf16_kernel   dX = dGl W_g^T (both operands K-major) and
-//                      dW_g = X^T dGl (both MN-major), read in place.
+//                      dW_g = X^T dGl (both MN-major), read in place, where
+//                      the product has fewer than 256 columns (else the CTA-pair
+//                      GEMM of bwd_gemm_sm103.cu).
 // dQ and dK/dV recompute S and dP each (two passes instead of atomics: the
 // result does not depend on the order of the CTAs, and each pass keeps its
 // accumulators in tensor memory).
@@ -313,7 +315,9 @@ constexpr int kAttnThreads = 384;
 constexpr int kRegsLow = 64;
 constexpr int kRegsHigh = 216;
 constexpr int kRegsLaunchMin = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
-constexpr int kRingNS = 4;          // dQ: K/V tile ring
+constexpr int kKNS = 3;             // dQ: K tile ring (K_j is read until dQ += dS_j K_j)
+constexpr int kVNS = 2;             // dQ: V tile ring (V_j is read by dP_j only)
+constexpr int kRingNS = kKNS + kVNS;
 constexpr int kQNS = 2;             // dK/dV: (Q, dY, lse, D) ring
 constexpr uint32_t VEC_BYTES = kTile * 4;   // 128 floats
 
@@ -354,15 +358,29 @@ __device__ __forceinline__ void stage_chunk32(uint8_t* chunk, int row, const uin
 struct DqCfg {
     static constexpr uint32_t OFF_Q = 0;                        // Q tile
     static constexpr uint32_t OFF_DY = TILE_BYTES;              // dY tile
-    static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // K_j, V_j, K_j+1, ...
-    static constexpr uint32_t OFF_STG = OFF_RING + kRingNS * TILE_BYTES;   // dQ output, 4 chunks
-    static constexpr uint32_t OFF_BAR = OFF_STG + 4 * STG_BYTES;
+    static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // K slots 0..kKNS-1, then V slots
+    static constexpr uint32_t OFF_STG = OFF_Q;                  // dQ output, 4 chunks (Q, dY are dead by then)
+    static constexpr uint32_t OFF_BAR = OFF_RING + kRingNS * TILE_BYTES;
     // full, empty, q_full, s_full, p_full, g_full, drain, s_read, dq_done
     static constexpr int NBAR = 2 * kRingNS + 7;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 };
+
+// Ring slot and phase of copy `item` (K_j = item 2j, V_j = item 2j + 1): K and V
+// have rings of their own, so that K_j + kKNS can load while K_j still waits for
+// dQ += dS_j K_j.
+__device__ __forceinline__ void dq_slot(int item, int& slot, uint32_t& phase) {
+    const int j = item >> 1;
+    if ((item & 1) == 0) {
+        slot = j % kKNS;
+        phase = (uint32_t)(j / kKNS) & 1u;
+    } else {
+        slot = kKNS + j % kVNS;
+        phase = (uint32_t)(j / kVNS) & 1u;
+    }
+}
 
 // Unit = (b, h, 128-row query tile), heaviest first (last tiles first when causal).
 // TMEM: S [0, 128), dP [128, 256), dQ [256, 384), dS (packed bf16) [384, 448):
@@ -440,8 +458,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
             for (int item = 0; item < 2 * nkv && ok; ++item) {
-                const int s = item % kRingNS;
-                const uint32_t ph = (item / kRingNS) & 1;
+                int s;
+                uint32_t ph;
+                dq_slot(item, s, ph);
                 if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.ctl))) break;
                 mbar_arrive_expect_tx(&full[s], TILE_BYTES);
                 armed |= 1u << s;
@@ -466,21 +485,23 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_after();
         const uint32_t q_lo = desc_sw128_lo(base + C::OFF_Q, 16);
         const uint32_t dy_lo = desc_sw128_lo(base + C::OFF_DY, 16);
-        auto ring_ready = [&](int item) -> bool {
-            const bool r = __all_sync(0xffffffffu, mbar_wait(&full[item % kRingNS], (item / kRingNS) & 1, abort_flag,
-                                                            args.ctl));
+        // wait for copy `item`; its ring slot
+        auto ring_ready = [&](int item, int& sl) -> bool {
+            uint32_t ph;
+            dq_slot(item, sl, ph);
+            const bool r = __all_sync(0xffffffffu, mbar_wait(&full[sl], ph, abort_flag, args.ctl));
             tc_fence_after();
             return r;
         };
         auto issue_S_dP = [&](int j) -> bool {
-            const int ik = 2 * j, iv = 2 * j + 1;
-            if (!ring_ready(ik)) return false;
-            mma_ss_k128<16384, 16384>(tmem + 0, q_lo, desc_sw128_lo(base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES, 16),
-                                      HI, idS, 0);
-            if (!ring_ready(iv)) return false;
-            mma_ss_k128<16384, 16384>(tmem + 128, dy_lo,
-                                      desc_sw128_lo(base + C::OFF_RING + (iv % kRingNS) * TILE_BYTES, 16), HI, idS, 0);
-            mma_commit_elect(&empty[iv % kRingNS]);   // V_j: read once
+            int sk, sv;
+            if (!ring_ready(2 * j, sk)) return false;
+            mma_ss_k128<16384, 16384>(tmem + 0, q_lo, desc_sw128_lo(base + C::OFF_RING + sk * TILE_BYTES, 16), HI, idS,
+                                      0);
+            if (!ring_ready(2 * j + 1, sv)) return false;
+            mma_ss_k128<16384, 16384>(tmem + 128, dy_lo, desc_sw128_lo(base + C::OFF_RING + sv * TILE_BYTES, 16), HI,
+                                      idS, 0);
+            mma_commit_elect(&empty[sv]);   // V_j: read once
             mma_commit_elect(s_full);
             return true;
         };
@@ -494,11 +515,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, j & 1, abort_flag, args.ctl)))) break;
             tc_fence_after();
             // dQ += dS_j K_j: dS (packed bf16) from TMEM, K_j as the MN-major B operand
-            const int ik = 2 * j;
-            mma_ts_k128(tmem + 256, tmem + 384, desc_sw128_lo(base + C::OFF_RING + (ik % kRingNS) * TILE_BYTES, 16384),
-                        HI, idO, j != 0);
+            int sk;
+            uint32_t phk;
+            dq_slot(2 * j, sk, phk);
+            mma_ts_k128(tmem + 256, tmem + 384, desc_sw128_lo(base + C::OFF_RING + sk * TILE_BYTES, 16384), HI, idO,
+                        j != 0);
             mma_commit_elect(dq_done);
-            mma_commit_elect(&empty[ik % kRingNS]);
+            mma_commit_elect(&empty[sk]);
         }
         if (ok) {
             mma_commit_elect(g_full);
@@ -608,7 +631,7 @@ struct DkvCfg {
     static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // [Q_i | dY_i | lse2_i | D_i] per stage
     static constexpr uint32_t STAGE = 2 * TILE_BYTES + 2 * VEC_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_RING + kQNS * STAGE;
-    static constexpr int NBAR = 2 * kQNS + 5;   // full, empty, kv_full, s_full, p_full, g_full, drain
+    static constexpr int NBAR = 2 * kQNS + 7;   // full, empty, kv_full, s_full[2], p_full[2], g_full, drain
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
@@ -616,10 +639,13 @@ struct DkvCfg {
 };
 
 // Unit = (b, kv head, 128-key tile), key tile 0 first (the most query tiles when causal).
-// Per step (query head h of the group, query tile t): S^T = K Q^T, dP^T = V dY^T;
-// one key row per thread: P^T and dS^T (packed bf16) over their first 64 columns;
-// then dV += P^T dY, dK += dS^T Q.
-// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 384), dK [384, 512).
+// Per step (query head h of the group, query tile t) two half steps u, one per
+// 64 queries of the tile: S^T = K Q_u^T, dP^T = V dY_u^T into buffer u % 2;
+// one key row per thread: P^T and dS^T (packed bf16) over the columns each
+// warpgroup read; then dV += P^T dY_u, dK += dS^T Q_u. With two buffers the
+// MMAs of half step u + 1 run while the rows of half step u are computed.
+// TMEM: buffer 0 S^T [0, 64), dP^T [64, 128); buffer 1 [128, 192), [192, 256);
+// dV [256, 384), dK [384, 512).
 __global__ void __launch_bounds__(kAttnThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdY,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -632,10 +658,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* full = bars;
     uint64_t* empty = bars + kQNS;
     uint64_t* kv_full = bars + 2 * kQNS;
-    uint64_t* s_full = kv_full + 1;
-    uint64_t* p_full = kv_full + 2;
-    uint64_t* g_full = kv_full + 3;
-    uint64_t* drain = kv_full + 4;
+    uint64_t* s_full = kv_full + 1;   // [2] S^T, dP^T of buffer u % 2 in tensor memory
+    uint64_t* p_full = kv_full + 3;   // [2] P^T, dS^T of buffer u % 2 written (256 row threads)
+    uint64_t* g_full = kv_full + 5;
+    uint64_t* drain = kv_full + 6;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const int warp = threadIdx.x / 32;
@@ -659,6 +685,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (args.causal && k0 - off > 0) t0 = (int)((k0 - off) / kTile);
     const int nqt = args.n_qtiles - t0;
     const int steps = n_heads * nqt;   // (head, query tile), head-major
+    const int subs = 2 * steps;        // half steps
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQNS; ++s) {
@@ -666,8 +693,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(&empty[s], 1);
         }
         mbar_init(kv_full, 1);
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 256);
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&s_full[u], 1);
+            mbar_init(&p_full[u], 256);
+        }
         mbar_init(g_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -718,7 +747,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
     } else if (warp == 1) {
-        constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);   // 128 keys x 64 queries
         constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
         constexpr uint32_t HI = desc_sw128_hi(1024);
         const uint32_t base = smem_u32(smem);
@@ -726,20 +755,37 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
         const uint32_t k_lo = desc_sw128_lo(base + C::OFF_K, 16);
         const uint32_t v_lo = desc_sw128_lo(base + C::OFF_V, 16);
-        for (int it = 0; it < steps && ok; ++it) {
-            const int s = it % kQNS;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (it / kQNS) & 1, abort_flag, args.ctl)))) break;
+        // S^T, dP^T of half step u: queries [64 (u % 2), 64 (u % 2) + 64) of the stage's
+        // tile (8 KB into each 64-column block), into buffer u % 2
+        auto issue_S = [&](int u) -> bool {
+            const int it = u >> 1, s = it % kQNS;
+            if ((u & 1) == 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / kQNS) & 1, abort_flag, args.ctl)))
+                    return false;
+                tc_fence_after();
+            }
+            const uint32_t st = base + C::OFF_RING + s * C::STAGE + (u & 1) * 8192;
+            const uint32_t buf = tmem + (u & 1) * 128;
+            mma_ss_k128<16384, 16384>(buf, k_lo, desc_sw128_lo(st, 16), HI, idS, 0);                 // S^T
+            mma_ss_k128<16384, 16384>(buf + 64, v_lo, desc_sw128_lo(st + TILE_BYTES, 16), HI, idS, 0);  // dP^T
+            mma_commit_elect(&s_full[u & 1]);
+            return true;
+        };
+        if (ok) ok = issue_S(0);
+        if (ok) ok = issue_S(1);
+        for (int u = 0; u < subs && ok; ++u) {
+            const int s = (u >> 1) % kQNS, hq = u & 1;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&p_full[hq], (u >> 1) & 1, abort_flag, args.ctl)))) break;
             tc_fence_after();
-            const uint32_t st = base + C::OFF_RING + s * C::STAGE;
-            mma_ss_k128<16384, 16384>(tmem + 0, k_lo, desc_sw128_lo(st, 16), HI, idS, 0);                // S^T
-            mma_ss_k128<16384, 16384>(tmem + 128, v_lo, desc_sw128_lo(st + TILE_BYTES, 16), HI, idS, 0);  // dP^T
-            mma_commit_elect(s_full);
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, it & 1, abort_flag, args.ctl)))) break;
-            tc_fence_after();
-            // dV += P^T dY, dK += dS^T Q: A from TMEM, B (dY, Q) MN-major
-            mma_ts_k128(tmem + 256, tmem + 0, desc_sw128_lo(st + TILE_BYTES, 16384), HI, idO, it != 0);
-            mma_ts_k128(tmem + 384, tmem + 128, desc_sw128_lo(st, 16384), HI, idO, it != 0);
-            mma_commit_elect(&empty[s]);
+            // dV += P^T dY_u, dK += dS^T Q_u: A from TMEM (each warpgroup's 32 queries packed
+            // over the first 16 of its 32 columns), B (dY_u, Q_u) MN-major
+            const uint32_t st = base + C::OFF_RING + s * C::STAGE + hq * 8192;
+            const uint32_t buf = tmem + hq * 128;
+            mma_ts_k64_split<32>(tmem + 256, buf, desc_sw128_lo(st + TILE_BYTES, 16384), HI, idO, u != 0);
+            mma_ts_k64_split<32>(tmem + 384, buf + 64, desc_sw128_lo(st, 16384), HI, idO, u != 0);
+            if (hq == 1) mma_commit_elect(&empty[s]);
+            // (the MMAs run in issue order: S^T of u + 2 overwrites this buffer after these read it)
+            if (u + 2 < subs && !(ok = issue_S(u + 2))) break;
         }
         if (ok) {
             mma_commit_elect(g_full);
@@ -748,7 +794,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp >= 4) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-        // ---- one key row per thread, query columns [64 wg, 64 wg + 64) of every step
+        // ---- one key row per thread, query columns [32 wg, 32 wg + 32) of every half step
         const int wg = (warp - 4) >> 2;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
@@ -757,66 +803,53 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float sl2 = kLog2e / sqrtf((float)HD);
         const float isq = 1.0f / sqrtf((float)HD);
         bool ok = true;
-        for (int it = 0; it < steps && ok; ++it) {
-            const int s = it % kQNS;
-            const int q0 = (t0 + it % nqt) * kTile;
-            // (both warpgroups decide together: the step has a 256-thread barrier)
-            ok = named_bar_and(2, 256, __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, args.ctl)));
-            if (!ok) break;
+        for (int u = 0; u < subs && ok; ++u) {
+            const int it = u >> 1, s = it % kQNS, hq = u & 1;
+            const long qc = (long)(t0 + it % nqt) * kTile + 64 * hq + 32 * wg;   // this thread's first query
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[hq], (u >> 1) & 1, abort_flag, args.ctl)))) break;
             tc_fence_after();
-            const float* L2 = reinterpret_cast<const float*>(smem + C::OFF_RING + s * C::STAGE + 2 * TILE_BYTES);
+            const float* L2 = reinterpret_cast<const float*>(smem + C::OFF_RING + s * C::STAGE + 2 * TILE_BYTES) +
+                              64 * hq + 32 * wg;
             const float* Dd = L2 + kTile;
-            // query column c (row q0 + c) sees this key when off + q0 + c >= kj
-            long cmin_l = args.causal ? kj - off - q0 : 0;
-            const int cmin = cmin_l < 0 ? 0 : (cmin_l > 128 ? 128 : (int)cmin_l);
-            // each chunk of 32 columns: load S^T and dP^T, compute, keep only the packed
-            // bf16 P^T and dS^T (the stores wait until both warpgroups have loaded)
-            uint32_t ppk[2][16], dpk[2][16];
+            // query column c (query qc + c) sees this key when off + qc + c >= kj
+            const long cmin_l = args.causal ? kj - off - qc : 0;
+            const int cmin = cmin_l < 0 ? 0 : (cmin_l > 32 ? 32 : (int)cmin_l);
+            const uint32_t buf = tmem + lane_base + hq * 128 + 32 * wg;
+            uint32_t sv[32], dp[32], ppk[16], dpk[16];
+            tmem_ld32(buf, sv);
+            tmem_ld32(buf + 64, dp);
+            tmem_wait_ld();
+            // p = exp2(s sl2 - lse2), dS = p (dP - D) (the 1/sqrt(d_k) is applied to
+            // dK in the epilogue), two columns per packed fp32 instruction
+            const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * wg + cc;
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tmem + lane_base + c * 32, sv);
-                tmem_ld32(tmem + lane_base + 128 + c * 32, dp);
-                tmem_wait_ld();
-                // p = exp2(s sl2 - lse2), dS = p (dP - D) (the 1/sqrt(d_k) is applied to
-                // dK in the epilogue), two columns per packed fp32 instruction
-                const float2 sl2x2 = make_float2(sl2, sl2);
+            for (int g4 = 0; g4 < 8; ++g4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(L2 + 4 * g4);
+                const float4 d4 = *reinterpret_cast<const float4*>(Dd + 4 * g4);
 #pragma unroll
-                for (int g4 = 0; g4 < 8; ++g4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(L2 + c * 32 + 4 * g4);
-                    const float4 d4 = *reinterpret_cast<const float4*>(Dd + c * 32 + 4 * g4);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int e = 4 * g4 + 2 * h2;
-                        const float2 nl = h2 ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-                        const float2 nd = h2 ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-                        const float2 x =
-                            __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl);
-                        float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        if (cmin > 0) {
-                            if (c * 32 + e < cmin) pr.x = 0.f;
-                            if (c * 32 + e + 1 < cmin) pr.y = 0.f;
-                        }
-                        const float2 ds = __fmul2_rn(
-                            pr, __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
-                        ppk[cc][2 * g4 + h2] = pack_bf16x2(pr.x, pr.y);
-                        dpk[cc][2 * g4 + h2] = pack_bf16x2(ds.x, ds.y);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int e = 4 * g4 + 2 * h2;
+                    const float2 nl = h2 ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+                    const float2 nd = h2 ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                    const float2 x =
+                        __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl);
+                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (cmin > 0) {
+                        if (e < cmin) pr.x = 0.f;
+                        if (e + 1 < cmin) pr.y = 0.f;
                     }
+                    const float2 ds = __fmul2_rn(
+                        pr, __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+                    ppk[2 * g4 + h2] = pack_bf16x2(pr.x, pr.y);
+                    dpk[2 * g4 + h2] = pack_bf16x2(ds.x, ds.y);
                 }
             }
-            // both warpgroups have read their columns of S^T and dP^T: the packed P^T
-            // and dS^T (over the first 64 columns of each) may now overwrite them
-            named_bar_sync(2, 256);
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * wg + cc;
-                tmem_st16(tmem + lane_base + c * 16, ppk[cc]);
-                tmem_st16(tmem + lane_base + 128 + c * 16, dpk[cc]);
-            }
+            // packed P^T and dS^T over the first 16 of the 32 columns this warpgroup read
+            tmem_st16(buf, ppk);
+            tmem_st16(buf + 64, dpk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[hq]);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
         tc_fence_after();
@@ -1117,14 +1150,20 @@ cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w
     }
     if (p.gate_mode == 0) return e;
 
-    // 4. the gate's weight and input gradients
+    // 4. the gate's weight and input gradients (on CTA pairs where N fills a 256-column tile)
     const int rows = p.B * p.Lq, G = gate_cols(p);
-    alignas(64) CUtensorMap tA, tB;
     // dX [rows x d_model] = dGl [rows x G] W_g^T: A = dGl (K = G contiguous), B^T = W_g [d_model][G]
-    if (!map_kmajor(&tA, ws + w.dGl, rows, G) || !map_kmajor(&tB, p.Wg, p.d_model, G)) return cudaErrorInvalidValue;
-    e = launch_gemm<false, false>(tA, tB, static_cast<__nv_bfloat16*>(g.dX), rows, p.d_model, G, rt, s);
+    if (p.d_model >= 256) {
+        e = launch_gemm_pair_bf16(ws + w.dGl, p.Wg, g.dX, rows, p.d_model, G, false, rt, s);
+    } else {
+        alignas(64) CUtensorMap tA, tB;
+        if (!map_kmajor(&tA, ws + w.dGl, rows, G) || !map_kmajor(&tB, p.Wg, p.d_model, G))
+            return cudaErrorInvalidValue;
+        e = launch_gemm<false, false>(tA, tB, static_cast<__nv_bfloat16*>(g.dX), rows, p.d_model, G, rt, s);
+    }
     if (e != cudaSuccess) return e;
     // dW_g [d_model x G] = X^T dGl: A stored as X [rows][d_model], B as dGl [rows][G]
+    if (G >= 256) return launch_gemm_pair_bf16(p.X, ws + w.dGl, g.dWg, p.d_model, G, rows, true, rt, s);
     alignas(64) CUtensorMap tA2, tB2;
     if (!map_mnmajor(&tA2, p.X, rows, p.d_model) || !map_mnmajor(&tB2, ws + w.dGl, rows, G))
         return cudaErrorInvalidValue;

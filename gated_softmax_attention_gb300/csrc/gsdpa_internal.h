@@ -129,6 +129,11 @@ bool bwd_supported(const Problem& p);
 BwdPlan plan_bwd(const Problem& p, int num_sms);
 cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w, char* ws, const Runtime& rt,
                             cudaStream_t s);
+// C [M x N] (bf16, row-major) = A B on CTA pairs (bwd_gemm_sm103.cu), for N >= 256.
+// ab_mn: A stored [K][M] and B stored [K][N]; else A stored [M][K] and B^T
+// stored [N][K]. Every row stride a multiple of 16 bytes, every base 16-byte aligned.
+cudaError_t launch_gemm_pair_bf16(const void* A, const void* Bm, void* C, int M, int N, int K, bool ab_mn,
+                                  const Runtime& rt, cudaStream_t s);
 // bf16 prefill kernels: where the first-token share accumulates (null without
 // it), its fixed-point scale 2^F with F = 43 - ceil(log2(L_q + 1)), the factor
 // 2^-F / L_q back to the mean, and the arrivals of a full set (4 per query tile).

@@ -140,6 +140,13 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* s
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
@@ -556,6 +563,35 @@ __device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, ui
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
         "}"
         ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// TS over K = 64 (four K = 16 steps) whose A columns lie in two runs of 16:
+// steps 0, 1 at a_tmem + 0, 8 and steps 2, 3 at a_tmem + A2, A2 + 8 (two
+// writers each packed their 32 columns of P over their own columns); B as in
+// mma_ts_k128.
+template <uint32_t A2>
+__device__ __forceinline__ void mma_ts_k64_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t"
+        "add.u32 bl, %2, 128;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, %6;\n\t"
+        "add.u32 bl, %2, 256;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "add.u32 ta, %1, %7;\n\t"
+        "add.u32 bl, %2, 384;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "n"(A2), "n"(A2 + 8)
         : "memory");
 }
 }  // namespace gsdpa

@@ -59,7 +59,8 @@ def _load():
             lib.gsdpa_oracle_bwd.argtypes = [dp] * 11 + [ctypes.c_int] * 9
             lib.gsdpa_oracle_bwd.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 9 + [ip, ip, ctypes.c_long, ip, ip,
-                                                                                   ctypes.c_long, dp, dp, dp, ctypes.c_int]
+                                                                                   ctypes.c_long, dp, dp, dp, dp,
+                                                                                   ctypes.c_int]
             lib.gsdpa_oracle_bwd_rows.restype = ctypes.c_int
             lib.gsdpa_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -178,8 +179,10 @@ def sink_share(p0):
 
 def gated_sdpa_bwd_rows(X, Q, K, V, W_g, dO, q_rows, k_rows, *, gate="elementwise", causal=True, n_threads=0):
     """The backward's outputs on sampled rows: dQ for the (b, i) pairs in
-    ``q_rows`` ([nq, H_q, d_k]) and dK, dV for the (b, j) pairs in ``k_rows``
-    ([nk, H_kv, d_k] each). Same definition as :func:`gated_sdpa_bwd`."""
+    ``q_rows`` ([nq, H_q, d_k]), dK, dV for the (b, j) pairs in ``k_rows``
+    ([nk, H_kv, d_k] each) and, with a gate, the gate path's input gradient
+    dX for the rows of ``q_rows`` ([nq, d_model]). Same definition as
+    :func:`gated_sdpa_bwd`."""
     gm = _GATE_CODES[gate]
     Q, K, V, dOd = _f64(Q), _f64(K), _f64(V), _f64(dO)
     B, Lq, Hq, dk = Q.shape
@@ -197,11 +200,15 @@ def gated_sdpa_bwd_rows(X, Q, K, V, W_g, dO, q_rows, k_rows, *, gate="elementwis
     dQ = np.empty((qr.shape[0], Hq, dk), np.float64)
     dK = np.empty((kr.shape[0], Hkv, dk), np.float64)
     dV = np.empty((kr.shape[0], Hkv, dk), np.float64)
+    dX = np.empty((qr.shape[0], d_model), np.float64) if gm != GATE_NONE else None
     ip = ctypes.c_int
     rc = _load().gsdpa_oracle_bwd_rows(
         _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(dOd), B, Lq, Lk, d_model, Hq, Hkv, dk, gm,
         int(bool(causal)), _ptr(qb, ip), _ptr(qi, ip), qr.shape[0], _ptr(kb, ip), _ptr(kj, ip), kr.shape[0],
-        _ptr(dQ), _ptr(dK), _ptr(dV), int(n_threads))
+        _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dX), int(n_threads))
     if rc != 0:
         raise ValueError("oracle rejected the shapes or rows")
-    return {"dQ": dQ, "dK": dK, "dV": dV}
+    out = {"dQ": dQ, "dK": dK, "dV": dV}
+    if dX is not None:
+        out["dX"] = dX
+    return out

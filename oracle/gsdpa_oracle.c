@@ -322,21 +322,24 @@ int gsdpa_oracle_bwd(const double* X, const double* Q, const double* K, const do
  * gsdpa_oracle_bwd: the same chain rule, in two passes.
  *   Pass 1, every row (b, i) and head h (parallel over rows): the row's
  *   softmax p, its log-denominator lse, the gate g, dy = dO g and
- *   Dsum = sum_j p_j dp_j (= sum_c dy_c y_c); dQ for the listed query rows.
+ *   Dsum = sum_j p_j dp_j (= sum_c dy_c y_c); dQ for the listed query rows
+ *   and, with a gate and dX_rows non-null, their dX = dGl W_g^T (dGl = dO y
+ *   sigma (1 - sigma), y = sum_j p_j V_j, summed over the head for a
+ *   headwise gate).
  *   Pass 2, every listed key row (b, j) (parallel over them): for each head h
  *   of kv(j)'s group and each query i that sees j,
  *     p_ij = exp(s_ij - lse_i), dp_ij = sum_c dy_ic V_jc,
  *     ds_ij = p_ij (dp_ij - Dsum_i),
  *     dK_j += ds_ij Q_i / sqrt(d_k),   dV_j += p_ij dy_i.
  *   qb, qi [nq]: query rows;  kb, kj [nk]: key rows
- *   dQ_rows [nq, H_q, d_k];  dK_rows, dV_rows [nk, H_kv, d_k]
+ *   dQ_rows [nq, H_q, d_k];  dK_rows, dV_rows [nk, H_kv, d_k];  dX_rows [nq, d_model] or null
  * Returns 0, or -1 on a shape the definition does not cover or no memory.
  */
 int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, const double* V,
                           const double* Wg, const double* dO,
                           int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk, int gate_mode, int causal,
                           const int* qb, const int* qi, long nq, const int* kb, const int* kj, long nk,
-                          double* dQ_rows, double* dK_rows, double* dV_rows, int n_threads)
+                          double* dQ_rows, double* dK_rows, double* dV_rows, double* dX_rows, int n_threads)
 {
     if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq > Lk) return -1;
     if (gate_mode < 0 || gate_mode > 2) return -1;
@@ -371,13 +374,14 @@ int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, con
         double* p = (double*)malloc(sizeof(double) * (size_t)Lk);
         double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
         double* y = (double*)malloc(sizeof(double) * (size_t)dk);
-        if (!p || !dp || !y) {
+        double* gv = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!p || !dp || !y || !gv) {
 #pragma omp atomic write
             failed = 1;
         }
 #pragma omp for schedule(dynamic, 4)
         for (long r = 0; r < rows; ++r) {
-            if (!p || !dp || !y) continue;
+            if (!p || !dp || !y || !gv) continue;
             const int b = (int)(r / Lq), i = (int)(r % Lq);
             const long a = (long)Lk - Lq + i;
             const long n_keys = causal ? a + 1 : Lk;
@@ -416,6 +420,7 @@ int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, con
                         for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + col];
                         g = 1.0 / (1.0 + exp(-gl));
                     }
+                    gv[c] = g;
                     dy[c] = dout[c] * g;
                 }
                 double ds_sum = 0.0;
@@ -436,10 +441,35 @@ int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, con
                         const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
                         for (int c = 0; c < dk; ++c) dq[c] += ds * k[c];
                     }
+                    if (dX_rows && gate_mode != ORACLE_GATE_NONE) {
+                        /* the gate's input gradient: dGl = dO . Y . sigma (1 - sigma) with Y = P V
+                         * the ungated output (summed over the head's columns for a headwise
+                         * gate), then dX = dGl W_g^T, accumulated over the heads */
+                        double* dx = dX_rows + qr * d_model;
+                        if (h == 0)
+                            for (int m = 0; m < d_model; ++m) dx[m] = 0.0;
+                        for (int c = 0; c < dk; ++c) y[c] = 0.0;
+                        for (long j = 0; j < n_keys; ++j) {
+                            const double* v = V + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                            for (int c = 0; c < dk; ++c) y[c] += p[j] * v[c];
+                        }
+                        if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
+                            for (int c = 0; c < dk; ++c) {
+                                const double dgl = dout[c] * y[c] * gv[c] * (1.0 - gv[c]);
+                                const long col = (long)h * dk + c;
+                                for (int m = 0; m < d_model; ++m) dx[m] += dgl * Wg[(long)m * gate_cols + col];
+                            }
+                        } else {
+                            double dgl = 0.0;
+                            for (int c = 0; c < dk; ++c) dgl += dout[c] * y[c];
+                            dgl *= g_head * (1.0 - g_head);
+                            for (int m = 0; m < d_model; ++m) dx[m] += dgl * Wg[(long)m * gate_cols + h];
+                        }
+                    }
                 }
             }
         }
-        free(p); free(dp); free(y);
+        free(p); free(dp); free(y); free(gv);
     }
     /* pass 2 */
     if (!failed) {

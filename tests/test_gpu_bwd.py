@@ -48,6 +48,8 @@ CASES = [
     _w("gqa_headwise_b2", B=2, L_q=257, L_k=257, H_q=8, H_kv=2, gate="headwise", seed=32),
     _w("no_gate_full_mask", L_q=200, L_k=300, gate="none", causal=False, seed=33),
     _w("elementwise_bottom_right_suffix", L_q=77, L_k=300, H_q=4, H_kv=1, seed=34),
+    # a wide gate: dW_g [2560 x 2048] takes 256 x 512 tiles (K = 72 rows: a full chunk and a ragged one)
+    _w("elementwise_wide_gate", L_q=72, L_k=72, d_model=2560, H_q=16, H_kv=4, seed=35),
 ]
 
 
@@ -84,8 +86,8 @@ def test_backward_matches_oracle(w):
 # ------------------------------------------------------------------ full size, the shape bench.py times
 
 def test_full_size_backward_sampled_rows_and_properties():
-    """The headline workload's backward: dQ on sampled query rows and dK, dV
-    on sampled key rows against the oracle's row form; and two properties of
+    """The headline workload's backward: dQ and dX on sampled query rows and
+    dK, dV on sampled key rows against the oracle's row form; and two properties of
     the whole tensors: the values' gradients sum to the rows' dy = dO G (rows
     of p sum to one), and sum(dX X) = sum(dW_g W_g) (both equal sum(dGl (X W_g)))."""
     from gated_softmax_attention_gb300.workloads import WORKLOADS
@@ -108,6 +110,7 @@ def test_full_size_backward_sampled_rows_and_properties():
     _check("full dQ rows", np.stack([got["dQ"][b, i] for b, i in q_rows]), ref["dQ"])
     _check("full dK rows", np.stack([got["dK"][b, j] for b, j in k_rows]), ref["dK"])
     _check("full dV rows", np.stack([got["dV"][b, j] for b, j in k_rows]), ref["dV"])
+    _check("full dX rows", np.stack([got["dX"][b, i] for b, i in q_rows]), ref["dX"])
     # properties of the whole tensors
     X = t["X"].double().numpy()
     W = t["W_g"].double().numpy()

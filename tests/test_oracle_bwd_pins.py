@@ -220,3 +220,7 @@ def test_bwd_rows_equals_full_backward(case):
     np.testing.assert_allclose(rows["dQ"], full["dQ"].reshape(-1, Hq, dk), rtol=1e-10, atol=1e-13)
     np.testing.assert_allclose(rows["dK"], full["dK"].reshape(-1, Hkv, dk), rtol=1e-10, atol=1e-13)
     np.testing.assert_allclose(rows["dV"], full["dV"].reshape(-1, Hkv, dk), rtol=1e-10, atol=1e-13)
+    if gate == "none":
+        assert "dX" not in rows
+    else:
+        np.testing.assert_allclose(rows["dX"], full["dX"].reshape(-1, dm), rtol=1e-10, atol=1e-13)
