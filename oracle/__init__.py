@@ -9,8 +9,10 @@ layer's definition written out; its header lists the page and section each
 step follows). This module compiles it with gcc on first use and exposes it
 to numpy.
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
-forms, invariants and a library routine (torch's CPU float64 SDPA); no
+Every function here is pinned by ``tests/test_oracle_pins.py`` (and, for
+the backward and the gate variants, ``tests/test_oracle_bwd_pins.py`` and
+``tests/test_oracle_variant_pins.py``) against closed forms, invariants and
+library routines (torch's CPU float64 SDPA and autograd, numpy matmul); no
 function is left with parity unpinned.
 """
 from __future__ import annotations
@@ -29,7 +31,14 @@ _lock = threading.Lock()
 _lib = None
 
 GATE_NONE, GATE_HEADWISE, GATE_ELEMENTWISE = 0, 1, 2
+GATE_HEADWISE_SHARED, GATE_ELEMENTWISE_SHARED, GATE_STATIC = 3, 4, 5
 _GATE_CODES = {"none": GATE_NONE, "headwise": GATE_HEADWISE, "elementwise": GATE_ELEMENTWISE}
+_VARIANT_GATE_CODES = dict(_GATE_CODES, headwise_shared=GATE_HEADWISE_SHARED,
+                           elementwise_shared=GATE_ELEMENTWISE_SHARED, static=GATE_STATIC)
+# the gate's function of its logit and its combination with the SDPA output y,
+# or (without a gate) a function of y alone
+GATE_FNS = {"sigmoid_mul": 0, "ns_sigmoid_mul": 1, "sigmoid_add": 2, "silu_add": 3, "identity_add": 4,
+            "silu_self": 5, "rmsnorm": 6}
 
 
 def build(force: bool = False) -> str:
@@ -56,6 +65,9 @@ def _load():
             lib.gsdpa_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
                 ip, ip, ctypes.c_long, ctypes.c_int]
             lib.gsdpa_oracle_fwd.restype = ctypes.c_int
+            lib.gsdpa_oracle_fwd_variant.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
+                ctypes.c_double, ctypes.c_int, ip, ip, ctypes.c_long, ctypes.c_int]
+            lib.gsdpa_oracle_fwd_variant.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd.argtypes = [dp] * 11 + [ctypes.c_int] * 9
             lib.gsdpa_oracle_bwd.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 9 + [ip, ip, ctypes.c_long, ip, ip,
@@ -131,6 +143,48 @@ def gated_sdpa(X, Q, K, V, W_g, *, gate="elementwise", causal=True, rows=None, n
     if rc != 0:
         raise ValueError("oracle rejected the shapes or rows")
     return (O, p0, lse) if return_lse else (O, p0)
+
+
+def gated_sdpa_variant(X, Q, K, V, W_g, *, gate="elementwise", gate_fn="sigmoid_mul", eps=1e-6, causal=True,
+                       rows=None, n_threads=0):
+    """The layer with one of the gate variants, in float64 (see the header of
+    ``gsdpa_oracle.c`` for the definitions and their sources).
+
+    ``gate``: "none", "headwise" (W_g [d_model, H_q]), "elementwise"
+    ([d_model, H_q*d_k]), "headwise_shared" ([d_model, 1]), "elementwise_shared"
+    ([d_model, d_k]) or "static" (W_g holds theta [H_q, d_k]; X is not read).
+    ``gate_fn``: "sigmoid_mul", "ns_sigmoid_mul", "sigmoid_add", "silu_add" or
+    "identity_add" with a gate; "silu_self" or "rmsnorm" (W_g holds gamma
+    [H_q, d_k], or None for 1) with ``gate == "none"``.
+    Returns (O, p0) shaped as :func:`gated_sdpa`'s.
+    """
+    gm = _VARIANT_GATE_CODES[gate]
+    fn = GATE_FNS[gate_fn]
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Lq, Hq, dk = Q.shape
+    _, Lk, Hkv, _ = K.shape
+    Xd = _f64(X) if (X is not None and gm not in (GATE_NONE, GATE_STATIC)) else None
+    Wd = _f64(W_g) if W_g is not None else None
+    d_model = Xd.shape[-1] if Xd is not None else 0
+    if rows is None:
+        O = np.empty((B, Lq, Hq, dk), np.float64)
+        p0 = np.empty((B, Lq, Hq), np.float64)
+        rb = ri = None
+        n = -1
+    else:
+        rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
+        rb = np.ascontiguousarray(rows[:, 0])
+        ri = np.ascontiguousarray(rows[:, 1])
+        n = rows.shape[0]
+        O = np.empty((n, Hq, dk), np.float64)
+        p0 = np.empty((n, Hq), np.float64)
+    rc = _load().gsdpa_oracle_fwd_variant(
+        _ptr(Xd), _ptr(Q), _ptr(K), _ptr(V), _ptr(Wd), _ptr(O), _ptr(p0), None,
+        B, Lq, Lk, d_model, Hq, Hkv, dk, gm, fn, float(eps), int(bool(causal)),
+        _ptr(rb, ctypes.c_int), _ptr(ri, ctypes.c_int), n, int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes, the gate variant or the rows")
+    return O, p0
 
 
 def gated_sdpa_bwd(X, Q, K, V, W_g, dO, *, gate="elementwise", causal=True):

@@ -35,6 +35,26 @@
  *                                  bias, head-major gate columns, one scalar
  *                                  per head when headwise).
  *   O[b,i,h,c] = y_c * 1/(1 + exp(-gl))         (gate NONE: O = y)
+ *
+ * Gate variants (gsdpa_oracle_fwd_variant; "GatedAttention [2025]", sec.
+ * 1.2.2 items (3)-(5), sec. 1.4.1 and sec. 1.4.2):
+ *   shapes: head-shared elementwise, W_g [d_model, d_k], gl = sum_m X W_g[m, c];
+ *           head-shared headwise, W_g [d_model, 1], gl = sum_m X W_g[m, 0]
+ *           (W_theta and the scores shared by every head, item (3b));
+ *           input-independent, theta [H_q, d_k] in place of W_g, gl = theta[h, c]
+ *           (a free parameter per head and column, sec. 1.4.2 (iii)).
+ *   functions of gl and the combination with y:
+ *           sigmoid, multiplied        O = y * s(gl),             s(x) = 1/(1+e^-x)
+ *           NS-sigmoid, multiplied     O = y * (0.5 + 0.5 s(gl))  (sec. 1.4.2 (iv))
+ *           sigmoid, added             O = y + s(gl)              (item (4b))
+ *           SiLU, added                O = y + gl s(gl)           (item (5); sec. 1.4.1)
+ *           identity, added            O = y + gl                 (sec. 1.4.1 (ii))
+ *   without W_g:
+ *           SiLU of the output         O = y * s(y)               (sec. 1.4.1 (i))
+ *           per-head RMSNorm           O = y / sqrt(mean_c y_c^2 + eps) * gamma[h, c]
+ *                                      (sec. 1.4.1, the norm applied to each
+ *                                      head's output before concatenation;
+ *                                      gamma given in place of W_g, or 1)
  *   p0[b,i,h]  = p_0, the attention weight on key 0 ("10 . 门控", sec. 3.4,
  *                the share of attention that lands on the first token).
  *   lse[b,i,h] = max s + log sum_j exp(s_j - max s), the log of the softmax
@@ -71,20 +91,65 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_GATE_NONE = 0, ORACLE_GATE_HEADWISE = 1, ORACLE_GATE_ELEMENTWISE = 2 };
+enum { ORACLE_GATE_NONE = 0, ORACLE_GATE_HEADWISE = 1, ORACLE_GATE_ELEMENTWISE = 2,
+       ORACLE_GATE_HEADWISE_SHARED = 3, ORACLE_GATE_ELEMENTWISE_SHARED = 4, ORACLE_GATE_STATIC = 5 };
+enum { ORACLE_FN_SIGMOID_MUL = 0, ORACLE_FN_NS_SIGMOID_MUL = 1, ORACLE_FN_SIGMOID_ADD = 2,
+       ORACLE_FN_SILU_ADD = 3, ORACLE_FN_IDENTITY_ADD = 4, ORACLE_FN_SILU_SELF = 5, ORACLE_FN_RMSNORM = 6 };
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* columns of W_g for a gate shape (0: no W_g read from X) */
+static long gate_width(int gate_mode, int Hq, int dk)
+{
+    switch (gate_mode) {
+    case ORACLE_GATE_HEADWISE: return Hq;
+    case ORACLE_GATE_ELEMENTWISE: return (long)Hq * dk;
+    case ORACLE_GATE_HEADWISE_SHARED: return 1;
+    case ORACLE_GATE_ELEMENTWISE_SHARED: return dk;
+    default: return 0;
+    }
+}
+
+/* gate logit of head h, column c of row x */
+static double gate_logit(const double* x, const double* Wg, int gate_mode, int d_model, int Hq, int dk, int h, int c)
+{
+    if (gate_mode == ORACLE_GATE_STATIC) return Wg[(long)h * dk + c];
+    long col;
+    switch (gate_mode) {
+    case ORACLE_GATE_HEADWISE: col = h; break;
+    case ORACLE_GATE_ELEMENTWISE: col = (long)h * dk + c; break;
+    case ORACLE_GATE_HEADWISE_SHARED: col = 0; break;
+    default: col = c; break;   /* elementwise, shared by the heads */
+    }
+    const long G = gate_width(gate_mode, Hq, dk);
+    double gl = 0.0;
+    for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * G + col];
+    return gl;
+}
+
+/* the gated output from y and the gate logit */
+static double gate_apply(double y, double gl, int gate_fn)
+{
+    switch (gate_fn) {
+    case ORACLE_FN_NS_SIGMOID_MUL: return y * (0.5 + 0.5 * sigmoid(gl));
+    case ORACLE_FN_SIGMOID_ADD: return y + sigmoid(gl);
+    case ORACLE_FN_SILU_ADD: return y + gl * sigmoid(gl);
+    case ORACLE_FN_IDENTITY_ADD: return y + gl;
+    default: return y * sigmoid(gl);
+    }
+}
 
 /* One query row (b, i), all heads. s is scratch of length >= L_k. */
 static void oracle_row(const double* X, const double* Q, const double* K, const double* V,
                        const double* Wg, double* O_row, double* p0_row, double* lse_row, double* s,
                        int b, int i, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
-                       int gate_mode, int causal)
+                       int gate_mode, int gate_fn, double eps, int causal)
 {
     const int group = Hq / Hkv;
     const long a = (long)Lk - Lq + i;
     const long n_keys = causal ? a + 1 : Lk;
     const double inv_sqrt_dk = 1.0 / sqrt((double)dk);
-    const double* x = X + ((long)b * Lq + i) * d_model;
-    const long gate_cols = (gate_mode == ORACLE_GATE_ELEMENTWISE) ? (long)Hq * dk : Hq;
+    const double* x = X ? X + ((long)b * Lq + i) * d_model : 0;
 
     for (int h = 0; h < Hq; ++h) {
         const int kvh = h / group;
@@ -109,27 +174,23 @@ static void oracle_row(const double* X, const double* Q, const double* K, const 
         if (p0_row) p0_row[h] = s[0];
         if (lse_row) lse_row[h] = mx + log(denom);
 
-        /* headwise gate: one logit for the head */
-        double g_head = 1.0;
-        if (gate_mode == ORACLE_GATE_HEADWISE) {
-            double gl = 0.0;
-            for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + h];
-            g_head = 1.0 / (1.0 + exp(-gl));
-        }
-
         double* o = O_row + (long)h * dk;
         for (int c = 0; c < dk; ++c) {
             double y = 0.0;
             for (long j = 0; j < n_keys; ++j)
                 y += s[j] * V[(((long)b * Lk + j) * Hkv + kvh) * dk + c];
-            double g = g_head;
-            if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
-                double gl = 0.0;
-                const long col = (long)h * dk + c;
-                for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * gate_cols + col];
-                g = 1.0 / (1.0 + exp(-gl));
-            }
-            o[c] = y * g;
+            o[c] = y;
+        }
+        if (gate_mode != ORACLE_GATE_NONE) {
+            for (int c = 0; c < dk; ++c)
+                o[c] = gate_apply(o[c], gate_logit(x, Wg, gate_mode, d_model, Hq, dk, h, c), gate_fn);
+        } else if (gate_fn == ORACLE_FN_SILU_SELF) {
+            for (int c = 0; c < dk; ++c) o[c] = o[c] * sigmoid(o[c]);
+        } else if (gate_fn == ORACLE_FN_RMSNORM) {
+            double ss = 0.0;
+            for (int c = 0; c < dk; ++c) ss += o[c] * o[c];
+            const double r = 1.0 / sqrt(ss / dk + eps);
+            for (int c = 0; c < dk; ++c) o[c] = o[c] * r * (Wg ? Wg[(long)h * dk + c] : 1.0);
         }
     }
 }
@@ -142,16 +203,22 @@ static void oracle_row(const double* X, const double* Q, const double* K, const 
  *   rows_b, rows_i : the (b, i) pairs when n_rows >= 0
  *   n_threads : OpenMP threads (<= 0: library default)
  */
-int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const double* V,
-                     const double* Wg, double* O, double* p0, double* lse,
-                     int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
-                     int gate_mode, int causal,
-                     const int* rows_b, const int* rows_i, long n_rows, int n_threads)
+int gsdpa_oracle_fwd_variant(const double* X, const double* Q, const double* K, const double* V,
+                             const double* Wg, double* O, double* p0, double* lse,
+                             int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
+                             int gate_mode, int gate_fn, double eps, int causal,
+                             const int* rows_b, const int* rows_i, long n_rows, int n_threads)
 {
     if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
     if (Lq > Lk) return -1;
-    if (gate_mode != ORACLE_GATE_NONE && (d_model < 1 || !X || !Wg)) return -1;
-    if (gate_mode < 0 || gate_mode > 2) return -1;
+    if (gate_mode < ORACLE_GATE_NONE || gate_mode > ORACLE_GATE_STATIC) return -1;
+    if (gate_fn < ORACLE_FN_SIGMOID_MUL || gate_fn > ORACLE_FN_RMSNORM) return -1;
+    /* the functions of the output alone take no gate; the gates take one of the five functions of gl */
+    if (gate_mode == ORACLE_GATE_NONE && gate_fn != ORACLE_FN_SIGMOID_MUL && gate_fn < ORACLE_FN_SILU_SELF) return -1;
+    if (gate_mode != ORACLE_GATE_NONE && gate_fn >= ORACLE_FN_SILU_SELF) return -1;
+    if (gate_mode == ORACLE_GATE_STATIC && !Wg) return -1;
+    if (gate_width(gate_mode, Hq, dk) > 0 && (d_model < 1 || !X || !Wg)) return -1;
+    if (gate_fn == ORACLE_FN_RMSNORM && !(eps >= 0.0)) return -1;
 
     const long total = (n_rows < 0) ? (long)B * Lq : n_rows;
     for (long r = 0; n_rows >= 0 && r < n_rows; ++r)
@@ -177,11 +244,23 @@ int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const do
             else            { b = rows_b[r];     i = rows_i[r]; }
             oracle_row(X, Q, K, V, Wg, O + r * (long)Hq * dk, p0 ? p0 + r * (long)Hq : 0,
                        lse ? lse + r * (long)Hq : 0, s,
-                       b, i, Lq, Lk, d_model, Hq, Hkv, dk, gate_mode, causal);
+                       b, i, Lq, Lk, d_model, Hq, Hkv, dk, gate_mode, gate_fn, eps, causal);
         }
         free(s);
     }
     return failed ? -1 : 0;
+}
+
+/* The layer with the default gate function (sigmoid, multiplied). */
+int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const double* V,
+                     const double* Wg, double* O, double* p0, double* lse,
+                     int B, int Lq, int Lk, int d_model, int Hq, int Hkv, int dk,
+                     int gate_mode, int causal,
+                     const int* rows_b, const int* rows_i, long n_rows, int n_threads)
+{
+    if (gate_mode < ORACLE_GATE_NONE || gate_mode > ORACLE_GATE_ELEMENTWISE) return -1;
+    return gsdpa_oracle_fwd_variant(X, Q, K, V, Wg, O, p0, lse, B, Lq, Lk, d_model, Hq, Hkv, dk, gate_mode,
+                                    ORACLE_FN_SIGMOID_MUL, 0.0, causal, rows_b, rows_i, n_rows, n_threads);
 }
 
 /*
