@@ -27,6 +27,8 @@ SIGNATURES = {
     "gsdpa_workspace_bytes": (_SZ, [_I] * 10),
     "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gsdpa_workspace_bytes_variant": (_SZ, [_I] * 11),
+    "gated_sdpa_fwd_variant": (_I, [_VP] * 7 + [_I] * 9 + [ctypes.c_float, _I, _I, _VP, _SZ, _VP]),
     "gsdpa_bwd_workspace_bytes": (_SZ, [_I] * 8),
     "gated_sdpa_bwd": (_I, [_VP] * 13 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_check_device_error": (_I, [_VP]),
@@ -166,6 +168,60 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
     if st != OK:
         raise GsdpaError(st, where)
     return out, sink, lse
+
+
+# gate shapes and gate functions of gated_sdpa_fwd_variant (gsdpa.h)
+VARIANT_GATE_CODES = dict(GATE_CODES, headwise_shared=3, elementwise_shared=4, static=5)
+GATE_FNS = {"sigmoid_mul": 0, "ns_sigmoid_mul": 1, "sigmoid_add": 2, "silu_add": 3, "identity_add": 4,
+            "silu_self": 5, "rmsnorm": 6}
+
+
+def workspace_bytes_variant(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise", gate_fn="sigmoid_mul",
+                            want_sink=False, dtype=BF16) -> int:
+    n = load().gsdpa_workspace_bytes_variant(B, L_q, L_k, d_model, H_q, H_kv, d_k, VARIANT_GATE_CODES[gate],
+                                             GATE_FNS[gate_fn], int(bool(want_sink)), dtype)
+    if n == ctypes.c_size_t(-1).value:
+        raise GsdpaError(ERR_INVALID_ARG, "gsdpa_workspace_bytes_variant")
+    return int(n)
+
+
+def gated_sdpa_fwd_variant(X, Q, K, V, W_g=None, *, gate="elementwise", gate_fn="sigmoid_mul", eps=1e-6,
+                           causal=True, out=None, sink=None, want_sink=False, workspace=None, stream=None):
+    """The forward with a gate variant (gated_sdpa_fwd_variant): ``gate`` one of
+    none, headwise, elementwise, headwise_shared (W_g [d_model, 1]),
+    elementwise_shared (W_g [d_model, d_k]), static (W_g = theta [H_q, d_k],
+    X unused); ``gate_fn`` one of GATE_FNS (rmsnorm: W_g = gamma [H_q, d_k] or
+    None). Returns (O, sink)."""
+    import torch
+    if Q.dtype == torch.bfloat16:
+        dtype = BF16
+    elif Q.dtype == torch.float32:
+        dtype = F32
+    else:
+        raise TypeError(f"unsupported dtype {Q.dtype}")
+    gm, fn = VARIANT_GATE_CODES[gate], GATE_FNS[gate_fn]
+    reads_x = gm not in (GATE_NONE, 5)
+    for t in [Q, K, V] + ([X] if reads_x else []) + ([W_g] if W_g is not None else []):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
+            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
+    B, L_q, H_q, d_k = Q.shape
+    L_k, H_kv = K.shape[1], K.shape[2]
+    d_model = X.shape[-1] if reads_x else 0
+    if out is None:
+        out = torch.empty_like(Q)
+    if sink is None and want_sink:
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
+    need = workspace_bytes_variant(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, gate_fn, sink is not None, dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gated_sdpa_fwd_variant(
+        _ptr(X) if reads_x else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), _ptr(sink),
+        B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, fn, float(eps), int(bool(causal)), dtype,
+        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+    if st != OK:
+        raise GsdpaError(st, "gated_sdpa_fwd_variant")
+    return out, sink
 
 
 def bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise") -> int:

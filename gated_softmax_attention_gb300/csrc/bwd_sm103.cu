@@ -1026,7 +1026,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfl
 
 }  // namespace
 
-bool bwd_supported(const Problem& p) { return p.dtype == 1 && p.dk == HD && p.Lq >= 1; }
+// (the gate variants of gated_sdpa_fwd_variant have no backward here)
+bool bwd_supported(const Problem& p) { return p.dtype == 1 && p.dk == HD && p.Lq >= 1 && p.gate_mode <= 2; }
 
 BwdPlan plan_bwd(const Problem& p, int num_sms) {
     BwdPlan w;

@@ -24,6 +24,7 @@
 // which reads each column of W_g once for the whole batch.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
+#include "gate_fn.cuh"
 
 #include <cmath>
 
@@ -50,6 +51,9 @@ struct DecodeArgs {
     float* sink;                  // [B, Hq] or null
     const float* gate_part;       // [gate_splits, B, gate_cols] or null
     int gate_splits, gate_mode, gate_cols;
+    const __nv_bfloat16* theta;   // input-independent gate [Hq, HD], or RMSNorm gamma [Hq, HD] (or null)
+    int gate_fn;                  // gsdpa_gate_fn
+    float eps;
     float* part_ml;               // [B, Hq, splits, 2]  (max in log2 units, sum)
     float* part_o;                // [B, Hq, splits, HD]
     float* part_x0;               // [B, Hq]  scaled score of key 0
@@ -346,25 +350,51 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         r1 += __ldcg(&args.part_o[(base + s2) * HD + dd + 1]) * sc;
     }
     const float inv = 1.0f / Lt;
-    float g0 = 1.f, g1 = 1.f;
+    // ---- the gate (gsdpa_gate_mode / gsdpa_gate_fn) on y = (r0, r1) * inv
+    float y0 = r0 * inv, y1 = r1 * inv;
+    const int fn = args.gate_fn;
     if (args.gate_mode != 0) {
-        pdl_wait();   // the gate-logit kernel has completed (a no-op after an ordinary launch)
         float gl0 = 0.f, gl1 = 0.f;
-        const long rowoff = (long)b * args.gate_cols;
-        const long gsz = (long)args.B * args.gate_cols;
-        for (int s2 = 0; s2 < args.gate_splits; ++s2) {
-            if (args.gate_mode == 2) {
-                gl0 += args.gate_part[s2 * gsz + rowoff + (long)head * HD + dd];
-                gl1 += args.gate_part[s2 * gsz + rowoff + (long)head * HD + dd + 1];
-            } else {
-                gl0 += args.gate_part[s2 * gsz + rowoff + head];
+        if (args.gate_mode == 5) {   // input-independent: theta [Hq, HD]
+            gl0 = __bfloat162float(args.theta[(long)head * HD + dd]);
+            gl1 = __bfloat162float(args.theta[(long)head * HD + dd + 1]);
+        } else {
+            pdl_wait();   // the gate-logit kernel has completed (a no-op after an ordinary launch)
+            // logit column of (head, dd): elementwise, headwise, headwise shared, elementwise shared
+            const int m = args.gate_mode;
+            const long c0 = m == 2 ? (long)head * HD + dd : (m == 1 ? head : (m == 3 ? 0 : dd));
+            const bool per_col = m == 2 || m == 4;
+            const long rowoff = (long)b * args.gate_cols;
+            const long gsz = (long)args.B * args.gate_cols;
+            for (int s2 = 0; s2 < args.gate_splits; ++s2) {
+                gl0 += args.gate_part[s2 * gsz + rowoff + c0];
+                if (per_col) gl1 += args.gate_part[s2 * gsz + rowoff + c0 + 1];
             }
+            if (!per_col) gl1 = gl0;
         }
-        if (args.gate_mode == 1) gl1 = gl0;
-        g0 = 1.0f / (1.0f + ex2_approx(-gl0 * kLog2e));
-        g1 = 1.0f / (1.0f + ex2_approx(-gl1 * kLog2e));
+        const bool add = gate_adds(fn);
+        y0 = gate_combine(y0, gate_value(gl0, fn), add);
+        y1 = gate_combine(y1, gate_value(gl1, fn), add);
+    } else if (fn == 5) {   // SiLU of the output
+        y0 *= sigmoid_tanh(y0);
+        y1 *= sigmoid_tanh(y1);
+    } else if (fn == 6) {
+        // per-head RMSNorm: the head's 128 columns live in 64 threads (two warps)
+        float ss = fmaf(y0, y0, y1 * y1);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+        float* red = reinterpret_cast<float*>(smem);   // (the merge above has read its arrays)
+        __syncthreads();
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        const float tot = red[(tid >> 6) * 2] + red[(tid >> 6) * 2 + 1];
+        const float rr = rsqrtf(tot / HD + args.eps);
+        const float ga0 = args.theta ? __bfloat162float(args.theta[(long)head * HD + dd]) : 1.f;
+        const float ga1 = args.theta ? __bfloat162float(args.theta[(long)head * HD + dd + 1]) : 1.f;
+        y0 *= rr * ga0;
+        y1 *= rr * ga1;
     }
-    __nv_bfloat162 outv = __floats2bfloat162_rn(r0 * inv * g0, r1 * inv * g1);
+    __nv_bfloat162 outv = __floats2bfloat162_rn(y0, y1);
     *reinterpret_cast<__nv_bfloat162*>(args.O + ((long)b * args.Hq + head) * HD + dd) = outv;
     if (args.sink && dd == 0) {
         const float x0 = __ldcg(&args.part_x0[(long)b * args.Hq + head]);
@@ -420,10 +450,13 @@ cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* w
     a.Q = static_cast<const __nv_bfloat16*>(p.Q);
     a.O = static_cast<__nv_bfloat16*>(p.O);
     a.sink = p.sink;
-    a.gate_part = p.gate_mode ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
+    a.gate_part = w.gate_splits ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.gate_mode = p.gate_mode;
     a.gate_cols = w.gate_cols;
+    a.theta = (p.gate_mode == 5 || p.gate_fn == 6) ? static_cast<const __nv_bfloat16*>(p.Wg) : nullptr;
+    a.gate_fn = p.gate_fn;
+    a.eps = p.eps;
     a.part_ml = reinterpret_cast<float*>(ws + w.dec_ml);
     a.part_o = reinterpret_cast<float*>(ws + w.dec_o);
     a.part_x0 = reinterpret_cast<float*>(ws + w.dec_x0);

@@ -20,6 +20,11 @@
 // swizzle) into a TMEM fp32 accumulator, warps 2..5 read it back and store.
 // Rows past the end of X and columns past the end of W_g load as zeros (TMA
 // out-of-bounds fill) and are not stored.
+//
+// The head-shared headwise gate (W_g [d_model, 1], one logit per row for
+// every head) is a matrix-vector product whose single column cannot be a
+// tensor-map operand (its rows are 2 bytes apart): gate_rowdot_kernel, one
+// warp per row, 16-byte loads of X and W_g.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -206,6 +211,39 @@ gate_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
 }
 
+// out[r] = sum_m X[r, m] w[m] (fp32), one warp per row; d_model a multiple of 8.
+// Runs first in the call, like the gate GEMM (zeroes the attention kernel's
+// per-call state, then lets it start).
+__global__ void __launch_bounds__(256) gate_rowdot_kernel(const __nv_bfloat16* __restrict__ X,
+                                                          const __nv_bfloat16* __restrict__ w, float* __restrict__ out,
+                                                          int rows, int d_model, ZeroJob zero) {
+    pdl_wait();
+    if (blockIdx.x == 0 && zero.n > 0) {
+        for (int k = threadIdx.x; k < zero.n; k += blockDim.x) zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
+    pdl_trigger();
+    const long r = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const __nv_bfloat16* x = X + r * d_model;
+    float acc = 0.f;
+    for (int m = lane * 8; m < d_model; m += 32 * 8) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + m);
+        const uint4 wv = *reinterpret_cast<const uint4*>(w + m);
+        const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc = fmaf(__uint_as_float(xa[q] << 16), __uint_as_float(wa[q] << 16), acc);
+            acc = fmaf(__uint_as_float(xa[q] & 0xffff0000u), __uint_as_float(wa[q] & 0xffff0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (lane == 0) out[r] = acc;
+}
+
 bool make_map2d(CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t stride1_bytes,
                 cuuint32_t b0, cuuint32_t b1) {
     cuuint64_t d[2] = {d0, d1};
@@ -261,6 +299,12 @@ cudaError_t launch_gate_logits_bf16(const Problem& p, const WorkspacePlan& w, ch
     *launched = false;
     if (w.gate_splits == 0) return cudaSuccess;
     *launched = true;
+    if (p.gate_mode == 3) {   // head-shared headwise: one split of [rows, 1]
+        const unsigned blocks = (unsigned)((w.gate_rows + 7) / 8);
+        return launch_dependent(gate_rowdot_kernel, dim3(blocks), dim3(256), 0, s,
+                                static_cast<const __nv_bfloat16*>(p.X), static_cast<const __nv_bfloat16*>(p.Wg),
+                                reinterpret_cast<float*>(ws + w.gate_part), w.gate_rows, p.d_model, zero);
+    }
     if (gate_col_tile(w.gate_cols) == 128) return launch_gate_t<128>(p, w, ws, rt, s, zero);
     return launch_gate_t<64>(p, w, ws, rt, s, zero);
 }

@@ -1,6 +1,12 @@
 // gate_sigmoid_sm103.cu -- the elementwise gate sigma(X W_g) for the bf16
 // prefill path, as fp16, on pairs of SMs.
 //
+// Also the gate's other functions of the logit (NS-sigmoid, SiLU, identity:
+// the FN template parameter, gsdpa_gate_fn's codes 0..4), the head-shared
+// elementwise gate (W_g [d_model, d_k]: the same kernel with d_k columns) and
+// the input-independent gate (gate_static_kernel: the value of theta [H_q, d_k]
+// with no product).
+//
 // Computes gate[r, c] = fp16( sigma( sum_m X[r, m] W_g[m, c] ) ) for every row
 // r of X viewed as [rows = B*L_q, d_model] and every column c of W_g
 // [d_model, cols = H_q*d_k] ("GatedAttention [2025]", sec. 1.2.2: the gate
@@ -39,6 +45,7 @@
 #include "gsdpa_internal.h"
 #include "sm103_pair.cuh"
 #include "sm103_ptx.cuh"
+#include "gate_fn.cuh"
 
 #include <cuda_fp16.h>
 
@@ -75,6 +82,15 @@ __device__ __forceinline__ uint32_t sigmoid2_h(float x0, float x1) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// The gate's value of two logits as fp16 for gate function FN (0..4).
+template <int FN>
+__device__ __forceinline__ uint32_t gate_value2_h(float x0, float x1) {
+    if (FN == 0 || FN == 2) return sigmoid2_h(x0, x1);
+    const __half2 r = __floats2half2_rn(gate_value(x0, FN), gate_value(x1, FN));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+template <int FN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmG, const SigArgs args) {
@@ -221,7 +237,7 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 uint32_t hv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    hv[e] = sigmoid2_h(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                    hv[e] = gate_value2_h<FN>(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
                 }
                 uint8_t* blk = smem + (tc >> 6) * 16384;
                 const uint32_t chunk0 = (uint32_t)(tc & 63) >> 3;   // 16-byte chunk of the 128-byte row
@@ -249,6 +265,24 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
 }
 
+// The input-independent gate: out[k] = fp16(value(theta[k])) for the H_q * d_k
+// parameters ("GatedAttention [2025]", sec. 1.4.2 (iii): a free q x d_k
+// parameter, then the gate function, multiplied with the SDPA output). Runs
+// first in the call, like the gate GEMM: it zeroes the attention kernel's
+// per-call state and lets it start.
+__global__ void __launch_bounds__(256) gate_static_kernel(const __nv_bfloat16* __restrict__ theta,
+                                                          __half* __restrict__ out, int n, int fn, ZeroJob zero) {
+    pdl_wait();
+    if (blockIdx.x == 0 && zero.n > 0) {
+        for (int k = threadIdx.x; k < zero.n; k += blockDim.x) zero.p[k] = 0;
+        __threadfence();
+        __syncthreads();
+    }
+    pdl_trigger();
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += gridDim.x * blockDim.x)
+        out[k] = __float2half_rn(gate_value(__bfloat162float(theta[k]), fn));
+}
+
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d, const cuuint64_t* st,
               const cuuint32_t* box) {
     cuuint32_t es[3] = {1, 1, 1};
@@ -259,10 +293,12 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d, c
 
 }  // namespace
 
-cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
-                                     cudaStream_t s, ZeroJob zero) {
+namespace {
+template <int FN>
+cudaError_t launch_gate_value_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                cudaStream_t s, ZeroJob zero) {
     alignas(64) CUtensorMap tmX, tmW, tmG;
-    const int rows = p.B * p.Lq, cols = p.Hq * p.dk;
+    const int rows = p.B * p.Lq, cols = gate_cols(p);
     if (rows == 0) return cudaSuccess;
     {
         const cuuint64_t d[2] = {(cuuint64_t)p.d_model, (cuuint64_t)rows};
@@ -298,16 +334,33 @@ cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, c
     a.zero = zero;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    static bool attr_done = false;
+    static bool attr_done = false;   // per template instance
     if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel<FN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (r != cudaSuccess) return r;
         attr_done = true;
     }
     const long tiles = (long)a.row_tiles * ((cols + 511) / 512);
-    return launch_dependent(gate_sigmoid_kernel, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX, tmW,
-                            tmG, a);
+    return launch_dependent(gate_sigmoid_kernel<FN>, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX,
+                            tmW, tmG, a);
+}
+}  // namespace
+
+cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                     cudaStream_t s, ZeroJob zero) {
+    if (p.gate_mode == 5) {
+        const int n = p.Hq * p.dk;
+        return launch_dependent(gate_static_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                                static_cast<const __nv_bfloat16*>(p.Wg), reinterpret_cast<__half*>(ws + w.gate_sig),
+                                n, p.gate_fn, zero);
+    }
+    switch (p.gate_fn) {
+    case 1: return launch_gate_value_t<1>(p, w, ws, rt, s, zero);
+    case 3: return launch_gate_value_t<3>(p, w, ws, rt, s, zero);
+    case 4: return launch_gate_value_t<4>(p, w, ws, rt, s, zero);
+    default: return launch_gate_value_t<0>(p, w, ws, rt, s, zero);   // sigmoid (multiplied or added)
+    }
 }
 
 }  // namespace gsdpa

@@ -61,13 +61,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int validate_shape(const Problem& p) {
     if (p.B < 0 || p.Lq < 0 || p.Lk < 1 || p.Lq > p.Lk) return GSDPA_ERR_INVALID_ARG;
     if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv != 0) return GSDPA_ERR_INVALID_ARG;
-    if (p.gate_mode < 0 || p.gate_mode > 2) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_mode < GSDPA_GATE_NONE || p.gate_mode > GSDPA_GATE_STATIC) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_fn < GSDPA_FN_SIGMOID_MUL || p.gate_fn > GSDPA_FN_RMSNORM) return GSDPA_ERR_INVALID_ARG;
+    // the functions of the output alone take no gate; a gate takes one of the five functions of its logit
+    if (p.gate_mode == GSDPA_GATE_NONE && p.gate_fn != GSDPA_FN_SIGMOID_MUL && p.gate_fn < GSDPA_FN_SILU_SELF)
+        return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_mode != GSDPA_GATE_NONE && p.gate_fn >= GSDPA_FN_SILU_SELF) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_fn == GSDPA_FN_RMSNORM && !(p.eps >= 0.f)) return GSDPA_ERR_INVALID_ARG;
     if (p.dtype != GSDPA_F32 && p.dtype != GSDPA_BF16) return GSDPA_ERR_INVALID_ARG;
-    if (p.gate_mode != GSDPA_GATE_NONE && p.d_model < 1) return GSDPA_ERR_INVALID_ARG;
+    if (gate_cols(p) > 0 && p.d_model < 1) return GSDPA_ERR_INVALID_ARG;
     if (p.dk != 64 && p.dk != 128) return GSDPA_ERR_UNSUPPORTED;
     if (p.dtype == GSDPA_BF16) {
         // TMA needs every row stride to be a multiple of 16 bytes.
-        if (p.gate_mode != GSDPA_GATE_NONE && p.d_model % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
+        if (gate_cols(p) > 0 && p.d_model % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
         if (p.gate_mode == GSDPA_GATE_HEADWISE && p.Hq % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
     }
     const long long units = (long long)((p.Lq + 127) / 128) * p.Hq * p.B;
@@ -104,20 +110,23 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
         w.sink_part = off;
         off = align256(off + sizeof(float) * (size_t)p.B * p.Hq * w.sink_tiles);
     }
-    // Gate logits computed ahead of the attention kernel: bf16 headwise
-    // prefill and bf16 decode (elementwise prefill keeps the gate in-CTA).
-    const bool gate_prepass = bf16 && p.gate_mode != GSDPA_GATE_NONE &&
-                              (decode || p.gate_mode == GSDPA_GATE_HEADWISE);
+    // Gate logits computed ahead of the attention kernel: bf16 headwise (and
+    // head-shared headwise) prefill and every bf16 decode gate that reads X
+    // (the elementwise prefill gates are computed ahead as values, below).
+    const bool gate_prepass = bf16 && gate_cols(p) > 0 && (decode || gate_headwise_family(p));
     if (gate_prepass) {
         w.gate_rows = p.B * p.Lq;
         w.gate_cols = gate_cols(p);
-        const int nt = gate_col_tile(w.gate_cols);
-        const int tiles = ((w.gate_rows + 127) / 128) * ((w.gate_cols + nt - 1) / nt);
-        const int nkc = (p.d_model + 63) / 64;
-        int splits = (num_sms + tiles - 1) / tiles;
-        int max_splits = nkc / 4 > 0 ? nkc / 4 : 1;
-        if (splits > max_splits) splits = max_splits;
-        if (splits < 1) splits = 1;
+        int splits = 1;   // head-shared headwise: one row-dot kernel, no split
+        if (p.gate_mode != GSDPA_GATE_HEADWISE_SHARED) {
+            const int nt = gate_col_tile(w.gate_cols);
+            const int tiles = ((w.gate_rows + 127) / 128) * ((w.gate_cols + nt - 1) / nt);
+            const int nkc = (p.d_model + 63) / 64;
+            splits = (num_sms + tiles - 1) / tiles;
+            int max_splits = nkc / 4 > 0 ? nkc / 4 : 1;
+            if (splits > max_splits) splits = max_splits;
+            if (splits < 1) splits = 1;
+        }
         w.gate_splits = splits;
         w.gate_part = off;
         off = align256(off + sizeof(float) * (size_t)splits * w.gate_rows * w.gate_cols);
@@ -131,12 +140,16 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms) {
         w.state_ints = 2 + (p.sink ? 2 * p.B * p.Hq : 0);
         off = align256(off + sizeof(int) * (size_t)w.state_ints);
     }
-    // Elementwise bf16 prefill: the gate sigma(X W_g) computed ahead of the
-    // attention kernel, whose epilogue multiplies by it.
-    if (bf16 && !decode && p.gate_mode == GSDPA_GATE_ELEMENTWISE) {
+    // Elementwise bf16 prefill (and its head-shared and input-independent
+    // forms): the gate's values computed ahead of the attention kernel, whose
+    // epilogue applies them -- [B*L_q, gate columns], or [H_q * d_k] for the
+    // input-independent gate.
+    if (bf16 && !decode && gate_elementwise_family(p)) {
         w.has_gate_sig = true;
         w.gate_sig = off;
-        off = align256(off + 2 * (size_t)p.B * p.Lq * p.Hq * p.dk);
+        const size_t n = p.gate_mode == GSDPA_GATE_STATIC ? (size_t)p.Hq * p.dk
+                                                          : (size_t)p.B * p.Lq * gate_cols(p);
+        off = align256(off + 2 * n);
     }
     if (decode) {
         const int chunks = (p.Hq / p.Hkv) / 4;
@@ -232,7 +245,7 @@ size_t gsdpa_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, int 
     p.gate_mode = gate_mode;
     p.dtype = dtype;
     p.sink = want_sink ? reinterpret_cast<float*>(16) : nullptr;
-    if (validate_shape(p) != GSDPA_OK) return (size_t)-1;
+    if (gate_mode > GSDPA_GATE_ELEMENTWISE || validate_shape(p) != GSDPA_OK) return (size_t)-1;
     if (B == 0 || L_q == 0) return 0;
     return plan_workspace(p, kPlanSms).total;
 }
@@ -314,8 +327,10 @@ int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, c
 namespace {
 int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
              float* lse, int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
-             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+             int dtype, void* workspace, size_t workspace_bytes, void* stream, int gate_fn = 0, float eps = 0.f) {
     Problem p{};
+    p.gate_fn = gate_fn;
+    p.eps = eps;
     p.lse = lse;
     p.X = X;
     p.Q = Q;
@@ -338,9 +353,11 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
     if (st != GSDPA_OK) return st;
     if (B == 0 || L_q == 0) return GSDPA_OK;
     if (!Q || !K || !V || !O) return GSDPA_ERR_INVALID_ARG;
-    if (gate_mode != GSDPA_GATE_NONE && (!X || !W_g)) return GSDPA_ERR_INVALID_ARG;
+    const bool reads_x = gate_cols(p) > 0;
+    if (reads_x && !X) return GSDPA_ERR_INVALID_ARG;
+    if (gate_mode != GSDPA_GATE_NONE && !W_g) return GSDPA_ERR_INVALID_ARG;   // (RMSNorm: gamma may be NULL)
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return GSDPA_ERR_ALIGNMENT;
-    if (gate_mode != GSDPA_GATE_NONE && (!aligned16(X) || !aligned16(W_g))) return GSDPA_ERR_ALIGNMENT;
+    if ((reads_x && !aligned16(X)) || (W_g && !aligned16(W_g))) return GSDPA_ERR_ALIGNMENT;
     if (sink && (reinterpret_cast<uintptr_t>(sink) & 3u)) return GSDPA_ERR_ALIGNMENT;
     if (sink && dtype == GSDPA_BF16 && !decode_supported(p) && (long)L_q > kSinkMaxLq) return GSDPA_ERR_UNSUPPORTED;
 
@@ -407,8 +424,37 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
 int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
                    int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
                    int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    // (the other gate shapes go through gated_sdpa_fwd_variant)
+    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
     return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
                     workspace, workspace_bytes, stream);
+}
+
+size_t gsdpa_workspace_bytes_variant(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                                     int gate_mode, int gate_fn, int want_sink, int dtype) {
+    Problem p{};
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.gate_fn = gate_fn;
+    p.dtype = dtype;
+    p.sink = want_sink ? reinterpret_cast<float*>(16) : nullptr;
+    if (validate_shape(p) != GSDPA_OK) return (size_t)-1;
+    if (B == 0 || L_q == 0) return 0;
+    return plan_workspace(p, kPlanSms).total;
+}
+
+int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,
+                           float* sink, int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                           int gate_mode, int gate_fn, float eps, int causal, int dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
+                    workspace, workspace_bytes, stream, gate_fn, eps);
 }
 
 int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,
@@ -418,6 +464,7 @@ int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void
     if (!lse) return GSDPA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(lse) & 3u) return GSDPA_ERR_ALIGNMENT;
     if (dtype != GSDPA_BF16 || L_q == 1) return GSDPA_ERR_UNSUPPORTED;   // the bf16 prefill kernels write it
+    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
     return fwd_impl(X, Q, K, V, W_g, O, sink, lse, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
                     workspace, workspace_bytes, stream);
 }

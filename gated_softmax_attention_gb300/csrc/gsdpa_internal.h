@@ -18,9 +18,11 @@ struct Problem {
     float* sink;
     float* lse;      // [B, Hq, Lq] natural-log softmax denominators, or null
     int B, Lq, Lk, d_model, Hq, Hkv, dk;
-    int gate_mode;   // 0 none, 1 headwise, 2 elementwise
+    int gate_mode;   // 0 none, 1 headwise, 2 elementwise, 3 headwise shared, 4 elementwise shared, 5 static
     int causal;
     int dtype;       // 0 f32, 1 bf16
+    int gate_fn = 0; // gsdpa_gate_fn
+    float eps = 0.f; // RMSNorm
 };
 
 struct Runtime {
@@ -54,9 +56,53 @@ struct WorkspacePlan {
 };
 
 WorkspacePlan plan_workspace(const Problem& p, int num_sms);
-// columns of W_g: H_q * d_k (elementwise), H_q (headwise), 0 (no gate)
+// columns of W_g: H_q * d_k (elementwise), H_q (headwise), 1 (headwise
+// shared), d_k (elementwise shared), 0 (no gate; the static gate's theta
+// [H_q, d_k] is not multiplied by X)
 inline int gate_cols(const Problem& p) {
-    return p.gate_mode == 2 ? p.Hq * p.dk : (p.gate_mode == 1 ? p.Hq : 0);
+    switch (p.gate_mode) {
+    case 1: return p.Hq;
+    case 2: return p.Hq * p.dk;
+    case 3: return 1;
+    case 4: return p.dk;
+    default: return 0;
+    }
+}
+// Gate families of the bf16 kernels: one value per (row, head) from logits
+// summed in the attention epilogue (headwise, headwise shared), or one value
+// per (row, head, column) computed ahead as fp16 (elementwise, elementwise
+// shared, static).
+inline bool gate_headwise_family(const Problem& p) { return p.gate_mode == 1 || p.gate_mode == 3; }
+inline bool gate_elementwise_family(const Problem& p) { return p.gate_mode == 2 || p.gate_mode == 4 || p.gate_mode == 5; }
+// The attention kernels' view of the gate: the GATE template parameter
+// (0 none, 1 headwise family, 2 elementwise family, 3 a function of the output
+// alone: SiLU or per-head RMSNorm) and the runtime fields.
+struct GateEpi {
+    int fn = 0;            // gsdpa_gate_fn
+    int g_rs = 0, g_hs = 0;   // elementwise family: value at row * g_rs + h * g_hs + c
+    int l_cols = 0, l_hs = 0; // headwise family: logit partials at (split * rows + row) * l_cols + h * l_hs
+    const void* gamma = nullptr;   // RMSNorm scale [H_q, d_k] (bf16) or null
+    float eps = 0.f;
+};
+inline int gate_template(const Problem& p) {
+    if (gate_headwise_family(p)) return 1;
+    if (gate_elementwise_family(p)) return 2;
+    return p.gate_fn >= 5 ? 3 : 0;
+}
+inline GateEpi gate_epi(const Problem& p) {
+    GateEpi g;
+    g.fn = p.gate_fn;
+    switch (p.gate_mode) {
+    case 2: g.g_rs = p.Hq * p.dk; g.g_hs = p.dk; break;
+    case 4: g.g_rs = p.dk; g.g_hs = 0; break;
+    case 5: g.g_rs = 0; g.g_hs = p.dk; break;
+    case 1: g.l_cols = p.Hq; g.l_hs = 1; break;
+    case 3: g.l_cols = 1; g.l_hs = 0; break;
+    default: break;
+    }
+    if (p.gate_fn == 6) g.gamma = p.Wg;
+    g.eps = p.eps;
+    return g;
 }
 
 // The dedicated decode kernel covers bf16, L_q == 1, d_k == 128 and query

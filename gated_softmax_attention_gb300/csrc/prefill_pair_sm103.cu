@@ -66,6 +66,7 @@
 #include "gsdpa_internal.h"
 #include "sm103_pair.cuh"
 #include "sm103_ptx.cuh"
+#include "gate_fn.cuh"
 
 #include <cmath>
 #include <cuda_fp16.h>
@@ -97,16 +98,19 @@ struct PairCfg {
     static constexpr int NBAR = 2 * NS + 11;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     // misc: TMEM address, abort flag, (unused), unit ring [4]; then the
-    // row statistics (m, l) of both warpgroups [2][128] for the merge
+    // row statistics (m, l) of both warpgroups [2][128] for the merge, and
+    // their partial sums of squares [2][128] (per-head RMSNorm)
     static constexpr uint32_t OFF_STATS = OFF_MISC + 64;
-    static constexpr uint32_t SMEM_BYTES = OFF_STATS + 2 * 128 * 8 + 1024;  // + alignment slack
+    static constexpr uint32_t OFF_SQ = OFF_STATS + 2 * 128 * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_SQ + 2 * 128 * 4 + 1024;  // + alignment slack
 };
 
 struct PairArgs {
     int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_blk;
-    const float* gate_part;  // headwise: [splits, B*Lq, Hq]
+    const float* gate_part;  // headwise family: logit partials [splits, B*Lq, ge.l_cols]
     int gate_splits;
-    const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*d_k]
+    const __half* gate_sig;  // elementwise family: the gate's values (row stride ge.g_rs, head stride ge.g_hs)
+    GateEpi ge;              // gate function and the gate's layout
     int* sched_counter;      // next unit to claim (0 at launch)
     unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
     float* sink;                    // [B, Hq] out
@@ -118,13 +122,6 @@ struct PairArgs {
     WaitCtl ctl;
 };
 
-// sigma(x) = 1/2 + tanh(x/2)/2: one MUFU operation (tanh.approx, relative
-// error about 2^-11, i.e. at most ~2.5e-4 absolute on the gate value).
-__device__ __forceinline__ float sigmoid_fast(float x) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-    return fmaf(0.5f, t, 0.5f);
-}
 
 template <int GATE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -151,6 +148,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     volatile int* abort_flag = abort_word;
     volatile int* sched = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);  // [4]
     float2* stats = reinterpret_cast<float2*>(smem + C::OFF_STATS);                   // [2][128]
+    float* sq = reinterpret_cast<float*>(smem + C::OFF_SQ);                           // [2][128]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -492,11 +490,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // elementwise gate: this row's 64 values of sigma(X W_g) for this warpgroup's
         // output columns, loaded before the last MMAs complete (hides the L2 latency)
         uint4 gq[GATE == 2 ? 8 : 1];
-        if (GATE != 0 && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
+        if ((GATE == 1 || GATE == 2) && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
         if (GATE == 2) {
             if (U.mine && i < args.Lq) {
                 const uint4* gsrc = reinterpret_cast<const uint4*>(
-                    args.gate_sig + (((long)b * args.Lq + i) * args.Hq + h) * kHD + p * 64);
+                    args.gate_sig + ((long)b * args.Lq + i) * args.ge.g_rs + (long)h * args.ge.g_hs + p * 64);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) gq[q] = __ldg(gsrc + q);
             } else {
@@ -537,15 +535,44 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     sink_old = atomicAdd(args.sink_word + (long)b * args.Hq + h, sink_add);
                 }
             }
+            const int fn = args.ge.fn;
+            const bool add = gate_adds(fn);
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
                 if (U.mine && i < args.Lq) {
                     const long rows = (long)args.B * args.Lq;
-                    const long idx = ((long)b * args.Lq + i) * args.Hq + h;
-                    for (int sg = 0; sg < args.gate_splits; ++sg) gl += args.gate_part[sg * rows * args.Hq + idx];
+                    const long idx = ((long)b * args.Lq + i) * args.ge.l_cols + (long)h * args.ge.l_hs;
+                    for (int sg = 0; sg < args.gate_splits; ++sg)
+                        gl += args.gate_part[sg * rows * args.ge.l_cols + idx];
                 }
-                g_head = sigmoid_fast(gl);
+                g_head = gate_value(gl, fn);
+            }
+            // per-head RMSNorm (no gate): this warpgroup's 64 columns' sum of squares,
+            // exchanged with the other warpgroup's through shared memory
+            float rr = 1.0f;
+            const __nv_bfloat16* gamma = nullptr;
+            if (GATE == 3 && fn == 6) {
+                float ss = 0.f;
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    const int col = p * 64 + cb * 16;
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tO0 + col, r0);
+                    if (has1) tmem_ld16(tO1 + col, r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float v = __uint_as_float(r0[e]) * s0;
+                        if (has1) v = fmaf(__uint_as_float(r1[e]), s1, v);
+                        ss = fmaf(v, v, ss);
+                    }
+                }
+                sq[p * 128 + row] = ss;
+                named_bar_sync(1, 256);
+                rr = rsqrtf((ss + sq[(p ^ 1) * 128 + row]) / kHD + args.ge.eps);
+                gamma = static_cast<const __nv_bfloat16*>(args.ge.gamma);
+                if (gamma) gamma += (long)h * kHD + p * 64;
             }
             const bool store = U.mine && i < args.Lq;
             uint4* dst = reinterpret_cast<uint4*>(args.O + (((long)b * args.Lq + i) * args.Hq + h) * kHD + p * 64);
@@ -555,6 +582,18 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 uint32_t r0[16], r1[16];
                 tmem_ld16(tO0 + col, r0);
                 if (has1) tmem_ld16(tO1 + col, r1);
+                uint32_t gmw[8];   // RMSNorm scale of these 16 columns (bf16 pairs)
+                if (GATE == 3 && fn == 6) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const uint4 w4 = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + cb * 16) + q)
+                                               : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+                        gmw[4 * q] = w4.x;
+                        gmw[4 * q + 1] = w4.y;
+                        gmw[4 * q + 2] = w4.z;
+                        gmw[4 * q + 3] = w4.w;
+                    }
+                }
                 tmem_wait_ld();
                 uint32_t packed[8];
 #pragma unroll
@@ -569,11 +608,17 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         // columns cb*16 + e, + 1 of this half: half2 number (e/2) % 4 of uint4 cb*2 + e/8
                         const uint32_t hw = (&gq[cb * 2 + (e >> 3)].x)[(e >> 1) & 3];
                         const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
-                        v0 *= g2.x;
-                        v1 *= g2.y;
+                        v0 = gate_combine(v0, g2.x, add);
+                        v1 = gate_combine(v1, g2.y, add);
                     } else if (GATE == 1) {
-                        v0 *= g_head;
-                        v1 *= g_head;
+                        v0 = gate_combine(v0, g_head, add);
+                        v1 = gate_combine(v1, g_head, add);
+                    } else if (GATE == 3 && fn == 5) {   // SiLU of the output
+                        v0 *= sigmoid_tanh(v0);
+                        v1 *= sigmoid_tanh(v1);
+                    } else if (GATE == 3 && fn == 6) {
+                        v0 *= rr * __uint_as_float(gmw[e >> 1] << 16);
+                        v1 *= rr * __uint_as_float(gmw[e >> 1] & 0xffff0000u);
                     }
                     packed[e / 2] = pack_bf16x2(v0, v1);
                 }
@@ -648,6 +693,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
+    a.ge = gate_epi(p);
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.lse = p.lse;
@@ -691,7 +737,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = GATE != 0 ? 1 : 0;
+    cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE>, tmQ, tmK, tmV, a);
 }
 
@@ -699,9 +745,12 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
 
 cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                      cudaStream_t s) {
-    if (p.gate_mode == 2) return launch_pair_t<2>(p, w, ws, rt, s);
-    if (p.gate_mode == 1) return launch_pair_t<1>(p, w, ws, rt, s);
-    return launch_pair_t<0>(p, w, ws, rt, s);
+    switch (gate_template(p)) {
+    case 1: return launch_pair_t<1>(p, w, ws, rt, s);
+    case 2: return launch_pair_t<2>(p, w, ws, rt, s);
+    case 3: return launch_pair_t<3>(p, w, ws, rt, s);
+    default: return launch_pair_t<0>(p, w, ws, rt, s);
+    }
 }
 
 }  // namespace gsdpa

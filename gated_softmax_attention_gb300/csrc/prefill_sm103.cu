@@ -41,6 +41,7 @@
 // from one unit to the next.
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
+#include "gate_fn.cuh"
 
 #include <cmath>
 #include <cuda_fp16.h>
@@ -83,9 +84,10 @@ struct PrefillCfg {
 
 struct PrefillArgs {
     int B, Lq, Lk, Hq, Hkv, d_model, causal, n_qtiles, n_pairs;
-    const float* gate_part;  // headwise: [splits, B*Lq, Hq]
+    const float* gate_part;  // headwise family: logit partials [splits, B*Lq, ge.l_cols]
     int gate_splits;
-    const __half* gate_sig;  // elementwise: sigma(X W_g) [B*Lq, Hq*HD]
+    const __half* gate_sig;  // elementwise family: the gate's values (row stride ge.g_rs, head stride ge.g_hs)
+    GateEpi ge;              // gate function and the gate's layout
     int* sched_counter;      // next unit to claim (0 at launch)
     unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
     float* sink;                    // [B, Hq] out
@@ -96,13 +98,6 @@ struct PrefillArgs {
     WaitCtl ctl;
 };
 
-// sigma(x) = 1/2 + tanh(x/2)/2: one MUFU operation (tanh.approx, relative
-// error about 2^-11, i.e. at most ~2.5e-4 absolute on the gate value).
-__device__ __forceinline__ float sigmoidf_fast(float x) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-    return fmaf(0.5f, t, 0.5f);
-}
 
 template <int HD, int GATE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -464,11 +459,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         // elementwise gate: this row's d_k values of sigma(X W_g), loaded before the
         // last MMAs complete so that the L2 / HBM latency hides behind the wait
         uint4 gq[GATE == 2 ? HD / 8 : 1];
-        if (GATE != 0 && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
+        if ((GATE == 1 || GATE == 2) && r == 0) pdl_wait();   // the gate kernel has completed (once per thread)
         if (GATE == 2) {
             if (i < args.Lq && my_nkv > 0) {
-                const uint4* gsrc =
-                    reinterpret_cast<const uint4*>(args.gate_sig + (((long)b * args.Lq + i) * args.Hq + h) * HD);
+                const uint4* gsrc = reinterpret_cast<const uint4*>(
+                    args.gate_sig + ((long)b * args.Lq + i) * args.ge.g_rs + (long)h * args.ge.g_hs);
 #pragma unroll
                 for (int q = 0; q < HD / 8; ++q) gq[q] = __ldg(gsrc + q);
             } else {
@@ -498,15 +493,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     sink_old = atomicAdd(args.sink_word + (long)b * args.Hq + h, sink_add);
                 }
             }
+            const int fn = args.ge.fn;
+            const bool add = gate_adds(fn);
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
                 if (i < args.Lq) {
                     const long rows = (long)args.B * args.Lq;
-                    const long idx = ((long)b * args.Lq + i) * args.Hq + h;
-                    for (int s = 0; s < args.gate_splits; ++s) gl += args.gate_part[s * rows * args.Hq + idx];
+                    const long idx = ((long)b * args.Lq + i) * args.ge.l_cols + (long)h * args.ge.l_hs;
+                    for (int s = 0; s < args.gate_splits; ++s)
+                        gl += args.gate_part[s * rows * args.ge.l_cols + idx];
                 }
-                g_head = sigmoidf_fast(gl);
+                g_head = gate_value(gl, fn);
+            }
+            // per-head RMSNorm (no gate): the row's mean square over its d_k columns first
+            float rr = 1.0f;
+            const __nv_bfloat16* gamma = nullptr;
+            if (GATE == 3 && fn == 6) {
+                float ss = 0.f;
+#pragma unroll
+                for (int cb = 0; cb < HD / 32; ++cb) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + cb * 32, orr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = __uint_as_float(orr[e]) * inv_l;
+                        ss = fmaf(v, v, ss);
+                    }
+                }
+                rr = rsqrtf(ss / HD + args.ge.eps);
+                gamma = static_cast<const __nv_bfloat16*>(args.ge.gamma);
+                if (gamma) gamma += (long)h * HD;
             }
             // 32 columns at a time: TMEM -> registers -> bf16 in a staging buffer ->
             // one TMA store of the tile's 128 rows (rows past L_q are clipped by the
@@ -518,6 +536,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             for (int cb = 0; cb < HD / 32; ++cb) {
                 uint32_t orr[32];
                 tmem_ld32(tO + cb * 32, orr);
+                uint32_t gmw[16];   // RMSNorm scale of these 32 columns (bf16 pairs)
+                if (GATE == 3 && fn == 6) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w4 = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + cb * 32) + q)
+                                               : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+                        gmw[4 * q] = w4.x;
+                        gmw[4 * q + 1] = w4.y;
+                        gmw[4 * q + 2] = w4.z;
+                        gmw[4 * q + 3] = w4.w;
+                    }
+                }
                 tmem_wait_ld();
                 uint32_t packed[16];
 #pragma unroll
@@ -528,11 +558,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         // columns cb*32 + e, + 1: half2 number (e/2) % 4 of uint4 cb*4 + e/8
                         const uint32_t hw = (&gq[cb * 4 + (e >> 3)].x)[(e >> 1) & 3];
                         const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
-                        v0 *= g2.x;
-                        v1 *= g2.y;
+                        v0 = gate_combine(v0, g2.x, add);
+                        v1 = gate_combine(v1, g2.y, add);
                     } else if (GATE == 1) {
-                        v0 *= g_head;
-                        v1 *= g_head;
+                        v0 = gate_combine(v0, g_head, add);
+                        v1 = gate_combine(v1, g_head, add);
+                    } else if (GATE == 3 && fn == 5) {   // SiLU of the output
+                        v0 *= sigmoid_tanh(v0);
+                        v1 *= sigmoid_tanh(v1);
+                    } else if (GATE == 3 && fn == 6) {
+                        v0 *= rr * __uint_as_float(gmw[e >> 1] << 16);
+                        v1 *= rr * __uint_as_float(gmw[e >> 1] & 0xffff0000u);
                     }
                     packed[e / 2] = pack_bf16x2(v0, v1);
                 }
@@ -617,6 +653,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_part = (GATE == 1) ? reinterpret_cast<const float*>(ws + w.gate_part) : nullptr;
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
+    a.ge = gate_epi(p);
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.lse = p.lse;
@@ -649,7 +686,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = GATE != 0 ? 1 : 0;
+    cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE>, tmQ, tmK, tmV, tmO, a);
 }
 
@@ -662,13 +699,19 @@ cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* 
         // traffic per SM). Shorter ones keep single-CTA units, whose finer
         // granularity balances causal work better across the SMs.
         if ((long)p.Lk >= kPairMinKeys) return launch_prefill_pair_bf16(p, w, ws, rt, s);
-        if (p.gate_mode == 2) return launch_prefill_t<128, 2>(p, w, ws, rt, s);
-        if (p.gate_mode == 1) return launch_prefill_t<128, 1>(p, w, ws, rt, s);
-        return launch_prefill_t<128, 0>(p, w, ws, rt, s);
+        switch (gate_template(p)) {
+        case 1: return launch_prefill_t<128, 1>(p, w, ws, rt, s);
+        case 2: return launch_prefill_t<128, 2>(p, w, ws, rt, s);
+        case 3: return launch_prefill_t<128, 3>(p, w, ws, rt, s);
+        default: return launch_prefill_t<128, 0>(p, w, ws, rt, s);
+        }
     }
-    if (p.gate_mode == 2) return launch_prefill_t<64, 2>(p, w, ws, rt, s);
-    if (p.gate_mode == 1) return launch_prefill_t<64, 1>(p, w, ws, rt, s);
-    return launch_prefill_t<64, 0>(p, w, ws, rt, s);
+    switch (gate_template(p)) {
+    case 1: return launch_prefill_t<64, 1>(p, w, ws, rt, s);
+    case 2: return launch_prefill_t<64, 2>(p, w, ws, rt, s);
+    case 3: return launch_prefill_t<64, 3>(p, w, ws, rt, s);
+    default: return launch_prefill_t<64, 0>(p, w, ws, rt, s);
+    }
 }
 
 }  // namespace gsdpa

@@ -6,7 +6,10 @@
 //
 // Computes O = softmax(Q K^T / sqrt(d_k) + causal) V (.) sigmoid(X W_g)
 // ("GatedAttention [2025]", sec. 1.2.1 and 1.2.2; "10 . 门控", sec. 3.2)
-// with an online (running max / running sum) softmax over key tiles.
+// with an online (running max / running sum) softmax over key tiles, and the
+// gate variants of gated_sdpa_fwd_variant (shared and input-independent gate
+// shapes, NS-sigmoid, additive gates, SiLU of the output, per-head RMSNorm;
+// sec. 1.2.2 items (3)-(5), 1.4.1, 1.4.2).
 //
 // Block: 32 query rows of one (b, h); 4 threads per row, thread part p owns
 // the head dimensions c = p + 4 t (interleaved so that the 4 threads of a row
@@ -28,7 +31,7 @@ __global__ void __launch_bounds__(kThreads)
 gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, const float* __restrict__ K,
                       const float* __restrict__ V, const float* __restrict__ Wg, float* __restrict__ O,
                       float* __restrict__ sink_part, int B, int Lq, int Lk, int d_model, int Hq, int Hkv,
-                      int gate_mode, int causal) {
+                      int gate_mode, int causal, int gate_fn, float eps) {
     constexpr int DPT = DK / kParts;  // dims per thread
     __shared__ float sK[kKeys][DK];
     __shared__ float sV[kKeys][DK];
@@ -57,31 +60,45 @@ gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, 
         g[t] = 1.f;
     }
 
-    // ---- gate logits: sigma(X W_g) for this row's columns
-    if (gate_mode == 2) {
-        const float* xp = X + ((long)b * Lq + ic) * d_model;
-        const long cols = (long)Hq * DK;
-        float acc[DPT];
+    // ---- the gate's logits for this row's columns (gsdpa_gate_mode): X W_g over
+    // the columns the gate shape gives, or theta for the input-independent gate
+    float gl[DPT];
 #pragma unroll
-        for (int t = 0; t < DPT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < DPT; ++t) gl[t] = 0.f;
+    const float* xp = X ? X + ((long)b * Lq + ic) * d_model : nullptr;
+    if (gate_mode == 2 || gate_mode == 4) {
+        // elementwise (W_g [d_model, H_q*DK], columns h*DK + c) or shared by the heads ([d_model, DK])
+        const long cols = gate_mode == 2 ? (long)Hq * DK : DK;
+        const long c0 = gate_mode == 2 ? (long)h * DK : 0;
         for (int m = 0; m < d_model; ++m) {
             const float xv = xp[m];
-            const float* wrow = Wg + (long)m * cols + (long)h * DK + part;
+            const float* wrow = Wg + (long)m * cols + c0 + part;
 #pragma unroll
-            for (int t = 0; t < DPT; ++t) acc[t] = fmaf(xv, wrow[kParts * t], acc[t]);
+            for (int t = 0; t < DPT; ++t) gl[t] = fmaf(xv, wrow[kParts * t], gl[t]);
         }
-#pragma unroll
-        for (int t = 0; t < DPT; ++t) g[t] = 1.f / (1.f + expf(-acc[t]));
-    } else if (gate_mode == 1) {
-        const float* xp = X + ((long)b * Lq + ic) * d_model;
+    } else if (gate_mode == 1 || gate_mode == 3) {
+        // headwise (W_g [d_model, H_q], column h) or shared by the heads ([d_model, 1])
+        const long cols = gate_mode == 1 ? Hq : 1;
+        const long c0 = gate_mode == 1 ? h : 0;
         float acc = 0.f;
-        for (int m = part; m < d_model; m += kParts) acc = fmaf(xp[m], Wg[(long)m * Hq + h], acc);
+        for (int m = part; m < d_model; m += kParts) acc = fmaf(xp[m], Wg[(long)m * cols + c0], acc);
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        const float gv = 1.f / (1.f + expf(-acc));
 #pragma unroll
-        for (int t = 0; t < DPT; ++t) g[t] = gv;
+        for (int t = 0; t < DPT; ++t) gl[t] = acc;
+    } else if (gate_mode == 5) {
+        // input-independent: theta [H_q, DK]
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) gl[t] = Wg[(long)h * DK + part + kParts * t];
     }
+    // the gate's value: sigma, NS-sigmoid, sigma, SiLU or identity of the logit
+#pragma unroll
+    for (int t = 0; t < DPT; ++t) {
+        const float sg = 1.f / (1.f + expf(-gl[t]));
+        g[t] = gate_fn == 1 ? 0.5f + 0.5f * sg : (gate_fn == 3 ? gl[t] * sg : (gate_fn == 4 ? gl[t] : sg));
+    }
+    const bool gated = gate_mode != 0;
+    const bool add = gate_fn >= 2 && gate_fn <= 4;
 
     // ---- online softmax over keys
     long key_end = Lk;
@@ -131,10 +148,28 @@ gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, 
     }
 
     const float inv_l = 1.f / l_run;
+    float y[DPT];
+#pragma unroll
+    for (int t = 0; t < DPT; ++t) {
+        y[t] = o[t] * inv_l;
+        if (gated) y[t] = add ? y[t] + g[t] : y[t] * g[t];
+        else if (gate_fn == 5) y[t] = y[t] / (1.f + expf(-y[t]));   // SiLU of the output
+    }
+    if (gate_fn == 6) {
+        // per-head RMSNorm: the row's mean square over its DK columns (4 threads), gamma or 1
+        float ss = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) ss = fmaf(y[t], y[t], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        const float rr = 1.f / sqrtf(ss / DK + eps);
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) y[t] *= rr * (Wg ? Wg[(long)h * DK + part + kParts * t] : 1.f);
+    }
     if (row_valid) {
         float* op = O + (((long)b * Lq + i) * Hq + h) * DK;
 #pragma unroll
-        for (int t = 0; t < DPT; ++t) op[part + kParts * t] = o[t] * inv_l * g[t];
+        for (int t = 0; t < DPT; ++t) op[part + kParts * t] = y[t];
     }
     if (sink_part) {
         if (part == 0) sRed[r] = row_valid ? expf(s0 - m_run) * inv_l : 0.f;
@@ -158,11 +193,13 @@ cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, 
     if (p.dk == 64) {
         gated_attn_f32_kernel<64><<<grid, kThreads, 0, s>>>(
             X, static_cast<const float*>(p.Q), static_cast<const float*>(p.K), static_cast<const float*>(p.V), Wg,
-            static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal);
+            static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal,
+            p.gate_fn, p.eps);
     } else {
         gated_attn_f32_kernel<128><<<grid, kThreads, 0, s>>>(
             X, static_cast<const float*>(p.Q), static_cast<const float*>(p.K), static_cast<const float*>(p.V), Wg,
-            static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal);
+            static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal,
+            p.gate_fn, p.eps);
     }
     return cudaGetLastError();
 }

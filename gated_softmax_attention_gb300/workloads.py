@@ -13,6 +13,14 @@ Recipe (the same on every machine):
   * bf16 workloads round each tensor once to bf16 (round to nearest even);
     the GPU path and the oracle both see exactly those values.
 
+Gate variants (``variant_weight``): a second generator seeded with
+``seed + 7919`` draws the variant's parameter as float32 standard normals:
+  * head-shared gates, W_g [d_model, 1] or [d_model, d_k], scaled by
+    1/sqrt(d_model) (so the logits X W_g are about N(0, 1));
+  * the input-independent gate, theta [H_q, d_k], unscaled;
+  * the RMSNorm scale, gamma [H_q, d_k] = 1 + 0.1 N(0, 1);
+then rounded once to the workload's dtype, like the other inputs.
+
 Layouts: X [B, L_q, d_model]; Q [B, L_q, H_q, d_k]; K, V [B, L_k, H_kv, d_k];
 W_g [d_model, H_q*d_k] (elementwise, head-major columns) or [d_model, H_q]
 (headwise). The model shapes follow the pages' settings: context 4096 for
@@ -138,3 +146,24 @@ def make_inputs(w: Workload, device="cpu"):
             continue
         out[k] = t.to(td).contiguous().to(device)
     return out
+
+
+def variant_weight(w: Workload, gate: str, gate_fn: str = "sigmoid_mul", device="cpu"):
+    """The parameter a gate variant reads in place of W_g: the head-shared
+    gates' W_g, the input-independent gate's theta, or the RMSNorm scale gamma
+    (None for the gates that use the workload's own W_g, and for a variant
+    without a parameter)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + 7919)
+    f = torch.float32
+    if gate == "headwise_shared":
+        t = torch.randn((w.d_model, 1), generator=g, dtype=f) / w.d_model ** 0.5
+    elif gate == "elementwise_shared":
+        t = torch.randn((w.d_model, w.d_k), generator=g, dtype=f) / w.d_model ** 0.5
+    elif gate == "static":
+        t = torch.randn((w.H_q, w.d_k), generator=g, dtype=f)
+    elif gate == "none" and gate_fn == "rmsnorm":
+        t = 1.0 + 0.1 * torch.randn((w.H_q, w.d_k), generator=g, dtype=f)
+    else:
+        return None
+    return t.to(torch_dtype(w)).contiguous().to(device)

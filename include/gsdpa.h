@@ -73,8 +73,25 @@ extern "C" {
 typedef enum {
     GSDPA_GATE_NONE = 0,         /* plain SDPA, W_g and X may be NULL */
     GSDPA_GATE_HEADWISE = 1,     /* one sigmoid per (token, head)     */
-    GSDPA_GATE_ELEMENTWISE = 2   /* one sigmoid per (token, head, c)  */
+    GSDPA_GATE_ELEMENTWISE = 2,  /* one sigmoid per (token, head, c)  */
+    /* gated_sdpa_fwd_variant only: */
+    GSDPA_GATE_HEADWISE_SHARED = 3,     /* W_g [d_model, 1]: one gate per token, every head */
+    GSDPA_GATE_ELEMENTWISE_SHARED = 4,  /* W_g [d_model, d_k]: one gate per (token, c), every head */
+    GSDPA_GATE_STATIC = 5               /* W_g holds theta [H_q, d_k]: the gate does not read X */
 } gsdpa_gate_mode;
+
+/* How the gate's logit gl acts on the SDPA output y (gated_sdpa_fwd_variant). */
+typedef enum {
+    GSDPA_FN_SIGMOID_MUL = 0,    /* y * sigma(gl)               (gated_sdpa_fwd's gate) */
+    GSDPA_FN_NS_SIGMOID_MUL = 1, /* y * (0.5 + 0.5 sigma(gl))                          */
+    GSDPA_FN_SIGMOID_ADD = 2,    /* y + sigma(gl)                                      */
+    GSDPA_FN_SILU_ADD = 3,       /* y + gl sigma(gl)                                   */
+    GSDPA_FN_IDENTITY_ADD = 4,   /* y + gl                                             */
+    GSDPA_FN_SILU_SELF = 5,      /* y * sigma(y), no gate (gate_mode NONE)             */
+    GSDPA_FN_RMSNORM = 6         /* per head: y / sqrt(mean_c y^2 + eps) * gamma[h, c],
+                                    no gate (gate_mode NONE); W_g holds gamma [H_q, d_k]
+                                    or is NULL for gamma = 1                            */
+} gsdpa_gate_fn;
 
 typedef enum {
     GSDPA_F32 = 0,               /* float32 in/out, float32 arithmetic (SIMT) */
@@ -138,6 +155,33 @@ GSDPA_API int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const 
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The forward with one of the gate variants of "GatedAttention [2025]"
+ * (sec. 1.2.2 items (3)-(5): head-shared gates, additive gating with sigmoid
+ * or SiLU; sec. 1.4.1: SiLU of the output with no parameters, additive gating
+ * without SiLU, per-head RMSNorm before concatenation; sec. 1.4.2: an
+ * input-independent gate, NS-sigmoid). The gate shape is gate_mode, how the
+ * gate acts on the SDPA output y is gate_fn:
+ *   gate_mode HEADWISE, ELEMENTWISE and the two _SHARED shapes: logit
+ *     gl = X W_g for the columns the shape gives; gate_fn one of
+ *     SIGMOID_MUL .. IDENTITY_ADD;
+ *   gate_mode STATIC: gl = theta[h, c] from W_g ([H_q, d_k], same dtype as
+ *     the call); X is not read and may be NULL; gate_fn as above;
+ *   gate_mode NONE: gate_fn SIGMOID_MUL (plain SDPA), SILU_SELF or RMSNORM
+ *     (W_g = gamma [H_q, d_k] or NULL; eps >= 0 is added to the mean square).
+ * Other combinations return GSDPA_ERR_INVALID_ARG. The gate's value is kept
+ * as fp16 between the gate pass and the attention kernel (bf16 path), as for
+ * gated_sdpa_fwd. Workspace: gsdpa_workspace_bytes_variant. All other
+ * arguments, alignment and errors as for gated_sdpa_fwd; gate_fn
+ * SIGMOID_MUL with gate_mode 0..2 is gated_sdpa_fwd.
+ */
+GSDPA_API size_t gsdpa_workspace_bytes_variant(int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                                               int gate_mode, int gate_fn, int want_sink, int dtype);
+GSDPA_API int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                                     void* O, float* sink, int B, int L_q, int L_k, int d_model, int H_q, int H_kv,
+                                     int d_k, int gate_mode, int gate_fn, float eps, int causal, int dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The forward a training step runs: gated_sdpa_fwd, and also, for every
  * batch b, query head h and query row i, the natural log of the softmax
  * denominator, lse[b, h, i] = log sum_j exp(s_j) over the row's visible
@@ -178,8 +222,10 @@ GSDPA_API size_t gsdpa_bwd_workspace_bytes(int B, int L_q, int L_k, int d_model,
  *                     over the query heads of the kv head's group).
  *   dX, dW_g        : out, like X and W_g (gated only; NULL allowed without a gate).
  *   workspace       : gsdpa_bwd_workspace_bytes(...) bytes, 256-byte aligned.
- * Every output is overwritten. bf16 and d_k = 128 only (GSDPA_ERR_UNSUPPORTED
- * otherwise); sm_103 device. Tensors 16-byte aligned, lse 4-byte aligned.
+ * Every output is overwritten. bf16, d_k = 128 and gate_mode NONE, HEADWISE
+ * or ELEMENTWISE with the sigmoid gate only (GSDPA_ERR_UNSUPPORTED otherwise:
+ * the variants of gated_sdpa_fwd_variant have no backward); sm_103 device.
+ * Tensors 16-byte aligned, lse 4-byte aligned.
  * Asynchronous on `stream`; errors as for gated_sdpa_fwd.
  */
 GSDPA_API int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g,

@@ -136,3 +136,45 @@ def test_bwd_workspace_and_validation(lib):
     bad = list(args)
     bad[8] = 24                           # dQ misaligned
     assert lib_.gated_sdpa_bwd(*bad) == gb.ERR_ALIGNMENT
+
+
+def call_variant(**kw):
+    base = dict(X=16, Q=16, K=16, V=16, W_g=16, O=16, sink=None, B=1, L_q=8, L_k=8, d_model=64, H_q=4, H_kv=4,
+                d_k=64, gate_mode=2, gate_fn=0, eps=1e-6, causal=1, dtype=0, workspace=None, workspace_bytes=0,
+                stream=None)
+    base.update(kw)
+    return int(gb.load().gated_sdpa_fwd_variant(*base.values()))
+
+
+def test_variant_validation_before_any_device_work(lib):
+    # a gate with a function of the output alone, or no gate with a function of a logit
+    assert call_variant(gate_mode=2, gate_fn=5) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=1, gate_fn=6) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=0, gate_fn=3) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=6) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_fn=7) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=0, gate_fn=6, eps=-1.0) == gb.ERR_INVALID_ARG
+    # the input-independent gate reads no X; RMSNorm's gamma may be absent; a shared gate reads X
+    assert call_variant(gate_mode=5, X=None, B=0) == gb.OK
+    assert call_variant(gate_mode=0, gate_fn=6, W_g=None, X=None, B=0) == gb.OK
+    assert call_variant(gate_mode=4, X=None) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=5, W_g=None) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=3, W_g=8) == gb.ERR_ALIGNMENT
+    # gated_sdpa_fwd keeps to the three base shapes
+    assert call(gate_mode=4) == gb.ERR_INVALID_ARG
+
+
+def test_variant_workspace_bytes(lib):
+    w = gb.workspace_bytes_variant
+    # the default variant needs what gated_sdpa_fwd needs
+    assert w(2, 300, 300, 256, 8, 2, 128, "elementwise", "sigmoid_mul", True, gb.BF16) == \
+        gb.workspace_bytes(2, 300, 300, 256, 8, 2, 128, "elementwise", True, gb.BF16)
+    # head-shared elementwise: fp16 values [B*L_q, d_k]; input-independent: [H_q * d_k]
+    n_sh = w(2, 300, 300, 256, 8, 2, 128, "elementwise_shared", "silu_add", False, gb.BF16)
+    n_st = w(2, 300, 300, 256, 8, 2, 128, "static", "sigmoid_mul", False, gb.BF16)
+    n_no = w(2, 300, 300, 256, 8, 2, 128, "none", "rmsnorm", False, gb.BF16)
+    assert n_sh >= n_no + 2 * 600 * 128 and n_st >= n_no + 2 * 8 * 128
+    # head-shared headwise: one split of [B*L_q, 1] logits (any H_q: no tensor map over W_g)
+    assert w(2, 300, 300, 256, 6, 2, 128, "headwise_shared", "sigmoid_mul", False, gb.BF16) >= n_no + 4 * 600
+    with pytest.raises(gb.GsdpaError):
+        w(2, 300, 300, 256, 8, 2, 128, "elementwise", "rmsnorm", False, gb.BF16)
