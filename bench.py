@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--decode-workload", default="bf16_decode_gqa_elementwise_Lk8192")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--profile-backward", action="store_true",
                     help="with --profile-workload: the training forward once, then --profile-calls backward calls")
     ap.add_argument("--decode-steps", type=int, default=0, help="0: same as --steps, capped at 200")
@@ -435,6 +436,11 @@ def run_ours(args, d: Dist):
         out["backward"] = run_backward(args, d, torch, gb, w, host, stream, peaks)
         out["gpu_launches"] += out["backward"]["gpu_launches"]
 
+    # ---- gate variants on the headline shape (context beside the metric)
+    if not args.no_variants:
+        out["variants"] = run_variants(args, d, torch, gb, w, host, stream, peaks)
+        out["gpu_launches"] += out["variants"]["gpu_launches"]
+
     # ---- extra workloads (context only), one stderr line each
     for name in [x for x in args.extra.split(",") if x]:
         wx = WORKLOADS[name]
@@ -494,6 +500,61 @@ def run_backward(args, d, torch, gb, w, host, stream, peaks):
                          "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                          "scope": "whole call (gate recompute, prep, dQ, dK/dV, dX and dW_g GEMMs)"},
             "gpu_launches": kernels * K}
+
+
+VARIANTS = [("elementwise", "sigmoid_mul"), ("elementwise", "ns_sigmoid_mul"), ("elementwise", "sigmoid_add"),
+            ("elementwise", "silu_add"), ("elementwise", "identity_add"), ("elementwise_shared", "sigmoid_mul"),
+            ("headwise", "sigmoid_mul"), ("headwise_shared", "sigmoid_mul"), ("static", "sigmoid_mul"),
+            ("none", "sigmoid_mul"), ("none", "silu_self"), ("none", "rmsnorm")]
+
+
+def run_variants(args, d, torch, gb, w, host, stream, peaks):
+    """Every gate variant (gated_sdpa_fwd_variant) on the headline shape: graph
+    replays of R calls over rotating input copies, like the headline step;
+    time per call and algorithmic TFLOP/s (the attention, plus the gate GEMM
+    where the gate reads X), and the ratio to the default gate's call."""
+    from gated_softmax_attention_gb300.workloads import variant_weight
+    dev = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
+    per_set = sum(v.numel() * v.element_size() for v in dev.values() if v is not None)
+    R = n_rotating_sets(per_set)
+    sets = [dev] + [{k: (v.clone() if v is not None else None) for k, v in dev.items()} for _ in range(R - 1)]
+    O = torch.empty_like(dev["Q"])
+    gen = torch.Generator().manual_seed(97)
+    rows = w.B * w.L_q
+    cols = {"elementwise": w.H_q * w.d_k, "headwise": w.H_q, "elementwise_shared": w.d_k, "headwise_shared": 1}
+    K = max(3, min(args.steps, 100))
+    res, launches, base_ms = [], 0, None
+    for gate, fn in VARIANTS:
+        if gate in ("elementwise", "headwise") and gate == w.gate:
+            W = [st["W_g"] for st in sets]
+        elif gate == "headwise":
+            W = [(torch.randn((w.d_model, w.H_q), generator=gen) * 0.02).to(torch.bfloat16).cuda()] * R
+        else:
+            W = [variant_weight(w, gate, fn, device="cuda")] * R
+        need = gb.workspace_bytes_variant(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, gate, fn, False,
+                                          gb.BF16)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        reads_x = gate not in ("none", "static")
+
+        def call(k, gate=gate, fn=fn, W=W, ws=ws, reads_x=reads_x):
+            st = sets[k % R]
+            gb.gated_sdpa_fwd_variant(st["X"] if reads_x else None, st["Q"], st["K"], st["V"], W[k % R], gate=gate,
+                                      gate_fn=fn, causal=w.causal, out=O, workspace=ws)
+
+        graphs = capture_steps(torch, call, R)
+        ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+        st = gb.check_device_error(stream)
+        if st != gb.OK:
+            raise RuntimeError(f"device error in the variants leg ({gate}/{fn}): {gb.status_string(st)}")
+        flops = w.attn_flops() + 2 * rows * w.d_model * cols.get(gate, 0)
+        if base_ms is None:
+            base_ms = ms
+        launches += (2 if gate != "none" else 1) * K
+        res.append({"gate": gate, "gate_fn": fn, "ms_per_call": round(ms, 5),
+                    "tflops": round(flops / (ms / 1e3) / 1e12, 2), "vs_default_call": round(ms / base_ms, 4)})
+        del graphs, ws
+    return {"workload": w.name, "scope": "whole call (gate pass + attention kernel), graph replays, inputs larger "
+                                         "than L2 in total", "steps": K, "results": res, "gpu_launches": launches}
 
 
 def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):

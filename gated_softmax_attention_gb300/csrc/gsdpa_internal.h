@@ -75,8 +75,8 @@ inline int gate_cols(const Problem& p) {
 inline bool gate_headwise_family(const Problem& p) { return p.gate_mode == 1 || p.gate_mode == 3; }
 inline bool gate_elementwise_family(const Problem& p) { return p.gate_mode == 2 || p.gate_mode == 4 || p.gate_mode == 5; }
 // The attention kernels' view of the gate: the GATE template parameter
-// (0 none, 1 headwise family, 2 elementwise family, 3 a function of the output
-// alone: SiLU or per-head RMSNorm) and the runtime fields.
+// (0 none, 1 headwise family, 2 elementwise family, 3 SiLU of the output,
+// 4 per-head RMSNorm) and the runtime fields.
 struct GateEpi {
     int fn = 0;            // gsdpa_gate_fn
     int g_rs = 0, g_hs = 0;   // elementwise family: value at row * g_rs + h * g_hs + c
@@ -87,7 +87,7 @@ struct GateEpi {
 inline int gate_template(const Problem& p) {
     if (gate_headwise_family(p)) return 1;
     if (gate_elementwise_family(p)) return 2;
-    return p.gate_fn >= 5 ? 3 : 0;
+    return p.gate_fn == 5 ? 3 : (p.gate_fn == 6 ? 4 : 0);
 }
 inline GateEpi gate_epi(const Problem& p) {
     GateEpi g;

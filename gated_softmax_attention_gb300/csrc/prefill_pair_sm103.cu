@@ -123,7 +123,7 @@ struct PairArgs {
 };
 
 
-template <int GATE>
+template <int GATE, bool ADD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const PairArgs args) {
@@ -536,7 +536,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
             }
             const int fn = args.ge.fn;
-            const bool add = gate_adds(fn);
+            constexpr bool add = ADD;   // the gate's value is added (else multiplied)
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
@@ -552,9 +552,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // exchanged with the other warpgroup's through shared memory
             float rr = 1.0f;
             const __nv_bfloat16* gamma = nullptr;
-            if (GATE == 3 && fn == 6) {
+            if (GATE == 4) {
                 float ss = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     const int col = p * 64 + cb * 16;
                     uint32_t r0[16], r1[16];
@@ -583,7 +583,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 tmem_ld16(tO0 + col, r0);
                 if (has1) tmem_ld16(tO1 + col, r1);
                 uint32_t gmw[8];   // RMSNorm scale of these 16 columns (bf16 pairs)
-                if (GATE == 3 && fn == 6) {
+                if (GATE == 4) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         const uint4 w4 = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + cb * 16) + q)
@@ -613,10 +613,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     } else if (GATE == 1) {
                         v0 = gate_combine(v0, g_head, add);
                         v1 = gate_combine(v1, g_head, add);
-                    } else if (GATE == 3 && fn == 5) {   // SiLU of the output
+                    } else if (GATE == 3) {   // SiLU of the output
                         v0 *= sigmoid_tanh(v0);
                         v1 *= sigmoid_tanh(v1);
-                    } else if (GATE == 3 && fn == 6) {
+                    } else if (GATE == 4) {
                         v0 *= rr * __uint_as_float(gmw[e >> 1] << 16);
                         v1 *= rr * __uint_as_float(gmw[e >> 1] & 0xffff0000u);
                     }
@@ -658,7 +658,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
     return r == CUDA_SUCCESS;
 }
 
-template <int GATE>
+template <int GATE, bool ADD = false>
 cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
     using C = PairCfg;
     alignas(64) CUtensorMap tmQ, tmK, tmV;
@@ -706,10 +706,10 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
         // The register split above only fits if the launch allocates enough
         // registers per thread; refuse to launch otherwise (it would not finish).
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_pair_kernel<GATE>);
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_pair_kernel<GATE, ADD>);
         if (r != cudaSuccess) return r;
         if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
-        r = cudaFuncSetAttribute(prefill_pair_kernel<GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        r = cudaFuncSetAttribute(prefill_pair_kernel<GATE, ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::SMEM_BYTES);
         if (r != cudaSuccess) return r;
         // A persistent grid must not exceed what is resident at once: pairs
@@ -719,7 +719,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         int n = 0;
-        r = cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<GATE>, &cfg);
+        r = cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<GATE, ADD>, &cfg);
         if (r != cudaSuccess) return r;
         if (n < 1) return cudaErrorInvalidConfiguration;
         max_pairs = n;
@@ -738,17 +738,19 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE>, tmQ, tmK, tmV, a);
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE, ADD>, tmQ, tmK, tmV, a);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                      cudaStream_t s) {
+    const bool add = gate_template(p) != 0 && (p.gate_fn >= 2 && p.gate_fn <= 4);   // additive gates
     switch (gate_template(p)) {
-    case 1: return launch_pair_t<1>(p, w, ws, rt, s);
-    case 2: return launch_pair_t<2>(p, w, ws, rt, s);
+    case 1: return add ? launch_pair_t<1, true>(p, w, ws, rt, s) : launch_pair_t<1>(p, w, ws, rt, s);
+    case 2: return add ? launch_pair_t<2, true>(p, w, ws, rt, s) : launch_pair_t<2>(p, w, ws, rt, s);
     case 3: return launch_pair_t<3>(p, w, ws, rt, s);
+    case 4: return launch_pair_t<4>(p, w, ws, rt, s);
     default: return launch_pair_t<0>(p, w, ws, rt, s);
     }
 }

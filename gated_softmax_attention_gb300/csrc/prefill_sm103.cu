@@ -99,7 +99,7 @@ struct PrefillArgs {
 };
 
 
-template <int HD, int GATE>
+template <int HD, int GATE, bool ADD>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -494,7 +494,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
             }
             const int fn = args.ge.fn;
-            const bool add = gate_adds(fn);
+            constexpr bool add = ADD;   // the gate's value is added (else multiplied)
             float g_head = 1.0f;
             if (GATE == 1) {
                 float gl = 0.f;
@@ -509,9 +509,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // per-head RMSNorm (no gate): the row's mean square over its d_k columns first
             float rr = 1.0f;
             const __nv_bfloat16* gamma = nullptr;
-            if (GATE == 3 && fn == 6) {
+            if (GATE == 4) {
                 float ss = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int cb = 0; cb < HD / 32; ++cb) {
                     uint32_t orr[32];
                     tmem_ld32(tO + cb * 32, orr);
@@ -537,7 +537,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 uint32_t orr[32];
                 tmem_ld32(tO + cb * 32, orr);
                 uint32_t gmw[16];   // RMSNorm scale of these 32 columns (bf16 pairs)
-                if (GATE == 3 && fn == 6) {
+                if (GATE == 4) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint4 w4 = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + cb * 32) + q)
@@ -563,10 +563,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     } else if (GATE == 1) {
                         v0 = gate_combine(v0, g_head, add);
                         v1 = gate_combine(v1, g_head, add);
-                    } else if (GATE == 3 && fn == 5) {   // SiLU of the output
+                    } else if (GATE == 3) {   // SiLU of the output
                         v0 *= sigmoid_tanh(v0);
                         v1 *= sigmoid_tanh(v1);
-                    } else if (GATE == 3 && fn == 6) {
+                    } else if (GATE == 4) {
                         v0 *= rr * __uint_as_float(gmw[e >> 1] << 16);
                         v1 *= rr * __uint_as_float(gmw[e >> 1] & 0xffff0000u);
                     }
@@ -613,7 +613,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
     return r == CUDA_SUCCESS;
 }
 
-template <int HD, int GATE>
+template <int HD, int GATE, bool ADD = false>
 cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
     using C = PrefillCfg<HD, GATE>;
     alignas(64) CUtensorMap tmQ, tmK, tmV, tmO;
@@ -665,10 +665,10 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
         // The register split above only fits if the launch allocates enough
         // registers per thread; refuse to launch otherwise (it would not finish).
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE>);
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE, ADD>);
         if (r != cudaSuccess) return r;
         if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
-        r = cudaFuncSetAttribute(prefill_kernel<HD, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        r = cudaFuncSetAttribute(prefill_kernel<HD, GATE, ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::SMEM_BYTES);
         if (r != cudaSuccess) return r;
         attr_done = true;
@@ -687,29 +687,32 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE>, tmQ, tmK, tmV, tmO, a);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD>, tmQ, tmK, tmV, tmO, a);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s) {
+    const bool add = gate_template(p) != 0 && (p.gate_fn >= 2 && p.gate_fn <= 4);   // additive gates
     if (p.dk == 128) {
         // Long key sequences: CTA pairs (M = 256 MMAs, half the operand
         // traffic per SM). Shorter ones keep single-CTA units, whose finer
         // granularity balances causal work better across the SMs.
         if ((long)p.Lk >= kPairMinKeys) return launch_prefill_pair_bf16(p, w, ws, rt, s);
         switch (gate_template(p)) {
-        case 1: return launch_prefill_t<128, 1>(p, w, ws, rt, s);
-        case 2: return launch_prefill_t<128, 2>(p, w, ws, rt, s);
+        case 1: return add ? launch_prefill_t<128, 1, true>(p, w, ws, rt, s) : launch_prefill_t<128, 1>(p, w, ws, rt, s);
+        case 2: return add ? launch_prefill_t<128, 2, true>(p, w, ws, rt, s) : launch_prefill_t<128, 2>(p, w, ws, rt, s);
         case 3: return launch_prefill_t<128, 3>(p, w, ws, rt, s);
+        case 4: return launch_prefill_t<128, 4>(p, w, ws, rt, s);
         default: return launch_prefill_t<128, 0>(p, w, ws, rt, s);
         }
     }
     switch (gate_template(p)) {
-    case 1: return launch_prefill_t<64, 1>(p, w, ws, rt, s);
-    case 2: return launch_prefill_t<64, 2>(p, w, ws, rt, s);
+    case 1: return add ? launch_prefill_t<64, 1, true>(p, w, ws, rt, s) : launch_prefill_t<64, 1>(p, w, ws, rt, s);
+    case 2: return add ? launch_prefill_t<64, 2, true>(p, w, ws, rt, s) : launch_prefill_t<64, 2>(p, w, ws, rt, s);
     case 3: return launch_prefill_t<64, 3>(p, w, ws, rt, s);
+    case 4: return launch_prefill_t<64, 4>(p, w, ws, rt, s);
     default: return launch_prefill_t<64, 0>(p, w, ws, rt, s);
     }
 }
