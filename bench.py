@@ -553,6 +553,32 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
         res.append({"gate": gate, "gate_fn": fn, "ms_per_call": round(ms, 5),
                     "tflops": round(flops / (ms / 1e3) / 1e12, 2), "vs_default_call": round(ms / base_ms, 4)})
         del graphs, ws
+    # the default gate with its fused statistics (gated_sdpa_fwd_stats: 20 bins, threshold 0.1)
+    import ctypes
+    stats = torch.empty(3 + 20, dtype=torch.int64, device="cuda")
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate, False, gb.BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def call_stats(k):
+        st = sets[k % R]
+        p = lambda t: ctypes.c_void_p(t.data_ptr())
+        rc = gb.load().gated_sdpa_fwd_stats(p(st["X"]), p(st["Q"]), p(st["K"]), p(st["V"]), p(st["W_g"]), p(O), None,
+                                            p(stats), 20, 0.1, w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k,
+                                            gb.GATE_CODES[w.gate], int(w.causal), gb.BF16, p(ws), need,
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if rc != gb.OK:
+            raise gb.GsdpaError(rc, "gated_sdpa_fwd_stats")
+
+    graphs = capture_steps(torch, call_stats, R)
+    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in the variants leg (statistics): {gb.status_string(st)}")
+    flops = w.attn_flops() + 2 * rows * w.d_model * cols.get(w.gate, 0)
+    launches += 2 * K
+    res.append({"gate": w.gate, "gate_fn": "sigmoid_mul + statistics (20 bins)", "ms_per_call": round(ms, 5),
+                "tflops": round(flops / (ms / 1e3) / 1e12, 2), "vs_default_call": round(ms / base_ms, 4)})
+    del graphs, ws
     return {"workload": w.name, "scope": "whole call (gate pass + attention kernel), graph replays, inputs larger "
                                          "than L2 in total", "steps": K, "results": res, "gpu_launches": launches}
 

@@ -28,6 +28,7 @@ SIGNATURES = {
     "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_workspace_bytes_variant": (_SZ, [_I] * 11),
+    "gated_sdpa_fwd_stats": (_I, [_VP] * 8 + [_I, ctypes.c_float] + [_I] * 10 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_variant": (_I, [_VP] * 7 + [_I] * 9 + [ctypes.c_float, _I, _I, _VP, _SZ, _VP]),
     "gsdpa_bwd_workspace_bytes": (_SZ, [_I] * 8),
     "gated_sdpa_bwd": (_I, [_VP] * 13 + [_I] * 10 + [_VP, _SZ, _VP]),
@@ -222,6 +223,38 @@ def gated_sdpa_fwd_variant(X, Q, K, V, W_g=None, *, gate="elementwise", gate_fn=
     if st != OK:
         raise GsdpaError(st, "gated_sdpa_fwd_variant")
     return out, sink
+
+
+def gated_sdpa_fwd_stats(X, Q, K, V, W_g, *, gate="elementwise", causal=True, n_bins=20, threshold=0.1, out=None,
+                         workspace=None, stream=None):
+    """gated_sdpa_fwd with the gate statistics: returns (O, stats) where stats is
+    a dict with count, mean (sum / 2^32 / count), below, hist (n_bins counts)."""
+    import torch
+    dtype = BF16 if Q.dtype == torch.bfloat16 else F32
+    gm = GATE_CODES[gate]
+    for t in [X, Q, K, V, W_g]:
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
+            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
+    B, L_q, H_q, d_k = Q.shape
+    L_k, H_kv = K.shape[1], K.shape[2]
+    d_model = X.shape[-1]
+    if out is None:
+        out = torch.empty_like(Q)
+    st = torch.empty(3 + n_bins, dtype=torch.int64, device=Q.device)
+    need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, False, dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    status = int(load().gated_sdpa_fwd_stats(
+        _ptr(X), _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), None, _ptr(st), int(n_bins), float(threshold),
+        B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
+        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+    if status != OK:
+        raise GsdpaError(status, "gated_sdpa_fwd_stats")
+    h = st.cpu().tolist()
+    count = h[0]
+    return out, {"count": count, "sum_fixed": h[1], "mean": (h[1] / 2.0 ** 32 / count) if count else 0.0,
+                 "below": h[2], "hist": h[3:]}
 
 
 def bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise") -> int:

@@ -54,6 +54,7 @@ struct DecodeArgs {
     const __nv_bfloat16* theta;   // input-independent gate [Hq, HD], or RMSNorm gamma [Hq, HD] (or null)
     int gate_fn;                  // gsdpa_gate_fn
     float eps;
+    GateStats gs;                 // gate statistics (sigmoid gate), or none
     float* part_ml;               // [B, Hq, splits, 2]  (max in log2 units, sum)
     float* part_o;                // [B, Hq, splits, HD]
     float* part_x0;               // [B, Hq]  scaled score of key 0
@@ -373,8 +374,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (!per_col) gl1 = gl0;
         }
         const bool add = gate_adds(fn);
-        y0 = gate_combine(y0, gate_value(gl0, fn), add);
-        y1 = gate_combine(y1, gate_value(gl1, fn), add);
+        const float gv0 = gate_value(gl0, fn), gv1 = gate_value(gl1, fn);
+        y0 = gate_combine(y0, gv0, add);
+        y1 = gate_combine(y1, gv1, add);
+        if (args.gs.out) {   // every thread of the block is here (the last arriver's)
+            const bool per_col = args.gate_mode == 2;
+            gate_stats_warp(args.gs, gv0, per_col || dd == 0);
+            gate_stats_warp(args.gs, gv1, per_col);
+        }
     } else if (fn == 5) {   // SiLU of the output
         y0 *= sigmoid_tanh(y0);
         y1 *= sigmoid_tanh(y1);
@@ -457,6 +464,7 @@ cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* w
     a.theta = (p.gate_mode == 5 || p.gate_fn == 6) ? static_cast<const __nv_bfloat16*>(p.Wg) : nullptr;
     a.gate_fn = p.gate_fn;
     a.eps = p.eps;
+    a.gs = p.stats;
     a.part_ml = reinterpret_cast<float*>(ws + w.dec_ml);
     a.part_o = reinterpret_cast<float*>(ws + w.dec_o);
     a.part_x0 = reinterpret_cast<float*>(ws + w.dec_x0);

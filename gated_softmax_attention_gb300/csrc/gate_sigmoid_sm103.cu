@@ -66,6 +66,7 @@ struct SigArgs {
     int rows, cols, d_model;
     int row_tiles, nkc;   // tiles of 256 rows; K chunks of 64
     ZeroJob zero;         // per-call state of the attention kernel, zeroed by CTA 0
+    GateStats st;         // gate statistics of the stored values (STATS instances)
     WaitCtl ctl;
 };
 
@@ -90,7 +91,7 @@ __device__ __forceinline__ uint32_t gate_value2_h(float x0, float x1) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FN>
+template <int FN, bool STATS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmG, const SigArgs args) {
@@ -222,6 +223,18 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const bool ok = __all_sync(0xffffffffu, pair::wait(acc_full, 0, ab, args.ctl));
         tc_fence_after();
+        // gate statistics of the fp16 values this thread stores: per-thread totals,
+        // and per-thread bin counters in the idle ring past the staged tile,
+        // bin-major [64 bins][256 threads] (64 KB): each thread owns its counters,
+        // a warp's 32 counters of one bin lie in 32 different banks, and the
+        // increments are shared-memory reductions whose result nobody waits for
+        const int et = (int)threadIdx.x - 64;   // epilogue thread 0..255
+        unsigned long long st_fx = 0;
+        unsigned st_n = 0, st_below = 0;
+        unsigned* st_h = reinterpret_cast<unsigned*>(smem + 8 * 16384);
+        if (STATS)
+            for (int k = 0; k < args.st.n_bins; ++k) st_h[k * 256 + et] = 0;
+        const bool row_ok = r0 + (int)rank * 128 + row < args.rows;
         if (ok) {
             // (every MMA has completed, so the ring is idle: stage the tile there as
             // [8 blocks of 64 columns][128 rows], 128-byte rows, 128B swizzle)
@@ -253,6 +266,65 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     if (lane == 0) mbar_arrive(&grp_ready[(k >> 2) * 2 + half]);
                 }
             }
+        }
+        if (STATS && ok) {
+            // this thread's 256 staged values, read back from the staging blocks
+            // (its own writes) 8 at a time, with no float-to-integer conversions
+            // (a slow pipe): a fp16 score s in [0, 1] times 2^24 is the integer
+            // (1024 + mantissa) << (exponent - 1), or the mantissa when subnormal;
+            // floor(s n_bins) is the low bits of s n_bins + 2^23 added rounding down.
+            const float nbf = (float)args.st.n_bins;
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k) {
+                const int c = half * 256 + k * 32;
+                const int tc = 256 * ((c & 255) >> 7) + 128 * (c >> 8) + (c & 127);
+                const uint8_t* blk = smem + (tc >> 6) * 16384;
+                const uint32_t chunk0 = (uint32_t)(tc & 63) >> 3;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(blk + sw128_offset((uint32_t)row, chunk0 + q));
+                    const uint32_t ws4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&ws4[j >> 1]));
+                        const float sv = (j & 1) ? f2.y : f2.x;
+                        const uint32_t hb = (j & 1) ? (ws4[j >> 1] >> 16) : (ws4[j >> 1] & 0xffffu);
+                        const uint32_t ex = (hb >> 10) & 31u, mn = hb & 1023u;
+                        const uint32_t fx = ex ? ((1024u + mn) << (ex - 1)) : mn;
+                        const bool valid = row_ok && c0 + tc + 8 * q + j < args.cols;
+                        st_n += valid;
+                        st_fx += valid ? fx : 0u;
+                        st_below += (valid && sv < args.st.threshold) ? 1u : 0u;
+                        int bin = __float_as_int(__fadd_rd(sv * nbf, 8388608.0f)) - 0x4B000000;
+                        bin = bin < args.st.n_bins ? bin : args.st.n_bins - 1;
+                        if (valid) atomicAdd(&st_h[bin * 256 + et], 1u);
+                    }
+                }
+            }
+            st_fx <<= 8;   // score * 2^24 -> score * 2^32
+        }
+        if (STATS) {
+            // this warp's totals and histogram into the call's counters
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) {
+                st_fx += __shfl_xor_sync(0xffffffffu, st_fx, sh);
+                st_n += __shfl_xor_sync(0xffffffffu, st_n, sh);
+                st_below += __shfl_xor_sync(0xffffffffu, st_below, sh);
+            }
+            if (lane == 0 && st_n) {
+                atomicAdd(args.st.out, (unsigned long long)st_n);
+                atomicAdd(args.st.out + 1, st_fx);
+                if (st_below) atomicAdd(args.st.out + 2, (unsigned long long)st_below);
+            }
+            // the CTA's histogram: 4 threads per bin each add 64 threads' counters
+            named_bar_sync(1, 256);
+            const int kb = et >> 2, q = et & 3;
+            unsigned hsum = 0;
+            if (kb < args.st.n_bins)
+                for (int u = 0; u < 64; ++u) hsum += st_h[kb * 256 + q * 64 + u];
+            hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
+            hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
+            if (kb < args.st.n_bins && q == 0 && hsum) atomicAdd(args.st.out + 3 + kb, (unsigned long long)hsum);
         }
         tc_fence_before();
     }
@@ -294,7 +366,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d, c
 }  // namespace
 
 namespace {
-template <int FN>
+template <int FN, bool STATS = false>
 cudaError_t launch_gate_value_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s, ZeroJob zero) {
     alignas(64) CUtensorMap tmX, tmW, tmG;
@@ -332,17 +404,18 @@ cudaError_t launch_gate_value_t(const Problem& p, const WorkspacePlan& w, char* 
     a.row_tiles = (rows + 255) / 256;
     a.nkc = (p.d_model + 63) / 64;
     a.zero = zero;
+    a.st = p.stats;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
     static bool attr_done = false;   // per template instance
     if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel<FN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel<FN, STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (r != cudaSuccess) return r;
         attr_done = true;
     }
     const long tiles = (long)a.row_tiles * ((cols + 511) / 512);
-    return launch_dependent(gate_sigmoid_kernel<FN>, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX,
+    return launch_dependent(gate_sigmoid_kernel<FN, STATS>, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX,
                             tmW, tmG, a);
 }
 }  // namespace
@@ -355,6 +428,7 @@ cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, c
                                 static_cast<const __nv_bfloat16*>(p.Wg), reinterpret_cast<__half*>(ws + w.gate_sig),
                                 n, p.gate_fn, zero);
     }
+    if (p.stats.out) return launch_gate_value_t<0, true>(p, w, ws, rt, s, zero);   // (sigmoid gate only)
     switch (p.gate_fn) {
     case 1: return launch_gate_value_t<1>(p, w, ws, rt, s, zero);
     case 3: return launch_gate_value_t<3>(p, w, ws, rt, s, zero);

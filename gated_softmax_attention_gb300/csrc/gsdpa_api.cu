@@ -327,10 +327,12 @@ int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, c
 namespace {
 int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O, float* sink,
              float* lse, int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
-             int dtype, void* workspace, size_t workspace_bytes, void* stream, int gate_fn = 0, float eps = 0.f) {
+             int dtype, void* workspace, size_t workspace_bytes, void* stream, int gate_fn = 0, float eps = 0.f,
+             GateStats stats = GateStats()) {
     Problem p{};
     p.gate_fn = gate_fn;
     p.eps = eps;
+    p.stats = stats;
     p.lse = lse;
     p.X = X;
     p.Q = Q;
@@ -379,6 +381,8 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = cudaSuccess;
+    if (stats.out) e = cudaMemsetAsync(stats.out, 0, sizeof(unsigned long long) * (3 + (size_t)stats.n_bins), s);
+    if (e != cudaSuccess) return GSDPA_ERR_LAUNCH;
     if (dtype == GSDPA_F32) {
         e = launch_f32_simt(p, w, ws, rt, s);
         if (e == cudaSuccess && sink) e = launch_sink_finalize(p, w, ws, s);
@@ -455,6 +459,21 @@ int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K, const vo
                            size_t workspace_bytes, void* stream) {
     return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
                     workspace, workspace_bytes, stream, gate_fn, eps);
+}
+
+int gated_sdpa_fwd_stats(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,
+                         float* sink, unsigned long long* stats, int n_bins, float threshold, int B, int L_q, int L_k,
+                         int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (gate_mode != GSDPA_GATE_HEADWISE && gate_mode != GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
+    if (!stats || n_bins < 1 || n_bins > 64 || !(threshold >= 0.f && threshold <= 1.f)) return GSDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(stats) & 7u) return GSDPA_ERR_ALIGNMENT;
+    GateStats st;
+    st.out = stats;
+    st.n_bins = n_bins;
+    st.threshold = threshold;
+    return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
+                    workspace, workspace_bytes, stream, 0, 0.f, st);
 }
 
 int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,

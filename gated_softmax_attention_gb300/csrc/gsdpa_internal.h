@@ -8,6 +8,14 @@
 
 namespace gsdpa {
 
+// Gate statistics of a call (gated_sdpa_fwd_stats): the device array
+// [3 + n_bins] of 64-bit counters, or null (not computed).
+struct GateStats {
+    unsigned long long* out = nullptr;
+    int n_bins = 0;
+    float threshold = 0.f;
+};
+
 struct Problem {
     const void* X;
     const void* Q;
@@ -23,6 +31,7 @@ struct Problem {
     int dtype;       // 0 f32, 1 bf16
     int gate_fn = 0; // gsdpa_gate_fn
     float eps = 0.f; // RMSNorm
+    GateStats stats; // gate statistics, or none
 };
 
 struct Runtime {

@@ -111,6 +111,7 @@ struct PairArgs {
     int gate_splits;
     const __half* gate_sig;  // elementwise family: the gate's values (row stride ge.g_rs, head stride ge.g_hs)
     GateEpi ge;              // gate function and the gate's layout
+    GateStats gs;            // gate statistics (headwise gate), or none
     int* sched_counter;      // next unit to claim (0 at launch)
     unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
     float* sink;                    // [B, Hq] out
@@ -547,6 +548,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         gl += args.gate_part[sg * rows * args.ge.l_cols + idx];
                 }
                 g_head = gate_value(gl, fn);
+                // (both warpgroups hold the row: warpgroup 0 counts it)
+                if (args.gs.out) gate_stats_warp(args.gs, g_head, p == 0 && U.mine && i < args.Lq);
             }
             // per-head RMSNorm (no gate): this warpgroup's 64 columns' sum of squares,
             // exchanged with the other warpgroup's through shared memory
@@ -694,6 +697,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
     a.ge = gate_epi(p);
+    a.gs = p.gate_mode == 1 ? p.stats : GateStats();
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.lse = p.lse;

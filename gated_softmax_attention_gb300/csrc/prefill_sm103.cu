@@ -88,6 +88,7 @@ struct PrefillArgs {
     int gate_splits;
     const __half* gate_sig;  // elementwise family: the gate's values (row stride ge.g_rs, head stride ge.g_hs)
     GateEpi ge;              // gate function and the gate's layout
+    GateStats gs;            // gate statistics (headwise gate), or none
     int* sched_counter;      // next unit to claim (0 at launch)
     unsigned long long* sink_word;  // [B, Hq] first-token share, fixed point + arrivals (0 at launch), or null
     float* sink;                    // [B, Hq] out
@@ -505,6 +506,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         gl += args.gate_part[s * rows * args.ge.l_cols + idx];
                 }
                 g_head = gate_value(gl, fn);
+                if (args.gs.out) gate_stats_warp(args.gs, g_head, i < args.Lq);
             }
             // per-head RMSNorm (no gate): the row's mean square over its d_k columns first
             float rr = 1.0f;
@@ -654,6 +656,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.gate_splits = w.gate_splits;
     a.gate_sig = (GATE == 2) ? reinterpret_cast<const __half*>(ws + w.gate_sig) : nullptr;
     a.ge = gate_epi(p);
+    a.gs = p.gate_mode == 1 ? p.stats : GateStats();
     a.sched_counter = reinterpret_cast<int*>(ws + w.state);
     set_sink_args(p, w, ws, a.n_qtiles, &a.sink_word, &a.sink, &a.sink_scale, &a.sink_inv, &a.sink_arrivals);
     a.lse = p.lse;

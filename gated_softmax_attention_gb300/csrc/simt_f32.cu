@@ -15,6 +15,7 @@
 // the head dimensions c = p + 4 t (interleaved so that the 4 threads of a row
 // read 4 consecutive floats). Keys stream through shared memory 32 at a time.
 #include "gsdpa_internal.h"
+#include "gate_fn.cuh"
 
 #include <cmath>
 
@@ -31,7 +32,7 @@ __global__ void __launch_bounds__(kThreads)
 gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, const float* __restrict__ K,
                       const float* __restrict__ V, const float* __restrict__ Wg, float* __restrict__ O,
                       float* __restrict__ sink_part, int B, int Lq, int Lk, int d_model, int Hq, int Hkv,
-                      int gate_mode, int causal, int gate_fn, float eps) {
+                      int gate_mode, int causal, int gate_fn, float eps, GateStats gs) {
     constexpr int DPT = DK / kParts;  // dims per thread
     __shared__ float sK[kKeys][DK];
     __shared__ float sV[kKeys][DK];
@@ -99,6 +100,12 @@ gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, 
     }
     const bool gated = gate_mode != 0;
     const bool add = gate_fn >= 2 && gate_fn <= 4;
+    if (gs.out) {
+        // gate statistics: each score once (headwise: one per row, from part 0)
+        const bool per_col = gate_mode == 2;
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) gate_stats_warp(gs, g[t], row_valid && (per_col || (part == 0 && t == 0)));
+    }
 
     // ---- online softmax over keys
     long key_end = Lk;
@@ -194,12 +201,12 @@ cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, 
         gated_attn_f32_kernel<64><<<grid, kThreads, 0, s>>>(
             X, static_cast<const float*>(p.Q), static_cast<const float*>(p.K), static_cast<const float*>(p.V), Wg,
             static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal,
-            p.gate_fn, p.eps);
+            p.gate_fn, p.eps, p.stats);
     } else {
         gated_attn_f32_kernel<128><<<grid, kThreads, 0, s>>>(
             X, static_cast<const float*>(p.Q), static_cast<const float*>(p.K), static_cast<const float*>(p.V), Wg,
             static_cast<float*>(p.O), sink_part, p.B, p.Lq, p.Lk, p.d_model, p.Hq, p.Hkv, p.gate_mode, p.causal,
-            p.gate_fn, p.eps);
+            p.gate_fn, p.eps, p.stats);
     }
     return cudaGetLastError();
 }

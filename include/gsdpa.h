@@ -182,6 +182,30 @@ GSDPA_API int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gated_sdpa_fwd that also measures the gate's scores ("GatedAttention
+ * [2025]", sec. 1.4.2: the mean gating score of Table 4, the score
+ * distribution of Figure 3, and the fraction of scores below a threshold):
+ *   stats     : device array of 3 + n_bins unsigned 64-bit counters, 8-byte
+ *               aligned, overwritten by the call:
+ *               [0] number of scores (B L_q H_q d_k elementwise, B L_q H_q headwise),
+ *               [1] sum over the scores of round(score * 2^32),
+ *               [2] number of scores < threshold,
+ *               [3 + k] scores s with min(floor(s n_bins), n_bins - 1) = k.
+ *               Integer counters: the result does not depend on the order of
+ *               the additions. The score is the value the call multiplies
+ *               by (bf16 path: the fp16 value of the elementwise gate; the
+ *               fp32 value of the headwise gate).
+ *   n_bins    : 1 .. 64.   threshold : in [0, 1].
+ * gate_mode HEADWISE or ELEMENTWISE (GSDPA_ERR_INVALID_ARG otherwise); other
+ * arguments, workspace and errors as for gated_sdpa_fwd (an empty problem
+ * enqueues nothing and leaves stats as they are).
+ */
+GSDPA_API int gated_sdpa_fwd_stats(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                                   void* O, float* sink, unsigned long long* stats, int n_bins, float threshold,
+                                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode,
+                                   int causal, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The forward a training step runs: gated_sdpa_fwd, and also, for every
  * batch b, query head h and query row i, the natural log of the softmax
  * denominator, lse[b, h, i] = log sum_j exp(s_j) over the row's visible

@@ -68,6 +68,9 @@ def _load():
             lib.gsdpa_oracle_fwd_variant.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 9 + [
                 ctypes.c_double, ctypes.c_int, ip, ip, ctypes.c_long, ctypes.c_int]
             lib.gsdpa_oracle_fwd_variant.restype = ctypes.c_int
+            lib.gsdpa_oracle_gate_scores.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int]
+            lib.gsdpa_oracle_gate_scores.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd.argtypes = [dp] * 11 + [ctypes.c_int] * 9
             lib.gsdpa_oracle_bwd.restype = ctypes.c_int
             lib.gsdpa_oracle_bwd_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 9 + [ip, ip, ctypes.c_long, ip, ip,
@@ -185,6 +188,34 @@ def gated_sdpa_variant(X, Q, K, V, W_g, *, gate="elementwise", gate_fn="sigmoid_
     if rc != 0:
         raise ValueError("oracle rejected the shapes, the gate variant or the rows")
     return O, p0
+
+
+def gate_scores(X, W_g, H_q, d_k, *, gate="elementwise"):
+    """sigma(X W_g) in float64 for every row and gate column: [B*L_q, H_q*d_k]
+    (elementwise) or [B*L_q, H_q] (headwise)."""
+    gm = _GATE_CODES[gate]
+    Xd, Wd = _f64(X), _f64(W_g)
+    d_model = Xd.shape[-1]
+    rows = Xd.size // d_model
+    G = H_q * d_k if gm == GATE_ELEMENTWISE else H_q
+    out = np.empty((rows, G), np.float64)
+    rc = _load().gsdpa_oracle_gate_scores(_ptr(Xd), _ptr(Wd), _ptr(out), rows, d_model, H_q, d_k, gm)
+    if rc != 0:
+        raise ValueError("oracle rejected the gate")
+    return out
+
+
+def gate_statistics(scores, n_bins, threshold):
+    """The gate statistics of "GatedAttention [2025]" sec. 1.4.2 (Table 4: the
+    mean gating score; Figure 3: the distribution; appendix: the fraction of
+    scores below a threshold) of an array of scores in [0, 1]: a dict with
+    count, mean, below (how many scores are < threshold) and hist (n_bins
+    equal bins over [0, 1]; bin k holds k/n <= s < (k+1)/n, 1 in the last)."""
+    s = np.asarray(scores, np.float64).ravel()
+    idx = np.minimum(np.floor(s * n_bins).astype(np.int64), n_bins - 1)
+    hist = np.bincount(idx, minlength=n_bins)
+    return {"count": int(s.size), "mean": float(s.mean()) if s.size else 0.0,
+            "below": int(np.count_nonzero(s < threshold)), "hist": hist}
 
 
 def gated_sdpa_bwd(X, Q, K, V, W_g, dO, *, gate="elementwise", causal=True):

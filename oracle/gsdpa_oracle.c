@@ -586,6 +586,31 @@ int gsdpa_oracle_bwd_rows(const double* X, const double* Q, const double* K, con
     return failed ? -1 : 0;
 }
 
+/*
+ * The gate's scores sigma(X W_g) of every row and gate column, for the gate
+ * statistics ("GatedAttention [2025]", sec. 1.4.2 (i), Table 4 and Figure 3:
+ * the mean gating score and the distribution of the scores):
+ *   scores[r, col] = 1 / (1 + exp(-sum_m X[r, m] W_g[m, col])),
+ *   r over the B * L_q rows, col over the H_q * d_k (elementwise) or H_q
+ *   (headwise) gate columns.
+ * Returns 0, or -1 for another gate mode.
+ */
+int gsdpa_oracle_gate_scores(const double* X, const double* Wg, double* scores, long rows, int d_model, int Hq,
+                             int dk, int gate_mode)
+{
+    if (gate_mode != ORACLE_GATE_HEADWISE && gate_mode != ORACLE_GATE_ELEMENTWISE) return -1;
+    if (rows < 0 || d_model < 1 || !X || !Wg || !scores) return -1;
+    const long G = gate_width(gate_mode, Hq, dk);
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r)
+        for (long col = 0; col < G; ++col) {
+            double gl = 0.0;
+            for (int m = 0; m < d_model; ++m) gl += X[r * d_model + m] * Wg[(long)m * G + col];
+            scores[r * G + col] = sigmoid(gl);
+        }
+    return 0;
+}
+
 /* Number of threads an OpenMP region would use (1 without OpenMP). */
 int gsdpa_oracle_max_threads(void)
 {

@@ -178,3 +178,21 @@ def test_variant_workspace_bytes(lib):
     assert w(2, 300, 300, 256, 6, 2, 128, "headwise_shared", "sigmoid_mul", False, gb.BF16) >= n_no + 4 * 600
     with pytest.raises(gb.GsdpaError):
         w(2, 300, 300, 256, 8, 2, 128, "elementwise", "rmsnorm", False, gb.BF16)
+
+
+def test_stats_validation_before_any_device_work(lib):
+    def c(**kw):
+        base = dict(X=16, Q=16, K=16, V=16, W_g=16, O=16, sink=None, stats=16, n_bins=10, threshold=0.1, B=1, L_q=8,
+                    L_k=8, d_model=64, H_q=4, H_kv=4, d_k=64, gate_mode=2, causal=1, dtype=0, workspace=None,
+                    workspace_bytes=0, stream=None)
+        base.update(kw)
+        return int(gb.load().gated_sdpa_fwd_stats(*base.values()))
+    assert c(gate_mode=0) == gb.ERR_INVALID_ARG       # statistics of a gate
+    assert c(gate_mode=4) == gb.ERR_INVALID_ARG
+    assert c(stats=None) == gb.ERR_INVALID_ARG
+    assert c(n_bins=0) == gb.ERR_INVALID_ARG
+    assert c(n_bins=65) == gb.ERR_INVALID_ARG
+    assert c(threshold=1.5) == gb.ERR_INVALID_ARG
+    assert c(threshold=float("nan")) == gb.ERR_INVALID_ARG
+    assert c(stats=12) == gb.ERR_ALIGNMENT
+    assert c(B=0) == gb.OK
