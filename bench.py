@@ -378,7 +378,7 @@ def run_ours(args, d: Dist):
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
                 "traffic": captured_traffic("prefill_kernel_bf16_mha_none_L2048.md",
-                                            ["prefill_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h"]),
+                                            ["prefill_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h", "gate_fn.cuh"]),
                 "kernel": "prefill_kernel<128,0> (attention kernel; gate-free call)", "kernel_ms": round(none_avg, 4),
                 "gated_call_ms": round(kern_avg, 4),
                 "gated_call_tflops": round(flops / (kern_avg / 1e3) / 1e12, 2)}
@@ -627,7 +627,7 @@ def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):
                          "peak_source": peaks["source"] + " STREAM-style copy",
                          "scope": "whole call (gate-logit pre-pass + decode kernel)",
                          "traffic_decode_kernel": captured_traffic("decode_kernel_bf16_decode_gqa_elementwise_Lk8192.md",
-                                                                   ["decode_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h"])},
+                                                                  ["decode_sm103.cu", "sm103_ptx.cuh", "gsdpa_internal.h", "gate_fn.cuh"])},
             "e2e": {"value": round(nbytes * E * d.world / e2e_s / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": O.numel() * O.element_size(), "steps": E},
             "gpu_launches": 2 * K}
