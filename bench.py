@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--profile-backward", action="store_true",
                     help="with --profile-workload: the training forward once, then --profile-calls backward calls")
     ap.add_argument("--decode-steps", type=int, default=0, help="0: same as --steps, capped at 200")
@@ -441,6 +442,11 @@ def run_ours(args, d: Dist):
         out["variants"] = run_variants(args, d, torch, gb, w, host, stream, peaks)
         out["gpu_launches"] += out["variants"]["gpu_launches"]
 
+    # ---- the whole layer (input projection, attention, output projection)
+    if not args.no_layer:
+        out["layer"] = run_layer(args, d, torch, gb, w, stream, peaks)
+        out["gpu_launches"] += out["layer"]["gpu_launches"]
+
     # ---- extra workloads (context only), one stderr line each
     for name in [x for x in args.extra.split(",") if x]:
         wx = WORKLOADS[name]
@@ -581,6 +587,43 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
     del graphs, ws
     return {"workload": w.name, "scope": "whole call (gate pass + attention kernel), graph replays, inputs larger "
                                          "than L2 in total", "steps": K, "results": res, "gpu_launches": launches}
+
+
+def run_layer(args, d, torch, gb, w, stream, peaks):
+    """gated_attention_layer on the headline shape: X W_in (Q, K, V and the
+    gate in one GEMM), the attention, O W_O -- graph replays over rotating X
+    copies; algorithmic FLOPs of the three."""
+    from gated_softmax_attention_gb300.workloads import layer_weights, make_inputs
+    X0 = make_inputs(w)["X"].cuda()
+    W_in, W_O = layer_weights(w, device="cuda")
+    R = n_rotating_sets(X0.numel() * X0.element_size() * 3)   # (X, Q/K/V/gate, O, Y move per call)
+    Xs = [X0] + [X0.clone() for _ in range(R - 1)]
+    Y = torch.empty_like(X0)
+    need = gb.layer_workspace_bytes(w.B, w.L_q, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def call(k):
+        gb.gated_attention_layer(Xs[k % R], W_in, W_O, H_q=w.H_q, H_kv=w.H_kv, d_k=w.d_k, gate=w.gate,
+                                 causal=w.causal, out=Y, workspace=ws)
+
+    graphs = capture_steps(torch, call, R)
+    K = max(3, min(args.steps, 100))
+    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in the layer leg: {gb.status_string(st)}")
+    rows = w.B * w.L_q
+    proj = 2 * rows * w.d_model * W_in.shape[1]
+    outp = 2 * rows * w.H_q * w.d_k * w.d_model
+    flops = proj + w.attn_flops() + outp
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": w.name, "metric": "gated attention layer TFLOP/s (bf16; X [W_Q|W_K|W_V|W_g], attention, "
+                                          "O W_O)", "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "flops_per_step": flops, "steps": K,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "scope": "whole call (projection GEMM, attention, output GEMM)"},
+            "gpu_launches": 3 * K}
 
 
 def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):

@@ -29,6 +29,8 @@ SIGNATURES = {
     "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_workspace_bytes_variant": (_SZ, [_I] * 11),
     "gated_sdpa_fwd_stats": (_I, [_VP] * 8 + [_I, ctypes.c_float] + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gsdpa_layer_workspace_bytes": (_SZ, [_I] * 7),
+    "gated_attention_layer": (_I, [_VP] * 4 + [_I] * 8 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_variant": (_I, [_VP] * 7 + [_I] * 9 + [ctypes.c_float, _I, _I, _VP, _SZ, _VP]),
     "gsdpa_bwd_workspace_bytes": (_SZ, [_I] * 8),
     "gated_sdpa_bwd": (_I, [_VP] * 13 + [_I] * 10 + [_VP, _SZ, _VP]),
@@ -255,6 +257,37 @@ def gated_sdpa_fwd_stats(X, Q, K, V, W_g, *, gate="elementwise", causal=True, n_
     count = h[0]
     return out, {"count": count, "sum_fixed": h[1], "mean": (h[1] / 2.0 ** 32 / count) if count else 0.0,
                  "below": h[2], "hist": h[3:]}
+
+
+def layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, gate="elementwise") -> int:
+    n = load().gsdpa_layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, GATE_CODES[gate])
+    if n == ctypes.c_size_t(-1).value:
+        raise GsdpaError(ERR_UNSUPPORTED, "gsdpa_layer_workspace_bytes")
+    return int(n)
+
+
+def gated_attention_layer(X, W_in, W_O, *, H_q, H_kv, d_k=128, gate="elementwise", causal=True, out=None,
+                          workspace=None, stream=None):
+    """The whole layer (gated_attention_layer): X [B, L, d_model] bf16, W_in
+    [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k)], W_O [H_q d_k, d_model]. Returns Y."""
+    import torch
+    for t in (X, W_in, W_O):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("inputs must be contiguous bf16 CUDA tensors")
+    B, L, d_model = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    need = layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, gate)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gated_attention_layer(_ptr(X), _ptr(W_in), _ptr(W_O), _ptr(out), B, L, d_model, H_q, H_kv, d_k,
+                                          GATE_CODES[gate], int(bool(causal)),
+                                          _ptr(workspace) if need > 0 else None, need if need > 0 else 0,
+                                          ctypes.c_void_p(s.cuda_stream)))
+    if st != OK:
+        raise GsdpaError(st, "gated_attention_layer")
+    return out
 
 
 def bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise") -> int:

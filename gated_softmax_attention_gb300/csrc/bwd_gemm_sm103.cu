@@ -28,6 +28,7 @@
 // soon as its four warps have staged it. Rows and columns past the end of C
 // and the K tail load as zeros (TMA out-of-bounds fill) and are not stored.
 #include "gsdpa_internal.h"
+#include "proj_internal.h"
 #include "sm103_pair.cuh"
 #include "sm103_ptx.cuh"
 
@@ -284,6 +285,14 @@ int gemm_pair_nh(int M, int N, int num_sms) {
     const long t2 = m_tiles * ((N + 511) / 512), t1 = m_tiles * ((N + 255) / 256);
     const long cost2 = (t2 + pairs - 1) / pairs * 5, cost1 = (t1 + pairs - 1) / pairs * 3;   // x2: 2.5, 1.5
     return cost2 <= cost1 ? 2 : 1;
+}
+
+cudaError_t launch_gemm_pair_bf16_kn(const void* A, const void* Bm, void* C, int M, int N, int K, const Runtime& rt,
+                                     cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (K <= 0) return cudaErrorInvalidValue;
+    return gemm_pair_nh(M, N, rt.num_sms) == 2 ? launch_t<false, true, 2>(A, Bm, C, M, N, K, rt, s)
+                                               : launch_t<false, true, 1>(A, Bm, C, M, N, K, rt, s);
 }
 
 cudaError_t launch_gemm_pair_bf16(const void* A, const void* Bm, void* C, int M, int N, int K, bool ab_mn,

@@ -3,6 +3,7 @@
 // device error word that bounded waits report into.
 #include "gsdpa.h"
 #include "gsdpa_internal.h"
+#include "proj_internal.h"
 #include "sm103_ptx.cuh"
 
 #include <atomic>
@@ -459,6 +460,102 @@ int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K, const vo
                            size_t workspace_bytes, void* stream) {
     return fwd_impl(X, Q, K, V, W_g, O, sink, nullptr, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
                     workspace, workspace_bytes, stream, gate_fn, eps);
+}
+
+}  // extern "C"
+
+namespace gsdpa {
+namespace {
+// The layer's problem and workspace: the attention's own plan, then Q, K, V
+// and the attention output (bf16), each 256-byte aligned.
+struct LayerPlan {
+    Problem p{};
+    WorkspacePlan w;
+    size_t q = 0, k = 0, v = 0, o = 0, total = 0;
+};
+int plan_layer(int B, int L, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, LayerPlan* lp) {
+    Problem& p = lp->p;
+    p.B = B;
+    p.Lq = L;
+    p.Lk = L;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.causal = causal ? 1 : 0;
+    p.dtype = GSDPA_BF16;
+    if (gate_mode != GSDPA_GATE_NONE && gate_mode != GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
+    if (d_model < 1) return GSDPA_ERR_INVALID_ARG;
+    const int st = validate_shape(p);
+    if (st != GSDPA_OK) return st;
+    if (d_k != 128 || d_model % 8 != 0 || d_model < 256 || (B > 0 && L < 2)) return GSDPA_ERR_UNSUPPORTED;
+    lp->w = plan_workspace(p, kPlanSms);
+    size_t off = lp->w.total;
+    const size_t rows = (size_t)B * L;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    lp->q = take(rows * H_q * d_k * 2);
+    lp->k = take(rows * H_kv * d_k * 2);
+    lp->v = take(rows * H_kv * d_k * 2);
+    lp->o = take(rows * H_q * d_k * 2);
+    lp->total = off;
+    return GSDPA_OK;
+}
+}  // namespace
+}  // namespace gsdpa
+
+extern "C" {
+
+size_t gsdpa_layer_workspace_bytes(int B, int L, int d_model, int H_q, int H_kv, int d_k, int gate_mode) {
+    LayerPlan lp;
+    if (plan_layer(B, L, d_model, H_q, H_kv, d_k, gate_mode, 1, &lp) != GSDPA_OK) return (size_t)-1;
+    if (B == 0 || L == 0) return 0;
+    return lp.total;
+}
+
+int gated_attention_layer(const void* X, const void* W_in, const void* W_O, void* Y, int B, int L, int d_model,
+                          int H_q, int H_kv, int d_k, int gate_mode, int causal, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    LayerPlan lp;
+    const int st = plan_layer(B, L, d_model, H_q, H_kv, d_k, gate_mode, causal, &lp);
+    if (st != GSDPA_OK) return st;
+    if (B == 0 || L == 0) return GSDPA_OK;
+    if (!X || !W_in || !W_O || !Y) return GSDPA_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W_in) || !aligned16(W_O) || !aligned16(Y)) return GSDPA_ERR_ALIGNMENT;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return GSDPA_ERR_LAUNCH;
+    if (!(dev->cc_major == 10 && dev->cc_minor == 3) || !encode_tiled_fn()) return GSDPA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < lp.total) return GSDPA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSDPA_ERR_ALIGNMENT;
+    char* ws = static_cast<char*>(workspace);
+    Runtime rt;
+    rt.err = dev->err;
+    rt.limit_ns = g_wait_limit_ns.load();
+    rt.num_sms = dev->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem p = lp.p;
+    p.X = X;
+    p.Q = ws + lp.q;
+    p.K = ws + lp.k;
+    p.V = ws + lp.v;
+    p.O = ws + lp.o;
+    const bool gated = gate_mode == GSDPA_GATE_ELEMENTWISE;
+    // 1. [Q | K | V | gate] = X W_in (zeroes the attention kernel's per-call state);
+    // 2. the attention (its gate values already in place); 3. Y = O W_O
+    ZeroJob zero;
+    zero.p = reinterpret_cast<int*>(ws + lp.w.state);
+    zero.n = lp.w.state_ints;
+    cudaError_t e = launch_proj_qkvg_bf16(X, W_in, ws + lp.q, ws + lp.k, ws + lp.v, gated ? ws + lp.w.gate_sig : nullptr,
+                                          B * L, d_model, H_q, H_kv, d_k, gated, zero, rt, s);
+    // (an ordinary launch: the attention reads Q, K, V from its first step)
+    if (e == cudaSuccess) e = launch_prefill_bf16_ordered(p, lp.w, ws, rt, s);
+    if (e == cudaSuccess) e = launch_gemm_pair_bf16_kn(ws + lp.o, W_O, Y, B * L, d_model, H_q * d_k, rt, s);
+    if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
+    return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
 }
 
 int gated_sdpa_fwd_stats(const void* X, const void* Q, const void* K, const void* V, const void* W_g, void* O,

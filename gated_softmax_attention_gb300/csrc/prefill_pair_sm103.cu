@@ -67,6 +67,7 @@
 #include "sm103_pair.cuh"
 #include "sm103_ptx.cuh"
 #include "gate_fn.cuh"
+#include "proj_internal.h"
 
 #include <cmath>
 #include <cuda_fp16.h>
@@ -662,7 +663,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 }
 
 template <int GATE, bool ADD = false>
-cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
+cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s,
+                          bool pdl = true) {
     using C = PairCfg;
     alignas(64) CUtensorMap tmQ, tmK, tmV;
     const cuuint64_t e = 2;
@@ -741,11 +743,17 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
+    cfg.numAttrs = ((GATE == 1 || GATE == 2) && pdl) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE, ADD>, tmQ, tmK, tmV, a);
 }
 
 }  // namespace
+
+cudaError_t launch_prefill_pair_bf16_ordered(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                             cudaStream_t s) {
+    if (p.gate_mode != 0 && p.gate_mode != 2) return cudaErrorInvalidValue;
+    return p.gate_mode == 2 ? launch_pair_t<2>(p, w, ws, rt, s, false) : launch_pair_t<0>(p, w, ws, rt, s, false);
+}
 
 cudaError_t launch_prefill_pair_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                      cudaStream_t s) {

@@ -42,6 +42,7 @@
 #include "gsdpa_internal.h"
 #include "sm103_ptx.cuh"
 #include "gate_fn.cuh"
+#include "proj_internal.h"
 
 #include <cmath>
 #include <cuda_fp16.h>
@@ -616,7 +617,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 }
 
 template <int HD, int GATE, bool ADD = false>
-cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s) {
+cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt, cudaStream_t s,
+                             bool pdl = true) {
     using C = PrefillCfg<HD, GATE>;
     alignas(64) CUtensorMap tmQ, tmK, tmV, tmO;
     const cuuint64_t e = 2;
@@ -689,11 +691,19 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (GATE == 1 || GATE == 2) ? 1 : 0;
+    cfg.numAttrs = ((GATE == 1 || GATE == 2) && pdl) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD>, tmQ, tmK, tmV, tmO, a);
 }
 
 }  // namespace
+
+cudaError_t launch_prefill_bf16_ordered(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                        cudaStream_t s) {
+    if ((long)p.Lk >= kPairMinKeys) return launch_prefill_pair_bf16_ordered(p, w, ws, rt, s);
+    if (p.dk != 128 || (p.gate_mode != 0 && p.gate_mode != 2) || p.gate_fn != 0) return cudaErrorInvalidValue;
+    return p.gate_mode == 2 ? launch_prefill_t<128, 2>(p, w, ws, rt, s, false)
+                            : launch_prefill_t<128, 0>(p, w, ws, rt, s, false);
+}
 
 cudaError_t launch_prefill_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                 cudaStream_t s) {

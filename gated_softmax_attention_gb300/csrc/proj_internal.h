@@ -1,0 +1,31 @@
+// proj_internal.h -- host-side launch interfaces of the layer's neighbouring
+// GEMMs (input projection, output projection). Not part of the public ABI.
+#pragma once
+#include "gsdpa_internal.h"
+
+namespace gsdpa {
+
+// X [rows, d_model] times W_in = [W_Q | W_K | W_V | W_g] [d_model, N] into Q
+// [rows, H_q d_k], K and V [rows, H_kv d_k] (bf16) and, when gated, the
+// elementwise gate sigma(X W_g) [rows, H_q d_k] (fp16) (proj_sm103.cu). d_k a
+// multiple of 128 (every output's width a multiple of 128 columns). Runs first
+// in a call: zeroes `zero`, then lets the next kernel start.
+cudaError_t launch_proj_qkvg_bf16(const void* X, const void* W_in, void* Qo, void* Ko, void* Vo, void* Go, int rows,
+                                  int d_model, int Hq, int Hkv, int dk, bool gated, ZeroJob zero, const Runtime& rt,
+                                  cudaStream_t s);
+
+// The bf16 prefill attention as an ordinary launch (not a programmatic
+// dependent of the kernel before it): for callers whose previous kernel
+// produces Q, K or V, which the attention kernel reads from its first step
+// (prefill_sm103.cu, prefill_pair_sm103.cu). Sigmoid gate, none or elementwise.
+cudaError_t launch_prefill_bf16_ordered(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                        cudaStream_t s);
+cudaError_t launch_prefill_pair_bf16_ordered(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
+                                             cudaStream_t s);
+
+// C [M x N] (bf16) = A B on CTA pairs with A stored [M][K] and B stored [K][N]
+// (bwd_gemm_sm103.cu), N >= 256: the output projection O W_O.
+cudaError_t launch_gemm_pair_bf16_kn(const void* A, const void* Bm, void* C, int M, int N, int K, const Runtime& rt,
+                                     cudaStream_t s);
+
+}  // namespace gsdpa

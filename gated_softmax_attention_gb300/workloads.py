@@ -21,6 +21,11 @@ Gate variants (``variant_weight``): a second generator seeded with
   * the RMSNorm scale, gamma [H_q, d_k] = 1 + 0.1 N(0, 1);
 then rounded once to the workload's dtype, like the other inputs.
 
+The whole layer (``layer_weights``): a generator seeded with ``seed + 104729``
+draws W_in [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k gated)] ~ N(0, 1/d_model)
+(so Q, K, V and the gate logits are about N(0, 1)) and W_O [H_q d_k, d_model]
+~ N(0, 1/(H_q d_k)); X is the workload's own.
+
 Layouts: X [B, L_q, d_model]; Q [B, L_q, H_q, d_k]; K, V [B, L_k, H_kv, d_k];
 W_g [d_model, H_q*d_k] (elementwise, head-major columns) or [d_model, H_q]
 (headwise). The model shapes follow the pages' settings: context 4096 for
@@ -167,3 +172,15 @@ def variant_weight(w: Workload, gate: str, gate_fn: str = "sigmoid_mul", device=
     else:
         return None
     return t.to(torch_dtype(w)).contiguous().to(device)
+
+
+def layer_weights(w: Workload, device="cpu"):
+    """(W_in, W_O) of the whole layer for workload ``w`` (see the recipe above)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + 104729)
+    f = torch.float32
+    n_in = (w.H_q + 2 * w.H_kv) * w.d_k + (w.H_q * w.d_k if w.gate != "none" else 0)
+    W_in = torch.randn((w.d_model, n_in), generator=g, dtype=f) / w.d_model ** 0.5
+    W_O = torch.randn((w.H_q * w.d_k, w.d_model), generator=g, dtype=f) / (w.H_q * w.d_k) ** 0.5
+    td = torch_dtype(w)
+    return W_in.to(td).contiguous().to(device), W_O.to(td).contiguous().to(device)

@@ -206,6 +206,31 @@ GSDPA_API int gated_sdpa_fwd_stats(const void* X, const void* Q, const void* K, 
                                    int causal, int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The whole layer around the attention ("GatedAttention [2025]", sec. 1.2.1:
+ * Q, K, V projected from the hidden state X; sec. 1.2.2: the gate reads X
+ * too; the heads' gated outputs concatenated and projected by W_O):
+ *   [Q | K | V | GL] = X W_in                    one GEMM (the four share X)
+ *   Y = (softmax(Q K^T / sqrt(d_k) + causal) V (.) sigma(GL)) W_O
+ * with the attention of gated_sdpa_fwd in between. Self-attention (L_q = L_k
+ * = L) without a cache.
+ *   X      : device bf16 [B, L, d_model].
+ *   W_in   : device bf16 [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k when gated)],
+ *            columns: the Q heads, the K heads, the V heads, then the
+ *            elementwise gate (head-major, like gated_sdpa_fwd's W_g).
+ *   W_O    : device bf16 [H_q d_k, d_model].
+ *   Y      : device bf16 [B, L, d_model] out.
+ *   gate_mode NONE or ELEMENTWISE; bf16, d_k = 128, L >= 2, d_model a
+ *   multiple of 8 and >= 256 (GSDPA_ERR_UNSUPPORTED otherwise).
+ * Q, K, V and the pre-W_O output live in the workspace (bf16), the gate as
+ * fp16, as in gated_sdpa_fwd. Pointers 16-byte aligned; asynchronous on
+ * `stream`; errors as for gated_sdpa_fwd.
+ */
+GSDPA_API size_t gsdpa_layer_workspace_bytes(int B, int L, int d_model, int H_q, int H_kv, int d_k, int gate_mode);
+GSDPA_API int gated_attention_layer(const void* X, const void* W_in, const void* W_O, void* Y, int B, int L,
+                                    int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The forward a training step runs: gated_sdpa_fwd, and also, for every
  * batch b, query head h and query row i, the natural log of the softmax
  * denominator, lse[b, h, i] = log sum_j exp(s_j) over the row's visible

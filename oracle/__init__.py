@@ -218,6 +218,26 @@ def gate_statistics(scores, n_bins, threshold):
             "below": int(np.count_nonzero(s < threshold)), "hist": hist}
 
 
+def gated_attention_layer(X, W_in, W_O, H_q, H_kv, d_k, *, gate="elementwise", causal=True, rows=None):
+    """The layer around the attention, in float64 ("GatedAttention [2025]",
+    sec. 1.2.1: Q = X W_Q, K = X W_K, V = X W_V; sec. 1.2.2: the gate
+    sigma(X W_g); the gated heads concatenated and projected by W_O):
+    W_in = [W_Q | W_K | W_V | W_g] [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k)],
+    W_O [H_q d_k, d_model]. The projections are matrix products (numpy), the
+    attention is :func:`gated_sdpa`. Returns Y [B, L, d_model], or
+    [n_rows, d_model] for the (b, i) pairs in ``rows``."""
+    Xd, Wi, Wo = _f64(X), _f64(W_in), _f64(W_O)
+    B, L, dm = Xd.shape
+    qc, kc = H_q * d_k, H_kv * d_k
+    P = Xd @ Wi
+    Q = np.ascontiguousarray(P[..., :qc]).reshape(B, L, H_q, d_k)
+    K = np.ascontiguousarray(P[..., qc:qc + kc]).reshape(B, L, H_kv, d_k)
+    V = np.ascontiguousarray(P[..., qc + kc:qc + 2 * kc]).reshape(B, L, H_kv, d_k)
+    Wg = np.ascontiguousarray(Wi[:, qc + 2 * kc:]) if gate != "none" else None
+    O, _ = gated_sdpa(Xd if gate != "none" else None, Q, K, V, Wg, gate=gate, causal=causal, rows=rows)
+    return O.reshape(O.shape[0], L, qc) @ Wo if rows is None else O.reshape(-1, qc) @ Wo
+
+
 def gated_sdpa_bwd(X, Q, K, V, W_g, dO, *, gate="elementwise", causal=True):
     """Backward of :func:`gated_sdpa` in float64, given dO = dL/dO [B, L_q, H_q, d_k].
 

@@ -42,8 +42,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_only_the_abi_is_exported(lib):
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", gb.LIB_PATH], capture_output=True, text=True).stdout
-    ours = {line.split()[-1] for line in out.splitlines() if line.split()[-1].startswith("gsdpa")
-            or line.split()[-1].startswith("gated_sdpa")}
+    ours = {line.split()[-1] for line in out.splitlines()
+            if line.split()[-1].startswith(("gsdpa", "gated_sdpa", "gated_attention"))}
     assert ours == set(declared_symbols())
 
 
@@ -196,3 +196,22 @@ def test_stats_validation_before_any_device_work(lib):
     assert c(threshold=float("nan")) == gb.ERR_INVALID_ARG
     assert c(stats=12) == gb.ERR_ALIGNMENT
     assert c(B=0) == gb.OK
+
+
+def test_layer_workspace_and_validation(lib):
+    n = gb.layer_workspace_bytes(2, 300, 256, 4, 2, 128, "elementwise")
+    rows = 600
+    # the attention's plan (state, fp16 gate) + Q, K, V, O in bf16
+    assert n >= rows * (4 + 2 + 2 + 4) * 128 * 2 + rows * 4 * 128 * 2 and n % 256 == 0
+    assert gb.layer_workspace_bytes(0, 300, 256, 4, 2, 128, "elementwise") == 0
+    for args in [(2, 300, 128, 4, 2, 128, "elementwise"),   # d_model < 256
+                 (2, 300, 256, 4, 2, 64, "elementwise"),    # d_k 64
+                 (2, 1, 256, 4, 2, 128, "elementwise"),     # one token
+                 (2, 300, 256, 4, 2, 128, "headwise")]:
+        with pytest.raises(gb.GsdpaError):
+            gb.layer_workspace_bytes(*args)
+    L = gb.load()
+    st = L.gated_attention_layer(16, 16, 16, 16, 2, 300, 256, 4, 2, 128, 2, 1, None, 0, None)
+    assert st == gb.ERR_WORKSPACE or st == gb.ERR_LAUNCH or st == gb.ERR_UNSUPPORTED   # (no device here)
+    assert L.gated_attention_layer(8, 16, 16, 16, 2, 300, 256, 4, 2, 128, 2, 1, None, 0, None) == gb.ERR_ALIGNMENT
+    assert L.gated_attention_layer(None, 16, 16, 16, 2, 300, 256, 4, 2, 128, 2, 1, None, 0, None) == gb.ERR_INVALID_ARG

@@ -1,0 +1,74 @@
+"""GPU parity of the whole layer (gated_attention_layer: one input-projection
+GEMM for Q, K, V and the gate, the attention, the output-projection GEMM)
+against the oracle's layer (numpy projections around the pinned attention
+oracle).
+
+Bar: the layer's bf16 bar (relative L1 <= 5e-3; max-abs 2e-2 on outputs of
+unit scale, scaled by max(1, max|ref|)). Beyond the attention's own rounding,
+Q, K, V and the attention output are rounded to bf16 and the gate to fp16
+before the next product (2^-9 and 2^-11 relative)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_softmax_attention_gb300 import binding as gb
+from gated_softmax_attention_gb300 import build as gbuild
+from gated_softmax_attention_gb300.workloads import Workload, layer_weights, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_L1 = 5e-3
+MAX_ABS = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    gbuild.build()
+    gb.load()
+    torch.cuda.init()
+
+
+def _w(**kw):
+    base = dict(name="layer", dtype="bf16", B=2, L_q=300, L_k=300, d_model=256, H_q=4, H_kv=2, d_k=128,
+                gate="elementwise", causal=True, seed=61)
+    base.update(kw)
+    return Workload(**base)
+
+
+def _check(what, got, ref):
+    err = np.abs(got - ref)
+    rel = err.sum() / np.abs(ref).sum()
+    scale = max(1.0, float(np.abs(ref).max()))
+    print(f"{what}: rel-L1 {rel:.2e} max-abs {err.max():.2e} max|ref| {np.abs(ref).max():.2e}")
+    assert rel <= REL_L1, f"{what}: rel-L1 {rel:.3e}"
+    assert err.max() <= MAX_ABS * scale, f"{what}: max-abs {err.max():.3e}"
+
+
+CASES = [_w(), _w(gate="none", seed=62), _w(causal=False, seed=63), _w(H_q=8, H_kv=8, L_q=257, L_k=257, seed=64)]
+
+
+@pytest.mark.parametrize("w", CASES, ids=["gqa_elementwise", "no_gate", "full_mask", "mha_ragged"])
+def test_layer_matches_oracle(w):
+    X = make_inputs(w)["X"] if w.gate != "none" else \
+        make_inputs(Workload(**{**w.__dict__, "gate": "elementwise"}))["X"]
+    W_in, W_O = layer_weights(w)
+    Y = gb.gated_attention_layer(X.cuda(), W_in.cuda(), W_O.cuda(), H_q=w.H_q, H_kv=w.H_kv, d_k=w.d_k, gate=w.gate,
+                                 causal=w.causal)
+    assert gb.check_device_error() == gb.OK
+    ref = oracle.gated_attention_layer(X, W_in, W_O, w.H_q, w.H_kv, w.d_k, gate=w.gate, causal=w.causal)
+    _check(w.gate, Y.double().cpu().numpy(), ref)
+
+
+def test_layer_sampled_rows_larger():
+    # 2048 rows, d_model 1024, 8 heads: the projection takes 256 x 512 tiles over several K chunks
+    w = _w(B=1, L_q=2048, L_k=2048, d_model=1024, H_q=8, H_kv=2, seed=65)
+    X = make_inputs(w)["X"]
+    W_in, W_O = layer_weights(w)
+    Y = gb.gated_attention_layer(X.cuda(), W_in.cuda(), W_O.cuda(), H_q=w.H_q, H_kv=w.H_kv, d_k=w.d_k)
+    assert gb.check_device_error() == gb.OK
+    rng = np.random.default_rng(9)
+    rows = sorted(set([(0, 0), (0, 127), (0, 128), (0, 2047)] + [(0, int(i)) for i in rng.integers(0, 2048, 12)]))
+    ref = oracle.gated_attention_layer(X, W_in, W_O, w.H_q, w.H_kv, w.d_k, rows=rows)
+    got = Y.double().cpu().numpy()
+    _check("rows", np.stack([got[b, i] for b, i in rows]), ref)
