@@ -268,40 +268,72 @@ gate_sigmoid_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
         }
         if (STATS && ok) {
-            // this thread's 256 staged values, read back from the staging blocks
-            // (its own writes) 8 at a time, with no float-to-integer conversions
-            // (a slow pipe): a fp16 score s in [0, 1] times 2^24 is the integer
-            // (1024 + mantissa) << (exponent - 1), or the mantissa when subnormal;
-            // floor(s n_bins) is the low bits of s n_bins + 2^23 added rounding down.
+            // this thread's 256 staged values, read back from the staging blocks (its
+            // own writes) as fp16 pairs, with few instructions per score (the pass
+            // runs on two warps per scheduler while the tensor pipe waits for it):
+            // - sum: float32 pairs, four partial sums of up to 64 scores each (at
+            //   most 64, so each partial is within 64 * 2^-24 of the exact sum),
+            //   rounded to fixed point once per thread;
+            // - below the threshold: a fp16 score s is below t exactly when it is
+            //   below t rounded up to fp16 (no fp16 value lies in between); the
+            //   packed comparison gives 1.0 or 0.0 per score and the packed fp16
+            //   counters stay exact (at most 128 per half);
+            // - bin: s n_bins + 2^23 rounded down (one fused multiply-add) holds
+            //   floor(s n_bins) in its low bits; the unsigned difference from 2^23's
+            //   bit pattern clamped to n_bins - 1 keeps any input on a counter.
             const float nbf = (float)args.st.n_bins;
+            const uint32_t last_bin = (uint32_t)args.st.n_bins - 1u;
+            const __half2 thr2 = __half2half2(__float2half_ru(args.st.threshold));
+            const uint32_t h_addr = smem_u32(st_h + et);   // this thread's counter of bin 0
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            __half2 below2 = __float2half2_rn(0.f);
+            auto count_bin = [&](float sv) {
+                uint32_t bin = __float_as_uint(__fmaf_rd(sv, nbf, 8388608.0f)) - 0x4B000000u;
+                bin = bin < last_bin ? bin : last_bin;
+                asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(h_addr + (bin << 10)));
+            };
 #pragma unroll 1
             for (int k = 0; k < 8; ++k) {
                 const int c = half * 256 + k * 32;
                 const int tc = 256 * ((c & 255) >> 7) + 128 * (c >> 8) + (c & 127);
+                const int col0 = c0 + tc;   // the gate column of the chunk's first value
+                if (!row_ok || col0 >= args.cols) continue;
+                const bool whole = col0 + 32 <= args.cols;
                 const uint8_t* blk = smem + (tc >> 6) * 16384;
                 const uint32_t chunk0 = (uint32_t)(tc & 63) >> 3;
 #pragma unroll 1
                 for (int q = 0; q < 4; ++q) {
                     const uint4 w4 = *reinterpret_cast<const uint4*>(blk + sw128_offset((uint32_t)row, chunk0 + q));
                     const uint32_t ws4[4] = {w4.x, w4.y, w4.z, w4.w};
+                    if (whole) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&ws4[j >> 1]));
-                        const float sv = (j & 1) ? f2.y : f2.x;
-                        const uint32_t hb = (j & 1) ? (ws4[j >> 1] >> 16) : (ws4[j >> 1] & 0xffffu);
-                        const uint32_t ex = (hb >> 10) & 31u, mn = hb & 1023u;
-                        const uint32_t fx = ex ? ((1024u + mn) << (ex - 1)) : mn;
-                        const bool valid = row_ok && c0 + tc + 8 * q + j < args.cols;
-                        st_n += valid;
-                        st_fx += valid ? fx : 0u;
-                        st_below += (valid && sv < args.st.threshold) ? 1u : 0u;
-                        int bin = __float_as_int(__fadd_rd(sv * nbf, 8388608.0f)) - 0x4B000000;
-                        bin = bin < args.st.n_bins ? bin : args.st.n_bins - 1;
-                        if (valid) atomicAdd(&st_h[bin * 256 + et], 1u);
+                        for (int x = 0; x < 4; ++x) {
+                            const __half2 h2 = *reinterpret_cast<const __half2*>(&ws4[x]);
+                            const float2 f2 = __half22float2(h2);
+                            if (x & 1) acc1 = __fadd2_rn(acc1, f2);
+                            else acc0 = __fadd2_rn(acc0, f2);
+                            below2 = __hadd2(below2, __hlt2(h2, thr2));
+                            count_bin(f2.x);
+                            count_bin(f2.y);
+                        }
+                    } else {
+                        // the last columns of the gate: scores past them are not counted
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (col0 + 8 * q + j >= args.cols) break;
+                            const __half hs = __ushort_as_half((unsigned short)(ws4[j >> 1] >> (16 * (j & 1))));
+                            const float sv = __half2float(hs);
+                            acc0.x += sv;
+                            st_below += __hlt(hs, __low2half(thr2)) ? 1u : 0u;
+                            count_bin(sv);
+                        }
                     }
                 }
+                st_n += whole ? 32u : (uint32_t)(args.cols - col0);
             }
-            st_fx <<= 8;   // score * 2^24 -> score * 2^32
+            const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            st_fx = __float2ull_rn(sum * 4294967296.0f);   // score * 2^32
+            st_below += (uint32_t)(__low2float(below2) + __high2float(below2));
         }
         if (STATS) {
             // this warp's totals and histogram into the call's counters

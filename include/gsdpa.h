@@ -188,11 +188,16 @@ GSDPA_API int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K
  *   stats     : device array of 3 + n_bins unsigned 64-bit counters, 8-byte
  *               aligned, overwritten by the call:
  *               [0] number of scores (B L_q H_q d_k elementwise, B L_q H_q headwise),
- *               [1] sum over the scores of round(score * 2^32),
+ *               [1] the sum of the scores times 2^32 in fixed point: exactly
+ *                   the sum of round(score * 2^32) for the headwise gate, the
+ *                   decode kernel and the float32 path; the bf16 elementwise
+ *                   prefill rounds each thread's float32 partial sums (of at
+ *                   most 256 scores) once, so its mean is within 2^-18 of the
+ *                   exact mean of the scores,
  *               [2] number of scores < threshold,
  *               [3 + k] scores s with min(floor(s n_bins), n_bins - 1) = k.
- *               Integer counters: the result does not depend on the order of
- *               the additions. The score is the value the call multiplies
+ *               Integer counters: the result does not depend on the order in
+ *               which threads add them (two calls give the same bits). The score is the value the call multiplies
  *               by (bf16 path: the fp16 value of the elementwise gate; the
  *               fp32 value of the headwise gate).
  *   n_bins    : 1 .. 64.   threshold : in [0, 1].
