@@ -39,8 +39,7 @@ namespace gsdpa {
 // Gate statistics ("GatedAttention [2025]", sec. 1.4.2: the mean gating score,
 // the distribution of the scores, the fraction below a threshold), as
 // integers so that the result does not depend on the order of the additions:
-//   stats[0] number of scores, stats[1] sum of round(score * 2^32) (the
-//   elementwise gate GEMM adds rounded float32 partial sums instead),
+//   stats[0] number of scores, stats[1] sum of round(score * 2^32),
 //   stats[2] number of scores < threshold, stats[3 + k] scores in bin k of
 //   n_bins equal bins over [0, 1] (bin min(floor(score * n_bins), n_bins - 1)).
 
