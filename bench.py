@@ -581,7 +581,7 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
     if st != gb.OK:
         raise RuntimeError(f"device error in the variants leg (statistics): {gb.status_string(st)}")
     flops = w.attn_flops() + 2 * rows * w.d_model * cols.get(w.gate, 0)
-    launches += 2 * K
+    launches += 3 * K   # counter zeroing, gate GEMM with the counting pass, attention kernel
     res.append({"gate": w.gate, "gate_fn": "sigmoid_mul + statistics (20 bins)", "ms_per_call": round(ms, 5),
                 "tflops": round(flops / (ms / 1e3) / 1e12, 2), "vs_default_call": round(ms / base_ms, 4)})
     del graphs, ws

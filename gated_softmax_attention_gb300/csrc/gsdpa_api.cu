@@ -186,6 +186,18 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 // sink[b,h] = (1 / L_q) * sum over query tiles of the per-tile sums of p(i -> key 0).
+// Zeroes the call's statistics counters as a programmatic dependent of the
+// kernel before it on the stream (a memset node there would end the overlap of
+// consecutive calls' kernels). Its own dependent, the call's first gate kernel,
+// may start its prologue at once: that kernel waits for this one to complete
+// before it touches global memory, and every statistics update of the call
+// comes after that wait, or after a wait on a kernel that made it.
+__global__ void stats_zero_kernel(unsigned long long* __restrict__ out, int n) {
+    pdl_trigger();
+    pdl_wait();
+    for (int k = threadIdx.x; k < n; k += blockDim.x) out[k] = 0;
+}
+
 __global__ void sink_finalize_kernel(const float* __restrict__ part, float* __restrict__ sink, int n, int tiles,
                                      float inv_lq) {
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -382,7 +394,13 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = cudaSuccess;
-    if (stats.out) e = cudaMemsetAsync(stats.out, 0, sizeof(unsigned long long) * (3 + (size_t)stats.n_bins), s);
+    if (stats.out) {
+        // (bf16: the call starts with a gate kernel that waits before touching memory;
+        // the float32 kernel is an ordinary launch)
+        const int n = 3 + stats.n_bins;
+        e = dtype == GSDPA_F32 ? cudaMemsetAsync(stats.out, 0, sizeof(unsigned long long) * (size_t)n, s)
+                               : launch_dependent(stats_zero_kernel, dim3(1), dim3(64), 0, s, stats.out, n);
+    }
     if (e != cudaSuccess) return GSDPA_ERR_LAUNCH;
     if (dtype == GSDPA_F32) {
         e = launch_f32_simt(p, w, ws, rt, s);
