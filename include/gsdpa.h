@@ -197,9 +197,10 @@ GSDPA_API int gated_sdpa_fwd_variant(const void* X, const void* Q, const void* K
  *               [2] number of scores < threshold,
  *               [3 + k] scores s with min(floor(s n_bins), n_bins - 1) = k.
  *               Integer counters: the result does not depend on the order in
- *               which threads add them (two calls give the same bits). The score is the value the call multiplies
- *               by (bf16 path: the fp16 value of the elementwise gate; the
- *               fp32 value of the headwise gate).
+ *               which threads add them (two calls give the same bits). The
+ *               score is the value the call multiplies by (bf16 path: the
+ *               fp16 value of the elementwise gate; the fp32 value of the
+ *               headwise gate).
  *   n_bins    : 1 .. 64.   threshold : in [0, 1].
  * gate_mode HEADWISE or ELEMENTWISE (GSDPA_ERR_INVALID_ARG otherwise); other
  * arguments, workspace and errors as for gated_sdpa_fwd (an empty problem
