@@ -471,41 +471,60 @@ def backward_flops(w):
 
 def run_backward(args, d, torch, gb, w, host, stream, peaks):
     """The backward call on the headline workload: graph replays of R calls,
-    each reading its own copy of the inputs (inputs larger than L2 in total)."""
+    each reading its own copy of the inputs (inputs larger than L2 in total).
+    The elementwise gate's values come from the training forward
+    (gated_sdpa_fwd_train_save_gate -> gated_sdpa_bwd_saved_gate); the call
+    that recomputes them (gated_sdpa_bwd) is timed beside it."""
     dev = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
     g = torch.Generator().manual_seed(4242)
     dO = torch.randn(dev["Q"].shape, generator=g).to(torch.bfloat16).cuda()
-    O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
-                                        causal=w.causal)
-    per_set = sum(v.numel() * v.element_size() for v in list(dev.values()) + [O, dO, lse] if v is not None)
+    saved = w.gate == "elementwise"
+    if saved:
+        O, _, lse, G = gb.gated_sdpa_fwd_train_save_gate(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"],
+                                                         causal=w.causal)
+    else:
+        O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
+                                            causal=w.causal)
+        G = None
+    per_set = sum(v.numel() * v.element_size() for v in list(dev.values()) + [O, dO, lse, G] if v is not None)
     R = n_rotating_sets(per_set)
-    sets = [dict(dev, O=O, dO=dO, lse=lse)]
+    sets = [dict(dev, O=O, dO=dO, lse=lse, G=G)]
     for _ in range(R - 1):
         sets.append({k: (v.clone() if v is not None else None) for k, v in sets[0].items()})
     need = gb.bwd_workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
-
-    def call(k):
-        st = sets[k % R]
-        gb.gated_sdpa_bwd(st["X"], st["Q"], st["K"], st["V"], st["W_g"], st["O"], st["dO"], st["lse"], gate=w.gate,
-                          causal=w.causal, workspace=ws)
-
-    graphs = capture_steps(torch, call, R)
     K = max(3, min(args.steps, 100))
-    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
-    st = gb.check_device_error(stream)
-    if st != gb.OK:
-        raise RuntimeError(f"device error in the backward leg: {gb.status_string(st)}")
+
+    def timed(use_saved):
+        def call(k):
+            st = sets[k % R]
+            gb.gated_sdpa_bwd(st["X"], st["Q"], st["K"], st["V"], st["W_g"], st["O"], st["dO"], st["lse"],
+                              gate=w.gate, causal=w.causal, workspace=ws, gate_saved=st["G"] if use_saved else None)
+
+        graphs = capture_steps(torch, call, R)
+        ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+        st = gb.check_device_error(stream)
+        if st != gb.OK:
+            raise RuntimeError(f"device error in the backward leg: {gb.status_string(st)}")
+        return ms
+
+    ms = timed(saved)
+    ms_recompute = timed(False) if saved else ms
     flops = backward_flops(w)
     tf = flops / (ms / 1e3) / 1e12
-    kernels = 6 if w.gate != "none" else 3
+    kernels = (5 if saved else 6) if w.gate != "none" else 3
     return {"workload": w.name, "metric": "gated attention bwd TFLOP/s (bf16; algorithmic: 5 attention products "
                                           "+ 2 gate GEMMs)", "value": round(tf, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 5), "flops_per_step": flops, "steps": K,
+            "gate": "saved by the training forward" if saved else "recomputed",
+            "with_gate_recompute": {"ms_per_step": round(ms_recompute, 5),
+                                    "tflops": round(flops / (ms_recompute / 1e3) / 1e12, 2)},
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-                         "scope": "whole call (gate recompute, prep, dQ, dK/dV, dX and dW_g GEMMs)"},
-            "gpu_launches": kernels * K}
+                         "scope": "whole call (prep, dQ, dK/dV, dX and dW_g GEMMs; the gate's values saved by "
+                                  "the training forward)" if saved else "whole call (gate recompute, prep, dQ, "
+                                  "dK/dV, dX and dW_g GEMMs)"},
+            "gpu_launches": kernels * K + ((6 * K) if saved else 0)}
 
 
 VARIANTS = [("elementwise", "sigmoid_mul"), ("elementwise", "ns_sigmoid_mul"), ("elementwise", "sigmoid_add"),

@@ -27,6 +27,7 @@ SIGNATURES = {
     "gsdpa_workspace_bytes": (_SZ, [_I] * 10),
     "gated_sdpa_fwd": (_I, [_VP] * 7 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gated_sdpa_fwd_train": (_I, [_VP] * 8 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gated_sdpa_fwd_train_save_gate": (_I, [_VP] * 9 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_workspace_bytes_variant": (_SZ, [_I] * 11),
     "gated_sdpa_fwd_stats": (_I, [_VP] * 8 + [_I, ctypes.c_float] + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_layer_workspace_bytes": (_SZ, [_I] * 7),
@@ -34,6 +35,7 @@ SIGNATURES = {
     "gated_sdpa_fwd_variant": (_I, [_VP] * 7 + [_I] * 9 + [ctypes.c_float, _I, _I, _VP, _SZ, _VP]),
     "gsdpa_bwd_workspace_bytes": (_SZ, [_I] * 8),
     "gated_sdpa_bwd": (_I, [_VP] * 13 + [_I] * 10 + [_VP, _SZ, _VP]),
+    "gated_sdpa_bwd_saved_gate": (_I, [_VP] * 14 + [_I] * 10 + [_VP, _SZ, _VP]),
     "gsdpa_check_device_error": (_I, [_VP]),
     "gsdpa_status_string": (ctypes.c_char_p, [_I]),
     "gsdpa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
@@ -134,7 +136,23 @@ def gated_sdpa_fwd_train(X, Q, K, V, W_g=None, *, gate="elementwise", causal=Tru
     return _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream)
 
 
-def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream):
+def gated_sdpa_fwd_train_save_gate(X, Q, K, V, W_g, *, causal=True, out=None, sink=None, want_sink=False, lse=None,
+                                   gate_out=None, workspace=None, stream=None):
+    """gated_sdpa_fwd_train for the elementwise gate that also returns the gate's
+    fp16 values [B * L_q, H_q * d_k] for gated_sdpa_bwd_saved_gate. Returns
+    (O, sink, lse, gate_out)."""
+    import torch
+    B, L_q, H_q, d_k = Q.shape
+    if lse is None:
+        lse = torch.empty((B, H_q, L_q), dtype=torch.float32, device=Q.device)
+    if gate_out is None:
+        gate_out = torch.empty((B * L_q, H_q * d_k), dtype=torch.float16, device=Q.device)
+    O, sink, lse = _fwd(X, Q, K, V, W_g, "elementwise", causal, out, sink, want_sink, lse, workspace, stream,
+                        gate_out=gate_out)
+    return O, sink, lse, gate_out
+
+
+def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream, gate_out=None):
     import torch
     if Q.dtype == torch.bfloat16:
         dtype = BF16
@@ -162,7 +180,10 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
             _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink)]
     tail = [B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
             _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)]
-    if lse is None:
+    if gate_out is not None:
+        st = int(load().gated_sdpa_fwd_train_save_gate(*args, _ptr(lse), _ptr(gate_out), *tail))
+        where = "gated_sdpa_fwd_train_save_gate"
+    elif lse is None:
         st = int(load().gated_sdpa_fwd(*args, *tail))
         where = "gated_sdpa_fwd"
     else:
@@ -297,9 +318,12 @@ def bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate="elementwise"
     return int(n)
 
 
-def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=True, workspace=None, stream=None):
+def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=True, workspace=None, stream=None,
+                   gate_saved=None):
     """Backward through the C ABI (bf16, d_k = 128): returns a dict with dQ, dK,
-    dV and, with a gate, dX (the gate path's share) and dW_g."""
+    dV and, with a gate, dX (the gate path's share) and dW_g. gate_saved (the
+    elementwise gate's values from gated_sdpa_fwd_train_save_gate) calls
+    gated_sdpa_bwd_saved_gate, which does not recompute them."""
     import torch
     gm = GATE_CODES[gate]
     for t in [Q, K, V, O, dO] + ([X, W_g] if gm != GATE_NONE else []):
@@ -316,13 +340,19 @@ def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=Tr
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
-    st = int(load().gated_sdpa_bwd(
-        _ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
-        _ptr(O), _ptr(dO), _ptr(lse), _ptr(out.get("dX")), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
-        _ptr(out.get("dW_g")), B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16,
-        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+    head = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
+            _ptr(O), _ptr(dO), _ptr(lse)]
+    rest = [_ptr(out.get("dX")), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), _ptr(out.get("dW_g")), B, L_q,
+            L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16, _ptr(workspace) if need > 0 else None,
+            need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)]
+    if gate_saved is not None:
+        if not (gate_saved.is_cuda and gate_saved.is_contiguous() and gate_saved.dtype == torch.float16):
+            raise ValueError("gate_saved must be a contiguous fp16 CUDA tensor")
+        st, where = int(load().gated_sdpa_bwd_saved_gate(*head, _ptr(gate_saved), *rest)), "gated_sdpa_bwd_saved_gate"
+    else:
+        st, where = int(load().gated_sdpa_bwd(*head, *rest)), "gated_sdpa_bwd"
     if st != OK:
-        raise GsdpaError(st, "gated_sdpa_bwd")
+        raise GsdpaError(st, where)
     return out
 
 

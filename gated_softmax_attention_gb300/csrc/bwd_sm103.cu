@@ -35,6 +35,7 @@
 // result does not depend on the order of the CTAs, and each pass keeps its
 // accumulators in tensor memory).
 #include "gsdpa_internal.h"
+#include "proj_internal.h"
 #include "sm103_ptx.cuh"
 
 #include <cuda_fp16.h>
@@ -1055,8 +1056,13 @@ BwdPlan plan_bwd(const Problem& p, int num_sms) {
 
 cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w, char* ws, const Runtime& rt,
                             cudaStream_t s) {
-    // 1. the gate again (sigma(X W_g) as fp16, or the headwise logits)
-    if (p.gate_mode == 2) {
+    return launch_bwd_bf16_saved(p, g, nullptr, w, ws, rt, s);
+}
+
+cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void* gate_saved, const BwdPlan& w,
+                                  char* ws, const Runtime& rt, cudaStream_t s) {
+    // 1. the gate again (sigma(X W_g) as fp16, unless the forward saved it, or the headwise logits)
+    if (p.gate_mode == 2 && !gate_saved) {
         cudaError_t e = launch_gate_sigmoid_bf16(p, w.fwd, ws, rt, s, ZeroJob());
         if (e != cudaSuccess) return e;
     } else if (p.gate_mode == 1) {
@@ -1069,7 +1075,9 @@ cudaError_t launch_bwd_bf16(const Problem& p, const BwdArgs& g, const BwdPlan& w
     pa.dO = static_cast<const __nv_bfloat16*>(g.dO);
     pa.O = static_cast<const __nv_bfloat16*>(g.O);
     pa.lse = g.lse;
-    pa.gate_sig = p.gate_mode == 2 ? reinterpret_cast<const __half*>(ws + w.fwd.gate_sig) : nullptr;
+    pa.gate_sig = p.gate_mode != 2 ? nullptr
+                  : gate_saved     ? static_cast<const __half*>(gate_saved)
+                                   : reinterpret_cast<const __half*>(ws + w.fwd.gate_sig);
     pa.gate_part = p.gate_mode == 1 ? reinterpret_cast<const float*>(ws + w.fwd.gate_part) : nullptr;
     pa.gate_splits = w.fwd.gate_splits;
     pa.dY = reinterpret_cast<__nv_bfloat16*>(ws + w.dY);

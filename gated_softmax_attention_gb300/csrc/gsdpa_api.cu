@@ -280,10 +280,11 @@ size_t gsdpa_bwd_workspace_bytes(int B, int L_q, int L_k, int d_model, int H_q, 
     return plan_bwd(p, kPlanSms).total;
 }
 
-int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, const void* O,
-                   const void* dO, const float* lse, void* dX, void* dQ, void* dK, void* dV, void* dW_g, int B,
-                   int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype,
-                   void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+int bwd_impl(const void* X, const void* Q, const void* K, const void* V, const void* W_g, const void* O, const void* dO,
+             const float* lse, const void* gate_saved, void* dX, void* dQ, void* dK, void* dV, void* dW_g, int B,
+             int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype,
+             void* workspace, size_t workspace_bytes, void* stream) {
     Problem p{};
     p.X = X;
     p.Q = Q;
@@ -332,9 +333,30 @@ int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, c
     g.dK = dK;
     g.dV = dV;
     g.dWg = dW_g;
-    const cudaError_t e = launch_bwd_bf16(p, g, w, static_cast<char*>(workspace), rt, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_bwd_bf16_saved(p, g, gate_saved, w, static_cast<char*>(workspace), rt,
+                                                static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
     return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
+}
+}  // namespace
+
+int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g, const void* O,
+                   const void* dO, const float* lse, void* dX, void* dQ, void* dK, void* dV, void* dW_g, int B,
+                   int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(X, Q, K, V, W_g, O, dO, lse, nullptr, dX, dQ, dK, dV, dW_g, B, L_q, L_k, d_model, H_q, H_kv, d_k,
+                    gate_mode, causal, dtype, workspace, workspace_bytes, stream);
+}
+
+int gated_sdpa_bwd_saved_gate(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                              const void* O, const void* dO, const float* lse, const void* gate_saved, void* dX,
+                              void* dQ, void* dK, void* dV, void* dW_g, int B, int L_q, int L_k, int d_model, int H_q,
+                              int H_kv, int d_k, int gate_mode, int causal, int dtype, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (gate_mode != GSDPA_GATE_ELEMENTWISE || !gate_saved) return GSDPA_ERR_INVALID_ARG;
+    if (!aligned16(gate_saved)) return GSDPA_ERR_ALIGNMENT;
+    return bwd_impl(X, Q, K, V, W_g, O, dO, lse, gate_saved, dX, dQ, dK, dV, dW_g, B, L_q, L_k, d_model, H_q, H_kv,
+                    d_k, gate_mode, causal, dtype, workspace, workspace_bytes, stream);
 }
 
 namespace {
@@ -601,6 +623,36 @@ int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, const void
     if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
     return fwd_impl(X, Q, K, V, W_g, O, sink, lse, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode, causal, dtype,
                     workspace, workspace_bytes, stream);
+}
+
+int gated_sdpa_fwd_train_save_gate(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
+                                   void* O, float* sink, float* lse, void* gate_out, int B, int L_q, int L_k,
+                                   int d_model, int H_q, int H_kv, int d_k, int gate_mode, int causal, int dtype,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (gate_mode != GSDPA_GATE_ELEMENTWISE || !gate_out) return GSDPA_ERR_INVALID_ARG;
+    if (!aligned16(gate_out)) return GSDPA_ERR_ALIGNMENT;
+    const int st = gated_sdpa_fwd_train(X, Q, K, V, W_g, O, sink, lse, B, L_q, L_k, d_model, H_q, H_kv, d_k, gate_mode,
+                                        causal, dtype, workspace, workspace_bytes, stream);
+    if (st != GSDPA_OK || B == 0 || L_q == 0) return st;
+    // the gate kernel's fp16 values, [B*L_q, H_q*d_k] at the start of their workspace region
+    Problem p{};
+    p.B = B;
+    p.Lq = L_q;
+    p.Lk = L_k;
+    p.d_model = d_model;
+    p.Hq = H_q;
+    p.Hkv = H_kv;
+    p.dk = d_k;
+    p.gate_mode = gate_mode;
+    p.causal = causal ? 1 : 0;
+    p.dtype = dtype;
+    p.sink = sink;
+    const WorkspacePlan w = plan_workspace(p, kPlanSms);
+    if (!w.has_gate_sig) return GSDPA_ERR_UNSUPPORTED;
+    const size_t bytes = (size_t)B * L_q * H_q * d_k * sizeof(__half);
+    const cudaError_t e = cudaMemcpyAsync(gate_out, static_cast<char*>(workspace) + w.gate_sig, bytes,
+                                          cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;
 }
 
 int gsdpa_check_device_error(void* stream) {

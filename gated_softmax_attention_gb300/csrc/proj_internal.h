@@ -28,4 +28,11 @@ cudaError_t launch_prefill_pair_bf16_ordered(const Problem& p, const WorkspacePl
 cudaError_t launch_gemm_pair_bf16_kn(const void* A, const void* Bm, void* C, int M, int N, int K, const Runtime& rt,
                                      cudaStream_t s);
 
+// The backward pass with the elementwise gate's values sigma(X W_g) (fp16
+// [B*L_q, H_q*d_k]) taken from `gate_saved`, where the training forward saved
+// them, instead of recomputing them (bwd_sm103.cu); gate_saved NULL
+// recomputes, as launch_bwd_bf16 does.
+cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void* gate_saved, const BwdPlan& w,
+                                  char* ws, const Runtime& rt, cudaStream_t s);
+
 }  // namespace gsdpa

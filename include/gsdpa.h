@@ -254,6 +254,23 @@ GSDPA_API int gated_sdpa_fwd_train(const void* X, const void* Q, const void* K, 
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gated_sdpa_fwd_train for the elementwise gate that also saves the gate's
+ * values for the backward pass (gated_sdpa_bwd_saved_gate then skips their
+ * recomputation, a GEMM of the size of the gate's):
+ *   gate_out : device fp16 [B * L_q, H_q * d_k], 16-byte aligned, overwritten
+ *              with sigma(X W_g) exactly as the forward multiplied by it.
+ * gate_mode ELEMENTWISE and gate_out non-NULL (GSDPA_ERR_INVALID_ARG
+ * otherwise); other arguments, workspace and errors as for
+ * gated_sdpa_fwd_train. The values are copied from the workspace after the
+ * call's kernels, on the same stream.
+ */
+GSDPA_API int gated_sdpa_fwd_train_save_gate(const void* X, const void* Q, const void* K, const void* V,
+                   const void* W_g, void* O, float* sink, float* lse, void* gate_out,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Workspace bytes gated_sdpa_bwd needs for this problem (bf16, d_k = 128);
  * (size_t)-1 for an invalid or unsupported shape, 0 for an empty one.
  */
@@ -285,6 +302,23 @@ GSDPA_API size_t gsdpa_bwd_workspace_bytes(int B, int L_q, int L_k, int d_model,
  */
 GSDPA_API int gated_sdpa_bwd(const void* X, const void* Q, const void* K, const void* V, const void* W_g,
                    const void* O, const void* dO, const float* lse,
+                   void* dX, void* dQ, void* dK, void* dV, void* dW_g,
+                   int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
+                   int gate_mode, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gated_sdpa_bwd for the elementwise gate with the gate's values taken from
+ * gate_saved (what gated_sdpa_fwd_train_save_gate wrote: fp16
+ * [B * L_q, H_q * d_k], 16-byte aligned) instead of recomputed from X and
+ * W_g. With the forward's own values the outputs equal gated_sdpa_bwd's bit
+ * for bit. gate_mode ELEMENTWISE and gate_saved non-NULL
+ * (GSDPA_ERR_INVALID_ARG otherwise); other arguments, workspace (the same
+ * gsdpa_bwd_workspace_bytes) and errors as for gated_sdpa_bwd.
+ */
+GSDPA_API int gated_sdpa_bwd_saved_gate(const void* X, const void* Q, const void* K, const void* V,
+                   const void* W_g, const void* O, const void* dO, const float* lse,
+                   const void* gate_saved,
                    void* dX, void* dQ, void* dK, void* dV, void* dW_g,
                    int B, int L_q, int L_k, int d_model, int H_q, int H_kv, int d_k,
                    int gate_mode, int causal, int dtype,

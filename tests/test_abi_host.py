@@ -215,3 +215,39 @@ def test_layer_workspace_and_validation(lib):
     assert st == gb.ERR_WORKSPACE or st == gb.ERR_LAUNCH or st == gb.ERR_UNSUPPORTED   # (no device here)
     assert L.gated_attention_layer(8, 16, 16, 16, 2, 300, 256, 4, 2, 128, 2, 1, None, 0, None) == gb.ERR_ALIGNMENT
     assert L.gated_attention_layer(None, 16, 16, 16, 2, 300, 256, 4, 2, 128, 2, 1, None, 0, None) == gb.ERR_INVALID_ARG
+
+
+def test_saved_gate_validation_before_any_device_work(lib):
+    # gated_sdpa_fwd_train_save_gate / gated_sdpa_bwd_saved_gate: elementwise
+    # gate and a 16-byte aligned gate buffer, checked before any device work
+    lib_ = gb.load()
+    ints = [1, 8, 8, 64, 4, 4, 128, 2, 1, gb.BF16]
+    fwd = [16] * 9 + ints + [None, 0, None]     # X, Q, K, V, W_g, O, sink, lse, gate_out
+    bad = list(fwd)
+    bad[9 + 7] = 1                                # headwise
+    assert lib_.gated_sdpa_fwd_train_save_gate(*bad) == gb.ERR_INVALID_ARG
+    bad = list(fwd)
+    bad[8] = None
+    assert lib_.gated_sdpa_fwd_train_save_gate(*bad) == gb.ERR_INVALID_ARG
+    bad = list(fwd)
+    bad[8] = 24
+    assert lib_.gated_sdpa_fwd_train_save_gate(*bad) == gb.ERR_ALIGNMENT
+    bad = list(fwd)
+    bad[9 + 9] = gb.F32                           # the training forward is bf16 only
+    assert lib_.gated_sdpa_fwd_train_save_gate(*bad) == gb.ERR_UNSUPPORTED
+    bwd = [16] * 14 + ints + [None, 0, None]    # X .. lse, gate_saved, dX, dQ, dK, dV, dW_g
+    bad = list(bwd)
+    bad[14 + 7] = 0                               # no gate
+    assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_INVALID_ARG
+    bad = list(bwd)
+    bad[8] = None
+    assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_INVALID_ARG
+    bad = list(bwd)
+    bad[8] = 40
+    assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_ALIGNMENT
+    bad = list(bwd)
+    bad[10] = 24                                  # dQ misaligned
+    assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_ALIGNMENT
+    bad = list(bwd)
+    bad[14 + 6] = 64                              # d_k 64 has no backward
+    assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_UNSUPPORTED

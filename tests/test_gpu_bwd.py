@@ -126,3 +126,26 @@ def test_full_size_backward_sampled_rows_and_properties():
     c = float((got["dW_g"] * W).sum())
     print(f"sum(dX X) {a:.6e}  sum(dW_g W_g) {c:.6e}")
     assert abs(a - c) <= 1e-2 * max(abs(a), abs(c))
+
+
+@pytest.mark.parametrize("w", [CASES[0], CASES[3]], ids=lambda w: w.name)
+def test_saved_gate_backward_equals_recompute(w):
+    # the training forward saves sigma(X W_g) as the attention multiplied by it;
+    # the backward that takes those values gives the recomputing backward's bits
+    t = make_inputs(w)
+    d = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    O, _, lse, G = gb.gated_sdpa_fwd_train_save_gate(d["X"], d["Q"], d["K"], d["V"], d["W_g"], causal=w.causal)
+    O2, _, lse2 = gb.gated_sdpa_fwd_train(d["X"], d["Q"], d["K"], d["V"], d["W_g"], gate=w.gate, causal=w.causal)
+    assert torch.equal(O, O2) and torch.equal(lse, lse2)
+    # the saved values are the gate scores: fp16 (2^-11 relative) of a
+    # tanh-approximated sigmoid of a float32-accumulated product
+    ref = oracle.gate_scores(t["X"], t["W_g"], w.H_q, w.d_k, gate="elementwise")
+    assert G.shape == ref.shape and np.abs(G.double().cpu().numpy() - ref).max() <= 2e-3
+    dO = _dO(w).cuda()
+    a = gb.gated_sdpa_bwd(d["X"], d["Q"], d["K"], d["V"], d["W_g"], O, dO, lse, gate=w.gate, causal=w.causal)
+    b = gb.gated_sdpa_bwd(d["X"], d["Q"], d["K"], d["V"], d["W_g"], O, dO, lse, gate=w.gate, causal=w.causal,
+                          gate_saved=G)
+    assert gb.check_device_error() == gb.OK
+    assert a.keys() == b.keys()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
