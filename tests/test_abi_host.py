@@ -251,3 +251,14 @@ def test_saved_gate_validation_before_any_device_work(lib):
     bad = list(bwd)
     bad[14 + 6] = 64                              # d_k 64 has no backward
     assert lib_.gated_sdpa_bwd_saved_gate(*bad) == gb.ERR_UNSUPPORTED
+
+
+def test_binding_signatures_match_the_header():
+    # every declaration's parameter count is the binding's argument count
+    text = open(HEADER).read()
+    decls = dict(re.findall(r"GSDPA_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", text))
+    assert decls.keys() == gb.SIGNATURES.keys()
+    for name, params in decls.items():
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(gb.SIGNATURES[name][1]) == n, name
