@@ -77,6 +77,8 @@ def _load():
                                                                                    ctypes.c_long, dp, dp, dp, dp,
                                                                                    ctypes.c_int]
             lib.gsdpa_oracle_bwd_rows.restype = ctypes.c_int
+            lib.gsdpa_oracle_softmax_stats.argtypes = [dp, dp, dp, dp] + [ctypes.c_int] * 8
+            lib.gsdpa_oracle_softmax_stats.restype = ctypes.c_int
             lib.gsdpa_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -272,6 +274,23 @@ def gated_sdpa_bwd(X, Q, K, V, W_g, dO, *, gate="elementwise", causal=True):
         out["dX"] = dX
         out["dW_g"] = dW
     return out
+
+
+def softmax_stats(Q, K, *, causal=True, n_threads=0):
+    """The softmax statistics of every query row and head in float64, without
+    the values or the gate (half the cost of the full layer): p0 [B, L_q, H_q],
+    the attention weight on key 0, and lse [B, L_q, H_q], the natural log of
+    the softmax denominator (max score + log of the sum of exp(score - max))."""
+    Q, K = _f64(Q), _f64(K)
+    B, Lq, Hq, dk = Q.shape
+    _, Lk, Hkv, _ = K.shape
+    p0 = np.empty((B, Lq, Hq), np.float64)
+    lse = np.empty((B, Lq, Hq), np.float64)
+    rc = _load().gsdpa_oracle_softmax_stats(_ptr(Q), _ptr(K), _ptr(p0), _ptr(lse), B, Lq, Lk, Hq, Hkv, dk,
+                                            int(bool(causal)), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes")
+    return p0, lse
 
 
 def sink_share(p0):

@@ -251,6 +251,66 @@ int gsdpa_oracle_fwd_variant(const double* X, const double* Q, const double* K, 
     return failed ? -1 : 0;
 }
 
+/*
+ * The softmax statistics of every query row and head, without the values or
+ * the gate: p0[b,i,h] = p_0 (the attention weight on key 0, "10 . 门控",
+ * sec. 3.4, the first-token share) and lse[b,i,h] = max s + log sum_j
+ * exp(s_j - max s), from the scores s_j of the header's definition (the SDPA
+ * equation of "GatedAttention [2025]", sec. 1.2.1, causal sum over j <= a).
+ * The same arithmetic as the scores and softmax of gsdpa_oracle_fwd, for
+ * problems where the full layer would cost twice as much (no P V products).
+ *   p0, lse : [B, L_q, H_q] (either may be null)
+ * Returns 0, or -1 on a shape the definition does not cover.
+ */
+int gsdpa_oracle_softmax_stats(const double* Q, const double* K, double* p0, double* lse,
+                               int B, int Lq, int Lk, int Hq, int Hkv, int dk, int causal, int n_threads)
+{
+    if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
+    if (Lq > Lk) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    const int group = Hq / Hkv;
+    const double inv_sqrt_dk = 1.0 / sqrt((double)dk);
+    const long total = (long)B * Lq * Hq;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < total; ++r) {
+            if (!s) continue;
+            const int h = (int)(r % Hq);
+            const int i = (int)((r / Hq) % Lq);
+            const int b = (int)(r / ((long)Hq * Lq));
+            const int kvh = h / group;
+            const long a = (long)Lk - Lq + i;
+            const long n_keys = causal ? a + 1 : Lk;
+            const double* q = Q + (((long)b * Lq + i) * Hq + h) * dk;
+            double mx = -INFINITY;
+            for (long j = 0; j < n_keys; ++j) {
+                const double* k = K + (((long)b * Lk + j) * Hkv + kvh) * dk;
+                double dot = 0.0;
+                for (int c = 0; c < dk; ++c) dot += q[c] * k[c];
+                s[j] = dot * inv_sqrt_dk;
+                if (s[j] > mx) mx = s[j];
+            }
+            double denom = 0.0;
+            for (long j = 0; j < n_keys; ++j) denom += exp(s[j] - mx);
+            if (p0) p0[r] = exp(s[0] - mx) / denom;
+            if (lse) lse[r] = mx + log(denom);
+        }
+        free(s);
+    }
+    return failed ? -1 : 0;
+}
+
 /* The layer with the default gate function (sigmoid, multiplied). */
 int gsdpa_oracle_fwd(const double* X, const double* Q, const double* K, const double* V,
                      const double* Wg, double* O, double* p0, double* lse,
