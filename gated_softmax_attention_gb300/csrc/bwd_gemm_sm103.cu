@@ -257,13 +257,12 @@ cudaError_t launch_t(const void* A, const void* Bm, void* Cm, int M, int N, int 
     if (!(A_MN ? map_bf16(&tmA, A, K, M, 64) : map_bf16(&tmA, A, M, K, 128))) return cudaErrorInvalidValue;
     if (!(B_MN ? map_bf16(&tmB, Bm, K, N, 64) : map_bf16(&tmB, Bm, N, K, 128))) return cudaErrorInvalidValue;
     if (!map_bf16(&tmC, Cm, M, N, 128)) return cudaErrorInvalidValue;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, NH>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;   // per template instance
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     PairGemmArgs a;
     a.m_tiles = (M + 255) / 256;
     a.nkc = (K + 63) / 64;

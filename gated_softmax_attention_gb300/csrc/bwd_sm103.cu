@@ -1003,13 +1003,12 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int K, int cols) {
 template <bool A_MN, bool B_MN>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfloat16* C, int M, int N, int K,
                         const Runtime& rt, cudaStream_t s) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gemm_bf16_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kGemmSmem);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;   // per template instance
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(gemm_bf16_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kGemmSmem);
+    });
+    if (r != cudaSuccess) return r;
     GemmArgs a;
     a.C = C;
     a.M = M;
@@ -1120,24 +1119,25 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     aa.Dv = reinterpret_cast<const float*>(ws + w.Dv);
     aa.ctl.err = rt.err;
     aa.ctl.limit_ns = rt.limit_ns;
-    static bool attr_done = false;
-    if (!attr_done) {
+    static PerDeviceSetup setup;
+    e = setup_once_per_device(setup, [](int&) {
         // The register split only fits if the launch allocates enough registers
         // per thread; refuse to launch otherwise (it would not finish).
         for (const void* k : {reinterpret_cast<const void*>(bwd_dq_kernel),
                               reinterpret_cast<const void*>(bwd_dkdv_kernel)}) {
             cudaFuncAttributes fa;
-            e = cudaFuncGetAttributes(&fa, k);
-            if (e != cudaSuccess) return e;
+            cudaError_t r = cudaFuncGetAttributes(&fa, k);
+            if (r != cudaSuccess) return r;
             if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
         }
-        e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t r =
+            cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg::SMEM_BYTES);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)DkvCfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     bwd_dq_kernel<<<(unsigned)((long)aa.n_qtiles * p.B * p.Hq), kAttnThreads, DqCfg::SMEM_BYTES, s>>>(
         tmQ, tmdY, tmK, tmV, tmdQ, aa);
     e = cudaGetLastError();

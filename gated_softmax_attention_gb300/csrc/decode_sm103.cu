@@ -474,12 +474,11 @@ cudaError_t launch_decode_bf16(const Problem& p, const WorkspacePlan& w, char* w
     cudaError_t e = cudaSuccess;
     if (!dependent) e = cudaMemsetAsync(a.counters, 0, w.dec_cnt_bytes, s);
     if (e != cudaSuccess) return e;
-    static bool attr_done = false;
-    if (!attr_done) {
-        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;
+    e = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    });
+    if (e != cudaSuccess) return e;
     const long units = (long)p.B * p.Hkv * a.chunks * a.splits;
     if (dependent)
         return launch_dependent(decode_kernel, dim3((unsigned)units), dim3(kThreads), SMEM_BYTES, s, tmK, tmV, a);

@@ -277,13 +277,12 @@ cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.zero = zero;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gate_logits_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;   // per template instance
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(gate_logits_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     const unsigned grid = (unsigned)(a.row_tiles * a.col_tiles * a.splits);
     return launch_dependent(gate_logits_kernel<NT>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, s, tmX, tmW, a);
 }

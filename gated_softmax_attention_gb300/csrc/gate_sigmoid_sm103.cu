@@ -439,13 +439,12 @@ cudaError_t launch_gate_value_t(const Problem& p, const WorkspacePlan& w, char* 
     a.st = p.stats;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    static bool attr_done = false;   // per template instance
-    if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(gate_sigmoid_kernel<FN, STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;   // per template instance
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(gate_sigmoid_kernel<FN, STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    });
+    if (r != cudaSuccess) return r;
     const long tiles = (long)a.row_tiles * ((cols + 511) / 512);
     return launch_dependent(gate_sigmoid_kernel<FN, STATS>, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX,
                             tmW, tmG, a);

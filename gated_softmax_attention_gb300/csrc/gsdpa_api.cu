@@ -27,7 +27,6 @@ std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 // is a pure function of the problem (152 SMs on GB300; a little headroom).
 constexpr int kPlanSms = 160;
 
-constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool ready = false;
     int num_sms = 0;
@@ -196,6 +195,21 @@ __global__ void stats_zero_kernel(unsigned long long* __restrict__ out, int n) {
     pdl_trigger();
     pdl_wait();
     for (int k = threadIdx.x; k < n; k += blockDim.x) out[k] = 0;
+}
+
+// Zeroes the attention kernel's per-call state when no gate kernel runs first
+// in the call (the gate kernels do it otherwise). A programmatic dependent of
+// the kernel before it on the stream, which may be the previous call's
+// attention kernel still using this state: it waits for that kernel to
+// complete, zeroes, and only then lets its own dependent, the attention
+// kernel, start (whose set-up thus overlaps this launch instead of following
+// a memset node).
+__global__ void state_zero_kernel(int* __restrict__ p, int n) {
+    pdl_wait();
+    for (int k = threadIdx.x; k < n; k += blockDim.x) p[k] = 0;
+    __threadfence();
+    __syncthreads();
+    pdl_trigger();
 }
 
 __global__ void sink_finalize_kernel(const float* __restrict__ part, float* __restrict__ sink, int n, int tiles,
@@ -431,7 +445,7 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
         // The per-call state of the attention kernel (the prefill kernel's unit
         // counter and share words, the decode kernel's split counters) is zeroed
         // by the gate kernel that runs first, before it lets the attention kernel
-        // start; without a gate kernel, by a memset.
+        // start; without a gate kernel, by state_zero_kernel in the same way.
         const bool decode = decode_supported(p);
         ZeroJob zero;
         if (decode) {
@@ -456,7 +470,8 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
         if (decode) {
             if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s, gate_launched);
         } else {
-            if (e == cudaSuccess && zero.n > 0) e = cudaMemsetAsync(zero.p, 0, sizeof(int) * (size_t)zero.n, s);
+            if (e == cudaSuccess && zero.n > 0)
+                e = launch_dependent(state_zero_kernel, dim3(1), dim3(256), 0, s, zero.p, zero.n);
             // (the prefill kernel also finishes the first-token share)
             if (e == cudaSuccess) e = launch_prefill_bf16(p, w, ws, rt, s);
         }

@@ -1,8 +1,10 @@
 // gsdpa_internal.h -- host-side launch interfaces shared by the .cu files of
 // libgsdpa.so. Not part of the public ABI (include/gsdpa.h is).
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -200,6 +202,39 @@ void set_sink_args(const Problem& p, const WorkspacePlan& w, char* ws, int n_qti
 // stream: it may be scheduled once every CTA of that kernel has signalled
 // (griddepcontrol.launch_dependents) or exited, and must itself wait
 // (griddepcontrol.wait) before it relies on that kernel's memory.
+// Devices one process can drive (indexes of the per-device tables).
+constexpr int kMaxDevices = 64;
+
+// One-time set-up of a kernel on each device: function attributes (dynamic
+// shared memory size) and occupancy queries belong to one device's context,
+// and one process may launch on several devices. `fn(int& value)` runs once
+// per device under a mutex (so concurrent first calls from several host
+// threads run it once) and may leave a result in `value` (e.g. the number of
+// resident CTA pairs); later calls on that device return at once with the
+// stored value. A failed set-up is retried on the next call.
+struct PerDeviceSetup {
+    std::mutex mu;
+    std::atomic<bool> done[kMaxDevices] = {};
+    int value[kMaxDevices] = {};
+};
+template <typename F>
+cudaError_t setup_once_per_device(PerDeviceSetup& st, F&& fn, int* value = nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!st.done[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(st.mu);
+        if (!st.done[dev].load(std::memory_order_relaxed)) {
+            e = fn(st.value[dev]);
+            if (e != cudaSuccess) return e;
+            st.done[dev].store(true, std::memory_order_release);
+        }
+    }
+    if (value) *value = st.value[dev];
+    return cudaSuccess;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                              Args... args) {

@@ -24,12 +24,13 @@ namespace {
 constexpr size_t kScratchBytes = 16u << 20;   // 16 MiB per device
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
 char* g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Host code must not use g_decode_scratch directly (that name is a host-side
 // stand-in): resolve the device address once per device, with it current.
+// The address is kept for the life of the process; a device or primary-context
+// reset would leave it stale (the header says no call may follow one).
 char* scratch_for_current_device(int* status) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -80,7 +81,10 @@ extern "C" GSDPA_API int gated_sdpa_decode_noalloc(const void* X, const void* Q,
     p.causal = 1;
     p.dtype = GSDPA_BF16;
     if (B < 0 || L_k < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return GSDPA_ERR_INVALID_ARG;
-    if (gate_mode < 0 || gate_mode > 2) return GSDPA_ERR_INVALID_ARG;
+    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_STATIC) return GSDPA_ERR_INVALID_ARG;
+    // (the head-shared and input-independent gates are valid modes of gated_sdpa_fwd
+    // that this entry point does not cover)
+    if (gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_UNSUPPORTED;
     if (gate_mode != GSDPA_GATE_NONE && (d_model < 1 || !X || !W_g)) return GSDPA_ERR_INVALID_ARG;
     if (B == 0) return GSDPA_OK;
     if (!Q || !K || !V || !O) return GSDPA_ERR_INVALID_ARG;

@@ -707,8 +707,10 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 
-    static int max_pairs = 0;  // per template instance: pairs that can be resident at once
-    if (max_pairs == 0) {
+    static PerDeviceSetup setup;   // per template instance; the value: pairs that can be resident at once
+    int max_pairs = 0;
+    const int num_sms = rt.num_sms;
+    cudaError_t r0 = setup_once_per_device(setup, [num_sms](int& resident) {
         // The register split above only fits if the launch allocates enough
         // registers per thread; refuse to launch otherwise (it would not finish).
         cudaFuncAttributes fa;
@@ -721,19 +723,23 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
         // A persistent grid must not exceed what is resident at once: pairs
         // need two SMs of one GPC, so this can be below half the SM count.
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(rt.num_sms & ~1));
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         int n = 0;
         r = cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<GATE, ADD>, &cfg);
         if (r != cudaSuccess) return r;
         if (n < 1) return cudaErrorInvalidConfiguration;
-        max_pairs = n;
-    }
+        resident = n;
+        return cudaSuccess;
+    }, &max_pairs);
+    if (r0 != cudaSuccess) return r0;
     const long units = (long)a.n_blk * p.Hq * p.B;
     const long pairs = units < max_pairs ? units : max_pairs;
-    // With a gate, the gate kernel just before this one lets it start early
-    // (programmatic dependent launch); the epilogues wait for it.
+    // The kernel just before this one in the call (a gate kernel, or the
+    // state-zeroing kernel when there is no gate) zeroes the per-call state and
+    // then lets this one start early (programmatic dependent launch); with a
+    // gate, the epilogues wait for that kernel to complete before reading it.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.blockDim = dim3(kThreads);
@@ -743,7 +749,7 @@ cudaError_t launch_pair_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = ((GATE == 1 || GATE == 2) && pdl) ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<GATE, ADD>, tmQ, tmK, tmV, a);
 }
 

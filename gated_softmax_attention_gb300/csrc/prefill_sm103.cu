@@ -665,23 +665,24 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 
-    static bool attr_done = false;  // per template instance
-    if (!attr_done) {
+    static PerDeviceSetup setup;   // per template instance
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
         // The register split above only fits if the launch allocates enough
         // registers per thread; refuse to launch otherwise (it would not finish).
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE, ADD>);
-        if (r != cudaSuccess) return r;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE, ADD>);
+        if (e != cudaSuccess) return e;
         if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
-        r = cudaFuncSetAttribute(prefill_kernel<HD, GATE, ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+        return cudaFuncSetAttribute(prefill_kernel<HD, GATE, ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     const long units = (long)a.n_pairs * p.Hq * p.B;
     const long grid = units < rt.num_sms ? units : rt.num_sms;   // persistent: one CTA per SM
-    // With a gate, the gate kernel just before this one lets it start early
-    // (programmatic dependent launch); the epilogues wait for it.
+    // The kernel just before this one in the call (a gate kernel, or the
+    // state-zeroing kernel when there is no gate) zeroes the per-call state and
+    // then lets this one start early (programmatic dependent launch); with a
+    // gate, the epilogues wait for that kernel to complete before reading it.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -691,7 +692,7 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = ((GATE == 1 || GATE == 2) && pdl) ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD>, tmQ, tmK, tmV, tmO, a);
 }
 

@@ -288,13 +288,11 @@ cudaError_t launch_proj_qkvg_bf16(const void* X, const void* W_in, void* Qo, voi
     a.zero = zero;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t r = cudaFuncSetAttribute(proj_qkvg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (r != cudaSuccess) return r;
-        attr_done = true;
-    }
+    static PerDeviceSetup setup;
+    cudaError_t r = setup_once_per_device(setup, [](int&) {
+        return cudaFuncSetAttribute(proj_qkvg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    });
+    if (r != cudaSuccess) return r;
     const long tiles = (long)a.row_tiles * ((N + 511) / 512);
     return launch_dependent(proj_qkvg_kernel, dim3((unsigned)(2 * tiles)), dim3(kThreads), kSmemBytes, s, tmX, tmW,
                             tmQ, tmK, tmV, tmG, a);

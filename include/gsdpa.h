@@ -349,16 +349,22 @@ GSDPA_API const char* gsdpa_status_string(int status);
  * holds until the process exits (see gsdpa_decode_noalloc_max_scratch()).
  *
  *   Arguments are those of gated_sdpa_fwd with L_q = 1, causal, bf16 implied.
- *   Covered shapes: d_k == 128 and H_q / H_kv a multiple of 4 (the dedicated
- *   decode kernel); others return GSDPA_ERR_UNSUPPORTED. A problem whose
- *   scratch exceeds the fixed array returns GSDPA_ERR_WORKSPACE (the size a
- *   problem needs is gsdpa_workspace_bytes(B, 1, L_k, ..., dtype = GSDPA_BF16)).
+ *   Covered gate modes: GSDPA_GATE_NONE, GSDPA_GATE_HEADWISE and
+ *   GSDPA_GATE_ELEMENTWISE (sigmoid gate); the head-shared and input-independent
+ *   modes return GSDPA_ERR_UNSUPPORTED, values outside gsdpa_gate_mode
+ *   GSDPA_ERR_INVALID_ARG. Covered shapes: d_k == 128 and H_q / H_kv a multiple
+ *   of 4 (the dedicated decode kernel); others return GSDPA_ERR_UNSUPPORTED. A
+ *   problem whose scratch exceeds the fixed array returns GSDPA_ERR_WORKSPACE
+ *   (the size a problem needs is gsdpa_workspace_bytes(B, 1, L_k, ...,
+ *   dtype = GSDPA_BF16)).
  *
  * The first call on a device resolves the array's device address (a runtime
  * query, no allocation); make that first call before any stream capture. The
- * array is shared by all calls on a device and keeps the last call's
- * contents; counters are cleared at the start of each call. Calls that overlap
- * on the device race on the array: serialise them.
+ * address is kept for the life of the process: no call may follow a
+ * cudaDeviceReset (or any reset of the device's primary context) in the same
+ * process. The array is shared by all calls on a device and keeps the last
+ * call's contents; counters are cleared at the start of each call. Calls that
+ * overlap on the device race on the array: serialise them.
  */
 GSDPA_API int gated_sdpa_decode_noalloc(const void* X, const void* Q, const void* K, const void* V,
                                         const void* W_g, void* O, float* sink,
