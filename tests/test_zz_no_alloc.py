@@ -4,15 +4,17 @@ Callers that cannot allocate device memory (code that must not make the
 device synchronise, allocator-less plugin hooks, fixed memory budgets) use
 this entry point: its scratch is a fixed array inside the library instead of
 a caller-supplied workspace. These tests call it through the C ABI and hold
-it to the same bf16 tolerance as the rest of the suite against the regular
-entry point, on two calls in a row with different inputs (the shared scratch
-keeps the previous call's contents). The file is named so that pytest
-collects it last.
+its outputs to the suite's bf16 tolerance against the float64 oracle, on
+calls in a row with different shapes and gates (the shared scratch keeps the
+previous call's contents): a gate-free call after a headwise one checks that
+the branch that clears the split counters with a memset (no gate kernel runs
+first) starts from zero. The file is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from gated_softmax_attention_gb300 import binding as gb
 from gated_softmax_attention_gb300 import build as gbuild
 from gated_softmax_attention_gb300.workloads import Workload, make_inputs
@@ -30,38 +32,32 @@ def lib():
     gb.load()
 
 
-def _close(got, ref, what):
+def _check(got, ref, what):
     g = got.double().cpu().numpy()
-    r = ref.double().cpu().numpy()
-    err = np.abs(g - r)
-    rel = err.sum() / max(np.abs(r).sum(), 1e-30)
+    err = np.abs(g - ref)
+    rel = err.sum() / max(np.abs(ref).sum(), 1e-30)
     assert err.max() <= BF16_MAX_ABS and rel <= BF16_REL_L1, f"{what}: max-abs {err.max():.3e} rel-L1 {rel:.3e}"
 
 
-def _inputs(w):
-    return {k: (v.cuda() if v is not None else None) for k, v in make_inputs(w).items()}
-
-
-def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
-    w1 = Workload("noalloc_a", "bf16", B=8, L_q=1, L_k=1000, d_model=512, H_q=16, H_kv=4, d_k=128,
-                  gate="elementwise", causal=True, seed=31)
-    w2 = Workload("noalloc_b", "bf16", B=5, L_q=1, L_k=3000, d_model=256, H_q=32, H_kv=8, d_k=128,
-                  gate="headwise", causal=True, seed=32)
-    calls = []
-    for w in (w1, w2):
-        t = _inputs(w)
-        ref, ref_sink = gb.gated_sdpa_fwd(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=w.gate, causal=True,
-                                          want_sink=True)
-        calls.append((w, t, ref, ref_sink))
+def test_noalloc_matches_the_oracle_on_calls_in_a_row():
+    ws = [Workload("noalloc_a", "bf16", B=8, L_q=1, L_k=1000, d_model=512, H_q=16, H_kv=4, d_k=128,
+                   gate="elementwise", causal=True, seed=31),
+          Workload("noalloc_b", "bf16", B=5, L_q=1, L_k=3000, d_model=256, H_q=32, H_kv=8, d_k=128,
+                   gate="headwise", causal=True, seed=32),
+          Workload("noalloc_c", "bf16", B=6, L_q=1, L_k=2500, d_model=256, H_q=16, H_kv=4, d_k=128,
+                   gate="none", causal=True, seed=33)]
+    host = [make_inputs(w) for w in ws]
+    dev = [{k: (v.cuda() if v is not None else None) for k, v in t.items()} for t in host]
     torch.cuda.synchronize()
-    # two no-alloc calls in a row, different shapes and gates: the second runs on
-    # the scratch the first one left behind
-    outs = [gb.decode_noalloc(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=w.gate, want_sink=True)
-            for (w, t, _, _) in calls]
+    # calls in a row on the one shared scratch array, each leaving its contents to the next
+    outs = [gb.decode_noalloc(d["X"], d["Q"], d["K"], d["V"], d["W_g"], gate=w.gate, want_sink=True)
+            for w, d in zip(ws, dev)]
     assert gb.check_device_error() == gb.OK
-    for (w, _, ref, ref_sink), (o, sink) in zip(calls, outs):
-        _close(o, ref, w.name)
-        assert torch.allclose(sink, ref_sink, atol=SINK_ABS), w.name
+    for w, t, (o, sink) in zip(ws, host, outs):
+        ref, p0 = oracle.gated_sdpa(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=w.gate, causal=True)
+        _check(o, ref, w.name)
+        sink_err = np.abs(sink.double().cpu().numpy() - oracle.sink_share(p0)).max()
+        assert sink_err <= SINK_ABS, f"{w.name}: first-token share {sink_err:.3e}"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
@@ -74,3 +70,14 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = gb.load().gated_sdpa_decode_noalloc(256, 256, 256, 256, 256, 256, None, B, L_k, d_model, H_q, H_kv, d_k,
                                              gb.GATE_ELEMENTWISE, None)
     assert st == gb.ERR_WORKSPACE
+
+
+def test_noalloc_reports_gate_modes_it_does_not_cover():
+    lib = gb.load()
+    args = (256, 256, 256, 256, 256, 256, None, 2, 1024, 256, 8, 2, 128)
+    # head-shared and input-independent gates: valid modes, not covered here
+    for mode in (3, 4, 5):
+        assert lib.gated_sdpa_decode_noalloc(*args, mode, None) == gb.ERR_UNSUPPORTED
+    # values outside the gate-mode enumeration
+    for mode in (-1, 6):
+        assert lib.gated_sdpa_decode_noalloc(*args, mode, None) == gb.ERR_INVALID_ARG
