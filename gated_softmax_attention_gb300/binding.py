@@ -152,6 +152,20 @@ def gated_sdpa_fwd_train_save_gate(X, Q, K, V, W_g, *, causal=True, out=None, si
     return O, sink, lse, gate_out
 
 
+def _workspace(workspace, need, device):
+    """(pointer, size in bytes) of the call's workspace: the caller's tensor,
+    whose real size is passed so that the library can reject one too small,
+    or a new one of the size the problem needs."""
+    import torch
+    if workspace is None:
+        if need <= 0:
+            return None, 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("the workspace must be a contiguous CUDA tensor")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, stream, gate_out=None):
     import torch
     if Q.dtype == torch.bfloat16:
@@ -173,13 +187,12 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
     if sink is None and want_sink:
         sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
     need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, sink is not None, dtype)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    workspace, ws_bytes = _workspace(workspace, need, Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
     args = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V),
             _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink)]
     tail = [B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
-            _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)]
+            _ptr(workspace), ws_bytes, ctypes.c_void_p(s.cuda_stream)]
     if gate_out is not None:
         st = int(load().gated_sdpa_fwd_train_save_gate(*args, _ptr(lse), _ptr(gate_out), *tail))
         where = "gated_sdpa_fwd_train_save_gate"
@@ -236,13 +249,12 @@ def gated_sdpa_fwd_variant(X, Q, K, V, W_g=None, *, gate="elementwise", gate_fn=
     if sink is None and want_sink:
         sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
     need = workspace_bytes_variant(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, gate_fn, sink is not None, dtype)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    workspace, ws_bytes = _workspace(workspace, need, Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
     st = int(load().gated_sdpa_fwd_variant(
         _ptr(X) if reads_x else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), _ptr(sink),
         B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, fn, float(eps), int(bool(causal)), dtype,
-        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+        _ptr(workspace), ws_bytes, ctypes.c_void_p(s.cuda_stream)))
     if st != OK:
         raise GsdpaError(st, "gated_sdpa_fwd_variant")
     return out, sink
@@ -265,13 +277,12 @@ def gated_sdpa_fwd_stats(X, Q, K, V, W_g, *, gate="elementwise", causal=True, n_
         out = torch.empty_like(Q)
     st = torch.empty(3 + n_bins, dtype=torch.int64, device=Q.device)
     need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, False, dtype)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    workspace, ws_bytes = _workspace(workspace, need, Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
     status = int(load().gated_sdpa_fwd_stats(
         _ptr(X), _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), None, _ptr(st), int(n_bins), float(threshold),
         B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
-        _ptr(workspace) if need > 0 else None, need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)))
+        _ptr(workspace), ws_bytes, ctypes.c_void_p(s.cuda_stream)))
     if status != OK:
         raise GsdpaError(status, "gated_sdpa_fwd_stats")
     h = st.cpu().tolist()
@@ -299,12 +310,11 @@ def gated_attention_layer(X, W_in, W_O, *, H_q, H_kv, d_k=128, gate="elementwise
     if out is None:
         out = torch.empty_like(X)
     need = layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, gate)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    workspace, ws_bytes = _workspace(workspace, need, X.device)
     s = stream if stream is not None else torch.cuda.current_stream()
     st = int(load().gated_attention_layer(_ptr(X), _ptr(W_in), _ptr(W_O), _ptr(out), B, L, d_model, H_q, H_kv, d_k,
                                           GATE_CODES[gate], int(bool(causal)),
-                                          _ptr(workspace) if need > 0 else None, need if need > 0 else 0,
+                                          _ptr(workspace), ws_bytes,
                                           ctypes.c_void_p(s.cuda_stream)))
     if st != OK:
         raise GsdpaError(st, "gated_attention_layer")
@@ -337,14 +347,13 @@ def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=Tr
         out["dX"] = torch.empty_like(X)
         out["dW_g"] = torch.empty_like(W_g)
     need = bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    workspace, ws_bytes = _workspace(workspace, need, Q.device)
     s = stream if stream is not None else torch.cuda.current_stream()
     head = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
             _ptr(O), _ptr(dO), _ptr(lse)]
     rest = [_ptr(out.get("dX")), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), _ptr(out.get("dW_g")), B, L_q,
-            L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16, _ptr(workspace) if need > 0 else None,
-            need if need > 0 else 0, ctypes.c_void_p(s.cuda_stream)]
+            L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16, _ptr(workspace),
+            ws_bytes, ctypes.c_void_p(s.cuda_stream)]
     if gate_saved is not None:
         if not (gate_saved.is_cuda and gate_saved.is_contiguous() and gate_saved.dtype == torch.float16):
             raise ValueError("gate_saved must be a contiguous fp16 CUDA tensor")

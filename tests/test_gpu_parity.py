@@ -203,6 +203,22 @@ def test_workspace_too_small_is_rejected():
     assert st == gb.ERR_WORKSPACE
 
 
+def test_binding_passes_the_real_workspace_size():
+    # a caller's workspace tensor smaller than the problem needs is rejected by
+    # the library (the binding passes the tensor's own size, not the size the
+    # problem needs), before anything is enqueued
+    w = small("bf16", gate="headwise", H_q=8, H_kv=2)
+    t = make_inputs(w)
+    dev = {k: v.cuda() for k, v in t.items()}
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate, True, gb.BF16)
+    short = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gb.GsdpaError) as ei:
+        gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate, causal=True,
+                          want_sink=True, workspace=short)
+    assert ei.value.status == gb.ERR_WORKSPACE
+    assert gb.check_device_error() == gb.OK
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled rows
 
 def sample_rows(w: Workload, n, seed=0):
