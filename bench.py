@@ -10,7 +10,12 @@ attention kernel -- head map and schedule, S = QK^T, online softmax, PV, the
 gate-multiply epilogue -- and the first-token share.
 The same run also times the decode workload (bf16, 64 single-query rows
 against an 8192-token cache, GQA 32/8, elementwise gate) and reports it under
-"decode" in GB/s, since the metric names both.
+"decode" in GB/s, since the metric names both; the other configurations of
+the metric (GQA headwise L4096, long-context GQA headwise L32768 with
+sink-like keys, the float32 parity case) under "configs"; the layer as
+unfused torch GPU ops under "unfused_context_ms" (context only); and, last in
+the line, a compact "summary" of every configuration's time and fraction of
+the measured peak.
 
 Timing: W untimed warm-up steps, then exactly K back-to-back steps bracketed
 by a barrier and a device synchronise and timed with one pair of CUDA events
@@ -53,6 +58,8 @@ def parse():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the GQA, long-context and float32 configurations")
+    ap.add_argument("--no-unfused", action="store_true", help="skip the unfused torch context leg")
     ap.add_argument("--profile-backward", action="store_true",
                     help="with --profile-workload: the training forward once, then --profile-calls backward calls")
     ap.add_argument("--decode-steps", type=int, default=0, help="0: same as --steps, capped at 200")
@@ -478,6 +485,43 @@ def run_ours(args, d: Dist):
         out["layer"] = run_layer(args, d, torch, gb, w, stream, peaks)
         out["gpu_launches"] += out["layer"]["gpu_launches"]
 
+    # ---- the other configurations of the metric: GQA headwise L4096 and the
+    # long-context GQA headwise L32768 with sink-like keys (whole call with the
+    # first-token share, and the attention kernel alone via the gate-free call),
+    # and the float32 parity configuration (FFMA path)
+    if not args.no_configs:
+        out["configs"] = {}
+        for name in ("bf16_gqa_headwise_L4096", "bf16_gqa_headwise_sink_L32768", "f32_mha_elementwise_L128"):
+            out["configs"][name] = run_config(args, d, torch, gb, WORKLOADS[name], make_inputs, stream, peaks)
+            out["gpu_launches"] += out["configs"][name]["gpu_launches"]
+
+    # ---- unfused GPU context (not the target): torch SDPA + X W_g + sigmoid-multiply
+    if not args.no_unfused:
+        out["unfused_context_ms"] = {
+            name: run_unfused(torch, WORKLOADS[name], make_inputs, stream)
+            for name in ("bf16_mha_elementwise_L2048", "bf16_gqa_headwise_L4096", "bf16_gqa_headwise_sink_L32768",
+                         "bf16_decode_gqa_elementwise_Lk8192")}
+
+    # ---- compact summary of every configuration, last in the line (so that a
+    # reader that keeps only the end of the line still sees every number)
+    pk = peaks["bf16_tflops"]
+    summ = {"bf16_mha_elementwise_L2048": {
+        "call_ms": out["ms_per_step"], "tflops": out["value"], "frac": round(out["value"] / pk, 4),
+        "attn_kernel_ms": roofline["kernel_ms"], "attn_frac": roofline["frac"]}}
+    for name, c in out.get("configs", {}).items():
+        summ[name] = {k: c[k] for k in ("call_ms", "tflops", "frac", "attn_kernel_ms", "attn_frac") if k in c}
+    if "decode" in out:
+        dec = out["decode"]
+        summ[dec["workload"]] = {"call_ms": dec["ms_per_step"], "gbs": dec["value"],
+                                 "frac": dec["roofline"]["frac"]}
+    if "backward" in out:
+        summ["backward_L2048"] = {"ms": out["backward"]["ms_per_step"], "frac": out["backward"]["roofline"]["frac"]}
+    if "layer" in out:
+        summ["layer_L2048"] = {"ms": out["layer"]["ms_per_step"], "frac": out["layer"]["roofline"]["frac"]}
+    if "unfused_context_ms" in out:
+        summ["unfused_torch_ms"] = out["unfused_context_ms"]
+    out["summary"] = summ
+
     # ---- extra workloads (context only), one stderr line each
     for name in [x for x in args.extra.split(",") if x]:
         wx = WORKLOADS[name]
@@ -491,6 +535,79 @@ def run_ours(args, d: Dist):
               file=sys.stderr)
         del hx, Ox
     return out
+
+
+def run_config(args, d, torch, gb, w, make_inputs, stream, peaks):
+    """One configuration of the metric, timed like the headline: CUDA graphs of
+    consecutive calls (inputs rotated past L2 where they fit in it), the call
+    with the first-token share and, for bf16, the same call without a gate
+    (the attention kernel alone, against the attention FLOPs)."""
+    host = make_inputs(w)
+    dev0 = {k: (v.cuda() if v is not None else None) for k, v in host.items()}
+    in_bytes = sum(v.numel() * v.element_size() for v in dev0.values() if v is not None)
+    R = n_rotating_sets(in_bytes)
+    sets = [dev0] + [{k: (v.clone() if v is not None else None) for k, v in dev0.items()} for _ in range(R - 1)]
+    outs = [torch.empty_like(dev0["Q"]) for _ in range(R)]
+    sink = torch.empty((w.B, w.H_q), dtype=torch.float32, device="cuda")
+    dtype = gb.BF16 if w.dtype == "bf16" else gb.F32
+    need = gb.workspace_bytes(w.B, w.L_q, w.L_k, w.d_model, w.H_q, w.H_kv, w.d_k, w.gate, True, dtype)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def call(k, gate=w.gate, want_sink=True):
+        dv = sets[k % R]
+        gb.gated_sdpa_fwd(dv["X"], dv["Q"], dv["K"], dv["V"], dv["W_g"] if gate != "none" else None, gate=gate,
+                          causal=w.causal, out=outs[k % R], sink=sink if want_sink else None, workspace=ws)
+
+    # about 50 ms of calls per timing (at least 5)
+    K = max(5, min(args.steps, int(0.05 / max(w.flops() / 1.2e15, 1e-6))))
+    d.barrier()
+    ms = time_steps(torch, capture_steps(torch, call, R), K, args.warmup, stream)
+    res = {"workload": w.name, "dtype": w.dtype, "call_ms": round(ms, 5), "steps": K,
+           "tflops": round(w.flops() / ms / 1e9, 2), "flops_per_call": w.flops()}
+    launches = K * (2 if w.dtype == "bf16" else 2)
+    if w.dtype == "bf16":
+        res["frac"] = round(w.flops() / ms / 1e9 / peaks["bf16_tflops"], 4)
+        ms_none = time_steps(torch, capture_steps(torch, lambda k: call(k, gate="none", want_sink=False), R), K,
+                             args.warmup, stream)
+        res["attn_kernel_ms"] = round(ms_none, 5)
+        res["attn_tflops"] = round(w.attn_flops() / ms_none / 1e9, 2)
+        res["attn_frac"] = round(w.attn_flops() / ms_none / 1e9 / peaks["bf16_tflops"], 4)
+        res["gated_vs_ungated_time_ratio"] = round(ms / ms_none, 4)
+        launches += 2 * K
+    else:
+        res["note"] = "float32 parity configuration (FFMA path, latency-bound at this size); context only"
+    res["gpu_launches"] = launches
+    res["l2"] = f"{R} rotating copies of the {in_bytes / 1e6:.0f} MB inputs"
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in {w.name}: {gb.status_string(st)}")
+    del sets, outs, ws, dev0
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_unfused(torch, w, make_inputs, stream):
+    """Context only (not the target): the gated layer as unfused torch GPU ops --
+    scaled_dot_product_attention on [B, H, L, d] views, sigmoid(X W_g) as its
+    own GEMM, and the gate multiply -- milliseconds per call (eager, events)."""
+    import torch.nn.functional as F
+    dev = {k: (v.cuda() if v is not None else None) for k, v in make_inputs(w).items()}
+    q, k, v = (dev[n].transpose(1, 2) for n in ("Q", "K", "V"))
+    # a single query row sees the whole cache (bottom-right alignment); torch's
+    # causal mask is top-left, so the decode case runs unmasked
+    causal = w.causal and w.L_q == w.L_k
+    gqa = w.H_q != w.H_kv
+
+    def call(_):
+        o = F.scaled_dot_product_attention(q, k, v, is_causal=causal, enable_gqa=gqa).transpose(1, 2)
+        g = torch.sigmoid(dev["X"] @ dev["W_g"])
+        return o * g.view(w.B, w.L_q, w.H_q, -1)
+
+    K = max(3, min(50, int(0.05 / max(w.flops() / 4e14, 1e-6))))
+    ms = time_calls(torch, call, K, 3, stream)
+    del dev, q, k, v
+    torch.cuda.empty_cache()
+    return round(ms, 4)
 
 
 def backward_flops(w):
@@ -689,8 +806,25 @@ def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):
                           sink=sink, workspace=ws, stream=stream)
 
     K = args.decode_steps or min(args.steps, 200)
+    # Each step is timed alone (an event pair around the call) after a read of
+    # 2x L2 of other data: the 2 GiB K/V sweep alone would evict W_g (32 MiB)
+    # too, but the read makes sure no input is in L2 when a call starts. (A read,
+    # not a write: dirty lines would be written back inside the next call.)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for _ in range(args.warmup):
+        flush.max()
+        step()
+    torch.cuda.synchronize()
     d.barrier()
-    ms = time_calls(torch, lambda k: step(), K, args.warmup, stream)   # 2.2 GB per step: inputs far larger than L2
+    for e0, e1 in evs:
+        flush.max()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / K
+    del flush
     st = gb.check_device_error(stream)
     if st != gb.OK:
         raise RuntimeError(f"device error in decode: {gb.status_string(st)}")
@@ -714,6 +848,7 @@ def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):
     e2e_ms = time_calls(torch, lambda k: e2e_step(), E, 2, stream)
     e2e_s = d.max(e2e_ms * E / 1e3)
     return {"workload": w.name, "value": round(gbs, 2), "unit": "GB/s", "steps": K,
+            "l2": "L2 flushed before every call (read of 2x L2); each call timed alone",
             "ms_per_step": round(s * 1e3 / K, 5), "bytes_per_step": nbytes,
             "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
