@@ -484,6 +484,11 @@ def run_ours(args, d: Dist):
     if not args.no_layer:
         out["layer"] = run_layer(args, d, torch, gb, w, stream, peaks)
         out["gpu_launches"] += out["layer"]["gpu_launches"]
+        # and on the two GQA configurations' shapes (headwise gate)
+        out["layer_configs"] = {}
+        for name in ("bf16_gqa_headwise_L4096", "bf16_gqa_headwise_sink_L32768"):
+            out["layer_configs"][name] = run_layer(args, d, torch, gb, WORKLOADS[name], stream, peaks)
+            out["gpu_launches"] += out["layer_configs"][name]["gpu_launches"]
 
     # ---- the other configurations of the metric: GQA headwise L4096 and the
     # long-context GQA headwise L32768 with sink-like keys (whole call with the
@@ -518,6 +523,8 @@ def run_ours(args, d: Dist):
         summ["backward_L2048"] = {"ms": out["backward"]["ms_per_step"], "frac": out["backward"]["roofline"]["frac"]}
     if "layer" in out:
         summ["layer_L2048"] = {"ms": out["layer"]["ms_per_step"], "frac": out["layer"]["roofline"]["frac"]}
+        for name, c in out.get("layer_configs", {}).items():
+            summ["layer_" + name.split("_")[-1]] = {"ms": c["ms_per_step"], "frac": c["roofline"]["frac"]}
     if "unfused_context_ms" in out:
         summ["unfused_torch_ms"] = out["unfused_context_ms"]
     out["summary"] = summ
@@ -757,9 +764,10 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
 
 
 def run_layer(args, d, torch, gb, w, stream, peaks):
-    """gated_attention_layer on the headline shape: X W_in (Q, K, V and the
-    gate in one GEMM), the attention, O W_O -- graph replays over rotating X
-    copies; algorithmic FLOPs of the three."""
+    """gated_attention_layer on workload w's shape: X W_in (Q, K, V and, for the
+    elementwise gate, the gate in one GEMM; the headwise gate's logits in a
+    pre-pass), the attention, O W_O -- graph replays over rotating X copies;
+    algorithmic FLOPs of the products."""
     from gated_softmax_attention_gb300.workloads import layer_weights, make_inputs
     X0 = make_inputs(w)["X"].cuda()
     W_in, W_O = layer_weights(w, device="cuda")
@@ -774,15 +782,18 @@ def run_layer(args, d, torch, gb, w, stream, peaks):
                                  causal=w.causal, out=Y, workspace=ws)
 
     graphs = capture_steps(torch, call, R)
-    K = max(3, min(args.steps, 100))
-    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
-    st = gb.check_device_error(stream)
-    if st != gb.OK:
-        raise RuntimeError(f"device error in the layer leg: {gb.status_string(st)}")
     rows = w.B * w.L_q
     proj = 2 * rows * w.d_model * W_in.shape[1]
     outp = 2 * rows * w.H_q * w.d_k * w.d_model
     flops = proj + w.attn_flops() + outp
+    K = max(3, min(args.steps, 100, int(0.05 / (flops / 1.2e15))))   # about 50 ms of calls
+    d.barrier()
+    ms = time_steps(torch, graphs, K, min(args.warmup, 5), stream)
+    st = gb.check_device_error(stream)
+    if st != gb.OK:
+        raise RuntimeError(f"device error in the layer leg: {gb.status_string(st)}")
+    del graphs, Xs, ws
+    torch.cuda.empty_cache()
     tf = flops / (ms / 1e3) / 1e12
     return {"workload": w.name, "metric": "gated attention layer TFLOP/s (bf16; X [W_Q|W_K|W_V|W_g], attention, "
                                           "O W_O)", "value": round(tf, 2), "unit": "TFLOP/s",
@@ -790,7 +801,7 @@ def run_layer(args, d, torch, gb, w, stream, peaks):
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                          "scope": "whole call (projection GEMM, attention, output GEMM)"},
-            "gpu_launches": 3 * K}
+            "gpu_launches": (4 if w.gate == "headwise" else 3) * K}
 
 
 def run_decode(args, d, torch, gb, w, make_inputs, stream, peaks):

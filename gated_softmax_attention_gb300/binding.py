@@ -301,7 +301,8 @@ def layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, gate="elementwise") -> 
 def gated_attention_layer(X, W_in, W_O, *, H_q, H_kv, d_k=128, gate="elementwise", causal=True, out=None,
                           workspace=None, stream=None):
     """The whole layer (gated_attention_layer): X [B, L, d_model] bf16, W_in
-    [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k)], W_O [H_q d_k, d_model]. Returns Y."""
+    [d_model, (H_q + 2 H_kv) d_k + G] (G = H_q d_k elementwise, H_q headwise,
+    0 without a gate), W_O [H_q d_k, d_model]. Returns Y."""
     import torch
     for t in (X, W_in, W_O):
         if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):

@@ -263,7 +263,8 @@ cudaError_t launch_gate_t(const Problem& p, const WorkspacePlan& w, char* ws, co
     const int rows = w.gate_rows, cols = w.gate_cols;
     if (!make_map2d(&tmX, p.X, (cuuint64_t)p.d_model, (cuuint64_t)rows, (cuuint64_t)p.d_model * 2, 64, 128))
         return cudaErrorInvalidValue;
-    if (!make_map2d(&tmW, p.Wg, (cuuint64_t)cols, (cuuint64_t)p.d_model, (cuuint64_t)cols * 2, 64, 64))
+    const cuuint64_t ld = (cuuint64_t)(p.wg_ld > 0 ? p.wg_ld : cols);
+    if (!make_map2d(&tmW, p.Wg, (cuuint64_t)cols, (cuuint64_t)p.d_model, ld * 2, 64, 64))
         return cudaErrorInvalidValue;
     GateArgs a;
     a.out = reinterpret_cast<float*>(ws + w.gate_part);

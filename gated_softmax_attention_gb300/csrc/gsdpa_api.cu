@@ -546,11 +546,13 @@ int plan_layer(int B, int L, int d_model, int H_q, int H_kv, int d_k, int gate_m
     p.gate_mode = gate_mode;
     p.causal = causal ? 1 : 0;
     p.dtype = GSDPA_BF16;
-    if (gate_mode != GSDPA_GATE_NONE && gate_mode != GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
+    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_INVALID_ARG;
     if (d_model < 1) return GSDPA_ERR_INVALID_ARG;
     const int st = validate_shape(p);
     if (st != GSDPA_OK) return st;
     if (d_k != 128 || d_model % 8 != 0 || d_model < 256 || (B > 0 && L < 2)) return GSDPA_ERR_UNSUPPORTED;
+    // (headwise: W_in's rows hold (H_q + 2 H_kv) d_k + H_q elements, a multiple of 8 for the tensor maps)
+    if (gate_mode == GSDPA_GATE_HEADWISE && H_q % 8 != 0) return GSDPA_ERR_UNSUPPORTED;
     lp->w = plan_workspace(p, kPlanSms);
     size_t off = lp->w.total;
     const size_t rows = (size_t)B * L;
@@ -605,15 +607,31 @@ int gated_attention_layer(const void* X, const void* W_in, const void* W_O, void
     p.V = ws + lp.v;
     p.O = ws + lp.o;
     const bool gated = gate_mode == GSDPA_GATE_ELEMENTWISE;
+    const int qkv_cols = (H_q + 2 * H_kv) * d_k;
     // 1. [Q | K | V | gate] = X W_in (zeroes the attention kernel's per-call state);
-    // 2. the attention (its gate values already in place); 3. Y = O W_O
+    // 2. the attention (its gate values already in place); 3. Y = O W_O.
+    // Headwise gate: its H_q columns of W_in are not part of the projection;
+    // the gate-logit pre-pass reads them (row length (H_q + 2 H_kv) d_k + H_q)
+    // after the projection, and the attention kernel runs as its programmatic
+    // dependent (it reads the logits only in its epilogues, after waiting for
+    // the pre-pass, which itself started only once Q, K, V were written).
     ZeroJob zero;
     zero.p = reinterpret_cast<int*>(ws + lp.w.state);
     zero.n = lp.w.state_ints;
+    const bool headwise = gate_mode == GSDPA_GATE_HEADWISE;
     cudaError_t e = launch_proj_qkvg_bf16(X, W_in, ws + lp.q, ws + lp.k, ws + lp.v, gated ? ws + lp.w.gate_sig : nullptr,
-                                          B * L, d_model, H_q, H_kv, d_k, gated, zero, rt, s);
-    // (an ordinary launch: the attention reads Q, K, V from its first step)
-    if (e == cudaSuccess) e = launch_prefill_bf16_ordered(p, lp.w, ws, rt, s);
+                                          B * L, d_model, H_q, H_kv, d_k, gated, zero, rt, s,
+                                          headwise ? qkv_cols + H_q : 0);
+    if (headwise) {
+        p.Wg = static_cast<const char*>(W_in) + (size_t)qkv_cols * 2;
+        p.wg_ld = qkv_cols + H_q;
+        bool launched = false;
+        if (e == cudaSuccess) e = launch_gate_logits_bf16(p, lp.w, ws, rt, s, &launched, ZeroJob());
+        if (e == cudaSuccess) e = launch_prefill_bf16(p, lp.w, ws, rt, s);
+    } else {
+        // (an ordinary launch: the attention reads Q, K, V from its first step)
+        if (e == cudaSuccess) e = launch_prefill_bf16_ordered(p, lp.w, ws, rt, s);
+    }
     if (e == cudaSuccess) e = launch_gemm_pair_bf16_kn(ws + lp.o, W_O, Y, B * L, d_model, H_q * d_k, rt, s);
     if (e == cudaErrorInvalidValue) return GSDPA_ERR_INVALID_ARG;
     return e == cudaSuccess ? GSDPA_OK : GSDPA_ERR_LAUNCH;

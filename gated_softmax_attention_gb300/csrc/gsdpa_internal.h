@@ -32,6 +32,7 @@ struct Problem {
     int causal;
     int dtype;       // 0 f32, 1 bf16
     int gate_fn = 0; // gsdpa_gate_fn
+    int wg_ld = 0;   // W_g row length in elements (0: its own width; the layer's W_g is a column block of W_in)
     float eps = 0.f; // RMSNorm
     GateStats stats; // gate statistics, or none
 };

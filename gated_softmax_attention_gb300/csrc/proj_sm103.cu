@@ -240,10 +240,11 @@ bool map2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, cuuint64_t 
 
 cudaError_t launch_proj_qkvg_bf16(const void* X, const void* W_in, void* Qo, void* Ko, void* Vo, void* Go, int rows,
                                   int d_model, int Hq, int Hkv, int dk, bool gated, ZeroJob zero, const Runtime& rt,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int w_ld) {
     if (rows == 0) return cudaSuccess;
     const int q_cols = Hq * dk, kv_cols = Hkv * dk;
     const int N = q_cols + 2 * kv_cols + (gated ? q_cols : 0);
+    if (w_ld <= 0) w_ld = N;   // W_in's row length (more than N when headwise gate columns follow)
     alignas(64) CUtensorMap tmX, tmW, tmQ, tmK, tmV, tmG;
     {
         const cuuint64_t d[2] = {(cuuint64_t)d_model, (cuuint64_t)rows};
@@ -258,7 +259,7 @@ cudaError_t launch_proj_qkvg_bf16(const void* X, const void* W_in, void* Qo, voi
     {
         // W viewed as (64 columns, d_model rows, N/64 column blocks)
         const cuuint64_t d[3] = {64, (cuuint64_t)d_model, (cuuint64_t)N / 64};
-        const cuuint64_t st[2] = {(cuuint64_t)N * 2, 128};
+        const cuuint64_t st[2] = {(cuuint64_t)w_ld * 2, 128};
         const cuuint32_t box[3] = {64, 64, 4};
         const cuuint32_t es[3] = {1, 1, 1};
         if (encode_tiled_fn()(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W_in), d, st, box, es,

@@ -179,7 +179,7 @@ def layer_weights(w: Workload, device="cpu"):
     g = torch.Generator(device="cpu")
     g.manual_seed(int(w.seed) + 104729)
     f = torch.float32
-    n_in = (w.H_q + 2 * w.H_kv) * w.d_k + (w.H_q * w.d_k if w.gate != "none" else 0)
+    n_in = (w.H_q + 2 * w.H_kv) * w.d_k + w.gate_cols   # the gate's columns: H_q d_k, H_q or none
     W_in = torch.randn((w.d_model, n_in), generator=g, dtype=f) / w.d_model ** 0.5
     W_O = torch.randn((w.H_q * w.d_k, w.d_model), generator=g, dtype=f) / (w.H_q * w.d_k) ** 0.5
     td = torch_dtype(w)

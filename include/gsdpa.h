@@ -220,16 +220,20 @@ GSDPA_API int gated_sdpa_fwd_stats(const void* X, const void* Q, const void* K, 
  * with the attention of gated_sdpa_fwd in between. Self-attention (L_q = L_k
  * = L) without a cache.
  *   X      : device bf16 [B, L, d_model].
- *   W_in   : device bf16 [d_model, (H_q + 2 H_kv) d_k (+ H_q d_k when gated)],
- *            columns: the Q heads, the K heads, the V heads, then the
- *            elementwise gate (head-major, like gated_sdpa_fwd's W_g).
+ *   W_in   : device bf16 [d_model, (H_q + 2 H_kv) d_k + G] with G = H_q d_k
+ *            (elementwise gate), H_q (headwise gate) or 0 (no gate);
+ *            columns: the Q heads, the K heads, the V heads, then the gate's
+ *            columns (head-major, like gated_sdpa_fwd's W_g).
  *   W_O    : device bf16 [H_q d_k, d_model].
  *   Y      : device bf16 [B, L, d_model] out.
- *   gate_mode NONE or ELEMENTWISE; bf16, d_k = 128, L >= 2, d_model a
- *   multiple of 8 and >= 256 (GSDPA_ERR_UNSUPPORTED otherwise).
+ *   gate_mode NONE, HEADWISE or ELEMENTWISE (GSDPA_ERR_INVALID_ARG
+ *   otherwise); bf16, d_k = 128, L >= 2, d_model a multiple of 8 and >= 256,
+ *   H_q a multiple of 8 with the headwise gate (GSDPA_ERR_UNSUPPORTED
+ *   otherwise).
  * Q, K, V and the pre-W_O output live in the workspace (bf16), the gate as
- * fp16, as in gated_sdpa_fwd. Pointers 16-byte aligned; asynchronous on
- * `stream`; errors as for gated_sdpa_fwd.
+ * fp16 values (elementwise) or float32 logits (headwise), as in
+ * gated_sdpa_fwd. Pointers 16-byte aligned; asynchronous on `stream`; errors
+ * as for gated_sdpa_fwd.
  */
 GSDPA_API size_t gsdpa_layer_workspace_bytes(int B, int L, int d_model, int H_q, int H_kv, int d_k, int gate_mode);
 GSDPA_API int gated_attention_layer(const void* X, const void* W_in, const void* W_O, void* Y, int B, int L,

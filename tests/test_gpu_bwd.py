@@ -4,16 +4,19 @@ The GPU side runs the training forward (O and the per-row log-denominators)
 and then the backward through the C ABI; the oracle computes the exact
 gradients of the same bf16-rounded inputs.
 
-Tolerance. The gradients round P, dS, dY and the gate gradient to bf16 (8
-significant bits) before their tensor-core products and use the forward's
-bf16 output for D = sum(dO O); each rounding is 2^-9 relative. The bar is
-the layer's bf16 bar -- max-abs error 2e-2 on outputs of unit scale, mean
-relative error (relative L1, sum|gpu - ref| / sum|ref|) <= 5e-3 -- with the
-max-abs bound scaled by the tensor's size where it exceeds 1 (dK and dV sum
-over every query of a key): max-abs <= 2e-2 max(1, max|ref|). Measured:
-relative L1 2.2e-3 to 3.2e-3; at the full headline size the sampled dQ rows
-reach max-abs 9.7e-3 (the bf16 rounding of O in D shifts every dS of a row
-the same way, so it does not average out over the keys).
+Tolerance. Each gradient element is a float32-accumulated sum of products
+whose factors passed through up to four bf16 roundings (P or dS, dY or the
+gate gradient, the operand of the last product, and the forward's bf16
+output in D = sum(dO O)), each 2^-9 relative. These errors are relative to
+the terms, so a gradient's error scales with its magnitude, and magnitudes
+grow with the fan-in: dK and dV sum over every query of a key, dW_g over every
+token. The bar is therefore relative L1 <= 5e-3 (as for the forward) and
+max-abs <= 2e-2 max(1, max|ref|): four roundings give 4 * 2^-9 = 7.8e-3 of
+the tensor's scale, with a 2.5x margin, which is the forward's unscaled 2e-2
+on any tensor of unit scale or less. Measured max-abs / max|ref|: 2.6e-3 to
+4.4e-3 (each case prints its numbers); at the full headline size the sampled
+dQ rows reach max-abs 9.7e-3 (the bf16 rounding of O in D shifts every dS of
+a row the same way, so it does not average out over the keys).
 """
 import numpy as np
 import pytest
@@ -62,7 +65,8 @@ def _check(name, got, ref):
     err = np.abs(got - ref)
     rel = err.sum() / max(np.abs(ref).sum(), 1e-30)
     scale = max(1.0, float(np.abs(ref).max()))
-    print(f"{name}: rel-L1 {rel:.2e}  max-abs {err.max():.2e}  max|ref| {np.abs(ref).max():.2e}")
+    print(f"{name}: rel-L1 {rel:.2e}  max-abs {err.max():.2e}  max|ref| {np.abs(ref).max():.2e}  "
+          f"ratio {err.max() / max(float(np.abs(ref).max()), 1e-30):.2e}")
     assert rel <= BWD_REL_L1, f"{name}: rel-L1 {rel:.3e}"
     assert err.max() <= BWD_MAX_ABS * scale, f"{name}: max-abs {err.max():.3e} vs bar {BWD_MAX_ABS * scale:.3e}"
 

@@ -3,10 +3,11 @@ GEMM for Q, K, V and the gate, the attention, the output-projection GEMM)
 against the oracle's layer (numpy projections around the pinned attention
 oracle).
 
-Bar: the layer's bf16 bar (relative L1 <= 5e-3; max-abs 2e-2 on outputs of
-unit scale, scaled by max(1, max|ref|)). Beyond the attention's own rounding,
-Q, K, V and the attention output are rounded to bf16 and the gate to fp16
-before the next product (2^-9 and 2^-11 relative)."""
+Bar: the layer's bf16 bar, unscaled: relative L1 <= 5e-3 and max-abs
+error <= 2e-2 (the outputs reach |Y| ~ 4; measured max-abs 6e-3 to 9e-3).
+Beyond the attention's own rounding, Q, K, V and the attention output are
+rounded to bf16 and the gate to fp16 before the next product (2^-9 and 2^-11
+relative)."""
 import numpy as np
 import pytest
 import torch
@@ -39,16 +40,17 @@ def _w(**kw):
 def _check(what, got, ref):
     err = np.abs(got - ref)
     rel = err.sum() / np.abs(ref).sum()
-    scale = max(1.0, float(np.abs(ref).max()))
     print(f"{what}: rel-L1 {rel:.2e} max-abs {err.max():.2e} max|ref| {np.abs(ref).max():.2e}")
     assert rel <= REL_L1, f"{what}: rel-L1 {rel:.3e}"
-    assert err.max() <= MAX_ABS * scale, f"{what}: max-abs {err.max():.3e}"
+    assert err.max() <= MAX_ABS, f"{what}: max-abs {err.max():.3e}"
 
 
-CASES = [_w(), _w(gate="none", seed=62), _w(causal=False, seed=63), _w(H_q=8, H_kv=8, L_q=257, L_k=257, seed=64)]
+CASES = [_w(), _w(gate="none", seed=62), _w(causal=False, seed=63), _w(H_q=8, H_kv=8, L_q=257, L_k=257, seed=64),
+         _w(gate="headwise", H_q=8, H_kv=2, seed=66), _w(gate="headwise", H_q=16, H_kv=2, L_q=257, L_k=257, seed=67)]
 
 
-@pytest.mark.parametrize("w", CASES, ids=["gqa_elementwise", "no_gate", "full_mask", "mha_ragged"])
+@pytest.mark.parametrize("w", CASES, ids=["gqa_elementwise", "no_gate", "full_mask", "mha_ragged", "gqa_headwise",
+                                          "gqa_headwise_ragged"])
 def test_layer_matches_oracle(w):
     X = make_inputs(w)["X"] if w.gate != "none" else \
         make_inputs(Workload(**{**w.__dict__, "gate": "elementwise"}))["X"]
@@ -72,3 +74,18 @@ def test_layer_sampled_rows_larger():
     ref = oracle.gated_attention_layer(X, W_in, W_O, w.H_q, w.H_kv, w.d_k, rows=rows)
     got = Y.double().cpu().numpy()
     _check("rows", np.stack([got[b, i] for b, i in rows]), ref)
+
+
+def test_headwise_layer_long_keys_sampled_rows():
+    # 16384 tokens: the attention runs on CTA pairs, after the gate-logit pre-pass
+    # that reads the headwise gate's columns of W_in (row length (H_q + 2 H_kv) d_k + H_q)
+    w = _w(B=1, L_q=16384, L_k=16384, d_model=256, H_q=8, H_kv=1, gate="headwise", seed=68)
+    X = make_inputs(w)["X"]
+    W_in, W_O = layer_weights(w)
+    Y = gb.gated_attention_layer(X.cuda(), W_in.cuda(), W_O.cuda(), H_q=w.H_q, H_kv=w.H_kv, d_k=w.d_k, gate=w.gate)
+    assert gb.check_device_error() == gb.OK
+    rng = np.random.default_rng(10)
+    rows = sorted(set([(0, 0), (0, 255), (0, 256), (0, 16383)] + [(0, int(i)) for i in rng.integers(0, 16384, 12)]))
+    ref = oracle.gated_attention_layer(X, W_in, W_O, w.H_q, w.H_kv, w.d_k, gate=w.gate, rows=rows)
+    got = Y.double().cpu().numpy()
+    _check("headwise rows", np.stack([got[b, i] for b, i in rows]), ref)

@@ -53,3 +53,17 @@ def test_rows_form_equals_the_full_layer():
     rows = [(0, 0), (1, 5), (0, 3)]
     got = oracle.gated_attention_layer(X, W_in, W_O, 4, 2, 3, rows=rows)
     np.testing.assert_allclose(got, np.stack([full[b, i] for b, i in rows]), rtol=1e-13, atol=1e-13)
+
+
+def test_headwise_layer_equals_elementwise_with_each_heads_column_repeated():
+    # the headwise gate (one scalar per head and token, "GatedAttention [2025]"
+    # sec. 1.2.2) is the elementwise gate whose d_k columns of head h all equal
+    # column h: the two layers agree when W_in's gate block is widened that way
+    Hq, Hkv, dk = 4, 2, 3
+    X, W_in, W_O = _inputs(seed=4, gated=False)
+    Wg_head = np.random.default_rng(5).standard_normal((X.shape[-1], Hq))
+    head = oracle.gated_attention_layer(X, np.concatenate([W_in, Wg_head], axis=1), W_O, Hq, Hkv, dk,
+                                        gate="headwise")
+    elem = oracle.gated_attention_layer(X, np.concatenate([W_in, np.repeat(Wg_head, dk, axis=1)], axis=1), W_O,
+                                        Hq, Hkv, dk, gate="elementwise")
+    np.testing.assert_allclose(head, elem, rtol=1e-12, atol=1e-12)
