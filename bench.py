@@ -685,6 +685,7 @@ def run_backward(args, d, torch, gb, w, host, stream, peaks):
 VARIANTS = [("elementwise", "sigmoid_mul"), ("elementwise", "ns_sigmoid_mul"), ("elementwise", "sigmoid_add"),
             ("elementwise", "silu_add"), ("elementwise", "identity_add"), ("elementwise_shared", "sigmoid_mul"),
             ("headwise", "sigmoid_mul"), ("headwise_shared", "sigmoid_mul"), ("static", "sigmoid_mul"),
+            ("elementwise_averaged", "sigmoid_mul"), ("headwise_averaged", "sigmoid_mul"),
             ("none", "sigmoid_mul"), ("none", "silu_self"), ("none", "rmsnorm")]
 
 
@@ -701,7 +702,8 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
     O = torch.empty_like(dev["Q"])
     gen = torch.Generator().manual_seed(97)
     rows = w.B * w.L_q
-    cols = {"elementwise": w.H_q * w.d_k, "headwise": w.H_q, "elementwise_shared": w.d_k, "headwise_shared": 1}
+    cols = {"elementwise": w.H_q * w.d_k, "headwise": w.H_q, "elementwise_shared": w.d_k, "headwise_shared": 1,
+            "elementwise_averaged": w.H_q * w.d_k, "headwise_averaged": w.H_q}
     K = max(3, min(args.steps, 100))
     res, launches, base_ms = [], 0, None
     for gate, fn in VARIANTS:
@@ -729,7 +731,8 @@ def run_variants(args, d, torch, gb, w, host, stream, peaks):
         flops = w.attn_flops() + 2 * rows * w.d_model * cols.get(gate, 0)
         if base_ms is None:
             base_ms = ms
-        launches += (2 if gate != "none" else 1) * K
+        # (a gate pass or the state-zeroing kernel, the averaging pass of the averaged gates, the attention)
+        launches += (3 if gate.endswith("_averaged") else 2) * K
         res.append({"gate": gate, "gate_fn": fn, "ms_per_call": round(ms, 5),
                     "tflops": round(flops / (ms / 1e3) / 1e12, 2), "vs_default_call": round(ms / base_ms, 4)})
         del graphs, ws

@@ -208,7 +208,8 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
 
 
 # gate shapes and gate functions of gated_sdpa_fwd_variant (gsdpa.h)
-VARIANT_GATE_CODES = dict(GATE_CODES, headwise_shared=3, elementwise_shared=4, static=5)
+VARIANT_GATE_CODES = dict(GATE_CODES, headwise_shared=3, elementwise_shared=4, static=5, headwise_averaged=6,
+                          elementwise_averaged=7)
 GATE_FNS = {"sigmoid_mul": 0, "ns_sigmoid_mul": 1, "sigmoid_add": 2, "silu_add": 3, "identity_add": 4,
             "silu_self": 5, "rmsnorm": 6}
 

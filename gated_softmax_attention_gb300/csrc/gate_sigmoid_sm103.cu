@@ -451,6 +451,80 @@ cudaError_t launch_gate_value_t(const Problem& p, const WorkspacePlan& w, char* 
 }
 }  // namespace
 
+namespace {
+// The head-shared gate read as an average over the heads ("GatedAttention
+// [2025]", sec. 1.3.2 (ii): the n x q x d_k scores averaged over the q query
+// heads into an n x d_k score that every head uses). Both kernels run between
+// the gate kernel and the attention kernel as programmatic dependents: they
+// let the attention kernel start at once (it reads the gate only in its
+// epilogues, after waiting for this kernel) and wait for the gate kernel
+// before they read its output.
+//
+// Elementwise: g [rows, H_q d_k] fp16 values; each thread averages one row's 8
+// consecutive columns c..c+7 over the heads (16-byte loads, fp32 sums) and
+// writes the average over head 0's values (only this thread touches them).
+__global__ void gate_average_values_kernel(__half* __restrict__ g, int rows, int Hq, int dk) {
+    pdl_trigger();
+    pdl_wait();
+    const int chunks = dk / 8;
+    const long t = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (long)rows * chunks) return;
+    const long r = t / chunks;
+    const int c = (int)(t % chunks) * 8;
+    __half* row = g + r * (long)Hq * dk;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int h = 0; h < Hq; ++h) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + (long)h * dk + c);
+        const __half2* hv = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            acc[2 * e] += f.x;
+            acc[2 * e + 1] += f.y;
+        }
+    }
+    const float inv = 1.0f / (float)Hq;
+    uint4 out;
+    __half2* ho = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ho[e] = __floats2half2_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    *reinterpret_cast<uint4*>(row + c) = out;
+}
+
+// Headwise: gl [rows, H_q] fp32 logits (one split); each thread turns one
+// row's H_q logits into values f(gl_h), averages them and writes the average,
+// a value, over column 0 (the attention epilogue then applies the identity).
+__global__ void gate_average_logits_kernel(float* __restrict__ gl, int rows, int Hq, int fn) {
+    pdl_trigger();
+    pdl_wait();
+    const long r = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    float* row = gl + r * Hq;
+    float acc = 0.f;
+    for (int h = 0; h < Hq; ++h) acc += gate_value(row[h], fn);
+    row[0] = acc / (float)Hq;
+}
+}  // namespace
+
+cudaError_t launch_gate_average_bf16(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s) {
+    const int rows = p.B * p.Lq;
+    if (rows == 0) return cudaSuccess;
+    if (p.gate_mode == 7) {
+        if (p.dk % 8 != 0) return cudaErrorInvalidValue;
+        const long n = (long)rows * (p.dk / 8);
+        return launch_dependent(gate_average_values_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                                reinterpret_cast<__half*>(ws + w.gate_sig), rows, p.Hq, p.dk);
+    }
+    if (p.gate_mode == 6) {
+        if (w.gate_splits != 1) return cudaErrorInvalidValue;   // (prefill plans one split)
+        return launch_dependent(gate_average_logits_kernel, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s,
+                                reinterpret_cast<float*>(ws + w.gate_part), rows, p.Hq, p.gate_fn);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gate_sigmoid_bf16(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,
                                      cudaStream_t s, ZeroJob zero) {
     if (p.gate_mode == 5) {

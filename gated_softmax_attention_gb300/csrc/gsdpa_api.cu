@@ -61,7 +61,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int validate_shape(const Problem& p) {
     if (p.B < 0 || p.Lq < 0 || p.Lk < 1 || p.Lq > p.Lk) return GSDPA_ERR_INVALID_ARG;
     if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv != 0) return GSDPA_ERR_INVALID_ARG;
-    if (p.gate_mode < GSDPA_GATE_NONE || p.gate_mode > GSDPA_GATE_STATIC) return GSDPA_ERR_INVALID_ARG;
+    if (p.gate_mode < GSDPA_GATE_NONE || p.gate_mode > GSDPA_GATE_ELEMENTWISE_AVERAGED) return GSDPA_ERR_INVALID_ARG;
     if (p.gate_fn < GSDPA_FN_SIGMOID_MUL || p.gate_fn > GSDPA_FN_RMSNORM) return GSDPA_ERR_INVALID_ARG;
     // the functions of the output alone take no gate; a gate takes one of the five functions of its logit
     if (p.gate_mode == GSDPA_GATE_NONE && p.gate_fn != GSDPA_FN_SIGMOID_MUL && p.gate_fn < GSDPA_FN_SILU_SELF)
@@ -417,6 +417,8 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
     if ((reads_x && !aligned16(X)) || (W_g && !aligned16(W_g))) return GSDPA_ERR_ALIGNMENT;
     if (sink && (reinterpret_cast<uintptr_t>(sink) & 3u)) return GSDPA_ERR_ALIGNMENT;
     if (sink && dtype == GSDPA_BF16 && !decode_supported(p) && (long)L_q > kSinkMaxLq) return GSDPA_ERR_UNSUPPORTED;
+    // (the averaged gates are built for the prefill kernels and the float32 path)
+    if (gate_averaged(p) && dtype == GSDPA_BF16 && decode_supported(p)) return GSDPA_ERR_UNSUPPORTED;
 
     const DeviceInfo* dev = device_info();
     if (!dev) return GSDPA_ERR_LAUNCH;
@@ -473,6 +475,8 @@ int fwd_impl(const void* X, const void* Q, const void* K, const void* V, const v
             gate_launched = true;
             zero.n = 0;
         }
+        // averaged gates: the heads' values averaged in place before the attention reads them
+        if (e == cudaSuccess && gate_averaged(p)) e = launch_gate_average_bf16(p, w, ws, s);
         if (decode) {
             if (e == cudaSuccess) e = launch_decode_bf16(p, w, ws, rt, s, gate_launched);
         } else {

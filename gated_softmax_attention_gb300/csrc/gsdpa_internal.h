@@ -73,19 +73,24 @@ WorkspacePlan plan_workspace(const Problem& p, int num_sms);
 // [H_q, d_k] is not multiplied by X)
 inline int gate_cols(const Problem& p) {
     switch (p.gate_mode) {
-    case 1: return p.Hq;
-    case 2: return p.Hq * p.dk;
+    case 1: case 6: return p.Hq;
+    case 2: case 7: return p.Hq * p.dk;
     case 3: return 1;
     case 4: return p.dk;
     default: return 0;
     }
 }
 // Gate families of the bf16 kernels: one value per (row, head) from logits
-// summed in the attention epilogue (headwise, headwise shared), or one value
-// per (row, head, column) computed ahead as fp16 (elementwise, elementwise
-// shared, static).
-inline bool gate_headwise_family(const Problem& p) { return p.gate_mode == 1 || p.gate_mode == 3; }
-inline bool gate_elementwise_family(const Problem& p) { return p.gate_mode == 2 || p.gate_mode == 4 || p.gate_mode == 5; }
+// summed in the attention epilogue (headwise, headwise shared, headwise
+// averaged), or one value per (row, head, column) computed ahead as fp16
+// (elementwise, elementwise shared, static, elementwise averaged).
+inline bool gate_headwise_family(const Problem& p) { return p.gate_mode == 1 || p.gate_mode == 3 || p.gate_mode == 6; }
+inline bool gate_elementwise_family(const Problem& p) {
+    return p.gate_mode == 2 || p.gate_mode == 4 || p.gate_mode == 5 || p.gate_mode == 7;
+}
+// The gate values of every head averaged over the heads (gate modes 6, 7): a
+// pass after the gate kernel leaves the average where head 0's value was.
+inline bool gate_averaged(const Problem& p) { return p.gate_mode == 6 || p.gate_mode == 7; }
 // The attention kernels' view of the gate: the GATE template parameter
 // (0 none, 1 headwise family, 2 elementwise family, 3 SiLU of the output,
 // 4 per-head RMSNorm) and the runtime fields.
@@ -110,6 +115,11 @@ inline GateEpi gate_epi(const Problem& p) {
     case 5: g.g_rs = 0; g.g_hs = p.dk; break;
     case 1: g.l_cols = p.Hq; g.l_hs = 1; break;
     case 3: g.l_cols = 1; g.l_hs = 0; break;
+    // averaged: every head reads column 0 of its row, where the averaging pass
+    // left the average of the heads' values (the headwise one as a value, so
+    // the epilogue's function is the identity; multiplied or added as before)
+    case 6: g.l_cols = p.Hq; g.l_hs = 0; g.fn = 4; break;
+    case 7: g.g_rs = p.Hq * p.dk; g.g_hs = 0; break;
     default: break;
     }
     if (p.gate_fn == 6) g.gamma = p.Wg;
@@ -131,6 +141,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
+
+// Gate modes 6, 7: average the gate values of every head over the heads, in
+// place (the average where head 0's value was), after the gate kernel and
+// before the attention kernel, as a programmatic dependent between them
+// (gate_sigmoid_sm103.cu).
+cudaError_t launch_gate_average_bf16(const Problem& p, const WorkspacePlan& w, char* ws, cudaStream_t s);
 
 // Launchers: return cudaSuccess or the launch error. `ws` is the workspace base.
 cudaError_t launch_f32_simt(const Problem& p, const WorkspacePlan& w, char* ws, const Runtime& rt,

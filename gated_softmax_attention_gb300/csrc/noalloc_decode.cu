@@ -81,9 +81,9 @@ extern "C" GSDPA_API int gated_sdpa_decode_noalloc(const void* X, const void* Q,
     p.causal = 1;
     p.dtype = GSDPA_BF16;
     if (B < 0 || L_k < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return GSDPA_ERR_INVALID_ARG;
-    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_STATIC) return GSDPA_ERR_INVALID_ARG;
-    // (the head-shared and input-independent gates are valid modes of gated_sdpa_fwd
-    // that this entry point does not cover)
+    if (gate_mode < GSDPA_GATE_NONE || gate_mode > GSDPA_GATE_ELEMENTWISE_AVERAGED) return GSDPA_ERR_INVALID_ARG;
+    // (the head-shared, input-independent and averaged gates are valid modes of
+    // gated_sdpa_fwd_variant that this entry point does not cover)
     if (gate_mode > GSDPA_GATE_ELEMENTWISE) return GSDPA_ERR_UNSUPPORTED;
     if (gate_mode != GSDPA_GATE_NONE && (d_model < 1 || !X || !W_g)) return GSDPA_ERR_INVALID_ARG;
     if (B == 0) return GSDPA_OK;

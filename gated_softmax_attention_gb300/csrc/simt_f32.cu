@@ -93,10 +93,44 @@ gated_attn_f32_kernel(const float* __restrict__ X, const float* __restrict__ Q, 
         for (int t = 0; t < DPT; ++t) gl[t] = Wg[(long)h * DK + part + kParts * t];
     }
     // the gate's value: sigma, NS-sigmoid, sigma, SiLU or identity of the logit
+    auto value = [&](float x) {
+        const float sg = 1.f / (1.f + expf(-x));
+        return gate_fn == 1 ? 0.5f + 0.5f * sg : (gate_fn == 3 ? x * sg : (gate_fn == 4 ? x : sg));
+    };
+    if (gate_mode == 6 || gate_mode == 7) {
+        // averaged over the heads: every head's value of its own logit (headwise
+        // W_g [d_model, H_q] or elementwise [d_model, H_q*DK]), then their mean
+        float acc[DPT];
 #pragma unroll
-    for (int t = 0; t < DPT; ++t) {
-        const float sg = 1.f / (1.f + expf(-gl[t]));
-        g[t] = gate_fn == 1 ? 0.5f + 0.5f * sg : (gate_fn == 3 ? gl[t] * sg : (gate_fn == 4 ? gl[t] : sg));
+        for (int t = 0; t < DPT; ++t) acc[t] = 0.f;
+        for (int hh = 0; hh < Hq; ++hh) {
+            if (gate_mode == 7) {
+                float glh[DPT];
+#pragma unroll
+                for (int t = 0; t < DPT; ++t) glh[t] = 0.f;
+                for (int m = 0; m < d_model; ++m) {
+                    const float xv = xp[m];
+                    const float* wrow = Wg + (long)m * Hq * DK + (long)hh * DK + part;
+#pragma unroll
+                    for (int t = 0; t < DPT; ++t) glh[t] = fmaf(xv, wrow[kParts * t], glh[t]);
+                }
+#pragma unroll
+                for (int t = 0; t < DPT; ++t) acc[t] += value(glh[t]);
+            } else {
+                float a1 = 0.f;
+                for (int m = part; m < d_model; m += kParts) a1 = fmaf(xp[m], Wg[(long)m * Hq + hh], a1);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+                const float v = value(a1);
+#pragma unroll
+                for (int t = 0; t < DPT; ++t) acc[t] += v;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) g[t] = acc[t] / (float)Hq;
+    } else {
+#pragma unroll
+        for (int t = 0; t < DPT; ++t) g[t] = value(gl[t]);
     }
     const bool gated = gate_mode != 0;
     const bool add = gate_fn >= 2 && gate_fn <= 4;

@@ -155,7 +155,8 @@ def make_inputs(w: Workload, device="cpu"):
 
 def variant_weight(w: Workload, gate: str, gate_fn: str = "sigmoid_mul", device="cpu"):
     """The parameter a gate variant reads in place of W_g: the head-shared
-    gates' W_g, the input-independent gate's theta, or the RMSNorm scale gamma
+    and averaged gates' W_g (scaled so that the logits are about N(0, 1)), the
+    input-independent gate's theta, or the RMSNorm scale gamma
     (None for the gates that use the workload's own W_g, and for a variant
     without a parameter)."""
     g = torch.Generator(device="cpu")
@@ -163,6 +164,10 @@ def variant_weight(w: Workload, gate: str, gate_fn: str = "sigmoid_mul", device=
     f = torch.float32
     if gate == "headwise_shared":
         t = torch.randn((w.d_model, 1), generator=g, dtype=f) / w.d_model ** 0.5
+    elif gate == "headwise_averaged":
+        t = torch.randn((w.d_model, w.H_q), generator=g, dtype=f) / w.d_model ** 0.5
+    elif gate == "elementwise_averaged":
+        t = torch.randn((w.d_model, w.H_q * w.d_k), generator=g, dtype=f) / w.d_model ** 0.5
     elif gate == "elementwise_shared":
         t = torch.randn((w.d_model, w.d_k), generator=g, dtype=f) / w.d_model ** 0.5
     elif gate == "static":

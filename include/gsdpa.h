@@ -77,7 +77,11 @@ typedef enum {
     /* gated_sdpa_fwd_variant only: */
     GSDPA_GATE_HEADWISE_SHARED = 3,     /* W_g [d_model, 1]: one gate per token, every head */
     GSDPA_GATE_ELEMENTWISE_SHARED = 4,  /* W_g [d_model, d_k]: one gate per (token, c), every head */
-    GSDPA_GATE_STATIC = 5               /* W_g holds theta [H_q, d_k]: the gate does not read X */
+    GSDPA_GATE_STATIC = 5,              /* W_g holds theta [H_q, d_k]: the gate does not read X */
+    GSDPA_GATE_HEADWISE_AVERAGED = 6,   /* W_g [d_model, H_q]: the H_q heads' gate values averaged,
+                                           one gate per token for every head */
+    GSDPA_GATE_ELEMENTWISE_AVERAGED = 7 /* W_g [d_model, H_q d_k]: the heads' gate values averaged
+                                           over the heads, one gate per (token, c) for every head */
 } gsdpa_gate_mode;
 
 /* How the gate's logit gl acts on the SDPA output y (gated_sdpa_fwd_variant). */
@@ -166,6 +170,13 @@ GSDPA_API int gated_sdpa_fwd(const void* X, const void* Q, const void* K, const 
  *     SIGMOID_MUL .. IDENTITY_ADD;
  *   gate_mode STATIC: gl = theta[h, c] from W_g ([H_q, d_k], same dtype as
  *     the call); X is not read and may be NULL; gate_fn as above;
+ *   gate_mode HEADWISE_AVERAGED, ELEMENTWISE_AVERAGED: the head-shared gate
+ *     read as an average over the query heads (sec. 1.3.2 (ii)): the
+ *     head-specific gate values v_h = f(gl_h) of every head h (gl = X W_g as
+ *     for HEADWISE, ELEMENTWISE; f the gate_fn's function of the logit) are
+ *     averaged, vbar = (1/H_q) sum_h v_h, and every head combines the same
+ *     vbar with its y (multiplied or added as gate_fn says); prefill only
+ *     (L_q == 1 decode calls return GSDPA_ERR_UNSUPPORTED);
  *   gate_mode NONE: gate_fn SIGMOID_MUL (plain SDPA), SILU_SELF or RMSNORM
  *     (W_g = gamma [H_q, d_k] or NULL; eps >= 0 is added to the mean square).
  * Other combinations return GSDPA_ERR_INVALID_ARG. The gate's value is kept

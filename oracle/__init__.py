@@ -32,9 +32,11 @@ _lib = None
 
 GATE_NONE, GATE_HEADWISE, GATE_ELEMENTWISE = 0, 1, 2
 GATE_HEADWISE_SHARED, GATE_ELEMENTWISE_SHARED, GATE_STATIC = 3, 4, 5
+GATE_HEADWISE_AVERAGED, GATE_ELEMENTWISE_AVERAGED = 6, 7
 _GATE_CODES = {"none": GATE_NONE, "headwise": GATE_HEADWISE, "elementwise": GATE_ELEMENTWISE}
 _VARIANT_GATE_CODES = dict(_GATE_CODES, headwise_shared=GATE_HEADWISE_SHARED,
-                           elementwise_shared=GATE_ELEMENTWISE_SHARED, static=GATE_STATIC)
+                           elementwise_shared=GATE_ELEMENTWISE_SHARED, static=GATE_STATIC,
+                           headwise_averaged=GATE_HEADWISE_AVERAGED, elementwise_averaged=GATE_ELEMENTWISE_AVERAGED)
 # the gate's function of its logit and its combination with the SDPA output y,
 # or (without a gate) a function of y alone
 GATE_FNS = {"sigmoid_mul": 0, "ns_sigmoid_mul": 1, "sigmoid_add": 2, "silu_add": 3, "identity_add": 4,
@@ -157,7 +159,9 @@ def gated_sdpa_variant(X, Q, K, V, W_g, *, gate="elementwise", gate_fn="sigmoid_
 
     ``gate``: "none", "headwise" (W_g [d_model, H_q]), "elementwise"
     ([d_model, H_q*d_k]), "headwise_shared" ([d_model, 1]), "elementwise_shared"
-    ([d_model, d_k]) or "static" (W_g holds theta [H_q, d_k]; X is not read).
+    ([d_model, d_k]), "static" (W_g holds theta [H_q, d_k]; X is not read), or
+    "headwise_averaged" / "elementwise_averaged" (W_g as for "headwise" /
+    "elementwise"; every head uses the mean over the heads of their values).
     ``gate_fn``: "sigmoid_mul", "ns_sigmoid_mul", "sigmoid_add", "silu_add" or
     "identity_add" with a gate; "silu_self" or "rmsnorm" (W_g holds gamma
     [H_q, d_k], or None for 1) with ``gate == "none"``.

@@ -49,6 +49,12 @@
  *           sigmoid, added             O = y + s(gl)              (item (4b))
  *           SiLU, added                O = y + gl s(gl)           (item (5); sec. 1.4.1)
  *           identity, added            O = y + gl                 (sec. 1.4.1 (ii))
+ *   shapes averaged over the heads ("GatedAttention [2025]", sec. 1.3.2 (ii):
+ *           the n x q x d_k scores averaged over the q query heads into one
+ *           n x d_k score every head uses): headwise averaged, W_g [d_model,
+ *           H_q]; elementwise averaged, W_g [d_model, H_q*d_k]; the value is
+ *           vbar = (1/H_q) sum_h' v(gl_h') with v the function below (its
+ *           value part), combined with y as the function says.
  *   without W_g:
  *           SiLU of the output         O = y * s(y)               (sec. 1.4.1 (i))
  *           per-head RMSNorm           O = y / sqrt(mean_c y_c^2 + eps) * gamma[h, c]
@@ -92,7 +98,8 @@
 #endif
 
 enum { ORACLE_GATE_NONE = 0, ORACLE_GATE_HEADWISE = 1, ORACLE_GATE_ELEMENTWISE = 2,
-       ORACLE_GATE_HEADWISE_SHARED = 3, ORACLE_GATE_ELEMENTWISE_SHARED = 4, ORACLE_GATE_STATIC = 5 };
+       ORACLE_GATE_HEADWISE_SHARED = 3, ORACLE_GATE_ELEMENTWISE_SHARED = 4, ORACLE_GATE_STATIC = 5,
+       ORACLE_GATE_HEADWISE_AVERAGED = 6, ORACLE_GATE_ELEMENTWISE_AVERAGED = 7 };
 enum { ORACLE_FN_SIGMOID_MUL = 0, ORACLE_FN_NS_SIGMOID_MUL = 1, ORACLE_FN_SIGMOID_ADD = 2,
        ORACLE_FN_SILU_ADD = 3, ORACLE_FN_IDENTITY_ADD = 4, ORACLE_FN_SILU_SELF = 5, ORACLE_FN_RMSNORM = 6 };
 
@@ -102,8 +109,8 @@ static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 static long gate_width(int gate_mode, int Hq, int dk)
 {
     switch (gate_mode) {
-    case ORACLE_GATE_HEADWISE: return Hq;
-    case ORACLE_GATE_ELEMENTWISE: return (long)Hq * dk;
+    case ORACLE_GATE_HEADWISE: case ORACLE_GATE_HEADWISE_AVERAGED: return Hq;
+    case ORACLE_GATE_ELEMENTWISE: case ORACLE_GATE_ELEMENTWISE_AVERAGED: return (long)Hq * dk;
     case ORACLE_GATE_HEADWISE_SHARED: return 1;
     case ORACLE_GATE_ELEMENTWISE_SHARED: return dk;
     default: return 0;
@@ -116,8 +123,8 @@ static double gate_logit(const double* x, const double* Wg, int gate_mode, int d
     if (gate_mode == ORACLE_GATE_STATIC) return Wg[(long)h * dk + c];
     long col;
     switch (gate_mode) {
-    case ORACLE_GATE_HEADWISE: col = h; break;
-    case ORACLE_GATE_ELEMENTWISE: col = (long)h * dk + c; break;
+    case ORACLE_GATE_HEADWISE: case ORACLE_GATE_HEADWISE_AVERAGED: col = h; break;
+    case ORACLE_GATE_ELEMENTWISE: case ORACLE_GATE_ELEMENTWISE_AVERAGED: col = (long)h * dk + c; break;
     case ORACLE_GATE_HEADWISE_SHARED: col = 0; break;
     default: col = c; break;   /* elementwise, shared by the heads */
     }
@@ -125,6 +132,24 @@ static double gate_logit(const double* x, const double* Wg, int gate_mode, int d
     double gl = 0.0;
     for (int m = 0; m < d_model; ++m) gl += x[m] * Wg[(long)m * G + col];
     return gl;
+}
+
+/* the gate's value from its logit (the function part of gate_apply) */
+static double gate_value_of(double gl, int gate_fn)
+{
+    switch (gate_fn) {
+    case ORACLE_FN_NS_SIGMOID_MUL: return 0.5 + 0.5 * sigmoid(gl);
+    case ORACLE_FN_SILU_ADD: return gl * sigmoid(gl);
+    case ORACLE_FN_IDENTITY_ADD: return gl;
+    default: return sigmoid(gl);   /* sigmoid, multiplied or added */
+    }
+}
+
+/* the gated output from y and a gate value: added for the additive functions, else multiplied */
+static double gate_combine_value(double y, double v, int gate_fn)
+{
+    return (gate_fn == ORACLE_FN_SIGMOID_ADD || gate_fn == ORACLE_FN_SILU_ADD || gate_fn == ORACLE_FN_IDENTITY_ADD)
+               ? y + v : y * v;
 }
 
 /* the gated output from y and the gate logit */
@@ -181,7 +206,15 @@ static void oracle_row(const double* X, const double* Q, const double* K, const 
                 y += s[j] * V[(((long)b * Lk + j) * Hkv + kvh) * dk + c];
             o[c] = y;
         }
-        if (gate_mode != ORACLE_GATE_NONE) {
+        if (gate_mode == ORACLE_GATE_HEADWISE_AVERAGED || gate_mode == ORACLE_GATE_ELEMENTWISE_AVERAGED) {
+            /* every head's gate value of its own logit, averaged over the heads */
+            for (int c = 0; c < dk; ++c) {
+                double vbar = 0.0;
+                for (int hh = 0; hh < Hq; ++hh)
+                    vbar += gate_value_of(gate_logit(x, Wg, gate_mode, d_model, Hq, dk, hh, c), gate_fn);
+                o[c] = gate_combine_value(o[c], vbar / Hq, gate_fn);
+            }
+        } else if (gate_mode != ORACLE_GATE_NONE) {
             for (int c = 0; c < dk; ++c)
                 o[c] = gate_apply(o[c], gate_logit(x, Wg, gate_mode, d_model, Hq, dk, h, c), gate_fn);
         } else if (gate_fn == ORACLE_FN_SILU_SELF) {
@@ -211,7 +244,7 @@ int gsdpa_oracle_fwd_variant(const double* X, const double* Q, const double* K, 
 {
     if (B < 1 || Lq < 1 || Lk < 1 || dk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
     if (Lq > Lk) return -1;
-    if (gate_mode < ORACLE_GATE_NONE || gate_mode > ORACLE_GATE_STATIC) return -1;
+    if (gate_mode < ORACLE_GATE_NONE || gate_mode > ORACLE_GATE_ELEMENTWISE_AVERAGED) return -1;
     if (gate_fn < ORACLE_FN_SIGMOID_MUL || gate_fn > ORACLE_FN_RMSNORM) return -1;
     /* the functions of the output alone take no gate; the gates take one of the five functions of gl */
     if (gate_mode == ORACLE_GATE_NONE && gate_fn != ORACLE_FN_SIGMOID_MUL && gate_fn < ORACLE_FN_SILU_SELF) return -1;

@@ -151,7 +151,8 @@ def test_variant_validation_before_any_device_work(lib):
     assert call_variant(gate_mode=2, gate_fn=5) == gb.ERR_INVALID_ARG
     assert call_variant(gate_mode=1, gate_fn=6) == gb.ERR_INVALID_ARG
     assert call_variant(gate_mode=0, gate_fn=3) == gb.ERR_INVALID_ARG
-    assert call_variant(gate_mode=6) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=8) == gb.ERR_INVALID_ARG
+    assert call_variant(gate_mode=7, X=None) == gb.ERR_INVALID_ARG   # the averaged gates read X
     assert call_variant(gate_fn=7) == gb.ERR_INVALID_ARG
     assert call_variant(gate_mode=0, gate_fn=6, eps=-1.0) == gb.ERR_INVALID_ARG
     # the input-independent gate reads no X; RMSNorm's gamma may be absent; a shared gate reads X

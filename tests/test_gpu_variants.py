@@ -1,5 +1,7 @@
 """GPU parity of the gate variants (gated_sdpa_fwd_variant) against the float64
-oracle: every gate shape with every function of its logit, SiLU of the
+oracle: every gate shape (head-specific, head-shared, input-independent, and
+the head-shared gate read as an average of the heads' values) with every
+function of its logit, SiLU of the
 output and the per-head RMSNorm (with and without its scale), on the float32
 path, the bf16 single-CTA prefill kernel (d_k 128 and 64), the CTA-pair
 prefill kernel (sampled rows of a 16384-key case) and the decode kernel.
@@ -95,6 +97,31 @@ def test_bf16_prefill_dk64(gate, fn):
     _full(_workload("bf16", gate, d_k=64, L_q=200, L_k=260), gate, fn)
 
 
+# the head-shared gate read as an average over the heads' values
+AVG_COMBOS = [(g, f) for g in ("elementwise_averaged", "headwise_averaged") for f in GATED_FNS]
+
+
+@pytest.mark.parametrize("gate,fn", AVG_COMBOS, ids=[f"{g}-{f}" for g, f in AVG_COMBOS])
+def test_averaged_f32(gate, fn):
+    _full(_workload("f32", gate, B=1, L_q=70, L_k=90, d_model=64, H_q=4, H_kv=2, d_k=64), gate, fn)
+
+
+@pytest.mark.parametrize("gate,fn", AVG_COMBOS, ids=[f"{g}-{f}" for g, f in AVG_COMBOS])
+def test_averaged_bf16_prefill(gate, fn):
+    _full(_workload("bf16", gate), gate, fn)
+
+
+def test_averaged_bf16_decode_is_unsupported():
+    w = _workload("bf16", "elementwise_averaged", B=4, L_q=1, L_k=700)
+    t = make_inputs(w)
+    W = variant_weight(w, "elementwise_averaged").cuda()
+    with pytest.raises(gb.GsdpaError) as ei:
+        gb.gated_sdpa_fwd_variant(t["X"].cuda(), t["Q"].cuda(), t["K"].cuda(), t["V"].cuda(), W,
+                                  gate="elementwise_averaged", gate_fn="sigmoid_mul", causal=True)
+    assert ei.value.status == gb.ERR_UNSUPPORTED
+    assert gb.check_device_error() == gb.OK
+
+
 @pytest.mark.parametrize("gate,fn", COMBOS, ids=[f"{g}-{f}" for g, f in COMBOS])
 def test_bf16_decode(gate, fn):
     _full(_workload("bf16", gate, B=4, L_q=1, L_k=700), gate, fn)
@@ -102,7 +129,8 @@ def test_bf16_decode(gate, fn):
 
 PAIR_COMBOS = [("elementwise", "sigmoid_add"), ("elementwise_shared", "ns_sigmoid_mul"),
                ("headwise", "silu_add"), ("headwise_shared", "identity_add"), ("static", "sigmoid_mul"),
-               ("none", "silu_self"), ("none", "rmsnorm")]
+               ("none", "silu_self"), ("none", "rmsnorm"), ("elementwise_averaged", "sigmoid_mul"),
+               ("headwise_averaged", "silu_add")]
 
 
 @pytest.mark.parametrize("gate,fn", PAIR_COMBOS, ids=[f"{g}-{f}" for g, f in PAIR_COMBOS])

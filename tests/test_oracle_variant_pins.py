@@ -144,3 +144,51 @@ def test_default_variant_matches_the_layer():
         a = oracle.gated_sdpa_variant(X, Q, K, V, W, gate=gate)[0]
         b = oracle.gated_sdpa(X, Q, K, V, W, gate=gate)[0]
         np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------------ head-shared gates read as averages
+
+@pytest.mark.parametrize("gate", ["elementwise_averaged", "headwise_averaged"])
+@pytest.mark.parametrize("fn", ["sigmoid_mul", "ns_sigmoid_mul", "sigmoid_add", "silu_add", "identity_add"])
+def test_averaged_gate_is_the_mean_of_the_heads_values(gate, fn):
+    # "GatedAttention [2025]" sec. 1.3.2 (ii): the scores of the q heads averaged
+    # into one score every head uses. numpy: each head's value of its own logit
+    # (scipy-free: 1/(1+e^-x)), the mean over the heads, combined with the
+    # pinned ungated output.
+    X, Q, K, V, rng = _inputs(seed=11)
+    B, Lq, Hq, dk = Q.shape
+    G = Hq * dk if gate == "elementwise_averaged" else Hq
+    W = rng.standard_normal((X.shape[-1], G))
+    y = _none(X, Q, K, V, True)
+    gl = X @ W
+    gl = gl.reshape(B, Lq, Hq, dk) if gate == "elementwise_averaged" else np.broadcast_to(gl[..., None], (B, Lq, Hq, dk))
+    v = {"sigmoid_mul": _sig(gl), "ns_sigmoid_mul": 0.5 + 0.5 * _sig(gl), "sigmoid_add": _sig(gl),
+         "silu_add": gl * _sig(gl), "identity_add": gl}[fn]
+    vbar = v.mean(axis=2, keepdims=True)              # [B, Lq, 1, dk]: every head the same
+    ref = y + vbar if fn in ("sigmoid_add", "silu_add", "identity_add") else y * vbar
+    got = oracle.gated_sdpa_variant(X, Q, K, V, W, gate=gate, gate_fn=fn)[0]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_averaged_gate_with_equal_heads_is_the_head_specific_gate():
+    # when every head has the same gate columns, the average is each head's own value
+    X, Q, K, V, rng = _inputs(seed=12)
+    Hq, dk = Q.shape[2], Q.shape[3]
+    Wc = rng.standard_normal((X.shape[-1], dk))
+    We = np.tile(Wc, (1, Hq))
+    got = oracle.gated_sdpa_variant(X, Q, K, V, We, gate="elementwise_averaged")[0]
+    ref = oracle.gated_sdpa(X, Q, K, V, We, gate="elementwise")[0]
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+    Wh = np.tile(rng.standard_normal((X.shape[-1], 1)), (1, Hq))
+    got = oracle.gated_sdpa_variant(X, Q, K, V, Wh, gate="headwise_averaged")[0]
+    ref = oracle.gated_sdpa(X, Q, K, V, Wh, gate="headwise")[0]
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_averaged_gate_with_one_head_is_the_head_specific_gate():
+    X, Q, K, V, rng = _inputs(Hq=1, Hkv=1, seed=13)
+    dk = Q.shape[3]
+    W = rng.standard_normal((X.shape[-1], dk))
+    got = oracle.gated_sdpa_variant(X, Q, K, V, W, gate="elementwise_averaged")[0]
+    ref = oracle.gated_sdpa(X, Q, K, V, W, gate="elementwise")[0]
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
