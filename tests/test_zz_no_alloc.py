@@ -75,9 +75,9 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
 def test_noalloc_reports_gate_modes_it_does_not_cover():
     lib = gb.load()
     args = (256, 256, 256, 256, 256, 256, None, 2, 1024, 256, 8, 2, 128)
-    # head-shared and input-independent gates: valid modes, not covered here
-    for mode in (3, 4, 5):
+    # head-shared, input-independent and averaged gates: valid modes, not covered here
+    for mode in (3, 4, 5, 6, 7):
         assert lib.gated_sdpa_decode_noalloc(*args, mode, None) == gb.ERR_UNSUPPORTED
     # values outside the gate-mode enumeration
-    for mode in (-1, 6):
+    for mode in (-1, 8):
         assert lib.gated_sdpa_decode_noalloc(*args, mode, None) == gb.ERR_INVALID_ARG
