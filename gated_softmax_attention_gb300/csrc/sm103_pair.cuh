@@ -76,6 +76,9 @@ __device__ __forceinline__ void store_remote_u32(uint32_t addr_cluster, uint32_t
 
 // Bounded wait (see mbar_wait): on giving up it records ERR_WAIT_TIMEOUT and
 // raises the abort flag of both CTAs, so that the other CTA's waits end too.
+// The limit is checked after the first unsuccessful retry and then every 32
+// tries (each try may suspend the thread for a while), so that a wait that is
+// not over at once gives up promptly under a tiny limit.
 struct PairAbort {
     volatile int* local;   // this CTA's flag
     uint32_t peer;         // the other CTA's flag, cluster address
@@ -85,7 +88,7 @@ static __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, cons
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if ((it & 31u) == 1) {
             if (*ab.local) return false;
             if (globaltimer_ns() - t0 > ctl.limit_ns) {
                 atomicOr(ctl.err, ERR_WAIT_TIMEOUT);
@@ -105,7 +108,7 @@ static __device__ __forceinline__ bool wait_acquire_cluster(uint64_t* bar, uint3
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (try_wait_acquire_cluster(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if ((it & 31u) == 1) {
             if (*ab.local) return false;
             if (globaltimer_ns() - t0 > ctl.limit_ns) {
                 atomicOr(ctl.err, ERR_WAIT_TIMEOUT);

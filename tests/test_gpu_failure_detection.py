@@ -77,16 +77,20 @@ CASES = [
     _small("headwise", gate="headwise", H_q=8, H_kv=2),
     _small("pair_long_keys", L_q=256, L_k=16384, H_q=2, H_kv=1),
     _small("decode", B=4, L_q=1, L_k=1000, H_q=16, H_kv=4),
+    # a long gate product: the gate GEMM's epilogue waits for 128 K chunks, far
+    # longer than a wait that is checked against its limit every 32 tries
+    _small("long_gate_product", d_model=8192),
 ]
 
 
 def test_real_kernels_give_up_cleanly_with_a_tiny_limit():
-    # Each real kernel (single-CTA prefill, headwise gate, CTA pair, decode) runs
-    # once with a 1 ns wait limit, so that any wait not satisfied at once runs
-    # out: it must report OK or a timeout (never a fault), and the next call with
-    # the default limit must be exact to the bar. A wait can be satisfied on its
-    # first try, so a single kernel may report OK; at least one of the four must
-    # report the timeout, which shows that a real kernel's give-up path fired.
+    # Each real kernel (single-CTA prefill, headwise gate, CTA pair, decode, the
+    # gate GEMM) runs once with a 1 ns wait limit, so that any wait not
+    # satisfied within its first 32 tries runs out: it must report OK or a
+    # timeout (never a fault), and the next call with the default limit must be
+    # exact to the bar. Short waits are satisfied before the limit is checked,
+    # so a single kernel may report OK; at least one case must report the
+    # timeout, which shows that a real kernel's give-up path fired.
     statuses = {}
     for w in CASES:
         t = make_inputs(w)
