@@ -104,6 +104,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     pair::cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent (the backward's gate-gradient GEMMs),
+    // it reads only what kernels that completed before its predecessor started
+    // wrote; it lets the next kernel start at once, and its last CTA leaves only
+    // after the predecessor has completed, so that the grid completes after it.
+    pdl_trigger();
 
     if (warp == 0) {
         // ---- TMA producer: this CTA's rows of A and its columns of B
@@ -236,6 +241,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         tc_fence_after();
         pair::tmem_dealloc(tmem, 256 * NH);
     }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) pdl_wait();
 }
 
 // bf16 [rows][cols] (cols contiguous) as boxes of 64 columns x box_rows rows, 128B swizzle
@@ -251,7 +257,7 @@ bool map_bf16(CUtensorMap* m, const void* base, int rows, int cols, cuuint32_t b
 
 template <bool A_MN, bool B_MN, int NH>
 cudaError_t launch_t(const void* A, const void* Bm, void* Cm, int M, int N, int K, const Runtime& rt,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool pdl) {
     using C = PairGemmCfg<NH>;
     alignas(64) CUtensorMap tmA, tmB, tmC;
     if (!(A_MN ? map_bf16(&tmA, A, K, M, 64) : map_bf16(&tmA, A, M, K, 128))) return cudaErrorInvalidValue;
@@ -269,6 +275,9 @@ cudaError_t launch_t(const void* A, const void* Bm, void* Cm, int M, int N, int 
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
     const long tiles = (long)a.m_tiles * ((N + 256 * NH - 1) / (256 * NH));
+    if (pdl)
+        return launch_dependent(gemm_pair_kernel<A_MN, B_MN, NH>, dim3((unsigned)(2 * tiles)), dim3(kThreads),
+                                C::SMEM_BYTES, s, tmA, tmB, tmC, a);
     gemm_pair_kernel<A_MN, B_MN, NH><<<(unsigned)(2 * tiles), kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, tmC, a);
     return cudaGetLastError();
 }
@@ -290,8 +299,8 @@ cudaError_t launch_gemm_pair_bf16_kn(const void* A, const void* Bm, void* C, int
                                      cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (K <= 0) return cudaErrorInvalidValue;
-    return gemm_pair_nh(M, N, rt.num_sms) == 2 ? launch_t<false, true, 2>(A, Bm, C, M, N, K, rt, s)
-                                               : launch_t<false, true, 1>(A, Bm, C, M, N, K, rt, s);
+    return gemm_pair_nh(M, N, rt.num_sms) == 2 ? launch_t<false, true, 2>(A, Bm, C, M, N, K, rt, s, false)
+                                               : launch_t<false, true, 1>(A, Bm, C, M, N, K, rt, s, false);
 }
 
 cudaError_t launch_gemm_pair_bf16(const void* A, const void* Bm, void* C, int M, int N, int K, bool ab_mn,
@@ -299,10 +308,10 @@ cudaError_t launch_gemm_pair_bf16(const void* A, const void* Bm, void* C, int M,
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (K <= 0) return cudaErrorInvalidValue;
     const int nh = gemm_pair_nh(M, N, rt.num_sms);
-    if (ab_mn) return nh == 2 ? launch_t<true, true, 2>(A, Bm, C, M, N, K, rt, s)
-                              : launch_t<true, true, 1>(A, Bm, C, M, N, K, rt, s);
-    return nh == 2 ? launch_t<false, false, 2>(A, Bm, C, M, N, K, rt, s)
-                   : launch_t<false, false, 1>(A, Bm, C, M, N, K, rt, s);
+    if (ab_mn) return nh == 2 ? launch_t<true, true, 2>(A, Bm, C, M, N, K, rt, s, true)
+                              : launch_t<true, true, 1>(A, Bm, C, M, N, K, rt, s, true);
+    return nh == 2 ? launch_t<false, false, 2>(A, Bm, C, M, N, K, rt, s, true)
+                   : launch_t<false, false, 1>(A, Bm, C, M, N, K, rt, s, true);
 }
 
 }  // namespace gsdpa

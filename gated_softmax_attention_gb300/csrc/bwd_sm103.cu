@@ -33,7 +33,12 @@
 //                      GEMM of bwd_gemm_sm103.cu).
 // dQ and dK/dV recompute S and dP each (two passes instead of atomics: the
 // result does not depend on the order of the CTAs, and each pass keeps its
-// accumulators in tensor memory).
+// accumulators in tensor memory). Every kernel after the prep kernel is a
+// programmatic dependent of the one before it: dQ waits for the prep kernel
+// before it reads; dK/dV and the gate-gradient GEMMs read nothing their
+// predecessor writes, so each starts on the SMs that its predecessor's last
+// CTAs leave free, and the last CTA of each waits for its predecessor before
+// it exits, so that the call completes after all of them.
 #include "gsdpa_internal.h"
 #include "proj_internal.h"
 #include "sm103_ptx.cuh"
@@ -83,6 +88,7 @@ struct PrepArgs {
 
 // One warp per (b, h, padded row i); lane c holds columns 4c .. 4c + 3.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepArgs a) {
+    pdl_trigger();   // the dQ kernel may start its set-up; it waits for this grid before reading
     const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= (long)a.B * a.Hq * a.Lq_pad) return;
@@ -448,6 +454,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // a programmatic dependent of the prep kernel: its outputs are read only
+    // after it has completed; then the dK/dV kernel may start
+    pdl_wait();
+    pdl_trigger();
     if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 
     if (warp == 0) {
@@ -716,6 +726,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // A programmatic dependent of the dQ kernel, whose output it does not read:
+    // its inputs come from kernels that completed before the dQ kernel's CTAs
+    // let it start. It lets the next kernel start at once; its last CTA leaves
+    // only after the dQ kernel has completed, so that this grid completes after it.
+    pdl_trigger();
     if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 
     if (warp == 0) {
@@ -918,6 +933,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) pdl_wait();
 }
 
 // ------------------------------------------------------------------ GQA: sum the heads' shares
@@ -1138,13 +1154,14 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
         return r;
     });
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<<<(unsigned)((long)aa.n_qtiles * p.B * p.Hq), kAttnThreads, DqCfg::SMEM_BYTES, s>>>(
-        tmQ, tmdY, tmK, tmV, tmdQ, aa);
-    e = cudaGetLastError();
+    // dQ overlaps the prep kernel's tail (it waits for it before reading); dK/dV
+    // and the gate-gradient GEMMs read only what the prep kernel and the
+    // caller wrote, so each starts on the SMs its predecessor's tail leaves free
+    e = launch_dependent(bwd_dq_kernel, dim3((unsigned)((long)aa.n_qtiles * p.B * p.Hq)), dim3(kAttnThreads),
+                         DqCfg::SMEM_BYTES, s, tmQ, tmdY, tmK, tmV, tmdQ, aa);
     if (e != cudaSuccess) return e;
-    bwd_dkdv_kernel<<<(unsigned)((long)aa.n_ktiles * p.B * (per_head ? p.Hq : p.Hkv)), kAttnThreads,
-                      DkvCfg::SMEM_BYTES, s>>>(tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
-    e = cudaGetLastError();
+    e = launch_dependent(bwd_dkdv_kernel, dim3((unsigned)((long)aa.n_ktiles * p.B * (per_head ? p.Hq : p.Hkv))),
+                         dim3(kAttnThreads), DkvCfg::SMEM_BYTES, s, tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
     if (e != cudaSuccess) return e;
     if (per_head) {
         const long rows_kv = (long)p.B * p.Lk;

@@ -13,7 +13,10 @@ grow with the fan-in: dK and dV sum over every query of a key, dW_g over every
 token. The bar is therefore relative L1 <= 5e-3 (as for the forward) and
 max-abs <= 2e-2 max(1, max|ref|): four roundings give 4 * 2^-9 = 7.8e-3 of
 the tensor's scale, with a 2.5x margin, which is the forward's unscaled 2e-2
-on any tensor of unit scale or less. Measured max-abs / max|ref|: 2.6e-3 to
+on any tensor of unit scale or less. An unscaled 2e-2 cannot hold beyond
+unit scale whatever the arithmetic: the gradients are returned as bf16, and
+a value in [8, 16) (dK and dV reach that) is stored within half a bf16 ulp,
+2^-5 = 0.031, of itself. Measured max-abs / max|ref|: 2.6e-3 to
 4.4e-3 (each case prints its numbers); at the full headline size the sampled
 dQ rows reach max-abs 9.7e-3 (the bf16 rounding of O in D shifts every dS of
 a row the same way, so it does not average out over the keys).
