@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", default="", help="comma-separated workloads to time as extra lines on stderr")
+    ap.add_argument("--profile-layer", action="store_true",
+                    help="with --profile-workload: --profile-calls calls of the whole layer (projection, attention, W_O)")
     ap.add_argument("--profile-workload", default="",
                     help="for profilers: only run --profile-calls untimed calls of this workload and exit")
     ap.add_argument("--profile-calls", type=int, default=3)
@@ -942,7 +944,13 @@ def run_profile(args):
         for _ in range(args.profile_calls):
             gb.gated_sdpa_bwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], O, dO, lse, gate=gate,
                               causal=w.causal)
-    for _ in range(0 if args.profile_backward else args.profile_calls):
+    if args.profile_layer:
+        from gated_softmax_attention_gb300.workloads import layer_weights
+        W_in, W_O = layer_weights(w)
+        X, W_in, W_O = dev["X"], W_in.cuda(), W_O.cuda()
+        for _ in range(args.profile_calls):
+            gb.gated_attention_layer(X, W_in, W_O, H_q=w.H_q, H_kv=w.H_kv, d_k=w.d_k, gate=w.gate, causal=w.causal)
+    for _ in range(0 if (args.profile_backward or args.profile_layer) else args.profile_calls):
         gb.gated_sdpa_fwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=gate, causal=w.causal, out=O)
     st = gb.check_device_error()
     print(json.dumps({"profile_workload": w.name, "gate": gate, "calls": args.profile_calls,
