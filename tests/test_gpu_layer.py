@@ -45,12 +45,15 @@ def _check(what, got, ref):
     assert err.max() <= MAX_ABS, f"{what}: max-abs {err.max():.3e}"
 
 
+# (one head, no gate: the projection's product is 384 columns wide, so its
+# second 256-column tile holds one 128-column group and one past the end)
 CASES = [_w(), _w(gate="none", seed=62), _w(causal=False, seed=63), _w(H_q=8, H_kv=8, L_q=257, L_k=257, seed=64),
-         _w(gate="headwise", H_q=8, H_kv=2, seed=66), _w(gate="headwise", H_q=16, H_kv=2, L_q=257, L_k=257, seed=67)]
+         _w(gate="headwise", H_q=8, H_kv=2, seed=66), _w(gate="headwise", H_q=16, H_kv=2, L_q=257, L_k=257, seed=67),
+         _w(gate="none", H_q=1, H_kv=1, seed=69)]
 
 
 @pytest.mark.parametrize("w", CASES, ids=["gqa_elementwise", "no_gate", "full_mask", "mha_ragged", "gqa_headwise",
-                                          "gqa_headwise_ragged"])
+                                          "gqa_headwise_ragged", "one_head_odd_width"])
 def test_layer_matches_oracle(w):
     X = make_inputs(w)["X"] if w.gate != "none" else \
         make_inputs(Workload(**{**w.__dict__, "gate": "elementwise"}))["X"]
