@@ -66,7 +66,8 @@ def test_layer_matches_oracle(w):
 
 
 def test_layer_sampled_rows_larger():
-    # 2048 rows, d_model 1024, 8 heads: the projection takes 256 x 512 tiles over several K chunks
+    # 2048 rows, d_model 1024, 8 heads: the projection's 80 tiles of 256 x 256 run two per CTA pair (both
+    # TMEM accumulators in turn), each over several K chunks
     w = _w(B=1, L_q=2048, L_k=2048, d_model=1024, H_q=8, H_kv=2, seed=65)
     X = make_inputs(w)["X"]
     W_in, W_O = layer_weights(w)
