@@ -429,6 +429,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // mref = -inf, has all scores -inf and P = 0)
             auto exps = [&](float mref) -> float {
                 const float neg_m = (mref == -INFINITY) ? 0.f : -mref;
+                // (both exponent arguments of a column pair in one packed fused multiply-add)
+                const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
                 float2 rs[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) rs[e] = make_float2(0.f, 0.f);
@@ -437,8 +439,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][e]), sl2, neg_m));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), sl2, neg_m));
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), sl2x2, nm2);
+                        const float p0 = ex2_approx(x.x);
+                        const float p1 = ex2_approx(x.y);
                         rs[(e >> 1) & 3] = __fadd2_rn(rs[(e >> 1) & 3], make_float2(p0, p1));
                         pk[e >> 1] = pack_bf16x2(p0, p1);
                     }
@@ -600,24 +604,23 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 tmem_wait_ld();
                 uint32_t packed[8];
+                const float2 s02 = make_float2(s0, s0), s12 = make_float2(s1, s1);
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
-                    float v0 = __uint_as_float(r0[e]) * s0;
-                    float v1 = __uint_as_float(r0[e + 1]) * s0;
-                    if (has1) {
-                        v0 = fmaf(__uint_as_float(r1[e]), s1, v0);
-                        v1 = fmaf(__uint_as_float(r1[e + 1]), s1, v1);
-                    }
+                    // column pairs in packed arithmetic (the same roundings as one at a time)
+                    float2 v = __fmul2_rn(make_float2(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1])), s02);
+                    if (has1) v = __ffma2_rn(make_float2(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1])), s12, v);
                     if (GATE == 2) {
                         // columns cb*16 + e, + 1 of this half: half2 number (e/2) % 4 of uint4 cb*2 + e/8
                         const uint32_t hw = (&gq[cb * 2 + (e >> 3)].x)[(e >> 1) & 3];
                         const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
-                        v0 = gate_combine(v0, g2.x, add);
-                        v1 = gate_combine(v1, g2.y, add);
+                        v = add ? __fadd2_rn(v, g2) : __fmul2_rn(v, g2);
                     } else if (GATE == 1) {
-                        v0 = gate_combine(v0, g_head, add);
-                        v1 = gate_combine(v1, g_head, add);
-                    } else if (GATE == 3) {   // SiLU of the output
+                        const float2 g2 = make_float2(g_head, g_head);
+                        v = add ? __fadd2_rn(v, g2) : __fmul2_rn(v, g2);
+                    }
+                    float v0 = v.x, v1 = v.y;
+                    if (GATE == 3) {   // SiLU of the output
                         v0 *= sigmoid_tanh(v0);
                         v1 *= sigmoid_tanh(v1);
                     } else if (GATE == 4) {

@@ -436,7 +436,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 m = m_new;
             }
             // P = exp2(s * scale - m): packed bf16 pairs written over S_t[0, 64) for the PV MMA
-            const float neg_m = -m;
+            // (the softmax is bound by the instructions it issues: both exponent
+            // arguments of a column pair come from one packed fused multiply-add)
+            const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
             float2 rs[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) rs[e] = make_float2(0.f, 0.f);
@@ -445,8 +447,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                                                sl2x2, nm2);
+                    const float p0 = ex2_approx(x.x);
+                    const float p1 = ex2_approx(x.y);
                     rs[(e >> 1) & 3] = __fadd2_rn(rs[(e >> 1) & 3], make_float2(p0, p1));
                     pk[e >> 1] = pack_bf16x2(p0, p1);
                 }
@@ -553,20 +557,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 tmem_wait_ld();
                 uint32_t packed[16];
+                const float2 inv2 = make_float2(inv_l, inv_l);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float v0 = __uint_as_float(orr[e]) * inv_l;
-                    float v1 = __uint_as_float(orr[e + 1]) * inv_l;
+                    // column pairs in packed multiplies (the same roundings as one at a time)
+                    float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), inv2);
                     if (GATE == 2) {
                         // columns cb*32 + e, + 1: half2 number (e/2) % 4 of uint4 cb*4 + e/8
                         const uint32_t hw = (&gq[cb * 4 + (e >> 3)].x)[(e >> 1) & 3];
                         const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
-                        v0 = gate_combine(v0, g2.x, add);
-                        v1 = gate_combine(v1, g2.y, add);
+                        v = add ? __fadd2_rn(v, g2) : __fmul2_rn(v, g2);
                     } else if (GATE == 1) {
-                        v0 = gate_combine(v0, g_head, add);
-                        v1 = gate_combine(v1, g_head, add);
-                    } else if (GATE == 3) {   // SiLU of the output
+                        const float2 g2 = make_float2(g_head, g_head);
+                        v = add ? __fadd2_rn(v, g2) : __fmul2_rn(v, g2);
+                    }
+                    float v0 = v.x, v1 = v.y;
+                    if (GATE == 3) {   // SiLU of the output
                         v0 *= sigmoid_tanh(v0);
                         v1 *= sigmoid_tanh(v1);
                     } else if (GATE == 4) {
