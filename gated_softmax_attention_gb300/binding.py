@@ -112,6 +112,63 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# The library receives bare pointers and sizes: it cannot see how large a
+# buffer is. Every tensor is therefore checked here against the sizes the
+# problem implies (dtype, element count, device, contiguity) before its
+# pointer is passed, so that a wrong-shaped argument raises instead of being
+# read or written past its end.
+def _expect(t, name, numel, dtype, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's tensors on {device}")
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements (shape {tuple(t.shape)}), the problem needs {numel}")
+
+
+def _stream(stream, device):
+    """The stream to launch on: the caller's, else the current stream of the
+    device that holds the tensors (which must then be the current device)."""
+    import torch
+    if stream is None:
+        if device.index != torch.cuda.current_device():
+            raise ValueError(f"the tensors are on {device} but the current device is "
+                             f"cuda:{torch.cuda.current_device()}: pass a stream of {device}")
+        return torch.cuda.current_stream()
+    if stream.device != device:
+        raise ValueError(f"the stream belongs to {stream.device}, the tensors to {device}")
+    return stream
+
+
+def _attn_dims(Q, K, V):
+    """(B, L_q, L_k, H_q, H_kv, d_k) from Q [B, L_q, H_q, d_k] and K, V [B, L_k, H_kv, d_k]."""
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q, K and V must be 4-D: [B, L, H, d_k]")
+    B, L_q, H_q, d_k = Q.shape
+    if tuple(K.shape) != tuple(V.shape) or K.shape[0] != B or K.shape[3] != d_k:
+        raise ValueError(f"K {tuple(K.shape)} and V {tuple(V.shape)} must be [B={B}, L_k, H_kv, d_k={d_k}]")
+    return B, L_q, K.shape[1], H_q, K.shape[2], d_k
+
+
+def _x_dim(X, B, L_q):
+    """d_model of X [B, L_q, d_model] (any shape with that element count and last dimension)."""
+    if X is None or X.dim() == 0:
+        raise ValueError("X is required")
+    d_model = X.shape[-1]
+    if X.numel() != B * L_q * d_model:
+        raise ValueError(f"X {tuple(X.shape)} must hold B * L_q = {B * L_q} rows of d_model = {d_model}")
+    return d_model
+
+
+# columns of W_g [d_model, G] (or the rows x columns of a table that does not read X)
+def _gate_cols(gate_mode, H_q, d_k):
+    return {GATE_HEADWISE: H_q, GATE_ELEMENTWISE: H_q * d_k, 3: 1, 4: d_k, 6: H_q, 7: H_q * d_k}[gate_mode]
+
+
 def gated_sdpa_fwd(X, Q, K, V, W_g=None, *, gate="elementwise", causal=True, out=None, sink=None,
                    want_sink=False, workspace=None, stream=None):
     """Gated attention forward through the C ABI on torch CUDA tensors.
@@ -163,6 +220,8 @@ def _workspace(workspace, need, device):
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     if not (workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("the workspace must be a contiguous CUDA tensor")
+    if workspace.device != device:
+        raise ValueError(f"the workspace is on {workspace.device}, the call's tensors on {device}")
     return workspace, workspace.numel() * workspace.element_size()
 
 
@@ -175,20 +234,29 @@ def _fwd(X, Q, K, V, W_g, gate, causal, out, sink, want_sink, lse, workspace, st
     else:
         raise TypeError(f"unsupported dtype {Q.dtype}")
     gm = GATE_CODES[gate]
-    tensors = [Q, K, V] + ([X, W_g] if gm != GATE_NONE else [])
-    for t in tensors:
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
-            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
-    B, L_q, H_q, d_k = Q.shape
-    L_k, H_kv = K.shape[1], K.shape[2]
-    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    B, L_q, L_k, H_q, H_kv, d_k = _attn_dims(Q, K, V)
+    dev = Q.device
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _expect(t, name, t.numel(), Q.dtype, dev)
+    d_model = 0
+    if gm != GATE_NONE:
+        d_model = _x_dim(X, B, L_q)
+        _expect(X, "X", B * L_q * d_model, Q.dtype, dev)
+        _expect(W_g, "W_g", d_model * _gate_cols(gm, H_q, d_k), Q.dtype, dev)
     if out is None:
         out = torch.empty_like(Q)
+    _expect(out, "out", Q.numel(), Q.dtype, dev)
     if sink is None and want_sink:
-        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    if sink is not None:
+        _expect(sink, "sink", B * H_q, torch.float32, dev)
+    if lse is not None:
+        _expect(lse, "lse", B * H_q * L_q, torch.float32, dev)
+    if gate_out is not None:
+        _expect(gate_out, "gate_out", B * L_q * H_q * d_k, torch.float16, dev)
     need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, sink is not None, dtype)
-    workspace, ws_bytes = _workspace(workspace, need, Q.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+    workspace, ws_bytes = _workspace(workspace, need, dev)
+    s = _stream(stream, dev)
     args = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V),
             _ptr(W_g) if gm != GATE_NONE else None, _ptr(out), _ptr(sink)]
     tail = [B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
@@ -239,19 +307,29 @@ def gated_sdpa_fwd_variant(X, Q, K, V, W_g=None, *, gate="elementwise", gate_fn=
         raise TypeError(f"unsupported dtype {Q.dtype}")
     gm, fn = VARIANT_GATE_CODES[gate], GATE_FNS[gate_fn]
     reads_x = gm not in (GATE_NONE, 5)
-    for t in [Q, K, V] + ([X] if reads_x else []) + ([W_g] if W_g is not None else []):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
-            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
-    B, L_q, H_q, d_k = Q.shape
-    L_k, H_kv = K.shape[1], K.shape[2]
-    d_model = X.shape[-1] if reads_x else 0
+    B, L_q, L_k, H_q, H_kv, d_k = _attn_dims(Q, K, V)
+    dev = Q.device
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _expect(t, name, t.numel(), Q.dtype, dev)
+    d_model = 0
+    if reads_x:
+        d_model = _x_dim(X, B, L_q)
+        _expect(X, "X", B * L_q * d_model, Q.dtype, dev)
+        _expect(W_g, "W_g", d_model * _gate_cols(gm, H_q, d_k), Q.dtype, dev)
+    elif gm == 5:
+        _expect(W_g, "W_g (theta)", H_q * d_k, Q.dtype, dev)
+    elif fn == GATE_FNS["rmsnorm"] and W_g is not None:
+        _expect(W_g, "W_g (gamma)", H_q * d_k, Q.dtype, dev)
     if out is None:
         out = torch.empty_like(Q)
+    _expect(out, "out", Q.numel(), Q.dtype, dev)
     if sink is None and want_sink:
-        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    if sink is not None:
+        _expect(sink, "sink", B * H_q, torch.float32, dev)
     need = workspace_bytes_variant(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, gate_fn, sink is not None, dtype)
-    workspace, ws_bytes = _workspace(workspace, need, Q.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+    workspace, ws_bytes = _workspace(workspace, need, dev)
+    s = _stream(stream, dev)
     st = int(load().gated_sdpa_fwd_variant(
         _ptr(X) if reads_x else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), _ptr(sink),
         B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, fn, float(eps), int(bool(causal)), dtype,
@@ -268,18 +346,21 @@ def gated_sdpa_fwd_stats(X, Q, K, V, W_g, *, gate="elementwise", causal=True, n_
     import torch
     dtype = BF16 if Q.dtype == torch.bfloat16 else F32
     gm = GATE_CODES[gate]
-    for t in [X, Q, K, V, W_g]:
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == Q.dtype):
-            raise ValueError("inputs must be contiguous CUDA tensors of one dtype")
-    B, L_q, H_q, d_k = Q.shape
-    L_k, H_kv = K.shape[1], K.shape[2]
-    d_model = X.shape[-1]
+    B, L_q, L_k, H_q, H_kv, d_k = _attn_dims(Q, K, V)
+    dev = Q.device
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _expect(t, name, t.numel(), Q.dtype, dev)
+    d_model = _x_dim(X, B, L_q)
+    _expect(X, "X", B * L_q * d_model, Q.dtype, dev)
+    if gm != GATE_NONE:   # (without a gate the library rejects the call)
+        _expect(W_g, "W_g", d_model * _gate_cols(gm, H_q, d_k), Q.dtype, dev)
     if out is None:
         out = torch.empty_like(Q)
-    st = torch.empty(3 + n_bins, dtype=torch.int64, device=Q.device)
+    _expect(out, "out", Q.numel(), Q.dtype, dev)
+    st = torch.empty(3 + n_bins, dtype=torch.int64, device=dev)
     need = workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate, False, dtype)
-    workspace, ws_bytes = _workspace(workspace, need, Q.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+    workspace, ws_bytes = _workspace(workspace, need, dev)
+    s = _stream(stream, dev)
     status = int(load().gated_sdpa_fwd_stats(
         _ptr(X), _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g), _ptr(out), None, _ptr(st), int(n_bins), float(threshold),
         B, L_q, L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), dtype,
@@ -305,15 +386,21 @@ def gated_attention_layer(X, W_in, W_O, *, H_q, H_kv, d_k=128, gate="elementwise
     [d_model, (H_q + 2 H_kv) d_k + G] (G = H_q d_k elementwise, H_q headwise,
     0 without a gate), W_O [H_q d_k, d_model]. Returns Y."""
     import torch
-    for t in (X, W_in, W_O):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
-            raise ValueError("inputs must be contiguous bf16 CUDA tensors")
+    if X.dim() != 3:
+        raise ValueError("X must be [B, L, d_model]")
     B, L, d_model = X.shape
+    dev = X.device
+    gm = GATE_CODES[gate]
+    G = 0 if gm == GATE_NONE else _gate_cols(gm, H_q, d_k)
+    _expect(X, "X", X.numel(), torch.bfloat16, dev)
+    _expect(W_in, "W_in", d_model * ((H_q + 2 * H_kv) * d_k + G), torch.bfloat16, dev)
+    _expect(W_O, "W_O", H_q * d_k * d_model, torch.bfloat16, dev)
     if out is None:
         out = torch.empty_like(X)
+    _expect(out, "out", X.numel(), torch.bfloat16, dev)
     need = layer_workspace_bytes(B, L, d_model, H_q, H_kv, d_k, gate)
-    workspace, ws_bytes = _workspace(workspace, need, X.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+    workspace, ws_bytes = _workspace(workspace, need, dev)
+    s = _stream(stream, dev)
     st = int(load().gated_attention_layer(_ptr(X), _ptr(W_in), _ptr(W_O), _ptr(out), B, L, d_model, H_q, H_kv, d_k,
                                           GATE_CODES[gate], int(bool(causal)),
                                           _ptr(workspace), ws_bytes,
@@ -338,27 +425,33 @@ def gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, *, gate="elementwise", causal=Tr
     gated_sdpa_bwd_saved_gate, which does not recompute them."""
     import torch
     gm = GATE_CODES[gate]
-    for t in [Q, K, V, O, dO] + ([X, W_g] if gm != GATE_NONE else []):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
-            raise ValueError("inputs must be contiguous bf16 CUDA tensors")
-    B, L_q, H_q, d_k = Q.shape
-    L_k, H_kv = K.shape[1], K.shape[2]
-    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    B, L_q, L_k, H_q, H_kv, d_k = _attn_dims(Q, K, V)
+    dev = Q.device
+    bf = torch.bfloat16
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _expect(t, name, t.numel(), bf, dev)
+    _expect(O, "O", Q.numel(), bf, dev)
+    _expect(dO, "dO", Q.numel(), bf, dev)
+    _expect(lse, "lse", B * H_q * L_q, torch.float32, dev)
+    d_model = 0
+    if gm != GATE_NONE:
+        d_model = _x_dim(X, B, L_q)
+        _expect(X, "X", B * L_q * d_model, bf, dev)
+        _expect(W_g, "W_g", d_model * _gate_cols(gm, H_q, d_k), bf, dev)
     out = {"dQ": torch.empty_like(Q), "dK": torch.empty_like(K), "dV": torch.empty_like(V)}
     if gm != GATE_NONE:
         out["dX"] = torch.empty_like(X)
         out["dW_g"] = torch.empty_like(W_g)
     need = bwd_workspace_bytes(B, L_q, L_k, d_model, H_q, H_kv, d_k, gate)
-    workspace, ws_bytes = _workspace(workspace, need, Q.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+    workspace, ws_bytes = _workspace(workspace, need, dev)
+    s = _stream(stream, dev)
     head = [_ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
             _ptr(O), _ptr(dO), _ptr(lse)]
     rest = [_ptr(out.get("dX")), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), _ptr(out.get("dW_g")), B, L_q,
             L_k, d_model, H_q, H_kv, d_k, gm, int(bool(causal)), BF16, _ptr(workspace),
             ws_bytes, ctypes.c_void_p(s.cuda_stream)]
     if gate_saved is not None:
-        if not (gate_saved.is_cuda and gate_saved.is_contiguous() and gate_saved.dtype == torch.float16):
-            raise ValueError("gate_saved must be a contiguous fp16 CUDA tensor")
+        _expect(gate_saved, "gate_saved", B * L_q * H_q * d_k, torch.float16, dev)
         st, where = int(load().gated_sdpa_bwd_saved_gate(*head, _ptr(gate_saved), *rest)), "gated_sdpa_bwd_saved_gate"
     else:
         st, where = int(load().gated_sdpa_bwd(*head, *rest)), "gated_sdpa_bwd"
@@ -373,16 +466,26 @@ def decode_noalloc(X, Q, K, V, W_g=None, *, gate="elementwise", out=None, sink=N
     memory). Same tensors as gated_sdpa_fwd with L_q == 1."""
     import torch
     gm = GATE_CODES[gate]
-    B, L_q, H_q, d_k = Q.shape
+    B, L_q, L_k, H_q, H_kv, d_k = _attn_dims(Q, K, V)
     if L_q != 1:
         raise ValueError("decode_noalloc takes one query row per sequence")
-    L_k, H_kv = K.shape[1], K.shape[2]
-    d_model = X.shape[-1] if gm != GATE_NONE else 0
+    dev = Q.device
+    bf = torch.bfloat16
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _expect(t, name, t.numel(), bf, dev)
+    d_model = 0
+    if gm != GATE_NONE:
+        d_model = _x_dim(X, B, L_q)
+        _expect(X, "X", B * d_model, bf, dev)
+        _expect(W_g, "W_g", d_model * _gate_cols(gm, H_q, d_k), bf, dev)
     if out is None:
         out = torch.empty_like(Q)
+    _expect(out, "out", Q.numel(), bf, dev)
     if sink is None and want_sink:
-        sink = torch.empty((B, H_q), dtype=torch.float32, device=Q.device)
-    s = stream if stream is not None else torch.cuda.current_stream()
+        sink = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    if sink is not None:
+        _expect(sink, "sink", B * H_q, torch.float32, dev)
+    s = _stream(stream, dev)
     st = int(load().gated_sdpa_decode_noalloc(
         _ptr(X) if gm != GATE_NONE else None, _ptr(Q), _ptr(K), _ptr(V), _ptr(W_g) if gm != GATE_NONE else None,
         _ptr(out), _ptr(sink), B, L_k, d_model, H_q, H_kv, d_k, gm, ctypes.c_void_p(s.cuda_stream)))

@@ -263,3 +263,36 @@ def test_binding_signatures_match_the_header():
         params = params.strip()
         n = 0 if params in ("", "void") else params.count(",") + 1
         assert len(gb.SIGNATURES[name][1]) == n, name
+
+
+def test_binding_shape_helpers():
+    # the sizes the binding derives from the tensors and checks every buffer against
+    import torch
+    Q = torch.empty(2, 5, 8, 16)
+    K = torch.empty(2, 7, 4, 16)
+    assert gb._attn_dims(Q, K, K.clone()) == (2, 5, 7, 8, 4, 16)
+    with pytest.raises(ValueError):
+        gb._attn_dims(Q, K, torch.empty(2, 6, 4, 16))        # V unlike K
+    with pytest.raises(ValueError):
+        gb._attn_dims(Q, torch.empty(2, 7, 4, 8), torch.empty(2, 7, 4, 8))   # d_k unlike Q's
+    with pytest.raises(ValueError):
+        gb._attn_dims(Q, torch.empty(3, 7, 4, 16), torch.empty(3, 7, 4, 16))  # batch unlike Q's
+    assert gb._x_dim(torch.empty(2, 5, 32), 2, 5) == 32
+    assert gb._x_dim(torch.empty(10, 32), 2, 5) == 32
+    with pytest.raises(ValueError):
+        gb._x_dim(torch.empty(2, 4, 32), 2, 5)
+    assert gb._gate_cols(gb.GATE_ELEMENTWISE, 8, 16) == 128
+    assert gb._gate_cols(gb.GATE_HEADWISE, 8, 16) == 8
+    assert [gb._gate_cols(m, 8, 16) for m in (3, 4, 6, 7)] == [1, 16, 8, 128]
+
+
+def test_binding_rejects_host_tensors_before_the_library():
+    # a host tensor is refused by the binding's own checks, before any pointer
+    # reaches the library
+    import torch
+    Q = torch.empty(1, 4, 2, 64, dtype=torch.bfloat16)
+    K = torch.empty(1, 4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        gb.gated_sdpa_fwd(None, Q, K, K.clone(), None, gate="none")
+    with pytest.raises(ValueError, match="CUDA"):
+        gb.decode_noalloc(None, Q[:, :1].contiguous(), K, K.clone(), None, gate="none")

@@ -219,6 +219,55 @@ def test_binding_passes_the_real_workspace_size():
     assert gb.check_device_error() == gb.OK
 
 
+BAD_ARGS = ["headwise_W_g_for_elementwise", "X_rows", "out_shape", "sink_size", "lse_size", "K_V_mismatch",
+            "dtype", "gate_out_dtype", "bwd_dO_shape", "bwd_lse_size"]
+
+
+@pytest.mark.parametrize("bad", BAD_ARGS)
+def test_binding_rejects_wrong_sized_tensors(bad):
+    # the library receives bare pointers: the binding checks each tensor against
+    # the sizes the problem implies and raises before anything is enqueued (a
+    # headwise W_g passed to the elementwise gate would otherwise be read far
+    # past its end)
+    w = small("bf16", gate="elementwise", H_q=4, H_kv=2, L_q=200, L_k=200)
+    t = {k: v.cuda() for k, v in make_inputs(w).items()}
+    X, Q, K, V, W_g = t["X"], t["Q"], t["K"], t["V"], t["W_g"]
+    kw = {}
+    if bad == "headwise_W_g_for_elementwise":
+        W_g = W_g[:, :w.H_q].contiguous()
+    elif bad == "X_rows":
+        X = X[:, :-1].contiguous()
+    elif bad == "out_shape":
+        kw["out"] = torch.empty_like(Q[:, :-1])
+    elif bad == "sink_size":
+        kw["sink"] = torch.empty(w.B * w.H_q - 1, dtype=torch.float32, device="cuda")
+    elif bad == "lse_size":
+        kw["lse"] = torch.empty(w.B * w.H_q * w.L_q - 1, dtype=torch.float32, device="cuda")
+    elif bad == "K_V_mismatch":
+        V = V[:, :-1].contiguous()
+    elif bad == "dtype":
+        W_g = W_g.float()
+    elif bad == "gate_out_dtype":
+        kw["gate_out"] = torch.empty((w.B * w.L_q, w.H_q * w.d_k), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    with pytest.raises(ValueError):
+        if bad.startswith("bwd_"):
+            O, _, lse = gb.gated_sdpa_fwd_train(X, Q, K, V, W_g, gate=w.gate)
+            dO = torch.randn_like(O)
+            if bad == "bwd_dO_shape":
+                dO = dO[:, :-1].contiguous()
+            else:
+                lse = lse[:, :, :-1].contiguous()
+            gb.gated_sdpa_bwd(X, Q, K, V, W_g, O, dO, lse, gate=w.gate)
+        elif bad in ("lse_size",):
+            gb.gated_sdpa_fwd_train(X, Q, K, V, W_g, gate=w.gate, **kw)
+        elif bad == "gate_out_dtype":
+            gb.gated_sdpa_fwd_train_save_gate(X, Q, K, V, W_g, **kw)
+        else:
+            gb.gated_sdpa_fwd(X, Q, K, V, W_g, gate=w.gate, **kw)
+    assert gb.check_device_error() == gb.OK
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled rows
 
 def sample_rows(w: Workload, n, seed=0):
