@@ -16,7 +16,7 @@
 // Headwise gates broadcast G over d_k, so dGl sums over the head's columns.
 //
 // Kernels (all tcgen05, accumulators in TMEM, operands staged by TMA):
-//   bwd_prep_kernel    one warp per (row, head): dY, D, dGl and lse in log2
+//   bwd_prep_kernel    four (row, head) rows per warp: dY, D, dGl and lse in log2
 //                      units into padded per-(b, h) arrays (whole 128-row
 //                      tiles are 512-byte bulk copies);
 //   bwd_dq_kernel      per (b, h, 128-row query tile): S = Q K^T and
@@ -86,65 +86,115 @@ struct PrepArgs {
     int B, Lq, Hq, Lq_pad, gate_mode;
 };
 
-// One warp per (b, h, padded row i); lane c holds columns 4c .. 4c + 3.
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepArgs a) {
+// Rows are taken in memory order, r = (b L_q + i) H_q + h (so one warp's rows
+// are consecutive 256-byte rows of dO, O and the gate), kPrepRows per warp,
+// with every load of a warp's rows issued before any is used: each warp keeps
+// kPrepRows x 768 bytes in flight. Lane c holds columns 4c .. 4c + 3 of each
+// row. The warps past the real rows write the padding rows' D (0) and lse2
+// (+inf: no weight), one entry per lane.
+constexpr int kPrepRows = 4;
+
+__global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
     pdl_trigger();   // the dQ kernel may start its set-up; it waits for this grid before reading
     const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (wid >= (long)a.B * a.Hq * a.Lq_pad) return;
-    const int i = (int)(wid % a.Lq_pad);
-    const long bh = wid / a.Lq_pad;
-    const int h = (int)(bh % a.Hq);
-    const int b = (int)(bh / a.Hq);
-    if (i >= a.Lq) {   // padding rows: no weight (p = exp2(s - inf) = 0), no D
-        if (lane == 0) {
-            a.Dv[wid] = 0.f;
-            a.lse2[wid] = INFINITY;
+    const long n_rows = (long)a.B * a.Lq * a.Hq;
+    const long real_warps = (n_rows + kPrepRows - 1) / kPrepRows;
+    if (wid >= real_warps) {
+        // padding rows i in [L_q, L_q_pad) of every (b, h)
+        const int pad = a.Lq_pad - a.Lq;
+        const long k = (wid - real_warps) * 32 + lane;
+        if (pad > 0 && k < (long)a.B * a.Hq * pad) {
+            const long at = (k / pad) * a.Lq_pad + a.Lq + k % pad;
+            a.Dv[at] = 0.f;
+            a.lse2[at] = INFINITY;
         }
         return;
     }
-    const long row = (long)b * a.Lq + i;
-    const long base = (row * a.Hq + h) * HD + lane * 4;
-    float dof[4], of[4];
-    unpack_bf16x4(*reinterpret_cast<const uint2*>(a.dO + base), dof);
-    unpack_bf16x4(*reinterpret_cast<const uint2*>(a.O + base), of);
-    float g[4] = {1.f, 1.f, 1.f, 1.f};
-    if (a.gate_mode == 2) {
-        const uint2 gw = *reinterpret_cast<const uint2*>(a.gate_sig + base);
-        const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gw.x));
-        const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gw.y));
-        g[0] = g01.x;
-        g[1] = g01.y;
-        g[2] = g23.x;
-        g[3] = g23.y;
-    } else if (a.gate_mode == 1) {
-        float gl = 0.f;
-        const long rows = (long)a.B * a.Lq;
-        for (int s = 0; s < a.gate_splits; ++s) gl += a.gate_part[(s * rows + row) * a.Hq + h];
-        const float gh = 1.0f / (1.0f + exp2f(-gl * kLog2e));
-        g[0] = g[1] = g[2] = g[3] = gh;
-    }
-    float d = 0.f, dgl_h = 0.f, dgl[4];
+    const long r0 = wid * kPrepRows;
+    uint2 dow[kPrepRows], ow[kPrepRows], gw[kPrepRows];
+    float glv[kPrepRows];   // headwise: the row's logit, summed over the split-K partials
+    float lse_l = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        d = fmaf(dof[e], of[e], d);
-        dgl[e] = dof[e] * of[e] * (1.0f - g[e]);
-        dgl_h += dgl[e];
+    for (int k = 0; k < kPrepRows; ++k) {
+        const long r = r0 + k;
+        glv[k] = 0.f;
+        if (r < n_rows) {
+            const long base = r * HD + lane * 4;
+            dow[k] = *reinterpret_cast<const uint2*>(a.dO + base);
+            ow[k] = *reinterpret_cast<const uint2*>(a.O + base);
+            if (a.gate_mode == 2) gw[k] = *reinterpret_cast<const uint2*>(a.gate_sig + base);
+            if (a.gate_mode == 1)
+                for (int s = 0; s < a.gate_splits; ++s) glv[k] += a.gate_part[s * n_rows + r];
+        }
     }
-    *reinterpret_cast<uint2*>(a.dY + base) =
-        make_uint2(pack_bf16x2(dof[0] * g[0], dof[1] * g[1]), pack_bf16x2(dof[2] * g[2], dof[3] * g[3]));
-    if (a.gate_mode == 2)
-        *reinterpret_cast<uint2*>(a.dGl + base) =
-            make_uint2(pack_bf16x2(dgl[0], dgl[1]), pack_bf16x2(dgl[2], dgl[3]));
+    // lane k < kPrepRows fetches row k's lse (natural log, [B, H_q, L_q])
+    if (lane < kPrepRows && r0 + lane < n_rows) {
+        const long r = r0 + lane;
+        const int h = (int)(r % a.Hq);
+        const long bi = r / a.Hq;   // b L_q + i
+        const long b = bi / a.Lq, i = bi % a.Lq;
+        lse_l = a.lse[(b * a.Hq + h) * a.Lq + i];
+    }
+    float dsum[kPrepRows], gsum[kPrepRows];
+#pragma unroll
+    for (int k = 0; k < kPrepRows; ++k) {
+        const long r = r0 + k;
+        dsum[k] = gsum[k] = 0.f;
+        if (r >= n_rows) continue;
+        const long base = r * HD + lane * 4;
+        float dof[4], of[4];
+        unpack_bf16x4(dow[k], dof);
+        unpack_bf16x4(ow[k], of);
+        float g[4] = {1.f, 1.f, 1.f, 1.f};
+        if (a.gate_mode == 2) {
+            const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gw[k].x));
+            const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gw[k].y));
+            g[0] = g01.x;
+            g[1] = g01.y;
+            g[2] = g23.x;
+            g[3] = g23.y;
+        } else if (a.gate_mode == 1) {
+            g[0] = g[1] = g[2] = g[3] = 1.0f / (1.0f + exp2f(-glv[k] * kLog2e));
+        }
+        float dgl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            dsum[k] = fmaf(dof[e], of[e], dsum[k]);
+            dgl[e] = dof[e] * of[e] * (1.0f - g[e]);
+            gsum[k] += dgl[e];
+        }
+        *reinterpret_cast<uint2*>(a.dY + base) =
+            make_uint2(pack_bf16x2(dof[0] * g[0], dof[1] * g[1]), pack_bf16x2(dof[2] * g[2], dof[3] * g[3]));
+        if (a.gate_mode == 2)
+            *reinterpret_cast<uint2*>(a.dGl + base) =
+                make_uint2(pack_bf16x2(dgl[0], dgl[1]), pack_bf16x2(dgl[2], dgl[3]));
+    }
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) {
-        d += __shfl_xor_sync(0xffffffffu, d, sh);
-        dgl_h += __shfl_xor_sync(0xffffffffu, dgl_h, sh);
+#pragma unroll
+        for (int k = 0; k < kPrepRows; ++k) {
+            dsum[k] += __shfl_xor_sync(0xffffffffu, dsum[k], sh);
+            gsum[k] += __shfl_xor_sync(0xffffffffu, gsum[k], sh);
+        }
     }
-    if (lane == 0) {
-        a.Dv[wid] = d;
-        a.lse2[wid] = a.lse[((long)b * a.Hq + h) * a.Lq + i] * kLog2e;
-        if (a.gate_mode == 1) a.dGl[row * a.Hq + h] = __float2bfloat16_rn(dgl_h);
+    // lane k < kPrepRows writes row k's D, lse2 and (headwise) dGl
+    float d_me = dsum[0], g_me = gsum[0];
+#pragma unroll
+    for (int k = 1; k < kPrepRows; ++k)
+        if (lane == k) {
+            d_me = dsum[k];
+            g_me = gsum[k];
+        }
+    if (lane < kPrepRows && r0 + lane < n_rows) {
+        const long r = r0 + lane;
+        const int h = (int)(r % a.Hq);
+        const long bi = r / a.Hq;
+        const long b = bi / a.Lq, i = bi % a.Lq;
+        const long at = (b * a.Hq + h) * a.Lq_pad + i;
+        a.Dv[at] = d_me;
+        a.lse2[at] = lse_l * kLog2e;
+        if (a.gate_mode == 1) a.dGl[r] = __float2bfloat16_rn(g_me);
     }
 }
 
@@ -152,7 +202,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepArgs a) {
 
 // C [M x N] (bf16, row-major, ldc) = A B with fp32 accumulation in TMEM.
 // A_MN: A stored as [K][M] (M contiguous), else [M][K]; B_MN: B stored as
-// [K][N], else B^T stored as [N][K]. 128 x 128 tiles, K chunks of 64.
+// [K][N], else B^T stored as [N][K]. 128 x 128 tiles, K chunks of 64. When
+// the tiles are too few to occupy the GPU (the narrow headwise dW_g), K is
+// split: split s writes its fp32 partial to part[s], summed into C afterwards.
 constexpr int kGemmThreads = 192;
 constexpr int kGemmNS = 4;
 constexpr uint32_t kGemmOpBytes = 128 * 64 * 2;   // 16 KB per operand per chunk
@@ -165,6 +217,8 @@ struct GemmArgs {
     __nv_bfloat16* C;
     int M, N, K, ldc;
     int m_tiles, nkc;
+    int tiles, splits;   // split s of tile t is CTA s * tiles + t
+    float* part;         // splits > 1: fp32 [splits, M, N]
     WaitCtl ctl;
 };
 
@@ -183,8 +237,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kGemmOffMisc + 4);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int m0 = (blockIdx.x % args.m_tiles) * 128;
-    const int n0 = (blockIdx.x / args.m_tiles) * 128;
+    const int tile = (int)blockIdx.x % args.tiles, split = (int)blockIdx.x / args.tiles;
+    const int m0 = (tile % args.m_tiles) * 128;
+    const int n0 = (tile / args.m_tiles) * 128;
+    // this CTA's K chunks [kc0, kc1) (possibly none: it then writes zeros)
+    const int per = (args.nkc + args.splits - 1) / args.splits;
+    const int kc0 = split * per;
+    const int kc1 = kc0 + per < args.nkc ? kc0 + per : args.nkc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGemmNS; ++s) {
@@ -210,7 +269,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
             bool ok = true;
-            for (int kc = 0; kc < args.nkc; ++kc) {
+            for (int kc = kc0; kc < kc1; ++kc) {
                 if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.ctl))) break;
                 mbar_arrive_expect_tx(&full[stage], kGemmStage);
                 armed |= 1u << stage;
@@ -244,7 +303,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         constexpr uint32_t idG = idesc_bf16_f32(128, 128, A_MN, B_MN);
         constexpr uint32_t HI = desc_sw128_hi(1024);
         const uint32_t base = smem_u32(smem);
-        for (int kc = 0; kc < args.nkc; ++kc) {
+        for (int kc = kc0; kc < kc1; ++kc) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, args.ctl)))) break;
             tc_fence_after();
             const uint32_t st = base + stage * kGemmStage;
@@ -255,7 +314,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_ss_elect(tmem, a0 + kk * (A_MN ? (2048 >> 4) : (32 >> 4)), HI,
-                             b0 + kk * (B_MN ? (2048 >> 4) : (32 >> 4)), HI, idG, (kc | kk) != 0 ? 1u : 0u);
+                             b0 + kk * (B_MN ? (2048 >> 4) : (32 >> 4)), HI, idG, ((kc - kc0) | kk) != 0 ? 1u : 0u);
             mma_commit_elect(&empty[stage]);
             if (++stage == kGemmNS) {
                 stage = 0;
@@ -273,10 +332,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-        const bool ok = args.nkc > 0 && __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, args.ctl));
+        const bool ok = kc1 > kc0 && __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, args.ctl));
         tc_fence_after();
         const int r = m0 + row;
         __nv_bfloat16* dst = args.C + (long)r * args.ldc;
+        float* pdst = args.splits > 1 ? args.part + ((long)split * args.M + r) * args.N : nullptr;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t v[32];
@@ -289,7 +349,17 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             const int c = n0 + cb * 32;
             if (r >= args.M) continue;
-            if (c + 32 <= args.N && (args.ldc & 7) == 0) {
+            if (pdst) {
+                if (c + 32 <= args.N && (args.N & 3) == 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<uint4*>(pdst + c + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c + e < args.N) pdst[c + e] = __uint_as_float(v[e]);
+                }
+            } else if (c + 32 <= args.N && (args.ldc & 7) == 0) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8)
                     *reinterpret_cast<uint4*>(dst + c + e) = make_uint4(
@@ -312,6 +382,16 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
+// C = sum over the K splits of their fp32 partials, rounded once to bf16.
+__global__ void __launch_bounds__(256) gemm_split_sum_kernel(const float* __restrict__ part,
+                                                            __nv_bfloat16* __restrict__ C, long mn, int splits) {
+    for (long k = (long)blockIdx.x * blockDim.x + threadIdx.x; k < mn; k += (long)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < splits; ++s) acc += part[s * mn + k];
+        C[k] = __float2bfloat16_rn(acc);
+    }
+}
+
 // ------------------------------------------------------------------ shared by dQ and dK/dV
 
 // warp 0 copies, warp 1 MMAs, warps 4..7 and 8..11: two warpgroups, one row
@@ -330,7 +410,8 @@ constexpr uint32_t VEC_BYTES = kTile * 4;   // 128 floats
 
 struct AttnArgs {
     int B, Lq, Lk, Hq, Hkv, causal, n_qtiles, n_ktiles, Lq_pad;
-    int per_head;        // dK/dV: one unit per query head, fp32 partials summed afterwards (GQA)
+    int hpu;             // dK/dV: query heads per unit; below the group size (GQA), each
+                         // unit writes its heads' fp32 share, summed afterwards
     const float* lse2;   // [B, Hq, Lq_pad] log2 units
     const float* Dv;     // [B, Hq, Lq_pad]
     WaitCtl ctl;
@@ -678,17 +759,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // unit: (b, kv head, key tile) summing over the group's heads, or with
-    // per_head (b, query head, key tile) writing that head's share
+    // unit: (b, chunk of hpu query heads, key tile) summing over its heads; with
+    // hpu = the group size a chunk is a kv head's whole group and the unit writes
+    // dK, dV, else it writes the chunk's share (fp32)
     const int group = args.Hq / args.Hkv;
-    const int heads = args.per_head ? args.Hq : args.Hkv;
-    const int per_tile = args.B * heads;
+    const int chunks = args.Hq / args.hpu;
+    const bool partial = args.hpu < group;
+    const int per_tile = args.B * chunks;
     const int kt = (int)blockIdx.x / per_tile;
-    const int hu = ((int)blockIdx.x % per_tile) % heads;
-    const int b = ((int)blockIdx.x % per_tile) / heads;
-    const int kvh = args.per_head ? hu / group : hu;
-    const int h_first = args.per_head ? hu : kvh * group;   // query heads of the unit: h_first ..
-    const int n_heads = args.per_head ? 1 : group;
+    const int hu = ((int)blockIdx.x % per_tile) % chunks;
+    const int b = ((int)blockIdx.x % per_tile) / chunks;
+    const int h_first = hu * args.hpu;   // query heads of the unit: h_first ..
+    const int kvh = h_first / group;
+    const int n_heads = args.hpu;
     const int k0 = kt * kTile;
     const long off = (long)args.Lk - args.Lq;
     // query tiles that see any key of this tile: query i sees key k0 when off + i >= k0
@@ -870,7 +953,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(g_full, 0, abort_flag, args.ctl));
         tc_fence_after();
         const bool ok_epi = named_bar_and(1, 256, ok);
-        if (ok_epi && !args.per_head) {
+        if (ok_epi && !partial) {
             // every MMA has completed and every copy landed: stage dV, dK (bf16) in the ring
             uint8_t* stg = smem + C::OFF_RING;
 #pragma unroll
@@ -1018,7 +1101,7 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int K, int cols) {
 
 template <bool A_MN, bool B_MN>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfloat16* C, int M, int N, int K,
-                        const Runtime& rt, cudaStream_t s) {
+                        int splits, float* part, const Runtime& rt, cudaStream_t s) {
     static PerDeviceSetup setup;   // per template instance
     cudaError_t r = setup_once_per_device(setup, [](int&) {
         return cudaFuncSetAttribute(gemm_bf16_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1033,17 +1116,67 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfl
     a.ldc = N;
     a.m_tiles = (M + 127) / 128;
     a.nkc = (K + 63) / 64;
+    a.tiles = a.m_tiles * ((N + 127) / 128);
+    // (the plan sized the partials for up to `splits`; one wave on this device's SMs)
+    const int fit = rt.num_sms / a.tiles;
+    a.splits = splits > 1 && part ? (fit < splits ? fit : splits) : 1;
+    if (a.splits < 1) a.splits = 1;
+    a.part = part;
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
-    const long tiles = (long)a.m_tiles * ((N + 127) / 128);
-    gemm_bf16_kernel<A_MN, B_MN><<<(unsigned)tiles, kGemmThreads, kGemmSmem, s>>>(tmA, tmB, a);
+    gemm_bf16_kernel<A_MN, B_MN><<<(unsigned)((long)a.tiles * a.splits), kGemmThreads, kGemmSmem, s>>>(tmA, tmB, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    const long mn = (long)M * N;
+    const long blocks = (mn + 255) / 256 < 4096 ? (mn + 255) / 256 : 4096;
+    gemm_split_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(part, C, mn, a.splits);
     return cudaGetLastError();
+}
+
+// Query heads per dK/dV unit under GQA: the largest divisor of the group size
+// whose heaviest unit (the first key tile, every query tile of its heads) is
+// at most 1.25 times one SM's average share of the work, so that the units,
+// taken heaviest first, still spread about evenly. Larger units load each K,
+// V tile for more heads and leave fewer fp32 shares to sum afterwards
+// (measured on GQA 32/4 L4096: one head per unit 520 us, two 484, four 478).
+int dkdv_heads_per_unit(const Problem& p, int num_sms) {
+    const int group = p.Hq / p.Hkv;
+    if (group <= 1) return 1;
+    const long nq = (p.Lq + kTile - 1) / kTile, nk = (p.Lk + kTile - 1) / kTile;
+    const long off = (long)p.Lk - p.Lq;
+    long steps = 0, heaviest = 0;   // (query tile, key tile) pairs of one head
+    for (long kt = 0; kt < nk; ++kt) {
+        long t0 = 0;
+        if (p.causal && kt * kTile - off > 0) t0 = (kt * kTile - off) / kTile;
+        const long n = nq - t0 > 0 ? nq - t0 : 0;
+        steps += n;
+        if (n > heaviest) heaviest = n;
+    }
+    const double share = (double)steps * p.B * p.Hq / (num_sms > 0 ? num_sms : 1);
+    int best = 1;
+    for (int d = 2; d <= group; ++d)
+        if (group % d == 0 && (double)d * heaviest <= 1.25 * share) best = d;
+    return best;
+}
+
+// K splits for a [M x N x K] product on the single-CTA kernel when the
+// 128 x 128 tiles are few: as many as fit in one wave, each split at least 8
+// K chunks long (the launch lowers it to one wave of the device's own SMs).
+int gemm_splits(int M, int N, int K, int num_sms) {
+    const int tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    const int nkc = (K + 63) / 64;
+    if (tiles >= num_sms / 2 || nkc < 16) return 1;
+    int splits = num_sms / tiles;
+    if (splits > nkc / 8) splits = nkc / 8;
+    return splits > 1 ? splits : 1;
 }
 
 }  // namespace
 
 // (the gate variants of gated_sdpa_fwd_variant have no backward here)
 bool bwd_supported(const Problem& p) { return p.dtype == 1 && p.dk == HD && p.Lq >= 1 && p.gate_mode <= 2; }
+
+int gate_col_tile(int cols);   // gate_gemm_sm103.cu
 
 BwdPlan plan_bwd(const Problem& p, int num_sms) {
     BwdPlan w;
@@ -1056,11 +1189,35 @@ BwdPlan plan_bwd(const Problem& p, int num_sms) {
         off = (off + bytes + 255) & ~size_t(255);
         return at;
     };
+    if (p.gate_mode == 1 && w.fwd.gate_splits > 0) {
+        // The backward recomputes the headwise logits alone on the device (the
+        // forward runs its pre-pass on a few SMs beside the attention kernel):
+        // split K so that the pre-pass covers every SM, partials in their own buffer.
+        const int nt = gate_col_tile(w.fwd.gate_cols);
+        const int tiles = ((w.fwd.gate_rows + 127) / 128) * ((w.fwd.gate_cols + nt - 1) / nt);
+        const int nkc = (p.d_model + 63) / 64;
+        int splits = (num_sms + tiles - 1) / tiles;
+        const int max_splits = nkc / 4 > 0 ? nkc / 4 : 1;
+        if (splits > max_splits) splits = max_splits;
+        if (splits > w.fwd.gate_splits) {
+            w.fwd.gate_splits = splits;
+            w.fwd.gate_part = take(sizeof(float) * (size_t)splits * w.fwd.gate_rows * w.fwd.gate_cols);
+        }
+    }
     w.Lq_pad = (p.Lq + kTile - 1) / kTile * kTile;
     w.dY = take((size_t)p.B * p.Lq * p.Hq * HD * 2);
     w.Dv = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     w.lse2 = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     if (p.gate_mode != 0) w.dGl = take((size_t)p.B * p.Lq * gate_cols(p) * 2);
+    if (p.gate_mode != 0) {   // the gate-gradient GEMMs that run on the single-CTA kernel
+        const int rows = p.B * p.Lq, G = gate_cols(p);
+        w.dx_splits = p.d_model >= 256 ? 1 : gemm_splits(rows, p.d_model, G, num_sms);
+        w.dwg_splits = G >= 256 ? 1 : gemm_splits(p.d_model, G, rows, num_sms);
+        size_t need = 0;
+        if (w.dx_splits > 1) need = (size_t)w.dx_splits * rows * p.d_model;
+        if (w.dwg_splits > 1 && (size_t)w.dwg_splits * p.d_model * G > need) need = (size_t)w.dwg_splits * p.d_model * G;
+        if (need) w.gemm_part = take(need * 4);   // (the two GEMMs run one after the other)
+    }
     if (p.Hq != p.Hkv) {   // GQA: dK, dV per query head, then summed over each group
         w.part_dK = take((size_t)p.B * p.Lk * p.Hq * HD * 4);
         w.part_dV = take((size_t)p.B * p.Lk * p.Hq * HD * 4);
@@ -1104,20 +1261,24 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     pa.Hq = p.Hq;
     pa.Lq_pad = w.Lq_pad;
     pa.gate_mode = p.gate_mode;
-    const long warps = (long)p.B * p.Hq * w.Lq_pad;
+    const long n_rows = (long)p.B * p.Lq * p.Hq;
+    const long pad_entries = (long)p.B * p.Hq * (w.Lq_pad - p.Lq);
+    const long warps = (n_rows + kPrepRows - 1) / kPrepRows + (pad_entries + 31) / 32;
     bwd_prep_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(pa);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     // 3. dQ, then dK and dV
     alignas(64) CUtensorMap tmQ, tmdY, tmK, tmV, tmdQ, tmdK, tmdV;
-    const bool per_head = p.Hq != p.Hkv;
+    const int hpu = dkdv_heads_per_unit(p, rt.num_sms);
+    const bool per_head = hpu < p.Hq / p.Hkv;
+    const int chunks = p.Hq / hpu;
     if (!map_tile(&tmQ, p.Q, p.B, p.Lq, p.Hq) || !map_tile(&tmdY, ws + w.dY, p.B, p.Lq, p.Hq) ||
         !map_tile(&tmK, p.K, p.B, p.Lk, p.Hkv) || !map_tile(&tmV, p.V, p.B, p.Lk, p.Hkv) ||
         !map_out(&tmdQ, g.dQ, p.B, p.Lq, p.Hq))
         return cudaErrorInvalidValue;
-    if (per_head ? !(map_out_f32(&tmdK, ws + w.part_dK, p.B, p.Lk, p.Hq) &&
-                     map_out_f32(&tmdV, ws + w.part_dV, p.B, p.Lk, p.Hq))
+    if (per_head ? !(map_out_f32(&tmdK, ws + w.part_dK, p.B, p.Lk, chunks) &&
+                     map_out_f32(&tmdV, ws + w.part_dV, p.B, p.Lk, chunks))
                  : !(map_out(&tmdK, g.dK, p.B, p.Lk, p.Hkv) && map_out(&tmdV, g.dV, p.B, p.Lk, p.Hkv)))
         return cudaErrorInvalidValue;
     AttnArgs aa;
@@ -1130,7 +1291,7 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     aa.n_qtiles = (p.Lq + kTile - 1) / kTile;
     aa.n_ktiles = (p.Lk + kTile - 1) / kTile;
     aa.Lq_pad = w.Lq_pad;
-    aa.per_head = per_head ? 1 : 0;
+    aa.hpu = hpu;
     aa.lse2 = reinterpret_cast<const float*>(ws + w.lse2);
     aa.Dv = reinterpret_cast<const float*>(ws + w.Dv);
     aa.ctl.err = rt.err;
@@ -1160,7 +1321,7 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     e = launch_dependent(bwd_dq_kernel, dim3((unsigned)((long)aa.n_qtiles * p.B * p.Hq)), dim3(kAttnThreads),
                          DqCfg::SMEM_BYTES, s, tmQ, tmdY, tmK, tmV, tmdQ, aa);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(bwd_dkdv_kernel, dim3((unsigned)((long)aa.n_ktiles * p.B * (per_head ? p.Hq : p.Hkv))),
+    e = launch_dependent(bwd_dkdv_kernel, dim3((unsigned)((long)aa.n_ktiles * p.B * chunks)),
                          dim3(kAttnThreads), DkvCfg::SMEM_BYTES, s, tmQ, tmdY, tmK, tmV, tmdK, tmdV, aa);
     if (e != cudaSuccess) return e;
     if (per_head) {
@@ -1168,9 +1329,9 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
         const long threads = rows_kv * p.Hkv * (HD / 4);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
         bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(ws + w.part_dK),
-                                                    static_cast<__nv_bfloat16*>(g.dK), rows_kv, p.Hkv, p.Hq / p.Hkv);
+                                                    static_cast<__nv_bfloat16*>(g.dK), rows_kv, p.Hkv, chunks / p.Hkv);
         bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(ws + w.part_dV),
-                                                    static_cast<__nv_bfloat16*>(g.dV), rows_kv, p.Hkv, p.Hq / p.Hkv);
+                                                    static_cast<__nv_bfloat16*>(g.dV), rows_kv, p.Hkv, chunks / p.Hkv);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1185,7 +1346,8 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
         alignas(64) CUtensorMap tA, tB;
         if (!map_kmajor(&tA, ws + w.dGl, rows, G) || !map_kmajor(&tB, p.Wg, p.d_model, G))
             return cudaErrorInvalidValue;
-        e = launch_gemm<false, false>(tA, tB, static_cast<__nv_bfloat16*>(g.dX), rows, p.d_model, G, rt, s);
+        e = launch_gemm<false, false>(tA, tB, static_cast<__nv_bfloat16*>(g.dX), rows, p.d_model, G, w.dx_splits,
+                                      reinterpret_cast<float*>(ws + w.gemm_part), rt, s);
     }
     if (e != cudaSuccess) return e;
     // dW_g [d_model x G] = X^T dGl: A stored as X [rows][d_model], B as dGl [rows][G]
@@ -1193,7 +1355,8 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     alignas(64) CUtensorMap tA2, tB2;
     if (!map_mnmajor(&tA2, p.X, rows, p.d_model) || !map_mnmajor(&tB2, ws + w.dGl, rows, G))
         return cudaErrorInvalidValue;
-    return launch_gemm<true, true>(tA2, tB2, static_cast<__nv_bfloat16*>(g.dWg), p.d_model, G, rows, rt, s);
+    return launch_gemm<true, true>(tA2, tB2, static_cast<__nv_bfloat16*>(g.dWg), p.d_model, G, rows, w.dwg_splits,
+                                   reinterpret_cast<float*>(ws + w.gemm_part), rt, s);
 }
 
 }  // namespace gsdpa

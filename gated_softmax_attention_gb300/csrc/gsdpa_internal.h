@@ -198,6 +198,8 @@ struct BwdPlan {
     size_t dGl = 0;      // bf16 [B*Lq, G]
     size_t part_dK = 0;  // GQA: float [B, Lk, Hq, 128], each query head's share
     size_t part_dV = 0;
+    int dx_splits = 1, dwg_splits = 1;   // K splits of the gate-gradient GEMMs on the single-CTA kernel
+    size_t gemm_part = 0;                // float [splits, M, N] partials of the split GEMM
 };
 bool bwd_supported(const Problem& p);
 BwdPlan plan_bwd(const Problem& p, int num_sms);

@@ -56,6 +56,9 @@ CASES = [
     _w("elementwise_bottom_right_suffix", L_q=77, L_k=300, H_q=4, H_kv=1, seed=34),
     # a wide gate: dW_g [2560 x 2048] takes 256 x 512 tiles (K = 72 rows: a full chunk and a ragged one)
     _w("elementwise_wide_gate", L_q=72, L_k=72, d_model=2560, H_q=16, H_kv=4, seed=35),
+    # a narrow gate over many rows: dW_g [256 x 8] has two 128 x 128 tiles and K = 1200 rows
+    # (19 chunks of 64, the last ragged), so K is split in two, partials summed afterwards
+    _w("headwise_split_k_dwg", B=4, L_q=300, L_k=300, H_q=8, H_kv=2, gate="headwise", seed=36),
 ]
 
 
@@ -156,3 +159,42 @@ def test_saved_gate_backward_equals_recompute(w):
     assert a.keys() == b.keys()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("B", [8, 32], ids=["chunks_of_four_heads", "whole_groups"])
+def test_gqa_backward_equals_repeated_heads(B):
+    """GQA 16/2 (groups of 8), L 1024: the dK/dV units take several query heads
+    each once the work is large enough (on 132 to 160 SMs: four heads per unit
+    at B = 8, whose fp32 shares are then summed over two chunks; a kv head's
+    whole group at B = 32, written directly). The gradients must equal the
+    MHA backward on K, V repeated over each group (the same O and lse), with dK
+    and dV summed over the group: dQ bit for bit (the same per-row arithmetic),
+    dK and dV within the bf16 roundings. Bound: the GQA value is T rounded once
+    and each MHA term t_h is rounded once, |error| <= 2^-8 |x| for each, so
+    |gqa - sum_h mha_h| <= 2^-8 (|sum| + 2 sum_h |mha_h|), plus float32
+    accumulation in different orders (1e-3 of the tensor's largest value).
+    The mean error is about 2^-9 of a value per rounding (measured rel-L1
+    2.2e-3 for dK at B = 8); the whole tensor takes the backward's 5e-3 bar."""
+    H_q, H_kv, L = 16, 2, 1024
+    group = H_q // H_kv
+    w = Workload(name="gqa_units", dtype="bf16", B=B, L_q=L, L_k=L, d_model=128, H_q=H_q, H_kv=H_kv, d_k=128,
+                 gate="none", causal=True, seed=37)
+    t = make_inputs(w)
+    Q, K, V = t["Q"].cuda(), t["K"].cuda(), t["V"].cuda()
+    dO = _dO(w).cuda()
+    O, _, lse = gb.gated_sdpa_fwd_train(None, Q, K, V, None, gate="none", causal=True)
+    g = gb.gated_sdpa_bwd(None, Q, K, V, None, O, dO, lse, gate="none", causal=True)
+    Kr = K.repeat_interleave(group, dim=2).contiguous()
+    Vr = V.repeat_interleave(group, dim=2).contiguous()
+    m = gb.gated_sdpa_bwd(None, Q, Kr, Vr, None, O, dO, lse, gate="none", causal=True)
+    assert gb.check_device_error() == gb.OK
+    assert torch.equal(g["dQ"], m["dQ"])
+    for k in ("dK", "dV"):
+        terms = m[k].double().view(B, L, H_kv, group, 128)
+        ssum = terms.sum(dim=3)
+        bound = 2.0 ** -8 * (ssum.abs() + 2 * terms.abs().sum(dim=3)) + 1e-3 * float(ssum.abs().max())
+        err = (g[k].double() - ssum).abs()
+        rel = float(err.sum() / ssum.abs().sum())
+        print(f"B={B} {k}: max err / bound {float((err / bound).max()):.3f}  rel-L1 {rel:.2e}")
+        assert bool((err <= bound).all()), k
+        assert rel <= BWD_REL_L1, k
