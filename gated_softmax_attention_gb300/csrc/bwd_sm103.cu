@@ -81,8 +81,8 @@ struct PrepArgs {
     int gate_splits;
     __nv_bfloat16* dY;         // [B, Lq, Hq, HD]
     __nv_bfloat16* dGl;        // [B*Lq, G] (G = Hq*HD | Hq) or null
-    float* Dv;                 // [B, Hq, Lq_pad]
-    float* lse2;               // [B, Hq, Lq_pad]: lse * log2(e); padding rows +inf
+    float* Dv;                 // [B, Hq, Lq_pad]: -D (negated: added as is by the kernels)
+    float* lse2;               // [B, Hq, Lq_pad]: -lse * log2(e); padding rows -inf
     int B, Lq, Hq, Lq_pad, gate_mode;
 };
 
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         if (pad > 0 && k < (long)a.B * a.Hq * pad) {
             const long at = (k / pad) * a.Lq_pad + a.Lq + k % pad;
             a.Dv[at] = 0.f;
-            a.lse2[at] = INFINITY;
+            a.lse2[at] = -INFINITY;
         }
         return;
     }
@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         const long bi = r / a.Hq;
         const long b = bi / a.Lq, i = bi % a.Lq;
         const long at = (b * a.Hq + h) * a.Lq_pad + i;
-        a.Dv[at] = d_me;
-        a.lse2[at] = lse_l * kLog2e;
+        a.Dv[at] = -d_me;
+        a.lse2[at] = -(lse_l * kLog2e);
         if (a.gate_mode == 1) a.dGl[r] = __float2bfloat16_rn(g_me);
     }
 }
@@ -412,8 +412,8 @@ struct AttnArgs {
     int B, Lq, Lk, Hq, Hkv, causal, n_qtiles, n_ktiles, Lq_pad;
     int hpu;             // dK/dV: query heads per unit; below the group size (GQA), each
                          // unit writes its heads' fp32 share, summed afterwards
-    const float* lse2;   // [B, Hq, Lq_pad] log2 units
-    const float* Dv;     // [B, Hq, Lq_pad]
+    const float* lse2;   // [B, Hq, Lq_pad] -lse in log2 units
+    const float* Dv;     // [B, Hq, Lq_pad] -D
     WaitCtl ctl;
 };
 
@@ -630,8 +630,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const long i = (long)q0 + row;
         const long pidx = ((long)b * args.Hq + h) * args.Lq_pad + i;
-        const float lse2 = args.lse2[pidx];
-        const float D = args.Dv[pidx];
+        const float nlse2 = args.lse2[pidx];   // (both stored negated)
+        const float nDv = args.Dv[pidx];
         const float sl2 = kLog2e / sqrtf((float)HD);
         const float isq = 1.0f / sqrtf((float)HD);
         bool ok = true;
@@ -654,20 +654,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // dS = p (dP - D), two columns per packed fp32 instruction (the 1/sqrt(d_k)
             // is applied to dQ in the epilogue); masks only where the tile needs them
             uint32_t pk[2][16];
-            const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2), nD = make_float2(-D, -D);
+            const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2), nD = make_float2(nDv, nDv);
+            if (lim < 127) {   // masked scores become -inf (p = 0), outside the main loop
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if ((2 * wg + cc) * 32 + e > lim) sv[cc][e] = __float_as_uint(-INFINITY);
+            }
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * wg + cc;
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[cc][e]), __uint_as_float(sv[cc][e + 1])),
                                                 sl2x2, nl2);
-                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (lim < 127) {
-                        const int col = c * 32 + e;
-                        if (col > lim) pr.x = 0.f;
-                        if (col + 1 > lim) pr.y = 0.f;
-                    }
+                    const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dp[cc][e]),
                                                                             __uint_as_float(dp[cc][e + 1])), nD));
                     pk[cc][e >> 1] = pack_bf16x2(ds.x, ds.y);
@@ -921,6 +922,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // p = exp2(s sl2 - lse2), dS = p (dP - D) (the 1/sqrt(d_k) is applied to
             // dK in the epilogue), two columns per packed fp32 instruction
             const float2 sl2x2 = make_float2(sl2, sl2);
+            if (cmin > 0) {   // masked scores become -inf (p = 0), outside the main loop
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e < cmin) sv[e] = __float_as_uint(-INFINITY);
+            }
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
                 const float4 l4 = *reinterpret_cast<const float4*>(L2 + 4 * g4);
@@ -928,15 +934,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int e = 4 * g4 + 2 * h2;
-                    const float2 nl = h2 ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-                    const float2 nd = h2 ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                    const float2 nl = h2 ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);   // (stored negated)
+                    const float2 nd = h2 ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
                     const float2 x =
                         __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl);
-                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (cmin > 0) {
-                        if (e < cmin) pr.x = 0.f;
-                        if (e + 1 < cmin) pr.y = 0.f;
-                    }
+                    const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     const float2 ds = __fmul2_rn(
                         pr, __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
                     ppk[2 * g4 + h2] = pack_bf16x2(pr.x, pr.y);
