@@ -50,6 +50,21 @@
 namespace gsdpa {
 namespace {
 
+// tcgen05.ld of 32 columns that also returns their maximum (the .red.max form):
+// the tile's row maximum comes with the load instead of a pass over the scores.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=f"(mx)
+        : "r"(taddr));
+}
+
 constexpr int kTile = 128;           // query rows per tile, keys per K/V tile
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -387,8 +402,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
+            float pmx[4];   // each 32-column load's maximum
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + c * 32, sr[c], pmx[c]);
             tmem_wait_ld();
 
             const int kv0 = j * kTile;
@@ -405,17 +421,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     for (int e = 0; e < 32; ++e)
                         if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
             }
-            float mx[8];
+            // tile row max: from the loads, or over the masked scores on the diagonal tiles
+            float rmax = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3]));
+            if (lim < 127) {
+                float mx[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[0][e + 8]));
+                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[0][e + 8]));
 #pragma unroll
-            for (int k = 16; k < 128; k += 16) {
+                for (int k = 16; k < 128; k += 16) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    mx[e] = fmax3(mx[e], __uint_as_float(sr[k >> 5][(k & 31) + e]),
-                                  __uint_as_float(sr[(k + 8) >> 5][((k + 8) & 31) + e]));
+                    for (int e = 0; e < 8; ++e)
+                        mx[e] = fmax3(mx[e], __uint_as_float(sr[k >> 5][(k & 31) + e]),
+                                      __uint_as_float(sr[(k + 8) >> 5][((k + 8) & 31) + e]));
+                }
+                rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             }
-            const float tmax = sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            const float tmax = sl2 * rmax;
             if (j == 0) x0 = __uint_as_float(sr[0][0]) * sl2;
             const float m_new = fmaxf(m, tmax);
             if (j == 0) {
