@@ -14,9 +14,18 @@
 //   dQ   = dS K,   dK = dS^T Q,   dV = p^T dY   (summed over a GQA group)
 //   dW_g = X^T dGl,   dX (gate path) = dGl W_g^T
 // Headwise gates broadcast G over d_k, so dGl sums over the head's columns.
+// Only the elementwise gate needs dY as a tensor (a bf16 operand of dP and
+// dV). A headwise gate is one value g_i per row and head (without a gate,
+// g_i = 1): then dY V^T = g_i (dO V^T) and p^T dY = (p g)^T dO, and with
+//   p'_ij = p_ij g_i = exp2(s_ij log2(e)/sqrt(d_k) - lse_i log2(e) + log2 g_i)
+//   dS_ij = p_ij (g_i dP'_ij - D_i) = p'_ij (dP'_ij - D_i / g_i),  dP' = dO V^T,
+// the kernels read dO itself and run unchanged on the row statistics
+// -lse log2(e) + log2 g and -D / g (g = 0: p' = 0 and the second one 0): no
+// bf16 rounding of dY, and no dY tensor written and read back.
 //
 // Kernels (all tcgen05, accumulators in TMEM, operands staged by TMA):
-//   bwd_prep_kernel    four (row, head) rows per warp: dY, D, dGl and lse in log2
+//   bwd_prep_kernel    four (row, head) rows per warp: dY (elementwise gate), D,
+//                      dGl and lse in log2 (both folded with g, headwise)
 //                      units into padded per-(b, h) arrays (whole 128-row
 //                      tiles are 512-byte bulk copies);
 //   bwd_dq_kernel      per (b, h, 128-row query tile): S = Q K^T and
@@ -79,10 +88,10 @@ struct PrepArgs {
     const __half* gate_sig;    // elementwise: sigma(X W_g) [B*Lq, Hq*HD] fp16, else null
     const float* gate_part;    // headwise: logit partials [splits, B*Lq, Hq], else null
     int gate_splits;
-    __nv_bfloat16* dY;         // [B, Lq, Hq, HD]
+    __nv_bfloat16* dY;         // elementwise gate: [B, Lq, Hq, HD], else null
     __nv_bfloat16* dGl;        // [B*Lq, G] (G = Hq*HD | Hq) or null
-    float* Dv;                 // [B, Hq, Lq_pad]: -D (negated: added as is by the kernels)
-    float* lse2;               // [B, Hq, Lq_pad]: -lse * log2(e); padding rows -inf
+    float* Dv;                 // [B, Hq, Lq_pad]: -D (negated: added as is by the kernels); headwise -D / g
+    float* lse2;               // [B, Hq, Lq_pad]: -lse * log2(e), headwise + log2 g; padding rows -inf
     int B, Lq, Hq, Lq_pad, gate_mode;
 };
 
@@ -124,9 +133,21 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
             dow[k] = *reinterpret_cast<const uint2*>(a.dO + base);
             ow[k] = *reinterpret_cast<const uint2*>(a.O + base);
             if (a.gate_mode == 2) gw[k] = *reinterpret_cast<const uint2*>(a.gate_sig + base);
-            if (a.gate_mode == 1)
-                for (int s = 0; s < a.gate_splits; ++s) glv[k] += a.gate_part[s * n_rows + r];
         }
+    }
+    if (a.gate_mode == 1) {
+        // the rows' logits: lane 8 k + j adds row k's split-K partials j, j + 8, ...
+        // (all of them loaded at once), then the eight lanes of a row add theirs
+        static_assert(kPrepRows * 8 == 32, "eight lanes per row");
+        const int kk = lane >> 3, jj = lane & 7;
+        float part = 0.f;
+        if (r0 + kk < n_rows)
+            for (int s = jj; s < a.gate_splits; s += 8) part += a.gate_part[s * n_rows + r0 + kk];
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+#pragma unroll
+        for (int k = 0; k < kPrepRows; ++k) glv[k] = __shfl_sync(0xffffffffu, part, 8 * k);
     }
     // lane k < kPrepRows fetches row k's lse (natural log, [B, H_q, L_q])
     if (lane < kPrepRows && r0 + lane < n_rows) {
@@ -136,11 +157,12 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         const long b = bi / a.Lq, i = bi % a.Lq;
         lse_l = a.lse[(b * a.Hq + h) * a.Lq + i];
     }
-    float dsum[kPrepRows], gsum[kPrepRows];
+    float dsum[kPrepRows], gsum[kPrepRows], ghv[kPrepRows];
 #pragma unroll
     for (int k = 0; k < kPrepRows; ++k) {
         const long r = r0 + k;
         dsum[k] = gsum[k] = 0.f;
+        ghv[k] = 1.f;
         if (r >= n_rows) continue;
         const long base = r * HD + lane * 4;
         float dof[4], of[4];
@@ -155,7 +177,8 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
             g[2] = g23.x;
             g[3] = g23.y;
         } else if (a.gate_mode == 1) {
-            g[0] = g[1] = g[2] = g[3] = 1.0f / (1.0f + exp2f(-glv[k] * kLog2e));
+            ghv[k] = 1.0f / (1.0f + exp2f(-glv[k] * kLog2e));
+            g[0] = g[1] = g[2] = g[3] = ghv[k];
         }
         float dgl[4];
 #pragma unroll
@@ -164,11 +187,12 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
             dgl[e] = dof[e] * of[e] * (1.0f - g[e]);
             gsum[k] += dgl[e];
         }
-        *reinterpret_cast<uint2*>(a.dY + base) =
-            make_uint2(pack_bf16x2(dof[0] * g[0], dof[1] * g[1]), pack_bf16x2(dof[2] * g[2], dof[3] * g[3]));
-        if (a.gate_mode == 2)
+        if (a.gate_mode == 2) {
+            *reinterpret_cast<uint2*>(a.dY + base) =
+                make_uint2(pack_bf16x2(dof[0] * g[0], dof[1] * g[1]), pack_bf16x2(dof[2] * g[2], dof[3] * g[3]));
             *reinterpret_cast<uint2*>(a.dGl + base) =
                 make_uint2(pack_bf16x2(dgl[0], dgl[1]), pack_bf16x2(dgl[2], dgl[3]));
+        }
     }
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) {
@@ -179,12 +203,13 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         }
     }
     // lane k < kPrepRows writes row k's D, lse2 and (headwise) dGl
-    float d_me = dsum[0], g_me = gsum[0];
+    float d_me = dsum[0], g_me = gsum[0], gh_me = ghv[0];
 #pragma unroll
     for (int k = 1; k < kPrepRows; ++k)
         if (lane == k) {
             d_me = dsum[k];
             g_me = gsum[k];
+            gh_me = ghv[k];
         }
     if (lane < kPrepRows && r0 + lane < n_rows) {
         const long r = r0 + lane;
@@ -192,9 +217,15 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         const long bi = r / a.Hq;
         const long b = bi / a.Lq, i = bi % a.Lq;
         const long at = (b * a.Hq + h) * a.Lq_pad + i;
-        a.Dv[at] = -d_me;
-        a.lse2[at] = -(lse_l * kLog2e);
-        if (a.gate_mode == 1) a.dGl[r] = __float2bfloat16_rn(g_me);
+        if (a.gate_mode == 1) {
+            // g folded into the row statistics (the kernels then read dO for dY)
+            a.Dv[at] = gh_me > 0.f ? -d_me / gh_me : 0.f;
+            a.lse2[at] = gh_me > 0.f ? log2f(gh_me) - lse_l * kLog2e : -INFINITY;
+            a.dGl[r] = __float2bfloat16_rn(g_me);
+        } else {
+            a.Dv[at] = -d_me;
+            a.lse2[at] = -(lse_l * kLog2e);
+        }
     }
 }
 
@@ -723,6 +754,7 @@ struct DkvCfg {
     static constexpr uint32_t OFF_V = TILE_BYTES;               // V_j
     static constexpr uint32_t OFF_RING = 2 * TILE_BYTES;        // [Q_i | dY_i | lse2_i | D_i] per stage
     static constexpr uint32_t STAGE = 2 * TILE_BYTES + 2 * VEC_BYTES;
+    static_assert(STAGE % 1024 == 0 && TILE_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
     static constexpr uint32_t OFF_BAR = OFF_RING + kQNS * STAGE;
     static constexpr int NBAR = 2 * kQNS + 7;   // full, empty, kv_full, s_full[2], p_full[2], g_full, drain
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -1207,7 +1239,7 @@ BwdPlan plan_bwd(const Problem& p, int num_sms) {
         }
     }
     w.Lq_pad = (p.Lq + kTile - 1) / kTile * kTile;
-    w.dY = take((size_t)p.B * p.Lq * p.Hq * HD * 2);
+    if (p.gate_mode == 2) w.dY = take((size_t)p.B * p.Lq * p.Hq * HD * 2);   // (else the kernels read dO)
     w.Dv = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     w.lse2 = take((size_t)p.B * p.Hq * w.Lq_pad * 4);
     if (p.gate_mode != 0) w.dGl = take((size_t)p.B * p.Lq * gate_cols(p) * 2);
@@ -1244,7 +1276,7 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
         cudaError_t e = launch_gate_logits_bf16(p, w.fwd, ws, rt, s, &launched, ZeroJob());
         if (e != cudaSuccess) return e;
     }
-    // 2. dY, D, dGl, lse in log2 units
+    // 2. dY (elementwise gate), D, dGl, lse in log2 units (headwise: g folded into the last two)
     PrepArgs pa;
     pa.dO = static_cast<const __nv_bfloat16*>(g.dO);
     pa.O = static_cast<const __nv_bfloat16*>(g.O);
@@ -1254,7 +1286,7 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
                                    : reinterpret_cast<const __half*>(ws + w.fwd.gate_sig);
     pa.gate_part = p.gate_mode == 1 ? reinterpret_cast<const float*>(ws + w.fwd.gate_part) : nullptr;
     pa.gate_splits = w.fwd.gate_splits;
-    pa.dY = reinterpret_cast<__nv_bfloat16*>(ws + w.dY);
+    pa.dY = p.gate_mode == 2 ? reinterpret_cast<__nv_bfloat16*>(ws + w.dY) : nullptr;
     pa.dGl = p.gate_mode ? reinterpret_cast<__nv_bfloat16*>(ws + w.dGl) : nullptr;
     pa.Dv = reinterpret_cast<float*>(ws + w.Dv);
     pa.lse2 = reinterpret_cast<float*>(ws + w.lse2);
@@ -1275,7 +1307,9 @@ cudaError_t launch_bwd_bf16_saved(const Problem& p, const BwdArgs& g, const void
     const int hpu = dkdv_heads_per_unit(p, rt.num_sms);
     const bool per_head = hpu < p.Hq / p.Hkv;
     const int chunks = p.Hq / hpu;
-    if (!map_tile(&tmQ, p.Q, p.B, p.Lq, p.Hq) || !map_tile(&tmdY, ws + w.dY, p.B, p.Lq, p.Hq) ||
+    // the dP / dV operand: dY with an elementwise gate, else dO itself (g folded into the row statistics)
+    const void* dy_op = p.gate_mode == 2 ? static_cast<const void*>(ws + w.dY) : g.dO;
+    if (!map_tile(&tmQ, p.Q, p.B, p.Lq, p.Hq) || !map_tile(&tmdY, dy_op, p.B, p.Lq, p.Hq) ||
         !map_tile(&tmK, p.K, p.B, p.Lk, p.Hkv) || !map_tile(&tmV, p.V, p.B, p.Lk, p.Hkv) ||
         !map_out(&tmdQ, g.dQ, p.B, p.Lq, p.Hq))
         return cudaErrorInvalidValue;

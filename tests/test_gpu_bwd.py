@@ -95,13 +95,16 @@ def test_backward_matches_oracle(w):
 
 # ------------------------------------------------------------------ full size, the shape bench.py times
 
-def test_full_size_backward_sampled_rows_and_properties():
-    """The headline workload's backward: dQ and dX on sampled query rows and
-    dK, dV on sampled key rows against the oracle's row form; and two properties of
-    the whole tensors: the values' gradients sum to the rows' dy = dO G (rows
-    of p sum to one), and sum(dX X) = sum(dW_g W_g) (both equal sum(dGl (X W_g)))."""
+@pytest.mark.parametrize("name", ["bf16_mha_elementwise_L2048", "bf16_gqa_headwise_L4096"])
+def test_full_size_backward_sampled_rows_and_properties(name):
+    """A full-size workload's backward (the headline shape; GQA 32/4 headwise
+    L4096, whose dK/dV units take four query heads each): dQ and dX on sampled
+    query rows and dK, dV on sampled key rows against the oracle's row form; and
+    two properties of the whole tensors: the values' gradients sum to the rows'
+    dy = dO G (rows of p sum to one), and sum(dX X) = sum(dW_g W_g) (both equal
+    sum(dGl (X W_g)))."""
     from gated_softmax_attention_gb300.workloads import WORKLOADS
-    w = WORKLOADS["bf16_mha_elementwise_L2048"]
+    w = WORKLOADS[name]
     t = make_inputs(w)
     dO = _dO(w)
     dev = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
@@ -124,7 +127,9 @@ def test_full_size_backward_sampled_rows_and_properties():
     # properties of the whole tensors
     X = t["X"].double().numpy()
     W = t["W_g"].double().numpy()
-    gate = 1.0 / (1.0 + np.exp(-(X @ W)))                                   # [B, L, H*d]
+    gate = 1.0 / (1.0 + np.exp(-(X @ W)))                                   # [B, L, H*d] or [B, L, H]
+    if w.gate == "headwise":
+        gate = np.repeat(gate, w.d_k, axis=-1)                              # one value per head, over d_k
     dy = dO.double().numpy().reshape(w.B, w.L_q, -1) * gate
     grp = w.H_q // w.H_kv
     dy_sum = dy.reshape(w.B, w.L_q, w.H_kv, grp, w.d_k).sum(axis=(1, 3))   # [B, H_kv, d]
