@@ -149,13 +149,27 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
 #pragma unroll
         for (int k = 0; k < kPrepRows; ++k) glv[k] = __shfl_sync(0xffffffffu, part, 8 * k);
     }
-    // lane k < kPrepRows fetches row k's lse (natural log, [B, H_q, L_q])
+    // lane k < kPrepRows fetches row k's lse (natural log, [B, H_q, L_q]); its
+    // (b, h, i), decoded once (32-bit divisions while the rows fit in 32 bits:
+    // a 64-bit division costs the warp as much as the rest of the row's work)
+    long bh = 0, i_row = 0;   // b H_q + h and i of the row of this lane
     if (lane < kPrepRows && r0 + lane < n_rows) {
         const long r = r0 + lane;
-        const int h = (int)(r % a.Hq);
-        const long bi = r / a.Hq;   // b L_q + i
-        const long b = bi / a.Lq, i = bi % a.Lq;
-        lse_l = a.lse[(b * a.Hq + h) * a.Lq + i];
+        long h, bi;
+        if (n_rows <= 0xffffffffL) {
+            const uint32_t r32 = (uint32_t)r, hq = (uint32_t)a.Hq, lq = (uint32_t)a.Lq;
+            const uint32_t bi32 = r32 / hq, b32 = bi32 / lq;
+            h = r32 - bi32 * hq;
+            bi = bi32;
+            i_row = bi32 - b32 * lq;
+            bh = (long)b32 * a.Hq + h;
+        } else {
+            h = r % a.Hq;
+            bi = r / a.Hq;   // b L_q + i
+            i_row = bi % a.Lq;
+            bh = (bi / a.Lq) * a.Hq + h;
+        }
+        lse_l = a.lse[bh * a.Lq + i_row];
     }
     float dsum[kPrepRows], gsum[kPrepRows], ghv[kPrepRows];
 #pragma unroll
@@ -213,10 +227,7 @@ __global__ void __launch_bounds__(256, 4) bwd_prep_kernel(const PrepArgs a) {
         }
     if (lane < kPrepRows && r0 + lane < n_rows) {
         const long r = r0 + lane;
-        const int h = (int)(r % a.Hq);
-        const long bi = r / a.Hq;
-        const long b = bi / a.Lq, i = bi % a.Lq;
-        const long at = (b * a.Hq + h) * a.Lq_pad + i;
+        const long at = bh * a.Lq_pad + i_row;
         if (a.gate_mode == 1) {
             // g folded into the row statistics (the kernels then read dO for dY)
             a.Dv[at] = gh_me > 0.f ? -d_me / gh_me : 0.f;
