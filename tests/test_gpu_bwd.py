@@ -166,6 +166,36 @@ def test_saved_gate_backward_equals_recompute(w):
         assert torch.equal(a[k], b[k]), k
 
 
+def test_backward_saturated_headwise_gates():
+    """Headwise gate values of exactly 1 and 0 (logits +200 and -200, X = 1): the
+    backward folds g into the row statistics (-lse log2 e + log2 g, -D / g), so
+    g = 0 takes its own branch (p' = 0, the second statistic 0). The heads with
+    g = 0 have zero gradients; those with g = 1 are plain attention's; all
+    match the oracle."""
+    w = _w("headwise_saturated", B=2, L_q=200, L_k=200, H_q=8, H_kv=2, gate="headwise", seed=38)
+    t = make_inputs(w)
+    t["X"] = torch.ones_like(t["X"])
+    W = torch.empty((w.d_model, w.H_q), dtype=torch.float32)
+    for h in range(w.H_q):
+        W[:, h] = (200.0 if h % 2 == 0 else -200.0) / w.d_model
+    t["W_g"] = W.to(torch.bfloat16)
+    dO = _dO(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    O, _, lse = gb.gated_sdpa_fwd_train(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], gate=w.gate,
+                                        causal=w.causal)
+    g = gb.gated_sdpa_bwd(dev["X"], dev["Q"], dev["K"], dev["V"], dev["W_g"], O, dO.cuda(), lse, gate=w.gate,
+                          causal=w.causal)
+    assert gb.check_device_error() == gb.OK
+    assert torch.all(g["dQ"][:, :, 1::2] == 0)   # the heads whose gate is 0
+    ref = oracle.gated_sdpa_bwd(t["X"], t["Q"], t["K"], t["V"], t["W_g"], dO, gate=w.gate, causal=w.causal)
+    for k in ref:
+        got = g[k].double().cpu().numpy()
+        if np.abs(ref[k]).max() < 1e-30:   # dX, dW_g: sigma(+-200) (1 - sigma) vanishes (1e-87 in float64)
+            assert np.abs(got).max() < 1e-30, k
+        else:
+            _check(f"{w.name} {k}", got, ref[k])
+
+
 @pytest.mark.parametrize("B", [8, 32], ids=["chunks_of_four_heads", "whole_groups"])
 def test_gqa_backward_equals_repeated_heads(B):
     """GQA 16/2 (groups of 8), L 1024: the dK/dV units take several query heads
