@@ -605,17 +605,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     packed[e / 2] = pack_bf16x2(v0, v1);
                 }
                 if (GATE == 0) {
-                    // Without a gate the row's 64 bytes go straight from registers
-                    // (no fence, barrier or copy per chunk: 36.65 -> 36.31 us per
-                    // call on the headline shape). With a gate the epilogue also
-                    // reads the gate from L2, and whole-line bulk stores leave L2
-                    // more room for that (direct stores: 58.9 -> 60.9 us).
+                    // Without a gate the row's 64 bytes go straight from registers,
+                    // as two whole 32-byte sectors (256-bit stores; the row starts
+                    // on a 256-byte boundary): no fence, barrier or bulk copy per
+                    // chunk (36.22 -> 35.13 us per call on the headline shape;
+                    // 16-byte stores gained a third of that). With a gate the
+                    // epilogue also reads the gate from L2, and the bulk copies'
+                    // whole-line writes leave L2 more room for it (these stores:
+                    // 58.10 -> 58.56 us for the gated call).
                     if (i < args.Lq) {
-                        uint4* dstg = reinterpret_cast<uint4*>(
-                            args.out + (((long)b * args.Lq + i) * args.Hq + h) * HD + cb * 32);
+                        const __nv_bfloat16* dstg = args.out + (((long)b * args.Lq + i) * args.Hq + h) * HD + cb * 32;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dstg[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                        for (int q = 0; q < 2; ++q)
+                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dstg + 16 * q),
+                                         "r"(packed[8 * q]), "r"(packed[8 * q + 1]), "r"(packed[8 * q + 2]),
+                                         "r"(packed[8 * q + 3]), "r"(packed[8 * q + 4]), "r"(packed[8 * q + 5]),
+                                         "r"(packed[8 * q + 6]), "r"(packed[8 * q + 7])
+                                         : "memory");
                     }
                 } else {
                     uint8_t* dst = stg + (cb & 1) * C::STG_BYTES + row * 64;
