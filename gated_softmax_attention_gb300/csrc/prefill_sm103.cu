@@ -112,17 +112,21 @@ struct PrefillArgs {
     double sink_inv;                // 2^-F / L_q
     int sink_arrivals;              // 4 warps per query tile
     float* lse;                     // [B, Hq, Lq] or null
-    __nv_bfloat16* out;             // O [B, Lq, Hq, HD] (the gate-free epilogue's direct stores)
+    __nv_bfloat16* out;             // O [B, Lq, Hq, HD] (the epilogue's direct stores)
     WaitCtl ctl;
 };
 
 
-template <int HD, int GATE, bool ADD>
+// DIRECT: the epilogue stores O from registers as whole 32-byte sectors (O
+// 32-byte aligned, no gate or the elementwise gate); otherwise it stages each
+// 32-column chunk in shared memory for a bulk tensor copy.
+template <int HD, int GATE, bool ADD, bool DIRECT>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                const PrefillArgs args) {
     using C = PrefillCfg<HD, GATE>;
+    static_assert(!DIRECT || GATE == 0 || GATE == 2, "direct stores only without a gate or with the elementwise one");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::OFF_Q;
@@ -493,7 +497,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const uint4* gsrc = reinterpret_cast<const uint4*>(
                     args.gate_sig + ((long)b * args.Lq + i) * args.ge.g_rs + (long)h * args.ge.g_hs);
 #pragma unroll
-                for (int q = 0; q < HD / 8; ++q) gq[q] = __ldg(gsrc + q);
+                // 256-bit loads, whole 32-byte sectors: the values live in the
+                // workspace (256-byte aligned) in rows of a multiple of d_k halves
+                for (int q = 0; q < HD / 16; ++q)
+                    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                                 : "=r"(gq[2 * q].x), "=r"(gq[2 * q].y), "=r"(gq[2 * q].z), "=r"(gq[2 * q].w),
+                                   "=r"(gq[2 * q + 1].x), "=r"(gq[2 * q + 1].y), "=r"(gq[2 * q + 1].z), "=r"(gq[2 * q + 1].w)
+                                 : "l"(gsrc + 2 * q));
             } else {
 #pragma unroll
                 for (int q = 0; q < HD / 8; ++q) gq[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -557,9 +567,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             // 32 columns at a time: TMEM -> registers -> bf16 in a staging buffer ->
             // one TMA store of the tile's 128 rows (rows past L_q are clipped by the
-            // tensor map; without a gate, stores from registers instead, below). The
-            // issuing thread has seen the store two chunks back finish reading its
-            // buffer before the barrier of the chunk in between.
+            // tensor map; without a gate or with the elementwise gate, stores from
+            // registers instead, below, when O is 32-byte aligned). The issuing
+            // thread has seen the store two chunks back finish reading its buffer
+            // before the barrier of the chunk in between.
             uint8_t* stg = smem + C::OFF_STG + t * 2 * C::STG_BYTES;
             const int sw = (row >> 1) & 3;   // 64-byte swizzle of this row's 16-byte pieces
 #pragma unroll
@@ -604,15 +615,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     }
                     packed[e / 2] = pack_bf16x2(v0, v1);
                 }
-                if (GATE == 0) {
-                    // Without a gate the row's 64 bytes go straight from registers,
-                    // as two whole 32-byte sectors (256-bit stores; the row starts
-                    // on a 256-byte boundary): no fence, barrier or bulk copy per
-                    // chunk (36.22 -> 35.13 us per call on the headline shape;
-                    // 16-byte stores gained a third of that). With a gate the
-                    // epilogue also reads the gate from L2, and the bulk copies'
-                    // whole-line writes leave L2 more room for it (these stores:
-                    // 58.10 -> 58.56 us for the gated call).
+                if (DIRECT) {
+                    // The row's 64 bytes go straight from registers, as two whole
+                    // 32-byte sectors (256-bit stores; O is 32-byte aligned and a row
+                    // is d_k halves): no fence, barrier or bulk copy per chunk. Without a
+                    // gate: 36.22 -> 35.13 us per call on the headline shape (16-byte
+                    // stores gained a third of that). The elementwise gate's values
+                    // are read as whole sectors too (above); with both, the gated
+                    // call went 58.10 -> 57.33 us (with 16-byte gate loads these
+                    // stores cost time instead: the partial-sector traffic competes
+                    // with the gate reads in L2). The headwise family keeps the bulk
+                    // copies (measured no better direct).
                     if (i < args.Lq) {
                         const __nv_bfloat16* dstg = args.out + (((long)b * args.Lq + i) * args.Hq + h) * HD + cb * 32;
 #pragma unroll
@@ -716,16 +729,25 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     a.ctl.err = rt.err;
     a.ctl.limit_ns = rt.limit_ns;
 
+    // The API asks 16-byte alignment of O; the 256-bit stores need 32, so a
+    // view that starts mid-sector takes the staged bulk copies instead.
+    constexpr bool kCanDirect = (GATE == 0 || GATE == 2);
+    const bool direct = kCanDirect && (reinterpret_cast<uintptr_t>(p.O) & 31u) == 0;
     static PerDeviceSetup setup;   // per template instance
     cudaError_t r = setup_once_per_device(setup, [](int&) {
         // The register split above only fits if the launch allocates enough
         // registers per thread; refuse to launch otherwise (it would not finish).
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<HD, GATE, ADD>);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_kernel<HD, GATE, ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)C::SMEM_BYTES);
+        for (int k = 0; k < (kCanDirect ? 2 : 1); ++k) {
+            const void* fn = k ? reinterpret_cast<const void*>(prefill_kernel<HD, GATE, ADD, kCanDirect>)
+                               : reinterpret_cast<const void*>(prefill_kernel<HD, GATE, ADD, false>);
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     });
     if (r != cudaSuccess) return r;
     const long units = (long)a.n_pairs * p.Hq * p.B;
@@ -744,7 +766,8 @@ cudaError_t launch_prefill_t(const Problem& p, const WorkspacePlan& w, char* ws,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD>, tmQ, tmK, tmV, tmO, a);
+    if (direct) return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD, kCanDirect>, tmQ, tmK, tmV, tmO, a);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HD, GATE, ADD, false>, tmQ, tmK, tmV, tmO, a);
 }
 
 }  // namespace

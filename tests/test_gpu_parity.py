@@ -219,6 +219,23 @@ def test_binding_passes_the_real_workspace_size():
     assert gb.check_device_error() == gb.OK
 
 
+@pytest.mark.parametrize("gate", ["none", "elementwise"])
+def test_output_view_off_a_32_byte_boundary(gate):
+    # The epilogue stores whole 32-byte sectors from registers when O is 32-byte
+    # aligned; an output view that is only 16-byte aligned (what the ABI asks)
+    # takes the staged bulk copies: same values either way.
+    w = small("bf16", gate=gate, H_q=4, H_kv=2, L_q=300, L_k=300)
+    t = {k: (v.cuda() if v is not None else None) for k, v in make_inputs(w).items()}
+    O_ref, _ = gb.gated_sdpa_fwd(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=gate, causal=True)
+    n = t["Q"].numel()
+    buf = torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(t["Q"].shape)   # 16 bytes past a 256-byte-aligned allocation
+    assert out.data_ptr() % 32 == 16
+    gb.gated_sdpa_fwd(t["X"], t["Q"], t["K"], t["V"], t["W_g"], gate=gate, causal=True, out=out)
+    assert gb.check_device_error() == gb.OK
+    assert torch.equal(out, O_ref)
+
+
 BAD_ARGS = ["headwise_W_g_for_elementwise", "X_rows", "out_shape", "sink_size", "lse_size", "K_V_mismatch",
             "dtype", "gate_out_dtype", "bwd_dO_shape", "bwd_lse_size"]
 
